@@ -1,0 +1,203 @@
+/*
+ * specverify.h -- libspecverify: batched draft-token verification by modified
+ * rejection sampling, on one NVIDIA GB300 (sm_103a).
+ *
+ * The operation (defined on the pages this library follows):
+ *  - tech-tldr.com "投機的デコーディングとドラフトモデル", section
+ *    受理判定の数理：修正版棄却サンプリング: keep proposal x_i when a uniform
+ *    r in [0,1) satisfies r < min(1, p(x_i)/q(x_i)); at the first failure stop
+ *    and draw one token from normalize(max(0, p - q)).
+ *  - r-jc.jp "LLM推論の高速化｜KVキャッシュと投機的デコーディングを自作で実測",
+ *    section 投機的デコーディングとは（speculative decoding の仕組み): per
+ *    position p = softmax(target logits / T), q = softmax(draft logits / T);
+ *    ordered tests, first-rejection break; after the loop row nacc supplies
+ *    the residual (a rejection happened) or p itself (all accepted: the bonus
+ *    token); one inverse-CDF draw; the caller then truncates its KV cache to
+ *    base + 1 + nacc.  Section 投機的デコーディングを実装して受理率と速度を実測:
+ *    at temperature 0 a proposal is kept iff it equals the target argmax.
+ *  - issoh.co.jp "Speculative Decoding（投機的デコーディング）とは？…",
+ *    section 受理・棄却の規則と出力分布が変わらない理由, steps 1-5.
+ *
+ * Conventions shared by every entry point
+ *  - Layouts are row-major and contiguous:
+ *      target_logits [B][Kmax+1][V], draft_logits [B][Kmax][V] (same dtype),
+ *      draft_tokens [B][Kmax] int32, uniforms [B][Kmax+1] float32,
+ *      temperature [B] float32, out_tokens [B][Kmax+1] int32,
+ *      out_num_accepted [B] int32,
+ *    where Kmax = max_b K[b] is computed from the host array K.
+ *  - Uniform slots: uniforms[b][i] for i < K[b] is the accept test of
+ *    position i; uniforms[b][K[b]] is the final draw (resample or bonus).
+ *    Slots past K[b] are never read.  Greedy sequences read no uniforms.
+ *  - temperature[b] == 0 selects greedy verification for sequence b; any
+ *    other usable value (finite, >= FLT_MIN) selects sampling at that T.
+ *  - Outputs: out_tokens[b][j] = draft_tokens[b][j] for j < n_b, the drawn
+ *    token at j = n_b, -1 after it; out_num_accepted[b] = n_b.  The caller
+ *    sets its KV length to base + 1 + n_b.
+ *  - Device-data errors never trap: a NaN or +inf logit, a row with no finite
+ *    entry, an unusable temperature, a token outside [0, V) or a uniform
+ *    outside [0,1) met on the path the method walks makes that sequence's
+ *    out_num_accepted -1 and its out_tokens row all -1.  Rows after the first
+ *    rejection are never read, so their contents cannot affect the result.
+ *  - Host-detectable argument errors return synchronously before any work is
+ *    queued.  Launches are asynchronous on `stream`; nothing synchronises the
+ *    device except spec_verify_host and sv_workspace_errors, which say so.
+ *  - All buffers are owned by the caller.  Device pointers must belong to
+ *    the current device.  16-byte-aligned logits with V*sizeof(elem) a
+ *    multiple of 16 take the bulk-copy (TMA) path; anything else is still
+ *    accepted and read with element loads.
+ */
+#ifndef SPECVERIFY_H
+#define SPECVERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SV_ABI_VERSION 1
+/* Largest per-sequence draft count: one warp ballot covers the accept bits. */
+#define SV_K_MAX 32
+
+typedef enum {
+    SV_OK = 0,
+    SV_ERR_INVALID_ARG = 1,   /* bad pointer, size, K[b] or dtype; nothing queued */
+    SV_ERR_CUDA = 2,          /* a CUDA runtime call failed */
+    SV_ERR_UNSUPPORTED = 3,   /* V beyond sv_max_vocab(dtype) */
+    SV_ERR_NO_MEMORY = 4,     /* workspace too small, or stream-ordered allocation failed */
+    SV_ERR_TIMEOUT = 5        /* a bounded device-side wait gave up (see sv_workspace_errors) */
+} sv_status;
+
+typedef enum { SV_DTYPE_F32 = 0, SV_DTYPE_BF16 = 1 } sv_dtype;
+
+/*
+ * Optional per-position diagnostics (device pointers; each may be NULL).
+ *   p_x, q_x    [B][Kmax] float32: p_i(x_i) and q_i(x_i) at every draft
+ *               position i < K[b] of a sampling sequence; NaN elsewhere
+ *               (greedy sequence, i >= K[b], unusable row or token).
+ *   resid_mass  [B][Kmax] float32: sum_j max(0, p_i(j) - q_i(j)), which is
+ *               1 - alpha_i, the rejection probability of position i.
+ *   final_row   [B] int32: the row the final token was drawn from (= n_b).
+ */
+typedef struct {
+    float* p_x;
+    float* q_x;
+    float* resid_mass;
+    int32_t* final_row;
+} sv_diag;
+
+/*
+ * Options for spec_verify_ex.  Zero-initialise for defaults.
+ *   diag            diagnostics (requesting any forces verify_all).
+ *   verify_all      1: sweep every row, including those after the first
+ *                   rejection (the results are identical; only the work and
+ *                   the diagnostics differ).  0: rows a known earlier
+ *                   rejection makes irrelevant are skipped.
+ *   chunks_per_cta  0: automatic.  Otherwise the number of vocabulary chunks
+ *                   each CTA of a row's cluster holds in shared memory
+ *                   (tuning; SV_ERR_UNSUPPORTED if the result does not fit).
+ */
+typedef struct {
+    sv_diag diag;
+    int32_t verify_all;
+    int32_t chunks_per_cta;
+} sv_options;
+
+/* Human-readable name of a status code (static storage). */
+const char* sv_status_string(sv_status status);
+
+/* SV_ABI_VERSION of the loaded library. */
+int32_t sv_abi_version(void);
+
+/* Largest vocabulary size spec_verify accepts for dtype (0 for a bad dtype). */
+int32_t sv_max_vocab(sv_dtype dtype);
+
+/*
+ * Bytes of device workspace spec_verify_ws / spec_verify_ex need for this
+ * shape (0 on invalid arguments).  The workspace holds per-row statistics,
+ * per-chunk partial sums, per-sequence counters and the uploaded K; each call
+ * re-initialises what it uses, so the buffer needs no clearing.
+ */
+size_t sv_workspace_size(int32_t B, int32_t Kmax, int32_t V, sv_dtype dtype);
+
+/*
+ * spec_verify -- verify B sequences (the entry point the pages' loop maps to).
+ *   target_logits     device, [B][Kmax+1][V], dtype.
+ *   draft_logits      device, [B][Kmax][V], dtype; may be NULL when every
+ *                     temperature is 0 (a sampling sequence then yields -1).
+ *   dtype             SV_DTYPE_F32 or SV_DTYPE_BF16 (both logit arrays).
+ *   draft_tokens      device, [B][Kmax] int32; may be NULL iff Kmax == 0.
+ *   uniforms          device, [B][Kmax+1] float32.
+ *   temperature       device, [B] float32 (0 = greedy).
+ *   B                 number of sequences, >= 0 (0 is a no-op).
+ *   K                 HOST, [B] int32, 0 <= K[b] <= SV_K_MAX.
+ *   V                 vocabulary size shared by target and draft, 1..sv_max_vocab.
+ *   out_tokens        device, [B][Kmax+1] int32 (written).
+ *   out_num_accepted  device, [B] int32 (written).
+ *   stream            CUDA stream; all work is queued on it.
+ * Scratch comes from the stream-ordered allocator (cudaMallocAsync) and is
+ * released on the same stream.
+ */
+sv_status spec_verify(const void* target_logits, const void* draft_logits, sv_dtype dtype,
+                      const int32_t* draft_tokens, const float* uniforms,
+                      const float* temperature, int32_t B, const int32_t* K, int32_t V,
+                      int32_t* out_tokens, int32_t* out_num_accepted, cudaStream_t stream);
+
+/*
+ * spec_verify_ws -- as spec_verify, with a caller-provided device workspace of
+ * at least sv_workspace_size(B, Kmax, V, dtype) bytes, 256-byte aligned.
+ * Calls that share one workspace must be ordered on one stream.
+ */
+sv_status spec_verify_ws(const void* target_logits, const void* draft_logits, sv_dtype dtype,
+                         const int32_t* draft_tokens, const float* uniforms,
+                         const float* temperature, int32_t B, const int32_t* K, int32_t V,
+                         int32_t* out_tokens, int32_t* out_num_accepted,
+                         void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * spec_verify_ex -- as spec_verify_ws plus options (may be NULL) and the
+ * per-position diagnostics.
+ */
+sv_status spec_verify_ex(const void* target_logits, const void* draft_logits, sv_dtype dtype,
+                         const int32_t* draft_tokens, const float* uniforms,
+                         const float* temperature, int32_t B, const int32_t* K, int32_t V,
+                         int32_t* out_tokens, int32_t* out_num_accepted,
+                         const sv_options* options, void* workspace, size_t workspace_bytes,
+                         cudaStream_t stream);
+
+/*
+ * Device-side error flags recorded in a workspace by the last call that used
+ * it (bit 0: a bounded shared-memory copy wait gave up).  Copies the word to
+ * *flags, clears it, and synchronises `stream`.  Returns SV_ERR_TIMEOUT when
+ * bit 0 was set, SV_OK otherwise.
+ */
+sv_status sv_workspace_errors(void* workspace, uint32_t* flags, cudaStream_t stream);
+
+/*
+ * Bytes of device staging spec_verify_host needs (inputs, outputs and the
+ * workspace), 0 on invalid arguments.
+ */
+size_t sv_host_staging_size(int32_t B, int32_t Kmax, int32_t V, sv_dtype dtype);
+
+/*
+ * spec_verify_host -- the same operation on HOST arrays (same layouts as
+ * above; pinned memory gives asynchronous copies, pageable memory works).
+ * Copies the inputs into `device_staging` (>= sv_host_staging_size bytes,
+ * 256-byte aligned), verifies, copies out_tokens / out_num_accepted back to
+ * the host arrays and synchronises `stream` before returning.
+ */
+sv_status spec_verify_host(const void* h_target_logits, const void* h_draft_logits,
+                           sv_dtype dtype, const int32_t* h_draft_tokens,
+                           const float* h_uniforms, const float* h_temperature, int32_t B,
+                           const int32_t* K, int32_t V, int32_t* h_out_tokens,
+                           int32_t* h_out_num_accepted, void* device_staging,
+                           size_t staging_bytes, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPECVERIFY_H */

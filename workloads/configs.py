@@ -31,8 +31,7 @@ from dataclasses import dataclass, field
 
 import numpy as np
 
-from .philox import (STREAM_DRAFT, STREAM_LOGITS, STREAM_UNIFORMS,
-                     philox4x32_10, u32_to_unit_float, uniform_grid)
+from .philox import STREAM_DRAFT, STREAM_LOGITS, STREAM_UNIFORMS, uniform_grid
 
 # The toy pair printed with the 200k-draw simulation (target p, draft q).
 TOY_P = np.array([0.40, 0.25, 0.15, 0.12, 0.08])
@@ -111,9 +110,8 @@ def temp_array(spec_t, B: int) -> np.ndarray:
 # Gumbel-max draft sampling on the host (small inputs)
 # ----------------------------------------------------------------------------
 def _gumbel_rows(seed: int, nrows: int, V: int) -> np.ndarray:
-    u = uniform_grid(seed, STREAM_DRAFT, nrows, V).astype(np.float64)
-    u = u + 2.0 ** -25                   # open interval (0, 1)
-    return -np.log(-np.log(u))
+    rng = np.random.Generator(np.random.PCG64([seed, STREAM_DRAFT]))
+    return rng.gumbel(size=(nrows, V))
 
 
 def draft_tokens_host(draft32: np.ndarray, K: np.ndarray, temps: np.ndarray,
@@ -124,13 +122,13 @@ def draft_tokens_host(draft32: np.ndarray, K: np.ndarray, temps: np.ndarray,
     if Kmax == 0:
         return tok
     g = _gumbel_rows(seed, B * Kmax, V).reshape(B, Kmax, V)
-    for b in range(B):
-        for i in range(int(K[b])):
-            row = draft32[b, i].astype(np.float64)
-            if temps[b] > 0:
-                tok[b, i] = int(np.argmax(row / float(temps[b]) + g[b, i]))
-            else:
-                tok[b, i] = int(np.argmax(row))
+    T = np.asarray(temps, np.float64).reshape(B, 1, 1)
+    d = draft32.astype(np.float64)
+    samp = np.argmax(d / np.where(T > 0, T, 1.0) + g, axis=-1)
+    greedy = np.argmax(d, axis=-1)
+    tok = np.where(T.reshape(B, 1) > 0, samp, greedy).astype(np.int32)
+    pad = np.arange(Kmax)[None, :] >= np.asarray(K).reshape(B, 1)
+    tok[pad] = 0
     return tok
 
 
