@@ -1,0 +1,394 @@
+#!/usr/bin/env python3
+"""Benchmark: batched draft-token verification on GB300.
+
+One step = one spec_verify call (every row of the hot path: row staging,
+softmax statistics, ratio test, first-rejection reduction, residual mass,
+final draw, outputs) over one batch of synthetic logits already resident in
+HBM.  Default workload: B=1024 sequences, K_b ~ U{1..8}, V=128256, bf16
+logits ~N(0, 2^2), draft = target + N(0, 1), half the sequences at T=1 and
+half greedy.  `--workload N` selects another of the benchmark workloads.
+
+Prints one JSON line (rank 0).  Under torchrun every rank verifies its own
+batch of the same shape (weak scaling, no collective on the data path); the
+timing is the max over ranks.
+
+`--impl reference` times the fp64 CPU oracle on a bounded sample of the same
+workload on the host cores instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "verified draft positions/sec and achieved HBM GB/s (% of GB300 peak), 1 GPU"
+UNIT = "positions/s"
+KERNEL_SOURCES = ["speculative_decoding_verification_04_gb300/csrc/spec_verify.cu",
+                  "speculative_decoding_verification_04_gb300/csrc/sv_ptx.cuh"]
+WORKLOAD_TEXT = {
+    0: "B=64 K=4 V=5 fp32 N(0,1) draft+N(0,1) T=1",
+    1: "B=1 K=4 V=32000 bf16 N(0,2^2) draft+N(0,1) T=1",
+    2: "B=64 K=5 V=128256 bf16 N(0,3^2) draft+N(0,0.5^2) T=1",
+    3: "B=256 K=8 V=151936 fp32 N(0,2^2) draft+N(0,1.5^2) T=0.7",
+    4: "B=1024 K_b~U{1..8} V=128256 bf16 N(0,2^2) draft+N(0,1^2) half T=1 half greedy",
+}
+
+
+def _source_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        h.update(open(os.path.join(ROOT, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def _peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm_gbs=float(d["hbm_gbs"]), source="measured")
+    return dict(hbm_gbs=6800.0, source="fallback")
+
+
+def _profile_traffic(widx: int):
+    """DRAM bytes per launch from the committed ncu summary of this workload,
+    if it was taken on the current kernel source; else None."""
+    pdir = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(pdir):
+        return None
+    want = _source_hash()
+    for f in sorted(os.listdir(pdir)):
+        if not f.endswith(".md"):
+            continue
+        text = open(os.path.join(pdir, f)).read()
+        m_w = re.search(r"^bench_workload:\s*(\d+)\s*$", text, re.M)
+        m_h = re.search(r"^kernel_source_sha256_16:\s*([0-9a-f]+)\s*$", text, re.M)
+        m_b = re.search(r"^dram_bytes_per_launch:\s*([0-9]+)\s*$", text, re.M)
+        if m_w and m_h and m_b and int(m_w.group(1)) == widx and m_h.group(1) == want:
+            return int(m_b.group(1))
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return dict(sm_mhz=statistics.median(sm), sm_max_mhz=max(smax), samples=len(sm),
+                    reasons=sorted(reasons))
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (baseline leg and reference arm)
+# ---------------------------------------------------------------------------
+def oracle_sample(widx: int, step_s: float, host=None):
+    """Pick n (first n sequences of the workload) so one oracle pass over them
+    takes about `step_s` seconds; returns the host inputs."""
+    import oracle
+    B = W.SPECS[widx].B
+    n = min(B, 4)
+    while True:
+        inp = host(n) if host else W.make_spec_host(widx, B=n)
+        t0 = time.perf_counter()
+        oracle.verify_inputs(inp)
+        dt = time.perf_counter() - t0
+        if dt >= 0.25 * step_s or n >= B:
+            break
+        n = min(B, max(n + 1, int(n * min(16.0, 0.3 * step_s / max(dt, 1e-4)))))
+    if dt < step_s and n < B:
+        n = min(B, max(n, int(n * step_s / max(dt, 1e-4))))
+        inp = host(n) if host else W.make_spec_host(widx, B=n)
+    return inp, n
+
+
+def oracle_rate(inp):
+    """Single-thread oracle throughput on host inputs: (positions/s, seconds)."""
+    import oracle
+    t0 = time.perf_counter()
+    oracle.verify_inputs(inp)
+    dt = time.perf_counter() - t0
+    return float(np.sum(inp["K"])) / dt, dt
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the fp64 oracle on the host cores
+# ---------------------------------------------------------------------------
+def run_reference(args):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    widx = args.workload
+    inp, n = oracle_sample(widx, step_s=0.5)
+    rates, secs = [], []
+    for step in range(args.warmup + args.steps):
+        rate, dt = oracle_rate(inp)
+        if step >= args.warmup:
+            rates.append(rate)
+            secs.append(dt)
+    value = float(statistics.median(rates))
+    line = dict(
+        impl="reference", metric=METRIC, value=value, unit=UNIT, n_gpus=args.gpus,
+        steps=args.steps, warmup=args.warmup, ms_per_step=round(1e3 * statistics.median(secs), 3),
+        higher_is_better=True, scaling="weak", vs_baseline=None, dtype="f64", data="synthetic",
+        config=dict(workload=WORKLOAD_TEXT[widx], bench_workload=widx, sample_sequences=n),
+        cpu_baseline=dict(value=value, unit=UNIT, cores=1, kind="oracle",
+                          sample=f"first {n} of {W.SPECS[widx].B} sequences of the workload "
+                                 f"({int(np.sum(inp['K']))} positions) per step, host-generated "
+                                 f"with the same recipe, single thread"),
+        e2e=dict(value=value, unit=UNIT, h2d_bytes_per_step=0, d2h_bytes_per_step=0))
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def run_ours(args):
+    import torch
+
+    import speculative_decoding_verification_04_gb300 as sv
+
+    world, rank, local = _dist()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    widx = args.workload
+
+    d = W.make_device(widx, dev)
+    B, Kmax, V = d["B"], d["Kmax"], d["V"]
+    K = np.asarray(d["K"], np.int32)
+    dcode = sv.SV_DTYPE_BF16 if d["dtype"] == "bf16" else sv.SV_DTYPE_F32
+    ws = sv.Workspace(B, Kmax, V, dcode, dev)
+    out_t = torch.empty((B, Kmax + 1), dtype=torch.int32, device=dev)
+    out_n = torch.empty((B,), dtype=torch.int32, device=dev)
+    call_args = (d["target"], d["draft"], d["tokens"], d["uniforms"], d["temperature"], K)
+    stream = torch.cuda.current_stream()
+
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+
+    def step(verify_all=False):
+        if verify_all:
+            sv.spec_verify_ex(*call_args, ws, verify_all=True, out_tokens=out_t,
+                              out_num_accepted=out_n)
+        else:
+            sv.spec_verify_ws(*call_args, ws, out_tokens=out_t, out_num_accepted=out_n)
+
+    def timed(nsteps, verify_all=False):
+        evs = []
+        for _ in range(nsteps):
+            flush.fill_(1)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            step(verify_all)
+            e1.record(stream)
+            evs.append((e0, e1))
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in evs]
+
+    for _ in range(max(args.warmup, 3)):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize()
+    nacc = out_n.cpu().numpy()
+    pos_per_step = int(K.sum())
+    bytes_need = W.bytes_needed(K, d["temperature_host"], nacc, V, d["dtype"], Kmax)
+    bytes_all = W.bytes_all_rows(K, d["temperature_host"], V, d["dtype"], Kmax)
+
+    # ---- timed region ----
+    clocks = ClockSampler(local) if rank == 0 else None
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    torch.cuda.nvtx.range_push("sv_timed")
+    times = timed(args.steps)
+    torch.cuda.nvtx.range_pop()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clk = clocks.stop() if clocks else None
+    total_ms = float(sum(times))
+    if dist:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * pos_per_step * args.steps / (total_ms / 1e3)
+    errs = sv.sv_workspace_errors(ws)
+
+    # verify-every-row variant of the same step (same outputs, all bytes read)
+    times_all = timed(max(3, args.steps // 2), verify_all=True)
+    ms_all = statistics.median(times_all)
+
+    peaks = _peaks()
+    med_ms = statistics.median(times)
+    achieved = bytes_need / (med_ms / 1e3) / 1e9
+    traffic = _profile_traffic(widx)
+    roofline = dict(bound="hbm", achieved=round(achieved, 1), peak=peaks["hbm_gbs"], unit="GB/s",
+                    frac=round(achieved / peaks["hbm_gbs"], 4), traffic=traffic,
+                    bytes_algorithmic=bytes_need, peak_source=peaks["source"],
+                    kernel="sv_verify_kernel")
+
+    # ---- end to end through the host entry point (pinned buffers) ----
+    e2e = None
+    if rank == 0 or world > 1:
+        def pinned(t):
+            h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+            h.copy_(t)
+            return h
+        h_t, h_d = pinned(d["target"]), pinned(d["draft"])
+        h_tok, h_uni, h_tmp = pinned(d["tokens"]), pinned(d["uniforms"]), pinned(d["temperature"])
+        staging = torch.empty(sv.sv_host_staging_size(B, Kmax, V, dcode), dtype=torch.uint8,
+                              device=dev)
+        h_ot = torch.empty((B, Kmax + 1), dtype=torch.int32, pin_memory=True)
+        h_on = torch.empty((B,), dtype=torch.int32, pin_memory=True)
+        host_args = (h_t, h_d, h_tok, h_uni, h_tmp, K, staging)
+        sv.spec_verify_host(*host_args, out_tokens=h_ot, out_num_accepted=h_on)
+        n_e2e = max(3, min(args.steps, 8))
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(n_e2e):
+            sv.spec_verify_host(*host_args, out_tokens=h_ot, out_num_accepted=h_on)
+        e2e_s = (time.perf_counter() - t0) / n_e2e
+        if dist:
+            t = torch.tensor([e2e_s], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_s = float(t.item())
+        same = bool(np.array_equal(h_on.numpy(), nacc))
+        h2d = sum(x.numel() * x.element_size() for x in (h_t, h_d, h_tok, h_uni, h_tmp))
+        d2h = h_ot.numel() * 4 + h_on.numel() * 4
+        e2e = dict(value=world * pos_per_step / e2e_s, unit=UNIT, h2d_bytes_per_step=h2d,
+                   d2h_bytes_per_step=d2h, ms_per_step=round(e2e_s * 1e3, 3),
+                   matches_device_run=same, api="spec_verify_host")
+        del h_t, h_d, staging
+
+    # ---- CPU oracle baseline on a bounded sample (rank 0, N=1 only) ----
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        def host_rows(n):
+            return _rows_to_host(d, np.arange(n))
+        inp, n = oracle_sample(widx, step_s=12.0, host=host_rows)
+        rate, dt = oracle_rate(inp)
+        cpu = dict(value=rate, unit=UNIT, cores=1, kind="oracle",
+                   sample=f"first {n} of {B} sequences of this workload "
+                          f"({int(np.sum(inp['K']))} positions, {dt:.1f} s, single thread)")
+
+    if rank == 0:
+        line = dict(
+            metric=METRIC, value=value, unit=UNIT, n_gpus=world, steps=args.steps,
+            warmup=args.warmup, ms_per_step=round(ms_per_step, 5), higher_is_better=True,
+            scaling="weak", vs_baseline=None, dtype="f32", data="synthetic",
+            config=dict(workload=WORKLOAD_TEXT[widx], bench_workload=widx, logits=d["dtype"],
+                        B=B, Kmax=Kmax, V=V, positions_per_step=pos_per_step,
+                        l2="flushed before every step (2x L2 write)", parallelism=f"dp{world}"),
+            roofline=roofline, cpu_baseline=cpu, e2e=e2e, gpu_launches=args.steps,
+            clocks=clk,
+            detail=dict(
+                mean_accepted=float(np.mean(nacc)), bytes_needed=bytes_need,
+                bytes_all_rows=bytes_all, ms_median=round(med_ms, 5),
+                ms_min=round(min(times), 5),
+                verify_all=dict(ms_median=round(ms_all, 5),
+                                gbs=round(bytes_all / (ms_all / 1e3) / 1e9, 1),
+                                frac=round(bytes_all / (ms_all / 1e3) / 1e9 / peaks["hbm_gbs"], 4)),
+                device_errors=errs, kernel_source_sha256_16=_source_hash()))
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def _rows_to_host(d, seqs):
+    import torch
+    idx = torch.as_tensor(np.asarray(seqs), device=d["target"].device, dtype=torch.long)
+
+    def host(t):
+        t = t.index_select(0, idx).cpu()
+        if t.dtype == torch.bfloat16:
+            return t.view(torch.int16).numpy().view(np.uint16)
+        return t.numpy()
+
+    return dict(target=host(d["target"]), draft=host(d["draft"]), dtype=d["dtype"],
+                tokens=host(d["tokens"]), uniforms=host(d["uniforms"]),
+                temperature=host(d["temperature"]), K=np.asarray(d["K"])[np.asarray(seqs)])
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=4, choices=[0, 1, 2, 3, 4])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,156 @@
+// sv_common.cuh -- shared device definitions of libspecverify: kernel
+// arguments, element access, the fixed-rounding softmax weight and residual
+// term, warp reductions and the per-row decision codes.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <float.h>
+#include <limits.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "sv_ptx.cuh"
+
+namespace sv {
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr int kMaxWarps = 16;
+constexpr int kMaxCluster = 16;
+constexpr uint32_t kWaitSpins = 1u << 22;   // bounded mbarrier polls (a few seconds)
+constexpr double kLog2e = 1.4426950408889634;
+constexpr int kFinalizeWarps = 4;           // sequences per finalize CTA
+
+// Per-row decision written by the sweep and read by the finaliser.
+enum : uint8_t {
+    kDecNone = 0,      // row not evaluated in this call
+    kDecAccept = 1,
+    kDecReject = 2,
+    kDecInvalid = 3,   // unusable input on this row
+    kDecBonus = 4      // position K_b evaluated and usable
+};
+
+enum : uint32_t { kErrWaitTimeout = 1u };
+
+struct Args {
+    const void* tgt;
+    const void* drf;
+    const int32_t* tok;
+    const float* uni;
+    const float* temp;
+    int32_t* out_tok;
+    int32_t* out_n;
+    int B, Kmax, V;
+    int n_items;           // B * (Kmax + 1): rows in position-major order
+    int nchunks, ncpc, C;
+    int early_exit, aligned;
+    // workspace
+    uint32_t* err;
+    int* next_item;        // claim counter of the persistent sweep
+    uint32_t* mask;        // per sequence: bit i set when position i rejected / unusable
+    uint8_t* dec;          // per row decision
+    const int32_t* K;
+    int32_t* argmax;       // per row (greedy)
+    float4* rowstat;       // per row: m_t, 1/S_t, m_d, 1/S_d
+    double* Pc;            // per (row, chunk): sum of exp2((l - m_t) c)
+    double* Rc;            // per (row, chunk): sum of max(0, p - q)
+    // diagnostics (nullable)
+    float* p_x;
+    float* q_x;
+    float* resid;
+    int32_t* final_row;
+};
+
+template <typename T> struct Elem;
+
+template <> struct Elem<float> {
+    static constexpr int E = 4;   // elements per 16-byte vector
+    __device__ static __forceinline__ void unpack(const uint4& w, float (&x)[4])
+    {
+        x[0] = __uint_as_float(w.x);
+        x[1] = __uint_as_float(w.y);
+        x[2] = __uint_as_float(w.z);
+        x[3] = __uint_as_float(w.w);
+    }
+    __device__ static __forceinline__ float load(const float* p) { return __ldg(p); }
+    __device__ static __forceinline__ void copy(float* dst, const float* src) { *dst = __ldg(src); }
+    __device__ static __forceinline__ void set_neg_inf(float* dst) { *dst = -INFINITY; }
+};
+
+template <> struct Elem<__nv_bfloat16> {
+    static constexpr int E = 8;
+    __device__ static __forceinline__ void unpack(const uint4& w, float (&x)[8])
+    {
+        const uint32_t v[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            x[2 * k] = __uint_as_float(v[k] << 16);
+            x[2 * k + 1] = __uint_as_float(v[k] & 0xffff0000u);
+        }
+    }
+    __device__ static __forceinline__ float load(const __nv_bfloat16* p)
+    {
+        const unsigned short h = __ldg(reinterpret_cast<const unsigned short*>(p));
+        return __uint_as_float(static_cast<uint32_t>(h) << 16);
+    }
+    __device__ static __forceinline__ void copy(__nv_bfloat16* dst, const __nv_bfloat16* src)
+    {
+        *reinterpret_cast<unsigned short*>(dst) = __ldg(reinterpret_cast<const unsigned short*>(src));
+    }
+    __device__ static __forceinline__ void set_neg_inf(__nv_bfloat16* dst)
+    {
+        *reinterpret_cast<unsigned short*>(dst) = 0xFF80u;
+    }
+};
+
+// exp2((l - m) * c): the unnormalised softmax weight, c = log2(e)/T, in one
+// fixed rounding sequence shared by the sweep and the finaliser.
+__device__ __forceinline__ float weight(float l, float m, float c)
+{
+    return ex2_approx(__fmul_rn(__fsub_rn(l, m), c));
+}
+
+// max(0, p - q) with p = e_t / S_t and q = e_d / S_d, fixed rounding sequence.
+__device__ __forceinline__ float resid_term(float et, float inv_st, float ed, float inv_sd)
+{
+    return fmaxf(__fsub_rn(__fmul_rn(et, inv_st), __fmul_rn(ed, inv_sd)), 0.0f);
+}
+
+__device__ __forceinline__ float warp_max_nan(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        v = max_nan(v, __shfl_xor_sync(kFull, v, o));
+    return v;
+}
+
+// Butterfly sum: every lane ends with the same value (IEEE addition commutes).
+__device__ __forceinline__ double warp_sum(double v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        v += __shfl_xor_sync(kFull, v, o);
+    return v;
+}
+
+__device__ __forceinline__ double warp_incl_scan(double v, int lane)
+{
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const double y = __shfl_up_sync(kFull, v, o);
+        if (lane >= o)
+            v += y;
+    }
+    return v;
+}
+
+__device__ __forceinline__ bool temperature_usable(float T)
+{
+    return T == 0.0f || (isfinite(T) && T >= FLT_MIN);
+}
+
+__device__ __forceinline__ uint32_t positions_below(int i)
+{
+    return i >= 32 ? 0xffffffffu : ((1u << i) - 1u);
+}
+
+}  // namespace sv

@@ -120,6 +120,25 @@ __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uin
         ::"r"(dst), "l"(src), "r"(bytes), "r"(mbar) : "memory");
 }
 
+// Order this thread's earlier generic-proxy shared-memory accesses before its
+// later bulk-copy (async-proxy) writes into the same buffer.
+__device__ __forceinline__ void fence_proxy_async()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Programmatic dependent launch: let the next kernel in the stream start
+// launching / wait until the previous kernel has completed and flushed.
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void griddep_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __device__ __forceinline__ float ex2_approx(float x)
 {
     float y;

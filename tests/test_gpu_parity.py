@@ -240,6 +240,9 @@ def test_full_size_workloads_sampled(dev, idx):
     d = W.make_device(idx, dev)
     B = d["B"]
     K = np.asarray(d["K"])
+    # the draft rows carry the workload's noise (they are not the target rows)
+    noise = (d["draft"][:, 0].float() - d["target"][:, 0].float()).std().item()
+    assert abs(noise - W.SPECS[idx].sigma_d) < 0.05 * W.SPECS[idx].sigma_d + 0.01
     ws = sv.Workspace(B, d["Kmax"], d["V"], dtype_code(d["dtype"]), dev)
     got_t, got_n = run_gpu(d, "ws", workspace=ws)
     assert sv.sv_workspace_errors(ws) == 0

@@ -243,7 +243,8 @@ def make_device(idx: int, device="cuda", B: int | None = None, V: int | None = N
         t32 = torch.randn((b1 - b0, Kmax + 1, V), generator=g, device=device,
                           dtype=torch.float32).mul_(s.sigma_t)
         tgt[b0:b1] = t32.to(tdt)
-        d32 = tgt[b0:b1, :Kmax].float()
+        # explicit copy: for fp32 logits .float() would alias the target rows
+        d32 = tgt[b0:b1, :Kmax].to(torch.float32, copy=True)
         d32.add_(torch.randn((b1 - b0, Kmax, V), generator=g, device=device,
                              dtype=torch.float32).mul_(s.sigma_d))
         drf[b0:b1] = d32.to(tdt)
