@@ -351,7 +351,8 @@ def run_ours(args):
                 verify_all=dict(ms_median=round(ms_all, 5),
                                 gbs=round(bytes_all / (ms_all / 1e3) / 1e9, 1),
                                 frac=round(bytes_all / (ms_all / 1e3) / 1e9 / peaks["hbm_gbs"], 4)),
-                device_errors=errs, kernel_source_sha256_16=_source_hash()))
+                device_errors=errs, kernel_source_sha256_16=_source_hash(),
+                geometry=sv.sv_geometry(B, Kmax, V, dcode)))
         print(json.dumps(line), flush=True)
     if dist:
         dist.barrier()

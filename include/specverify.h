@@ -116,6 +116,19 @@ int32_t sv_abi_version(void);
 int32_t sv_max_vocab(sv_dtype dtype);
 
 /*
+ * Launch geometry a call of this shape would use on the current device
+ * (diagnostic; queries the device, queues no work).  out8 receives:
+ *   [0] cluster size C (CTAs per row), [1] vocabulary chunks per CTA,
+ *   [2] shared-memory slots per CTA, [3] clusters in the persistent grid,
+ *   [4] threads per CTA, [5] dynamic shared memory per CTA (bytes),
+ *   [6] 1 if work is claimed per row (small batches), 0 per sequence,
+ *   [7] vocabulary chunks per row.
+ * chunks_per_cta = 0 selects the automatic choice (as sv_options does).
+ */
+sv_status sv_geometry(int32_t B, int32_t Kmax, int32_t V, sv_dtype dtype, int32_t chunks_per_cta,
+                      int32_t* out8);
+
+/*
  * Bytes of device workspace spec_verify_ws / spec_verify_ex need for this
  * shape (0 on invalid arguments).  The workspace holds per-row statistics,
  * per-chunk partial sums, per-sequence counters and the uploaded K; each call

@@ -79,6 +79,8 @@ def _load():
     lib.sv_abi_version.restype = i32
     lib.sv_workspace_errors.argtypes = [P, ctypes.POINTER(ctypes.c_uint32), P]
     lib.sv_workspace_errors.restype = ctypes.c_int
+    lib.sv_geometry.argtypes = [i32, i32, i32, ctypes.c_int, i32, P]
+    lib.sv_geometry.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -98,6 +100,18 @@ def sv_abi_version() -> int:
 
 def sv_max_vocab(dtype: int) -> int:
     return int(_load().sv_max_vocab(int(dtype)))
+
+
+GEOMETRY_FIELDS = ("cluster_ctas", "chunks_per_cta", "slots", "clusters", "threads",
+                   "smem_bytes", "per_row", "chunks")
+
+
+def sv_geometry(B: int, Kmax: int, V: int, dtype: int, chunks_per_cta: int = 0) -> dict:
+    """Launch geometry a call of this shape would use on the current device."""
+    out = (ctypes.c_int32 * 8)()
+    st = _load().sv_geometry(int(B), int(Kmax), int(V), int(dtype), int(chunks_per_cta), out)
+    _check(st, "sv_geometry")
+    return dict(zip(GEOMETRY_FIELDS, [int(v) for v in out]))
 
 
 def sv_workspace_size(B: int, Kmax: int, V: int, dtype: int) -> int:

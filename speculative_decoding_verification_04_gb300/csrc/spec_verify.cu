@@ -40,8 +40,9 @@ constexpr int kStaticSmemReserve = 2048;     // static __shared__ of the sweep, 
 constexpr int kChunksPerCta = 8;             // default slice: 8 chunk pairs = 64 KB per stage
 
 struct Geom {
-    int s = 0, nv = 0, ch = 0, nchunks = 0, ncpc = 0, C = 0, nwarps = 0, stages = 0;
+    int s = 0, nv = 0, ch = 0, nchunks = 0, ncpc = 0, C = 0, nwarps = 0, nslot = 0;
     int clusters = 0;   // persistent grid size (clusters)
+    int per_row = 0;    // slots claim rows (small batches) instead of sequences
     size_t smem = 0;
 };
 
@@ -65,19 +66,22 @@ static int n_chunks(int V, int s)
     return (V + ch - 1) / ch;
 }
 
-static size_t smem_for(int ncpc, int ch, int s, int stages)
+// nslot x (target + draft chunk) per owned chunk, one mbarrier per chunk and
+// stage, one fp32 chunk partial per chunk
+static size_t smem_for(int ncpc, int ch, int s, int nslot)
 {
-    return (size_t)stages * ncpc * (size_t)ch * (size_t)s * 2 + (size_t)stages * ncpc * 8;
+    return (size_t)nslot * ncpc * (size_t)ch * (size_t)s * 2 + (size_t)nslot * ncpc * 8 +
+           (size_t)ncpc * 4;
 }
 
-static int max_ncpc(int ch, int s, int stages)
+static int max_ncpc(int ch, int s, int nslot)
 {
-    return (int)((kSmemPerCtaMax - kStaticSmemReserve) / smem_for(1, ch, s, stages));
+    return (int)((kSmemPerCtaMax - kStaticSmemReserve) / smem_for(1, ch, s, nslot));
 }
 
 // ---- workspace layout ----
 struct WsLayout {
-    size_t err, next_item, mask, dec, K, header_end, argmax, rowstat, Pc, Rc, total;
+    size_t err, next_unit, dec, K, order, header_end, argmax, rowstat, Pc, Rc, total;
 };
 
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -90,16 +94,16 @@ static bool ws_layout(int B, int Kmax, int V, sv_dtype dt, WsLayout* L)
     const size_t nch = (size_t)n_chunks(V, elem_size(dt));
     size_t o = 0;
     L->err = o;
-    L->next_item = o + 4;
+    L->next_unit = o + 4;
     o = align256(o + 16);
-    L->mask = o;     o = align256(o + (size_t)B * 4);
     L->dec = o;      o = align256(o + R);
     L->K = o;        o = align256(o + (size_t)B * 4);
+    L->order = o;    o = align256(o + (size_t)B * 4);
     L->header_end = o;
     L->argmax = o;   o = align256(o + R * 4);
     L->rowstat = o;  o = align256(o + R * 16);
-    L->Pc = o;       o = align256(o + R * nch * 8);
-    L->Rc = o;       o = align256(o + R * nch * 8);
+    L->Pc = o;       o = align256(o + R * nch * 4);
+    L->Rc = o;       o = align256(o + R * nch * 4);
     L->total = o;
     return true;
 }
@@ -192,7 +196,7 @@ static cudaError_t capacity_nv(const Geom& g, int dev, int* n)
     }
 }
 
-// Chunks per CTA, cluster size and stage count for a given ncpc request.
+// Chunks per CTA, cluster size and slot count for a given ncpc request.
 static bool shape_geometry(int V, sv_dtype dt, int ncpc, Geom* g)
 {
     const int s = elem_size(dt);
@@ -205,60 +209,80 @@ static bool shape_geometry(int V, sv_dtype dt, int ncpc, Geom* g)
     if (C > kMaxCluster)
         return false;
     ncpc = (g->nchunks + C - 1) / C;   // balance the chunks over the cluster
-    int stages = 2;
-    if (ncpc > max_ncpc(g->ch, s, 2))
-        stages = 1;
-    if (ncpc > max_ncpc(g->ch, s, 1))
+    int nslot = 3;
+    while (nslot > 1 && ncpc > max_ncpc(g->ch, s, nslot))
+        --nslot;
+    if (ncpc > max_ncpc(g->ch, s, nslot))
         return false;
     g->ncpc = ncpc;
     g->C = C;
-    g->stages = stages;
-    g->nwarps = std::min(ncpc, kMaxWarps);
-    g->smem = smem_for(ncpc, g->ch, s, stages);
+    g->nslot = nslot;
+    g->nwarps = std::min(ncpc, kMaxWarps - 1) + 1;   // compute warps + the scheduler warp
+    g->smem = smem_for(ncpc, g->ch, s, nslot);
     return true;
 }
 
-// Pick the geometry of one launch: by default 8 chunk pairs (64 KB) per CTA
-// and stage, a wider spread over the cluster when there are few rows, and a
-// cluster shape the device can co-schedule.
-static sv_status pick_geometry(int V, sv_dtype dt, long long items, int nsm, int override_ncpc,
+static sv_status capacity_of(const Geom& g, sv_dtype dt, int dev, int* cap)
+{
+    const cudaError_t e = dt == SV_DTYPE_BF16 ? capacity_nv<__nv_bfloat16>(g, dev, cap)
+                                              : capacity_nv<float>(g, dev, cap);
+    return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
+// Pick the geometry of one launch.  Candidates: every cluster size from the
+// smallest whose slice fits shared memory up to 16 (one slice of at most
+// kChunksPerCta chunk pairs per CTA by default); keep the one that keeps the
+// most SMs busy, preferring more slots, then smaller clusters.
+static sv_status pick_geometry(int V, sv_dtype dt, int B, int Kmax, int nsm, int override_ncpc,
                                int dev, Geom* g)
 {
     const int s = elem_size(dt);
     const int nch = n_chunks(V, s);
-    int ncpc;
+    const long long rows = (long long)B * (Kmax + 1);
+    std::vector<int> cand;
     if (override_ncpc > 0) {
-        ncpc = override_ncpc;
+        cand.push_back(override_ncpc);
     } else {
-        ncpc = std::min(kChunksPerCta, nch);
-        if ((nch + ncpc - 1) / ncpc > kMaxCluster)
-            ncpc = (nch + kMaxCluster - 1) / kMaxCluster;
-        // few rows: spread each row over more CTAs while clusters stay portable
-        while (ncpc > 1) {
-            const int half = (ncpc + 1) / 2;
-            const int C2 = (nch + half - 1) / half;
-            const long long ctas = items * (long long)((nch + ncpc - 1) / ncpc);
-            if (C2 > 8 || ctas >= (long long)nsm)
+        const int base = std::min(kChunksPerCta, nch);
+        for (int C = (nch + base - 1) / base; C <= kMaxCluster; ++C) {
+            const int ncpc = (nch + C - 1) / C;
+            if (cand.empty() || cand.back() != ncpc)
+                cand.push_back(ncpc);
+            if (ncpc == 1)
                 break;
-            ncpc = half;
         }
+        if (cand.empty())   // V needs more than kChunksPerCta chunks per CTA even at C = 16
+            cand.push_back((nch + kMaxCluster - 1) / kMaxCluster);
     }
-    for (;;) {
-        if (!shape_geometry(V, dt, ncpc, g))
-            return SV_ERR_UNSUPPORTED;
+    Geom best;
+    long long best_score = -1;
+    for (int ncpc : cand) {
+        Geom t;
+        if (!shape_geometry(V, dt, ncpc, &t))
+            continue;
         int cap = 0;
-        const cudaError_t e = dt == SV_DTYPE_BF16 ? capacity_nv<__nv_bfloat16>(*g, dev, &cap)
-                                                  : capacity_nv<float>(*g, dev, &cap);
-        if (e != cudaSuccess)
-            return SV_ERR_CUDA;
-        if (cap > 0) {
-            g->clusters = (int)std::min<long long>(cap, items);
-            return SV_OK;
+        const sv_status st = capacity_of(t, dt, dev, &cap);
+        if (st != SV_OK)
+            return st;
+        if (cap <= 0)
+            continue;
+        // sequences are the units unless there are fewer of them than clusters
+        t.per_row = B < cap ? 1 : 0;
+        const long long units = t.per_row ? rows : (long long)B;
+        const long long want = t.per_row ? units : (units + t.nslot - 1) / t.nslot;
+        t.clusters = (int)std::min<long long>(cap, std::max<long long>(1, want));
+        const long long ctas = (long long)t.clusters * t.C;
+        const long long busy_sms = std::min<long long>(ctas, nsm);
+        const long long score = busy_sms * 16 + t.nslot * 4 + (kMaxCluster - t.C) / 4;
+        if (score > best_score) {
+            best_score = score;
+            best = t;
         }
-        if (override_ncpc > 0 || g->C == 1)
-            return SV_ERR_UNSUPPORTED;
-        ncpc = g->ncpc + 1;   // smaller clusters
     }
+    if (best_score < 0)
+        return SV_ERR_UNSUPPORTED;
+    *g = best;
+    return SV_OK;
 }
 
 template <typename T, int NV>
@@ -270,7 +294,7 @@ static cudaError_t launch_pair(const Args& a, const Geom& g, cudaStream_t st, in
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[1];
     sweep_config(&cfg, attr, g, g.clusters, st);
-    e = cudaLaunchKernelEx(&cfg, sv_sweep_kernel<T, NV>, a, g.stages);
+    e = cudaLaunchKernelEx(&cfg, sv_sweep_kernel<T, NV>, a, g.nslot);
     if (e != cudaSuccess)
         return e;
     cudaLaunchConfig_t fcfg = {};
@@ -295,6 +319,27 @@ static cudaError_t launch_nv(const Args& a, const Geom& g, cudaStream_t st, int 
     case 4: return launch_pair<T, 4>(a, g, st, dev);
     default: return launch_pair<T, 8>(a, g, st, dev);
     }
+}
+
+static sv_status device_sms(int* dev_out, int* nsm_out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return SV_ERR_CUDA;
+    int nsm;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        nsm = g_dev[dev].nsm;
+    }
+    if (nsm == 0) {
+        if (cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return SV_ERR_CUDA;
+        std::lock_guard<std::mutex> lk(g_mu);
+        g_dev[dev].nsm = nsm;
+    }
+    *dev_out = dev;
+    *nsm_out = nsm;
+    return SV_OK;
 }
 
 struct Call {
@@ -349,9 +394,10 @@ static sv_status run(const Call& c, int kmax, const sv_options* opt, void* ws, s
         return SV_ERR_INVALID_ARG;
     if (!ws || ws_bytes < L.total || ((uintptr_t)ws & 255))
         return SV_ERR_NO_MEMORY;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
-        return SV_ERR_CUDA;
+    int dev = 0, nsm = 0;
+    sv_status st = device_sms(&dev, &nsm);
+    if (st != SV_OK)
+        return st;
     cudaPointerAttributes pa;
     if (cudaPointerGetAttributes(&pa, c.tgt) != cudaSuccess)
         return SV_ERR_CUDA;
@@ -359,23 +405,10 @@ static sv_status run(const Call& c, int kmax, const sv_options* opt, void* ws, s
         return SV_ERR_INVALID_ARG;
     if (pa.type == cudaMemoryTypeDevice && pa.device != dev)
         return SV_ERR_INVALID_ARG;
-    int nsm;
-    {
-        std::lock_guard<std::mutex> lk(g_mu);
-        nsm = g_dev[dev].nsm;
-    }
-    if (nsm == 0) {
-        if (cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-            return SV_ERR_CUDA;
-        std::lock_guard<std::mutex> lk(g_mu);
-        g_dev[dev].nsm = nsm;
-    }
-    const long long items = (long long)c.B * (kmax + 1);
     Geom g;
-    const sv_status gs =
-        pick_geometry(c.V, c.dtype, items, nsm, opt ? opt->chunks_per_cta : 0, dev, &g);
-    if (gs != SV_OK)
-        return gs;
+    st = pick_geometry(c.V, c.dtype, c.B, kmax, nsm, opt ? opt->chunks_per_cta : 0, dev, &g);
+    if (st != SV_OK)
+        return st;
     if ((long long)g.clusters * g.C > 0x7fffffffLL)
         return SV_ERR_UNSUPPORTED;
 
@@ -384,10 +417,21 @@ static sv_status run(const Call& c, int kmax, const sv_options* opt, void* ws, s
     if (want_diag && ((dg->p_x == nullptr) != (dg->q_x == nullptr)))
         return SV_ERR_INVALID_ARG;   // p_x and q_x are written together
 
-    // Header: zeroed error word, claim counter, masks and decisions, then K.
+    // Header: zeroed error word, claim counter and decisions; K; the claim
+    // order (sequences by K, longest first, so the tail holds short ones).
     thread_local std::vector<unsigned char> hdr;
     hdr.assign(L.header_end, 0);
     memcpy(hdr.data() + L.K, c.K, (size_t)c.B * 4);
+    {
+        int32_t* ord = reinterpret_cast<int32_t*>(hdr.data() + L.order);
+        int cnt[SV_K_MAX + 2] = {0};
+        for (int b = 0; b < c.B; ++b)
+            ++cnt[SV_K_MAX - c.K[b] + 1];
+        for (int k = 1; k <= SV_K_MAX + 1; ++k)
+            cnt[k] += cnt[k - 1];
+        for (int b = 0; b < c.B; ++b)
+            ord[cnt[SV_K_MAX - c.K[b]]++] = b;
+    }
     unsigned char* base = static_cast<unsigned char*>(ws);
     if (cudaMemcpyAsync(base, hdr.data(), L.header_end, cudaMemcpyHostToDevice, stream) !=
         cudaSuccess)
@@ -404,30 +448,57 @@ static sv_status run(const Call& c, int kmax, const sv_options* opt, void* ws, s
     a.B = c.B;
     a.Kmax = kmax;
     a.V = c.V;
-    a.n_items = (int)items;
+    a.per_row = g.per_row;
+    a.n_units = g.per_row ? c.B * (kmax + 1) : c.B;
     a.nchunks = g.nchunks;
     a.ncpc = g.ncpc;
     a.C = g.C;
     a.early_exit = (want_diag || (opt && opt->verify_all)) ? 0 : 1;
+    a.has_draft = c.drf != nullptr ? 1 : 0;
     const uintptr_t al = (uintptr_t)c.tgt | (c.drf ? (uintptr_t)c.drf : 0);
     a.aligned = ((al & 15) == 0) && (((size_t)c.V * g.s) % 16 == 0);
     a.err = reinterpret_cast<uint32_t*>(base + L.err);
-    a.next_item = reinterpret_cast<int*>(base + L.next_item);
-    a.mask = reinterpret_cast<uint32_t*>(base + L.mask);
+    a.next_unit = reinterpret_cast<int*>(base + L.next_unit);
     a.dec = base + L.dec;
     a.K = reinterpret_cast<const int32_t*>(base + L.K);
+    a.order = reinterpret_cast<const int32_t*>(base + L.order);
     a.argmax = reinterpret_cast<int32_t*>(base + L.argmax);
     a.rowstat = reinterpret_cast<float4*>(base + L.rowstat);
-    a.Pc = reinterpret_cast<double*>(base + L.Pc);
-    a.Rc = reinterpret_cast<double*>(base + L.Rc);
+    a.Pc = reinterpret_cast<float*>(base + L.Pc);
+    a.Rc = reinterpret_cast<float*>(base + L.Rc);
     a.p_x = want_diag ? dg->p_x : nullptr;
     a.q_x = want_diag ? dg->q_x : nullptr;
     a.resid = want_diag ? dg->resid_mass : nullptr;
     a.final_row = want_diag ? dg->final_row : nullptr;
+    a.want_pq = a.p_x != nullptr ? 1 : 0;
+    a.want_resid = a.resid != nullptr ? 1 : 0;
+    a.want_final = a.final_row != nullptr ? 1 : 0;
 
     const cudaError_t e = c.dtype == SV_DTYPE_BF16 ? launch_nv<__nv_bfloat16>(a, g, stream, dev)
                                                    : launch_nv<float>(a, g, stream, dev);
     return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
+// Launch geometry a call would use (for reports and tests).
+static sv_status geometry_of(int B, int Kmax, int V, sv_dtype dt, int ncpc, int32_t* out)
+{
+    int dev = 0, nsm = 0;
+    sv_status st = device_sms(&dev, &nsm);
+    if (st != SV_OK)
+        return st;
+    Geom g;
+    st = pick_geometry(V, dt, B, Kmax, nsm, ncpc, dev, &g);
+    if (st != SV_OK)
+        return st;
+    out[0] = g.C;
+    out[1] = g.ncpc;
+    out[2] = g.nslot;
+    out[3] = g.clusters;
+    out[4] = 32 * g.nwarps;
+    out[5] = (int32_t)g.smem;
+    out[6] = g.per_row;
+    out[7] = g.nchunks;
+    return SV_OK;
 }
 
 }  // namespace sv
@@ -459,6 +530,17 @@ int32_t sv_max_vocab(sv_dtype dtype)
     const int s = sv::elem_size(dtype);
     const int ch = 32 * 8 * (16 / s);   // chunk size at large V
     return sv::kMaxCluster * sv::max_ncpc(ch, s, 1) * ch;
+}
+
+sv_status sv_geometry(int32_t B, int32_t Kmax, int32_t V, sv_dtype dtype, int32_t chunks_per_cta,
+                      int32_t* out8)
+{
+    if (!out8 || B < 1 || Kmax < 0 || Kmax > SV_K_MAX || V < 1 || chunks_per_cta < 0 ||
+        (dtype != SV_DTYPE_F32 && dtype != SV_DTYPE_BF16))
+        return SV_ERR_INVALID_ARG;
+    if (V > sv_max_vocab(dtype))
+        return SV_ERR_UNSUPPORTED;
+    return sv::geometry_of(B, Kmax, V, dtype, chunks_per_cta, out8);
 }
 
 size_t sv_workspace_size(int32_t B, int32_t Kmax, int32_t V, sv_dtype dtype)

@@ -40,19 +40,26 @@ struct Args {
     int32_t* out_tok;
     int32_t* out_n;
     int B, Kmax, V;
-    int n_items;           // B * (Kmax + 1): rows in position-major order
+    int per_row;           // 1: slots claim single rows; 0: slots claim whole sequences
+    int n_units;           // claimable units: B sequences, or B * (Kmax + 1) rows
     int nchunks, ncpc, C;
     int early_exit, aligned;
+    // Which optional buffers were supplied.  Decided on the host: device code
+    // never branches on a pointer's null-ness.
+    int has_draft;         // draft logits
+    int want_pq;           // diagnostics p_x and q_x
+    int want_resid;        // diagnostic resid_mass
+    int want_final;        // diagnostic final_row
     // workspace
     uint32_t* err;
-    int* next_item;        // claim counter of the persistent sweep
-    uint32_t* mask;        // per sequence: bit i set when position i rejected / unusable
+    int* next_unit;        // claim counter of the persistent sweep
     uint8_t* dec;          // per row decision
     const int32_t* K;
+    const int32_t* order;  // sequences in claim order (longest K first)
     int32_t* argmax;       // per row (greedy)
     float4* rowstat;       // per row: m_t, 1/S_t, m_d, 1/S_d
-    double* Pc;            // per (row, chunk): sum of exp2((l - m_t) c)
-    double* Rc;            // per (row, chunk): sum of max(0, p - q)
+    float* Pc;             // per (row, chunk): sum of exp2((l - m_t) c)
+    float* Rc;             // per (row, chunk): sum of max(0, p - q)
     // diagnostics (nullable)
     float* p_x;
     float* q_x;
@@ -102,8 +109,15 @@ template <> struct Elem<__nv_bfloat16> {
     }
 };
 
-// exp2((l - m) * c): the unnormalised softmax weight, c = log2(e)/T, in one
-// fixed rounding sequence shared by the sweep and the finaliser.
+// c = log2(e) / T, the factor that turns (l - m) into an exp2 argument; one
+// correctly rounded fp32 division shared by the sweep and the finaliser.
+__device__ __forceinline__ float log2e_over(float T)
+{
+    return __fdiv_rn(1.44269504088896341f, T);
+}
+
+// exp2((l - m) * c): the unnormalised softmax weight, in one fixed rounding
+// sequence shared by the sweep and the finaliser.
 __device__ __forceinline__ float weight(float l, float m, float c)
 {
     return ex2_approx(__fmul_rn(__fsub_rn(l, m), c));
@@ -124,13 +138,50 @@ __device__ __forceinline__ float warp_max_nan(float v)
 }
 
 // Butterfly sum: every lane ends with the same value (IEEE addition commutes).
-__device__ __forceinline__ double warp_sum(double v)
+__device__ __forceinline__ float warp_sum(float v)
 {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1)
         v += __shfl_xor_sync(kFull, v, o);
     return v;
 }
+
+// Error-free sum: s = fl(a + b) and a + b = s + e exactly (Knuth's TwoSum).
+// Symmetric in (a, b), so butterfly partners compute identical pairs.
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e)
+{
+    s = a + b;
+    const float bb = s - a;
+    e = (a - (s - bb)) + (b - bb);
+}
+
+// Compensated butterfly sum over the warp; every lane ends with the same value.
+__device__ __forceinline__ float warp_sum_comp(float v)
+{
+    float s = v, c = 0.0f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float so = __shfl_xor_sync(kFull, s, o);
+        const float co = __shfl_xor_sync(kFull, c, o);
+        float t, e;
+        two_sum(s, so, t, e);
+        s = t;
+        c = (c + co) + e;
+    }
+    return s + c;
+}
+
+// Compensated (Neumaier) fp32 running sum.
+struct CompSum {
+    float s = 0.0f, c = 0.0f;
+    __device__ __forceinline__ void add(float v)
+    {
+        const float t = s + v;
+        c += fabsf(s) >= fabsf(v) ? (s - t) + v : (v - t) + s;
+        s = t;
+    }
+    __device__ __forceinline__ float value() const { return s + c; }
+};
 
 __device__ __forceinline__ double warp_incl_scan(double v, int lane)
 {
@@ -148,9 +199,5 @@ __device__ __forceinline__ bool temperature_usable(float T)
     return T == 0.0f || (isfinite(T) && T >= FLT_MIN);
 }
 
-__device__ __forceinline__ uint32_t positions_below(int i)
-{
-    return i >= 32 ? 0xffffffffu : ((1u << i) - 1u);
-}
 
 }  // namespace sv

@@ -28,16 +28,16 @@ __device__ int draw_token(const Args& a, int b, int Kb, float Tb, int n, float u
     constexpr int L = CH / 32;   // contiguous elements per lane in the chunk scan
     const int nchunks = a.nchunks;
     const size_t r = (size_t)b * (a.Kmax + 1) + n;
-    bool resid = n < Kb;
+    bool resid = n < Kb && a.has_draft != 0;
     const int per = (nchunks + 31) / 32;
     const int lo = min(nchunks, lane * per), hi = min(nchunks, lo + per);
     int chunk = -1;
     double tloc = 0.0;
     for (int attempt = 0; attempt < 2 && chunk < 0; ++attempt) {
-        const double* sums = (resid ? a.Rc : a.Pc) + r * nchunks;
+        const float* sums = (resid ? a.Rc : a.Pc) + r * nchunks;
         double ls = 0.0;
         for (int c = lo; c < hi; ++c)
-            ls += __ldcg(sums + c);
+            ls += (double)__ldcg(sums + c);
         const double inc = warp_incl_scan(ls, lane);
         const double S = __shfl_sync(kFull, inc, 31);
         const double up = __shfl_up_sync(kFull, inc, 1);
@@ -53,7 +53,7 @@ __device__ int draw_token(const Args& a, int b, int Kb, float Tb, int n, float u
         int cand = -1, lastpos = -1;
         double cum = excl, bcand = 0.0, blast = 0.0;
         for (int c = lo; c < hi; ++c) {
-            const double s = __ldcg(sums + c);
+            const double s = (double)__ldcg(sums + c);
             const double before = cum;
             cum += s;
             if (s > 0.0) {
@@ -85,7 +85,7 @@ __device__ int draw_token(const Args& a, int b, int Kb, float Tb, int n, float u
         return -1;
 
     const float4 st = __ldcg(a.rowstat + r);   // m_t, 1/S_t, m_d, 1/S_d
-    const float c = (float)(kLog2e / (double)Tb);
+    const float c = log2e_over(Tb);
     const T* tg = static_cast<const T*>(a.tgt) + r * (size_t)a.V;
     const T* dg = resid ? static_cast<const T*>(a.drf) + ((size_t)b * a.Kmax + n) * (size_t)a.V
                         : nullptr;
@@ -98,23 +98,30 @@ __device__ int draw_token(const Args& a, int b, int Kb, float Tb, int n, float u
             return et;
         return resid_term(et, st.y, weight(EL::load(dg + e0 + j), st.z, c), st.w);
     };
-    double ls = 0.0;
+    // lane-contiguous spans: compensated fp32 sums, fp64 scan across lanes
+    CompSum span;
     int lastpos = -1;
     for (int j = j0; j < j1; ++j) {
         const float v = value(j);
-        ls += (double)v;
+        span.add(v);
         if (v > 0.0f)
             lastpos = j;
     }
+    const double ls = (double)span.s + (double)span.c;
     const double inc = warp_incl_scan(ls, lane);
     const double up = __shfl_up_sync(kFull, inc, 1);
-    double cum = lane == 0 ? 0.0 : up;
+    const double excl = lane == 0 ? 0.0 : up;
+    // the mass this lane's span must still cover, small enough for fp32
+    const float t_lane = (float)(tloc - excl);
     int cand = INT_MAX;
-    for (int j = j0; j < j1; ++j) {
-        cum += (double)value(j);
-        if (tloc < cum) {
-            cand = j;
-            break;
+    if (t_lane < (float)ls) {   // spans before the target lane cannot hold it
+        CompSum cum;
+        for (int j = j0; j < j1; ++j) {
+            cum.add(value(j));
+            if (t_lane < cum.value()) {
+                cand = j;
+                break;
+            }
         }
     }
     const int best = __reduce_min_sync(kFull, cand);
@@ -159,19 +166,19 @@ __global__ void __launch_bounds__(kFinalizeWarps * 32) sv_finalize_kernel(const 
         orow[j] = bad ? -1 : (j < n ? __ldg(a.tok + (size_t)b * a.Kmax + j) : (j == n ? token : -1));
     if (lane == 0) {
         a.out_n[b] = bad ? -1 : n;
-        if (a.final_row)
+        if (a.want_final)
             a.final_row[b] = bad ? -1 : n;
     }
-    if (a.resid) {
+    if (a.want_resid) {
         for (int i = lane; i < a.Kmax; i += 32) {
             float v = NAN;
             if (!greedy && i < Kb) {
                 const uint8_t di = ld_cg_u8(a.dec + rb + i);
                 if (di == kDecAccept || di == kDecReject) {
-                    const double* rc = a.Rc + (rb + i) * a.nchunks;
+                    const float* rc = a.Rc + (rb + i) * a.nchunks;
                     double s = 0.0;
                     for (int c = 0; c < a.nchunks; ++c)
-                        s += __ldcg(rc + c);
+                        s += (double)__ldcg(rc + c);
                     v = (float)s;
                 }
             }
