@@ -99,11 +99,19 @@ typedef struct {
  *   chunks_per_cta  0: automatic.  Otherwise the number of vocabulary chunks
  *                   each CTA of a row's cluster holds in shared memory
  *                   (tuning; SV_ERR_UNSUPPORTED if the result does not fit).
+ *   slots           0: automatic.  Otherwise how many rows (1..3) each CTA
+ *                   keeps staged in shared memory at once (tuning; capped
+ *                   by what fits).
+ *   chunks_per_warp 0: automatic.  Otherwise how many of the CTA's chunks
+ *                   each compute warp reduces (tuning: fewer warps per CTA
+ *                   let more CTAs share an SM).
  */
 typedef struct {
     sv_diag diag;
     int32_t verify_all;
     int32_t chunks_per_cta;
+    int32_t slots;
+    int32_t chunks_per_warp;
 } sv_options;
 
 /* Human-readable name of a status code (static storage). */
@@ -123,10 +131,10 @@ int32_t sv_max_vocab(sv_dtype dtype);
  *   [4] threads per CTA, [5] dynamic shared memory per CTA (bytes),
  *   [6] 1 if work is claimed per row (small batches), 0 per sequence,
  *   [7] vocabulary chunks per row.
- * chunks_per_cta = 0 selects the automatic choice (as sv_options does).
+ * Zero tuning arguments select the automatic choice (as in sv_options).
  */
 sv_status sv_geometry(int32_t B, int32_t Kmax, int32_t V, sv_dtype dtype, int32_t chunks_per_cta,
-                      int32_t* out8);
+                      int32_t slots, int32_t chunks_per_warp, int32_t* out8);
 
 /*
  * Bytes of device workspace spec_verify_ws / spec_verify_ex need for this

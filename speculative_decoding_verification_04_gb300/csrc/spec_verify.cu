@@ -37,7 +37,7 @@ namespace sv {
 // ---------------------------------------------------------------------------
 constexpr int kSmemPerCtaMax = 227 * 1024;   // opt-in dynamic shared memory limit
 constexpr int kStaticSmemReserve = 2048;     // static __shared__ of the sweep, rounded up
-constexpr int kChunksPerCta = 8;             // default slice: 8 chunk pairs = 64 KB per stage
+constexpr int kMaxChunksPerWarp = 4;         // automatic choice searches 1..4 chunks per warp
 
 struct Geom {
     int s = 0, nv = 0, ch = 0, nchunks = 0, ncpc = 0, C = 0, nwarps = 0, nslot = 0;
@@ -117,6 +117,8 @@ static std::mutex g_mu;
 static DeviceInfo g_dev[64];
 // cudaOccupancyMaxActiveClusters per (device, kernel, cluster size, warps, smem)
 static std::map<std::tuple<int, int, int, int, size_t>, int> g_fit;
+// chosen geometry per (device, V, dtype, B, Kmax, tuning overrides)
+static std::map<std::tuple<int, int, int, int, int, int, int>, Geom> g_pick;
 
 template <typename T, int NV>
 static cudaError_t prepare_kernels(int dev)
@@ -197,7 +199,7 @@ static cudaError_t capacity_nv(const Geom& g, int dev, int* n)
 }
 
 // Chunks per CTA, cluster size and slot count for a given ncpc request.
-static bool shape_geometry(int V, sv_dtype dt, int ncpc, Geom* g)
+static bool shape_geometry(int V, sv_dtype dt, int ncpc, int want_slots, int cpw, Geom* g)
 {
     const int s = elem_size(dt);
     g->s = s;
@@ -209,7 +211,10 @@ static bool shape_geometry(int V, sv_dtype dt, int ncpc, Geom* g)
     if (C > kMaxCluster)
         return false;
     ncpc = (g->nchunks + C - 1) / C;   // balance the chunks over the cluster
-    int nslot = 3;
+    // One slot unless asked: a row in flight costs its whole slice of shared
+    // memory, and independent CTAs overlap their rows' dependent chains
+    // better than extra slots of one CTA do.
+    int nslot = want_slots > 0 ? std::min(want_slots, kMaxSlots) : 1;
     while (nslot > 1 && ncpc > max_ncpc(g->ch, s, nslot))
         --nslot;
     if (ncpc > max_ncpc(g->ch, s, nslot))
@@ -217,7 +222,9 @@ static bool shape_geometry(int V, sv_dtype dt, int ncpc, Geom* g)
     g->ncpc = ncpc;
     g->C = C;
     g->nslot = nslot;
-    g->nwarps = std::min(ncpc, kMaxWarps - 1) + 1;   // compute warps + the scheduler warp
+    cpw = std::max(1, cpw);
+    // compute warps (each reduces up to cpw of the CTA's chunks) + the scheduler warp
+    g->nwarps = std::min((ncpc + cpw - 1) / cpw, kMaxWarps - 1) + 1;
     g->smem = smem_for(ncpc, g->ch, s, nslot);
     return true;
 }
@@ -229,13 +236,26 @@ static sv_status capacity_of(const Geom& g, sv_dtype dt, int dev, int* cap)
     return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
-// Pick the geometry of one launch.  Candidates: every cluster size from the
-// smallest whose slice fits shared memory up to 16 (one slice of at most
-// kChunksPerCta chunk pairs per CTA by default); keep the one that keeps the
-// most SMs busy, preferring more slots, then smaller clusters.
+// Pick the geometry of one launch.  Candidates: every cluster size 1..16
+// whose slice fits shared memory, with 1..kMaxChunksPerWarp chunks per compute
+// warp.  A row occupies its cluster's shared memory from the moment its copy
+// is issued until its decision (and residual pass) are done, so throughput
+// follows the bytes of logits the device keeps resident at once: the score is
+// resident clusters x CTAs x chunks, then more compute warps, then larger
+// clusters (shorter rows).  The choice is cached per shape.
 static sv_status pick_geometry(int V, sv_dtype dt, int B, int Kmax, int nsm, int override_ncpc,
-                               int dev, Geom* g)
+                               int want_slots, int want_cpw, int dev, Geom* g)
 {
+    const auto key = std::make_tuple(dev, V, (int)dt, B, Kmax, override_ncpc * 64 + want_slots * 8,
+                                     want_cpw);
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        auto it = g_pick.find(key);
+        if (it != g_pick.end()) {
+            *g = it->second;
+            return SV_OK;
+        }
+    }
     const int s = elem_size(dt);
     const int nch = n_chunks(V, s);
     const long long rows = (long long)B * (Kmax + 1);
@@ -243,44 +263,49 @@ static sv_status pick_geometry(int V, sv_dtype dt, int B, int Kmax, int nsm, int
     if (override_ncpc > 0) {
         cand.push_back(override_ncpc);
     } else {
-        const int base = std::min(kChunksPerCta, nch);
-        for (int C = (nch + base - 1) / base; C <= kMaxCluster; ++C) {
+        for (int C = 1; C <= kMaxCluster; ++C) {
             const int ncpc = (nch + C - 1) / C;
             if (cand.empty() || cand.back() != ncpc)
                 cand.push_back(ncpc);
             if (ncpc == 1)
                 break;
         }
-        if (cand.empty())   // V needs more than kChunksPerCta chunks per CTA even at C = 16
-            cand.push_back((nch + kMaxCluster - 1) / kMaxCluster);
     }
     Geom best;
     long long best_score = -1;
     for (int ncpc : cand) {
-        Geom t;
-        if (!shape_geometry(V, dt, ncpc, &t))
-            continue;
-        int cap = 0;
-        const sv_status st = capacity_of(t, dt, dev, &cap);
-        if (st != SV_OK)
-            return st;
-        if (cap <= 0)
-            continue;
-        // sequences are the units unless there are fewer of them than clusters
-        t.per_row = B < cap ? 1 : 0;
-        const long long units = t.per_row ? rows : (long long)B;
-        const long long want = t.per_row ? units : (units + t.nslot - 1) / t.nslot;
-        t.clusters = (int)std::min<long long>(cap, std::max<long long>(1, want));
-        const long long ctas = (long long)t.clusters * t.C;
-        const long long busy_sms = std::min<long long>(ctas, nsm);
-        const long long score = busy_sms * 16 + t.nslot * 4 + (kMaxCluster - t.C) / 4;
-        if (score > best_score) {
-            best_score = score;
-            best = t;
+        const int cpw_lo = want_cpw > 0 ? want_cpw : 1;
+        const int cpw_hi = want_cpw > 0 ? want_cpw : kMaxChunksPerWarp;
+        for (int cpw = cpw_lo; cpw <= cpw_hi; ++cpw) {
+            Geom t;
+            if (!shape_geometry(V, dt, ncpc, want_slots, cpw, &t))
+                continue;
+            if (want_cpw <= 0 && cpw > 1 && (t.ncpc + cpw - 2) / (cpw - 1) == (t.ncpc + cpw - 1) / cpw)
+                continue;   // same warp count as cpw - 1
+            int cap = 0;
+            const sv_status st = capacity_of(t, dt, dev, &cap);
+            if (st != SV_OK)
+                return st;
+            if (cap <= 0)
+                continue;
+            // sequences are the units unless there are fewer of them than clusters
+            t.per_row = B < cap ? 1 : 0;
+            const long long units = t.per_row ? rows : (long long)B;
+            const long long want = t.per_row ? units : (units + t.nslot - 1) / t.nslot;
+            t.clusters = (int)std::min<long long>(cap, std::max<long long>(1, want));
+            const long long resident = (long long)t.clusters * t.C * t.ncpc * t.nslot;
+            const long long score = (resident * 32 + (t.nwarps - 1)) * 32 + t.C;
+            if (score > best_score) {
+                best_score = score;
+                best = t;
+            }
         }
     }
     if (best_score < 0)
         return SV_ERR_UNSUPPORTED;
+    (void)nsm;
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_pick[key] = best;
     *g = best;
     return SV_OK;
 }
@@ -406,7 +431,8 @@ static sv_status run(const Call& c, int kmax, const sv_options* opt, void* ws, s
     if (pa.type == cudaMemoryTypeDevice && pa.device != dev)
         return SV_ERR_INVALID_ARG;
     Geom g;
-    st = pick_geometry(c.V, c.dtype, c.B, kmax, nsm, opt ? opt->chunks_per_cta : 0, dev, &g);
+    st = pick_geometry(c.V, c.dtype, c.B, kmax, nsm, opt ? opt->chunks_per_cta : 0,
+                       opt ? opt->slots : 0, opt ? opt->chunks_per_warp : 0, dev, &g);
     if (st != SV_OK)
         return st;
     if ((long long)g.clusters * g.C > 0x7fffffffLL)
@@ -480,14 +506,15 @@ static sv_status run(const Call& c, int kmax, const sv_options* opt, void* ws, s
 }
 
 // Launch geometry a call would use (for reports and tests).
-static sv_status geometry_of(int B, int Kmax, int V, sv_dtype dt, int ncpc, int32_t* out)
+static sv_status geometry_of(int B, int Kmax, int V, sv_dtype dt, int ncpc, int slots, int cpw,
+                             int32_t* out)
 {
     int dev = 0, nsm = 0;
     sv_status st = device_sms(&dev, &nsm);
     if (st != SV_OK)
         return st;
     Geom g;
-    st = pick_geometry(V, dt, B, Kmax, nsm, ncpc, dev, &g);
+    st = pick_geometry(V, dt, B, Kmax, nsm, ncpc, slots, cpw, dev, &g);
     if (st != SV_OK)
         return st;
     out[0] = g.C;
@@ -533,14 +560,15 @@ int32_t sv_max_vocab(sv_dtype dtype)
 }
 
 sv_status sv_geometry(int32_t B, int32_t Kmax, int32_t V, sv_dtype dtype, int32_t chunks_per_cta,
-                      int32_t* out8)
+                      int32_t slots, int32_t chunks_per_warp, int32_t* out8)
 {
-    if (!out8 || B < 1 || Kmax < 0 || Kmax > SV_K_MAX || V < 1 || chunks_per_cta < 0 ||
+    if (!out8 || B < 1 || Kmax < 0 || Kmax > SV_K_MAX || V < 1 || chunks_per_cta < 0 || slots < 0 ||
+        chunks_per_warp < 0 ||
         (dtype != SV_DTYPE_F32 && dtype != SV_DTYPE_BF16))
         return SV_ERR_INVALID_ARG;
     if (V > sv_max_vocab(dtype))
         return SV_ERR_UNSUPPORTED;
-    return sv::geometry_of(B, Kmax, V, dtype, chunks_per_cta, out8);
+    return sv::geometry_of(B, Kmax, V, dtype, chunks_per_cta, slots, chunks_per_warp, out8);
 }
 
 size_t sv_workspace_size(int32_t B, int32_t Kmax, int32_t V, sv_dtype dtype)
@@ -566,7 +594,8 @@ sv_status spec_verify_ex(const void* target_logits, const void* draft_logits, sv
     const sv_status st = sv::check_args(c, &kmax);
     if (st != SV_OK)
         return st;
-    if (options && options->chunks_per_cta < 0)
+    if (options && (options->chunks_per_cta < 0 || options->slots < 0 ||
+                    options->chunks_per_warp < 0))
         return SV_ERR_INVALID_ARG;
     return sv::run(c, kmax, options, workspace, workspace_bytes, stream);
 }

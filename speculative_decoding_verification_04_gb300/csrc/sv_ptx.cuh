@@ -31,6 +31,19 @@ __device__ __forceinline__ void cluster_arrive()
     asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 }
 
+// Arrive without release semantics (threads that publish nothing to peers).
+__device__ __forceinline__ void cluster_arrive_relaxed()
+{
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+
+// Release this thread's earlier writes (distributed shared memory stores) at
+// cluster scope; used before a relaxed arrive by the threads that publish.
+__device__ __forceinline__ void fence_cluster()
+{
+    asm volatile("fence.acq_rel.cluster;" ::: "memory");
+}
+
 __device__ __forceinline__ void cluster_wait()
 {
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");

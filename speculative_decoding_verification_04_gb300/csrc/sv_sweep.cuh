@@ -513,10 +513,11 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) sv_sweep_kernel(const Args 
                     const int cl = s_claim[xp];
                     st_cluster_s32(map_to_rank(smem_addr(&s_claim[xp]), (uint32_t)lane), cl);
                 }
+                fence_cluster();   // the pushes above are released to the peers
             }
         }
-        cluster_arrive();
-        cluster_wait();   // the one cluster exchange of this row
+        cluster_arrive_relaxed();
+        cluster_wait();   // the one cluster exchange of this row (acquire)
 
         // ---- warp 0: cluster combine (lane r = rank r) and the decision ----
         if (warp == 0) {
@@ -624,25 +625,32 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) sv_sweep_kernel(const Args 
                 }
             }
         }
-        if (s_bad && !poisoned_before && tid == 0)
-            atomicOr(a.err, kErrWaitTimeout);
-        __syncthreads();   // stage s consumed; s_pc, s_w*, s_res free for the next row
         if (tid == 0) {
+            if (s_bad && !poisoned_before)
+                atomicOr(a.err, kErrWaitTimeout);
+            // nobody reads slot s's shared state again before the barrier below
             s_uses[s] += 1;
             s_active[s] = next_active ? 1 : 0;
             if (next_active)
                 s_desc[s] = schedule(a, np.i, np.b, np.Kb, np.T);
         }
-        __syncthreads();
+        __syncthreads();   // stage s consumed; s_pc, s_w*, s_res free; slot s rescheduled
         if (next_active) {
             if (cw >= 0)
                 issue_row<T, NV>(a, sm, s_desc[s], s, c0, nck, cw, nwc, lane, s_bad != 0);
             if (cw == 0 && lane == 0)
                 describe<T>(a, s_desc[s]);
         }
-        // the next row processed may be this slot's (one slot, or the others
-        // idle): its descriptor must be complete before anyone copies it
-        __syncthreads();
+        // If the next row processed is this slot's again (one slot, or the
+        // other slots idle), its descriptor must be complete before it is read.
+        bool same_next = true;
+        for (int t = 1; t < nslot; ++t)
+            if (s_active[(s + t) % nslot]) {
+                same_next = false;
+                break;
+            }
+        if (same_next)
+            __syncthreads();
     }
 }
 
