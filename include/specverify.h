@@ -167,6 +167,42 @@ sv_status spec_verify(const void* target_logits, const void* draft_logits, sv_dt
                       const float* temperature, int32_t B, const int32_t* K, int32_t V,
                       int32_t* out_tokens, int32_t* out_num_accepted, cudaStream_t stream);
 
+/* Size of the fixed scratch array spec_verify_noalloc works in (16 MiB). */
+#define SV_STATIC_SCRATCH_BYTES (16u << 20)
+
+/*
+ * spec_verify_noalloc -- as spec_verify, for callers that cannot allocate
+ * device memory at call time: a serving loop that has handed all free device
+ * memory to its KV-cache pool (a cudaMalloc would fail there), or a caller
+ * with no allocator of its own (plain C, no PyTorch) that must not pay an
+ * allocation on every verification step.  The pages define no counterpart of
+ * this entry point; it is the same verification as spec_verify_ws.
+ *
+ * Scratch: a fixed array of SV_STATIC_SCRATCH_BYTES in this library's own
+ * device module (one per device), instead of a workspace argument.  Shapes
+ * whose sv_workspace_size(B, Kmax, V, dtype) exceeds SV_STATIC_SCRATCH_BYTES
+ * return SV_ERR_NO_MEMORY before any work is queued.  Nothing in the array
+ * needs to start at zero: each call uploads the header it uses (error word,
+ * claim counter, per-row decisions, K and the claim order) before its kernels
+ * run.  The per-call header is assembled in a static host array.
+ *
+ * Set-up: the first call on a device resolves the array's address on that
+ * device (cudaGetSymbolAddress, with the device current) and sets kernel
+ * attributes; make that first call before any stream capture.  The first call
+ * with a new shape also records its launch geometry in a small host cache.
+ * No call allocates device memory (no cudaMalloc, cudaMallocAsync or
+ * cudaFree).
+ *
+ * Calls share the one array per device and the one host header array:
+ * overlapping calls (other streams, other host threads) race and give
+ * undefined results.  Order them on one stream, from one host thread.
+ * sv_workspace_errors does not apply (there is no workspace handle).
+ */
+sv_status spec_verify_noalloc(const void* target_logits, const void* draft_logits, sv_dtype dtype,
+                              const int32_t* draft_tokens, const float* uniforms,
+                              const float* temperature, int32_t B, const int32_t* K, int32_t V,
+                              int32_t* out_tokens, int32_t* out_num_accepted, cudaStream_t stream);
+
 /*
  * spec_verify_ws -- as spec_verify, with a caller-provided device workspace of
  * at least sv_workspace_size(B, Kmax, V, dtype) bytes, 256-byte aligned.

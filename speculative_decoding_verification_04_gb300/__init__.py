@@ -64,6 +64,8 @@ def _load():
     P, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
     common = [P, P, ctypes.c_int, P, P, P, i32, P, i32, P, P]
     lib.spec_verify.argtypes = common + [P]
+    lib.spec_verify_noalloc.argtypes = common + [P]
+    lib.spec_verify_noalloc.restype = ctypes.c_int
     lib.spec_verify_ws.argtypes = common + [P, sz, P]
     lib.spec_verify_ex.argtypes = common + [ctypes.POINTER(SVOptions), P, sz, P]
     lib.spec_verify_host.argtypes = common + [P, sz, P]
@@ -220,6 +222,36 @@ def spec_verify(target, draft, draft_tokens, uniforms, temperature, K, out_token
                              _dptr(out_num_accepted), sp)
     _check(st, "spec_verify")
     return out_tokens, out_num_accepted
+
+
+def spec_verify_noalloc(target, draft, draft_tokens, uniforms, temperature, K, out_tokens,
+                        out_num_accepted, stream=None):
+    """spec_verify for callers that cannot allocate device memory per call.
+
+    Works in the library's fixed device scratch array (SV_STATIC_SCRATCH_BYTES,
+    16 MiB per device) instead of a workspace, so nothing is allocated: not by
+    the library and not here (the outputs are the caller's).  Overlapping calls
+    share that array and race; order them on one stream from one thread.  The
+    first call on a device resolves the array's address and should come before
+    any stream capture.  Shapes needing more scratch raise SpecVerifyError
+    with SV_ERR_NO_MEMORY."""
+    import torch
+    if out_tokens is None or out_num_accepted is None:
+        raise ValueError("spec_verify_noalloc writes into caller-provided outputs")
+    k, kp, B, Kmax, V = _common(target, draft, draft_tokens, uniforms, temperature, K)
+    _require(out_tokens, "out_tokens", torch.int32)
+    _require(out_num_accepted, "out_num_accepted", torch.int32)
+    if tuple(out_tokens.shape) != (B, Kmax + 1) or tuple(out_num_accepted.shape) != (B,):
+        raise ValueError("out_tokens must be [B, Kmax+1] and out_num_accepted [B]")
+    sp, _ = _stream(stream)
+    st = _load().spec_verify_noalloc(_dptr(target), _dptr(draft), _dtype_code(target),
+                                     _dptr(draft_tokens), _dptr(uniforms), _dptr(temperature), B,
+                                     kp, V, _dptr(out_tokens), _dptr(out_num_accepted), sp)
+    _check(st, "spec_verify_noalloc")
+    return out_tokens, out_num_accepted
+
+
+SV_STATIC_SCRATCH_BYTES = 16 << 20
 
 
 def spec_verify_ws(target, draft, draft_tokens, uniforms, temperature, K, workspace: Workspace,

@@ -111,7 +111,15 @@ static bool ws_layout(int B, int Kmax, int V, sv_dtype dt, WsLayout* L)
 struct DeviceInfo {
     int nsm = 0;
     bool attrs_set[2][4] = {};
+    void* static_scratch = nullptr;   // device address of g_static_scratch on this device
 };
+
+// Scratch of spec_verify_noalloc: a fixed device array in the library's own
+// module (one copy per device, resolved once per device with
+// cudaGetSymbolAddress), and the host array its per-call header is staged in.
+// Neither needs initial contents: every call rewrites the header it uses.
+static __device__ __align__(256) unsigned char g_static_scratch[SV_STATIC_SCRATCH_BYTES];
+static unsigned char g_static_header[SV_STATIC_SCRATCH_BYTES];
 
 static std::mutex g_mu;
 static DeviceInfo g_dev[64];
@@ -367,6 +375,26 @@ static sv_status device_sms(int* dev_out, int* nsm_out)
     return SV_OK;
 }
 
+// Device address of the static scratch on the current device (resolved on
+// the first call per device).
+static sv_status static_scratch(void** out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return SV_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_dev[dev].static_scratch) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) {
+            (void)cudaGetLastError();
+            return SV_ERR_CUDA;
+        }
+        g_dev[dev].static_scratch = p;
+    }
+    *out = g_dev[dev].static_scratch;
+    return SV_OK;
+}
+
 struct Call {
     const void* tgt;
     const void* drf;
@@ -409,8 +437,10 @@ static sv_status check_args(const Call& c, int* kmax_out)
     return SV_OK;
 }
 
+// host_header: where the per-call header is assembled before its upload
+// (nullptr: a per-thread buffer of this library).
 static sv_status run(const Call& c, int kmax, const sv_options* opt, void* ws, size_t ws_bytes,
-                     cudaStream_t stream)
+                     cudaStream_t stream, unsigned char* host_header = nullptr)
 {
     if (c.B == 0)
         return SV_OK;
@@ -445,11 +475,17 @@ static sv_status run(const Call& c, int kmax, const sv_options* opt, void* ws, s
 
     // Header: zeroed error word, claim counter and decisions; K; the claim
     // order (sequences by K, longest first, so the tail holds short ones).
-    thread_local std::vector<unsigned char> hdr;
-    hdr.assign(L.header_end, 0);
-    memcpy(hdr.data() + L.K, c.K, (size_t)c.B * 4);
+    thread_local std::vector<unsigned char> hdr_tls;
+    unsigned char* hdr = host_header;
+    if (!hdr) {
+        hdr_tls.assign(L.header_end, 0);
+        hdr = hdr_tls.data();
+    } else {
+        memset(hdr, 0, L.header_end);
+    }
+    memcpy(hdr + L.K, c.K, (size_t)c.B * 4);
     {
-        int32_t* ord = reinterpret_cast<int32_t*>(hdr.data() + L.order);
+        int32_t* ord = reinterpret_cast<int32_t*>(hdr + L.order);
         int cnt[SV_K_MAX + 2] = {0};
         for (int b = 0; b < c.B; ++b)
             ++cnt[SV_K_MAX - c.K[b] + 1];
@@ -459,7 +495,7 @@ static sv_status run(const Call& c, int kmax, const sv_options* opt, void* ws, s
             ord[cnt[SV_K_MAX - c.K[b]]++] = b;
     }
     unsigned char* base = static_cast<unsigned char*>(ws);
-    if (cudaMemcpyAsync(base, hdr.data(), L.header_end, cudaMemcpyHostToDevice, stream) !=
+    if (cudaMemcpyAsync(base, hdr, L.header_end, cudaMemcpyHostToDevice, stream) !=
         cudaSuccess)
         return SV_ERR_CUDA;
 
@@ -632,6 +668,29 @@ sv_status spec_verify(const void* target_logits, const void* draft_logits, sv_dt
     if (cudaFreeAsync(ws, stream) != cudaSuccess && st == SV_OK)
         st = SV_ERR_CUDA;
     return st;
+}
+
+sv_status spec_verify_noalloc(const void* target_logits, const void* draft_logits, sv_dtype dtype,
+                              const int32_t* draft_tokens, const float* uniforms,
+                              const float* temperature, int32_t B, const int32_t* K, int32_t V,
+                              int32_t* out_tokens, int32_t* out_num_accepted, cudaStream_t stream)
+{
+    const sv::Call c{target_logits, draft_logits, dtype, draft_tokens, uniforms, temperature,
+                     B, K, V, out_tokens, out_num_accepted};
+    int kmax = 0;
+    sv_status st = sv::check_args(c, &kmax);
+    if (st != SV_OK || B == 0)
+        return st;
+    const size_t bytes = sv_workspace_size(B, kmax, V, dtype);
+    if (bytes == 0)
+        return SV_ERR_INVALID_ARG;
+    if (bytes > SV_STATIC_SCRATCH_BYTES)
+        return SV_ERR_NO_MEMORY;   // this shape needs more scratch than the static array holds
+    void* ws = nullptr;
+    st = sv::static_scratch(&ws);
+    if (st != SV_OK)
+        return st;
+    return sv::run(c, kmax, nullptr, ws, SV_STATIC_SCRATCH_BYTES, stream, sv::g_static_header);
 }
 
 sv_status sv_workspace_errors(void* workspace, uint32_t* flags, cudaStream_t stream)
