@@ -49,8 +49,8 @@ class SVDiag(ctypes.Structure):
 
 class SVOptions(ctypes.Structure):
     _fields_ = [("diag", SVDiag), ("verify_all", ctypes.c_int32),
-                ("chunks_per_cta", ctypes.c_int32), ("slots", ctypes.c_int32),
-                ("chunks_per_warp", ctypes.c_int32)]
+                ("chunks_per_cta", ctypes.c_int32), ("chunks_per_warp", ctypes.c_int32),
+                ("ring_stages", ctypes.c_int32)]
 
 
 def _load():
@@ -105,16 +105,16 @@ def sv_max_vocab(dtype: int) -> int:
     return int(_load().sv_max_vocab(int(dtype)))
 
 
-GEOMETRY_FIELDS = ("cluster_ctas", "chunks_per_cta", "slots", "clusters", "threads",
+GEOMETRY_FIELDS = ("cluster_ctas", "chunks_per_cta", "ring_stages", "clusters", "threads",
                    "smem_bytes", "per_row", "chunks")
 
 
 def sv_geometry(B: int, Kmax: int, V: int, dtype: int, chunks_per_cta: int = 0,
-                slots: int = 0, chunks_per_warp: int = 0) -> dict:
+                chunks_per_warp: int = 0, ring_stages: int = 0) -> dict:
     """Launch geometry a call of this shape would use on the current device."""
     out = (ctypes.c_int32 * 8)()
     st = _load().sv_geometry(int(B), int(Kmax), int(V), int(dtype), int(chunks_per_cta),
-                             int(slots), int(chunks_per_warp), out)
+                             int(chunks_per_warp), int(ring_stages), out)
     _check(st, "sv_geometry")
     return dict(zip(GEOMETRY_FIELDS, [int(v) for v in out]))
 
@@ -270,7 +270,7 @@ def spec_verify_ws(target, draft, draft_tokens, uniforms, temperature, K, worksp
 
 def spec_verify_ex(target, draft, draft_tokens, uniforms, temperature, K, workspace: Workspace,
                    diag: dict | None = None, verify_all: bool = False, chunks_per_cta: int = 0,
-                   slots: int = 0, chunks_per_warp: int = 0, out_tokens=None,
+                   chunks_per_warp: int = 0, ring_stages: int = 0, out_tokens=None,
                    out_num_accepted=None, stream=None):
     """spec_verify_ex; ``diag`` maps p_x / q_x / resid_mass / final_row to tensors."""
     k, kp, B, Kmax, V = _common(target, draft, draft_tokens, uniforms, temperature, K)
@@ -284,8 +284,8 @@ def spec_verify_ex(target, draft, draft_tokens, uniforms, temperature, K, worksp
                 setattr(opt.diag, name, t.data_ptr())
     opt.verify_all = 1 if verify_all else 0
     opt.chunks_per_cta = int(chunks_per_cta)
-    opt.slots = int(slots)
     opt.chunks_per_warp = int(chunks_per_warp)
+    opt.ring_stages = int(ring_stages)
     sp, _ = _stream(stream)
     st = _load().spec_verify_ex(_dptr(target), _dptr(draft), _dtype_code(target),
                                 _dptr(draft_tokens), _dptr(uniforms), _dptr(temperature), B, kp, V,

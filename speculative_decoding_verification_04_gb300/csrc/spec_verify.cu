@@ -36,23 +36,31 @@ namespace sv {
 // host side
 // ---------------------------------------------------------------------------
 constexpr int kSmemPerCtaMax = 227 * 1024;   // opt-in dynamic shared memory limit
-constexpr int kStaticSmemReserve = 2048;     // static __shared__ of the sweep, rounded up
-constexpr int kMaxChunksPerWarp = 4;         // automatic choice searches 1..4 chunks per warp
+constexpr int kMaxVocab = 1 << 22;           // vocabulary limit of the ABI (int32 indices stay small)
+constexpr int kAutoRing = 4;                 // default stages per warp
+constexpr int kAutoWarps = 4;                // default warps per CTA
+constexpr int kAutoCluster = 8;              // default CTAs per row
 
 struct Geom {
-    int s = 0, nv = 0, ch = 0, nchunks = 0, ncpc = 0, C = 0, nwarps = 0, nslot = 0;
+    int s = 0, nv = 0, ch = 0, nchunks = 0;
+    int ncpc = 0;       // chunks per CTA
+    int C = 0;          // CTAs per cluster (per row)
+    int nw = 0;         // warps per CTA
+    int R = 0;          // ring stages per warp
+    int kw = 0;         // most chunks of one warp
     int clusters = 0;   // persistent grid size (clusters)
-    int per_row = 0;    // slots claim rows (small batches) instead of sequences
+    int per_row = 0;    // clusters claim rows (small batches) instead of sequences
     size_t smem = 0;
 };
 
 static int elem_size(sv_dtype dt) { return dt == SV_DTYPE_BF16 ? 2 : 4; }
 
-// 16-byte vectors per lane per chunk: large chunks once V spans two of them.
+// 16-byte vectors per lane per chunk (a chunk is 32 * nv * 16 bytes): 4 once
+// V spans two such chunks, smaller for small vocabularies.
 static int pick_nv(int V, int s)
 {
     const int E = 16 / s;
-    for (int nv = 8; nv > 1; nv >>= 1)
+    for (int nv = 4; nv > 1; nv >>= 1)
         if ((long long)V >= 2LL * 32 * nv * E)
             return nv;
     return 1;
@@ -64,19 +72,6 @@ static int n_chunks(int V, int s)
 {
     const int ch = chunk_elems(V, s);
     return (V + ch - 1) / ch;
-}
-
-// nslot x (target + draft chunk) per owned chunk, one mbarrier per chunk and
-// stage, one fp32 chunk partial per chunk
-static size_t smem_for(int ncpc, int ch, int s, int nslot)
-{
-    return (size_t)nslot * ncpc * (size_t)ch * (size_t)s * 2 + (size_t)nslot * ncpc * 8 +
-           (size_t)ncpc * 4;
-}
-
-static int max_ncpc(int ch, int s, int nslot)
-{
-    return (int)((kSmemPerCtaMax - kStaticSmemReserve) / smem_for(1, ch, s, nslot));
 }
 
 // ---- workspace layout ----
@@ -132,12 +127,12 @@ template <typename T, int NV>
 static cudaError_t prepare_kernels(int dev)
 {
     const int ti = sizeof(T) == 2 ? 1 : 0;
-    const int ni = NV == 1 ? 0 : NV == 2 ? 1 : NV == 4 ? 2 : 3;
+    const int ni = NV == 1 ? 0 : NV == 2 ? 1 : 2;
     std::lock_guard<std::mutex> lk(g_mu);
     if (!g_dev[dev].attrs_set[ti][ni]) {
         auto kern = sv_sweep_kernel<T, NV>;
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             kSmemPerCtaMax - kStaticSmemReserve);
+                                             kSmemPerCtaMax);
         if (e != cudaSuccess)
             return e;
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -153,7 +148,7 @@ static void sweep_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, con
 {
     *cfg = cudaLaunchConfig_t{};
     cfg->gridDim = dim3((unsigned)(clusters * g.C), 1, 1);
-    cfg->blockDim = dim3((unsigned)(32 * g.nwarps), 1, 1);
+    cfg->blockDim = dim3((unsigned)(32 * g.nw), 1, 1);
     cfg->dynamicSmemBytes = g.smem;
     cfg->stream = st;
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -171,7 +166,7 @@ static cudaError_t cluster_capacity(const Geom& g, int dev, int* n)
     cudaError_t e = prepare_kernels<T, NV>(dev);
     if (e != cudaSuccess)
         return e;
-    const auto key = std::make_tuple(dev, (int)sizeof(T) * 16 + NV, g.C, g.nwarps, g.smem);
+    const auto key = std::make_tuple(dev, (int)sizeof(T) * 16 + NV, g.C, g.nw, g.smem);
     {
         std::lock_guard<std::mutex> lk(g_mu);
         auto it = g_fit.find(key);
@@ -201,40 +196,28 @@ static cudaError_t capacity_nv(const Geom& g, int dev, int* n)
     switch (g.nv) {
     case 1: return cluster_capacity<T, 1>(g, dev, n);
     case 2: return cluster_capacity<T, 2>(g, dev, n);
-    case 4: return cluster_capacity<T, 4>(g, dev, n);
-    default: return cluster_capacity<T, 8>(g, dev, n);
+    default: return cluster_capacity<T, 4>(g, dev, n);
     }
 }
 
-// Chunks per CTA, cluster size and slot count for a given ncpc request.
-static bool shape_geometry(int V, sv_dtype dt, int ncpc, int want_slots, int cpw, Geom* g)
+// Geometry for a cluster size C (balanced chunks per CTA), nw warps per CTA
+// and R stages per warp; false if it does not fit.
+static bool shape_geometry(int V, sv_dtype dt, int C, int nw, int R, Geom* g)
 {
     const int s = elem_size(dt);
     g->s = s;
     g->nv = pick_nv(V, s);
     g->ch = 32 * g->nv * (16 / s);
     g->nchunks = (V + g->ch - 1) / g->ch;
-    ncpc = std::max(1, std::min(ncpc, g->nchunks));
-    const int C = (g->nchunks + ncpc - 1) / ncpc;
-    if (C > kMaxCluster)
-        return false;
-    ncpc = (g->nchunks + C - 1) / C;   // balance the chunks over the cluster
-    // One slot unless asked: a row in flight costs its whole slice of shared
-    // memory, and independent CTAs overlap their rows' dependent chains
-    // better than extra slots of one CTA do.
-    int nslot = want_slots > 0 ? std::min(want_slots, kMaxSlots) : 1;
-    while (nslot > 1 && ncpc > max_ncpc(g->ch, s, nslot))
-        --nslot;
-    if (ncpc > max_ncpc(g->ch, s, nslot))
-        return false;
-    g->ncpc = ncpc;
-    g->C = C;
-    g->nslot = nslot;
-    cpw = std::max(1, cpw);
-    // compute warps (each reduces up to cpw of the CTA's chunks) + the scheduler warp
-    g->nwarps = std::min((ncpc + cpw - 1) / cpw, kMaxWarps - 1) + 1;
-    g->smem = smem_for(ncpc, g->ch, s, nslot);
-    return true;
+    C = std::max(1, std::min(C, std::min(kMaxCluster, g->nchunks)));
+    g->ncpc = (g->nchunks + C - 1) / C;
+    g->C = (g->nchunks + g->ncpc - 1) / g->ncpc;   // no CTA without chunks
+    nw = std::max(1, std::min(nw, std::min(kMaxWarps, kMaxParts / g->C)));
+    g->nw = std::min(nw, g->ncpc);
+    g->kw = (g->ncpc + g->nw - 1) / g->nw;
+    g->R = std::max(1, std::min(R, std::min(kMaxRing, g->kw)));
+    g->smem = sweep_layout(g->nw, g->R, g->ch * s, g->kw).total;
+    return g->smem <= (size_t)kSmemPerCtaMax;
 }
 
 static sv_status capacity_of(const Geom& g, sv_dtype dt, int dev, int* cap)
@@ -244,17 +227,12 @@ static sv_status capacity_of(const Geom& g, sv_dtype dt, int dev, int* cap)
     return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
-// Pick the geometry of one launch.  Candidates: every cluster size 1..16
-// whose slice fits shared memory, with 1..kMaxChunksPerWarp chunks per compute
-// warp.  A row occupies its cluster's shared memory from the moment its copy
-// is issued until its decision (and residual pass) are done, so throughput
-// follows the bytes of logits the device keeps resident at once: the score is
-// resident clusters x CTAs x chunks, then more compute warps, then larger
-// clusters (shorter rows).  The choice is cached per shape.
-static sv_status pick_geometry(int V, sv_dtype dt, int B, int Kmax, int nsm, int override_ncpc,
-                               int want_slots, int want_cpw, int dev, Geom* g)
+// Pick the geometry of one launch (cached per shape).  Tuning overrides:
+// chunks per CTA (sets C), chunks per warp (sets nw), ring stages.
+static sv_status pick_geometry(int V, sv_dtype dt, int B, int Kmax, int override_ncpc,
+                               int want_cpw, int want_ring, int dev, Geom* g)
 {
-    const auto key = std::make_tuple(dev, V, (int)dt, B, Kmax, override_ncpc * 64 + want_slots * 8,
+    const auto key = std::make_tuple(dev, V, (int)dt, B, Kmax, override_ncpc * 64 + want_ring,
                                      want_cpw);
     {
         std::lock_guard<std::mutex> lk(g_mu);
@@ -266,55 +244,32 @@ static sv_status pick_geometry(int V, sv_dtype dt, int B, int Kmax, int nsm, int
     }
     const int s = elem_size(dt);
     const int nch = n_chunks(V, s);
-    const long long rows = (long long)B * (Kmax + 1);
-    std::vector<int> cand;
-    if (override_ncpc > 0) {
-        cand.push_back(override_ncpc);
-    } else {
-        for (int C = 1; C <= kMaxCluster; ++C) {
-            const int ncpc = (nch + C - 1) / C;
-            if (cand.empty() || cand.back() != ncpc)
-                cand.push_back(ncpc);
-            if (ncpc == 1)
-                break;
-        }
+    int C = kAutoCluster;
+    if (override_ncpc > 0)
+        C = (nch + override_ncpc - 1) / override_ncpc;
+    int nw = kAutoWarps;
+    if (want_cpw > 0) {
+        const int ncpc = (nch + std::min(C, nch) - 1) / std::min(C, nch);
+        nw = (ncpc + want_cpw - 1) / want_cpw;
     }
-    Geom best;
-    long long best_score = -1;
-    for (int ncpc : cand) {
-        const int cpw_lo = want_cpw > 0 ? want_cpw : 1;
-        const int cpw_hi = want_cpw > 0 ? want_cpw : kMaxChunksPerWarp;
-        for (int cpw = cpw_lo; cpw <= cpw_hi; ++cpw) {
-            Geom t;
-            if (!shape_geometry(V, dt, ncpc, want_slots, cpw, &t))
-                continue;
-            if (want_cpw <= 0 && cpw > 1 && (t.ncpc + cpw - 2) / (cpw - 1) == (t.ncpc + cpw - 1) / cpw)
-                continue;   // same warp count as cpw - 1
-            int cap = 0;
-            const sv_status st = capacity_of(t, dt, dev, &cap);
-            if (st != SV_OK)
-                return st;
-            if (cap <= 0)
-                continue;
-            // sequences are the units unless there are fewer of them than clusters
-            t.per_row = B < cap ? 1 : 0;
-            const long long units = t.per_row ? rows : (long long)B;
-            const long long want = t.per_row ? units : (units + t.nslot - 1) / t.nslot;
-            t.clusters = (int)std::min<long long>(cap, std::max<long long>(1, want));
-            const long long resident = (long long)t.clusters * t.C * t.ncpc * t.nslot;
-            const long long score = (resident * 32 + (t.nwarps - 1)) * 32 + t.C;
-            if (score > best_score) {
-                best_score = score;
-                best = t;
-            }
-        }
-    }
-    if (best_score < 0)
+    const int R = want_ring > 0 ? want_ring : kAutoRing;
+    Geom t;
+    if (C > kMaxCluster || !shape_geometry(V, dt, C, nw, R, &t))
         return SV_ERR_UNSUPPORTED;
-    (void)nsm;
+    int cap = 0;
+    const sv_status st = capacity_of(t, dt, dev, &cap);
+    if (st != SV_OK)
+        return st;
+    if (cap <= 0)
+        return SV_ERR_UNSUPPORTED;
+    // sequences are the units unless there are fewer of them than clusters
+    const long long rows = (long long)B * (Kmax + 1);
+    t.per_row = B < cap ? 1 : 0;
+    const long long units = t.per_row ? rows : (long long)B;
+    t.clusters = (int)std::min<long long>(cap, std::max<long long>(1, units));
     std::lock_guard<std::mutex> lk(g_mu);
-    g_pick[key] = best;
-    *g = best;
+    g_pick[key] = t;
+    *g = t;
     return SV_OK;
 }
 
@@ -327,7 +282,7 @@ static cudaError_t launch_pair(const Args& a, const Geom& g, cudaStream_t st, in
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[1];
     sweep_config(&cfg, attr, g, g.clusters, st);
-    e = cudaLaunchKernelEx(&cfg, sv_sweep_kernel<T, NV>, a, g.nslot);
+    e = cudaLaunchKernelEx(&cfg, sv_sweep_kernel<T, NV>, a);
     if (e != cudaSuccess)
         return e;
     cudaLaunchConfig_t fcfg = {};
@@ -349,8 +304,7 @@ static cudaError_t launch_nv(const Args& a, const Geom& g, cudaStream_t st, int 
     switch (g.nv) {
     case 1: return launch_pair<T, 1>(a, g, st, dev);
     case 2: return launch_pair<T, 2>(a, g, st, dev);
-    case 4: return launch_pair<T, 4>(a, g, st, dev);
-    default: return launch_pair<T, 8>(a, g, st, dev);
+    default: return launch_pair<T, 4>(a, g, st, dev);
     }
 }
 
@@ -437,8 +391,64 @@ static sv_status check_args(const Call& c, int* kmax_out)
     return SV_OK;
 }
 
+// Per host thread and device: pinned buffers the per-call header is staged in,
+// used round-robin.  An event recorded after each upload guards a buffer's
+// reuse, so a call blocks only if the GPU is kHeaderSlots calls behind.
+// Pinned staging keeps the upload asynchronous (a pageable source would make
+// the copy wait for the stream's earlier work).  The buffers live as long as
+// the thread (they are small: the header is B * (Kmax + 9) bytes and up).
+constexpr int kHeaderSlots = 4;
+struct HeaderSlot {
+    unsigned char* buf = nullptr;
+    size_t cap = 0;
+    cudaEvent_t done = nullptr;
+    bool used = false;
+};
+struct HeaderRing {
+    HeaderSlot slot[kHeaderSlots];
+    int next = 0;
+};
+static thread_local HeaderRing tl_header[64];
+
+// A pinned slot of at least `need` bytes on device `dev` (nullptr if pinned
+// memory is unavailable; the caller then stages in pageable memory).
+static HeaderSlot* header_slot(int dev, size_t need, sv_status* st)
+{
+    HeaderRing& hr = tl_header[dev];
+    HeaderSlot& sl = hr.slot[hr.next];
+    hr.next = (hr.next + 1) % kHeaderSlots;
+    *st = SV_OK;
+    if (sl.used) {
+        if (cudaEventSynchronize(sl.done) != cudaSuccess) {
+            *st = SV_ERR_CUDA;
+            return nullptr;
+        }
+        sl.used = false;
+    }
+    if (!sl.done && cudaEventCreateWithFlags(&sl.done, cudaEventDisableTiming) != cudaSuccess) {
+        (void)cudaGetLastError();
+        sl.done = nullptr;
+        return nullptr;
+    }
+    if (sl.cap < need) {
+        if (sl.buf)
+            (void)cudaFreeHost(sl.buf);
+        sl.buf = nullptr;
+        sl.cap = 0;
+        const size_t cap = std::max(need, (size_t)4096);
+        if (cudaHostAlloc(reinterpret_cast<void**>(&sl.buf), cap, cudaHostAllocDefault) !=
+            cudaSuccess) {
+            (void)cudaGetLastError();
+            sl.buf = nullptr;
+            return nullptr;
+        }
+        sl.cap = cap;
+    }
+    return &sl;
+}
+
 // host_header: where the per-call header is assembled before its upload
-// (nullptr: a per-thread buffer of this library).
+// (nullptr: a pinned per-thread slot, else a pageable per-thread buffer).
 static sv_status run(const Call& c, int kmax, const sv_options* opt, void* ws, size_t ws_bytes,
                      cudaStream_t stream, unsigned char* host_header = nullptr)
 {
@@ -461,8 +471,8 @@ static sv_status run(const Call& c, int kmax, const sv_options* opt, void* ws, s
     if (pa.type == cudaMemoryTypeDevice && pa.device != dev)
         return SV_ERR_INVALID_ARG;
     Geom g;
-    st = pick_geometry(c.V, c.dtype, c.B, kmax, nsm, opt ? opt->chunks_per_cta : 0,
-                       opt ? opt->slots : 0, opt ? opt->chunks_per_warp : 0, dev, &g);
+    st = pick_geometry(c.V, c.dtype, c.B, kmax, opt ? opt->chunks_per_cta : 0,
+                       opt ? opt->chunks_per_warp : 0, opt ? opt->ring_stages : 0, dev, &g);
     if (st != SV_OK)
         return st;
     if ((long long)g.clusters * g.C > 0x7fffffffLL)
@@ -477,12 +487,20 @@ static sv_status run(const Call& c, int kmax, const sv_options* opt, void* ws, s
     // order (sequences by K, longest first, so the tail holds short ones).
     thread_local std::vector<unsigned char> hdr_tls;
     unsigned char* hdr = host_header;
+    HeaderSlot* slot = nullptr;
     if (!hdr) {
-        hdr_tls.assign(L.header_end, 0);
-        hdr = hdr_tls.data();
-    } else {
-        memset(hdr, 0, L.header_end);
+        sv_status hs = SV_OK;
+        slot = header_slot(dev, L.header_end, &hs);
+        if (hs != SV_OK)
+            return hs;
+        if (slot) {
+            hdr = slot->buf;
+        } else {
+            hdr_tls.assign(L.header_end, 0);
+            hdr = hdr_tls.data();
+        }
     }
+    memset(hdr, 0, L.header_end);
     memcpy(hdr + L.K, c.K, (size_t)c.B * 4);
     {
         int32_t* ord = reinterpret_cast<int32_t*>(hdr + L.order);
@@ -498,6 +516,11 @@ static sv_status run(const Call& c, int kmax, const sv_options* opt, void* ws, s
     if (cudaMemcpyAsync(base, hdr, L.header_end, cudaMemcpyHostToDevice, stream) !=
         cudaSuccess)
         return SV_ERR_CUDA;
+    if (slot) {
+        if (cudaEventRecord(slot->done, stream) != cudaSuccess)
+            return SV_ERR_CUDA;
+        slot->used = true;
+    }
 
     Args a;
     a.tgt = c.tgt;
@@ -515,6 +538,8 @@ static sv_status run(const Call& c, int kmax, const sv_options* opt, void* ws, s
     a.nchunks = g.nchunks;
     a.ncpc = g.ncpc;
     a.C = g.C;
+    a.ring = g.R;
+    a.kw = g.kw;
     a.early_exit = (want_diag || (opt && opt->verify_all)) ? 0 : 1;
     a.has_draft = c.drf != nullptr ? 1 : 0;
     const uintptr_t al = (uintptr_t)c.tgt | (c.drf ? (uintptr_t)c.drf : 0);
@@ -542,7 +567,7 @@ static sv_status run(const Call& c, int kmax, const sv_options* opt, void* ws, s
 }
 
 // Launch geometry a call would use (for reports and tests).
-static sv_status geometry_of(int B, int Kmax, int V, sv_dtype dt, int ncpc, int slots, int cpw,
+static sv_status geometry_of(int B, int Kmax, int V, sv_dtype dt, int ncpc, int cpw, int ring,
                              int32_t* out)
 {
     int dev = 0, nsm = 0;
@@ -550,14 +575,14 @@ static sv_status geometry_of(int B, int Kmax, int V, sv_dtype dt, int ncpc, int 
     if (st != SV_OK)
         return st;
     Geom g;
-    st = pick_geometry(V, dt, B, Kmax, nsm, ncpc, slots, cpw, dev, &g);
+    st = pick_geometry(V, dt, B, Kmax, ncpc, cpw, ring, dev, &g);
     if (st != SV_OK)
         return st;
     out[0] = g.C;
     out[1] = g.ncpc;
-    out[2] = g.nslot;
+    out[2] = g.R;
     out[3] = g.clusters;
-    out[4] = 32 * g.nwarps;
+    out[4] = 32 * g.nw;
     out[5] = (int32_t)g.smem;
     out[6] = g.per_row;
     out[7] = g.nchunks;
@@ -590,21 +615,19 @@ int32_t sv_max_vocab(sv_dtype dtype)
 {
     if (dtype != SV_DTYPE_F32 && dtype != SV_DTYPE_BF16)
         return 0;
-    const int s = sv::elem_size(dtype);
-    const int ch = 32 * 8 * (16 / s);   // chunk size at large V
-    return sv::kMaxCluster * sv::max_ncpc(ch, s, 1) * ch;
+    return sv::kMaxVocab;
 }
 
 sv_status sv_geometry(int32_t B, int32_t Kmax, int32_t V, sv_dtype dtype, int32_t chunks_per_cta,
-                      int32_t slots, int32_t chunks_per_warp, int32_t* out8)
+                      int32_t chunks_per_warp, int32_t ring_stages, int32_t* out8)
 {
-    if (!out8 || B < 1 || Kmax < 0 || Kmax > SV_K_MAX || V < 1 || chunks_per_cta < 0 || slots < 0 ||
-        chunks_per_warp < 0 ||
+    if (!out8 || B < 1 || Kmax < 0 || Kmax > SV_K_MAX || V < 1 || chunks_per_cta < 0 ||
+        chunks_per_warp < 0 || ring_stages < 0 ||
         (dtype != SV_DTYPE_F32 && dtype != SV_DTYPE_BF16))
         return SV_ERR_INVALID_ARG;
     if (V > sv_max_vocab(dtype))
         return SV_ERR_UNSUPPORTED;
-    return sv::geometry_of(B, Kmax, V, dtype, chunks_per_cta, slots, chunks_per_warp, out8);
+    return sv::geometry_of(B, Kmax, V, dtype, chunks_per_cta, chunks_per_warp, ring_stages, out8);
 }
 
 size_t sv_workspace_size(int32_t B, int32_t Kmax, int32_t V, sv_dtype dtype)
@@ -630,7 +653,7 @@ sv_status spec_verify_ex(const void* target_logits, const void* draft_logits, sv
     const sv_status st = sv::check_args(c, &kmax);
     if (st != SV_OK)
         return st;
-    if (options && (options->chunks_per_cta < 0 || options->slots < 0 ||
+    if (options && (options->chunks_per_cta < 0 || options->ring_stages < 0 ||
                     options->chunks_per_warp < 0))
         return SV_ERR_INVALID_ARG;
     return sv::run(c, kmax, options, workspace, workspace_bytes, stream);

@@ -40,9 +40,11 @@ struct Args {
     int32_t* out_tok;
     int32_t* out_n;
     int B, Kmax, V;
-    int per_row;           // 1: slots claim single rows; 0: slots claim whole sequences
+    int per_row;           // 1: clusters claim single rows; 0: whole sequences
     int n_units;           // claimable units: B sequences, or B * (Kmax + 1) rows
-    int nchunks, ncpc, C;
+    int nchunks, ncpc, C;  // chunks per row, chunks per CTA, CTAs per cluster
+    int ring;              // shared-memory stages per warp
+    int kw;                // most chunks any warp owns (stride of its chunk statistics)
     int early_exit, aligned;
     // Which optional buffers were supplied.  Decided on the host: device code
     // never branches on a pointer's null-ness.

@@ -6,7 +6,11 @@
 //  * mbarrier init / arrive.expect_tx / bounded try_wait;
 //  * the non-tensor bulk copy global -> shared (cp.async.bulk, the 1-D TMA
 //    path), completing on an mbarrier transaction count;
-//  * ex2.approx and the NaN-propagating max.
+//  * st.async: a store into another cluster CTA's shared memory that
+//    completes on that CTA's mbarrier transaction count;
+//  * ex2.approx, the NaN-propagating max (scalar, three-input and bf16x2) and
+//    the packed two-lane fp32 arithmetic of sm_100+ (add/sub/mul .f32x2, each
+//    lane rounded to nearest like its scalar form).
 #pragma once
 
 #include <stdint.h>
@@ -164,6 +168,71 @@ __device__ __forceinline__ float max_nan(float a, float b)
     float y;
     asm("max.NaN.f32 %0, %1, %2;" : "=f"(y) : "f"(a), "f"(b));
     return y;
+}
+
+// max of three with NaN propagation (sm_100+ three-input form)
+__device__ __forceinline__ float max3_nan(float a, float b, float c)
+{
+    float y;
+    asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(y) : "f"(a), "f"(b), "f"(c));
+    return y;
+}
+
+// lane-wise max of two packed bf16 pairs, NaN-propagating
+__device__ __forceinline__ uint32_t bmax2_nan(uint32_t a, uint32_t b)
+{
+    uint32_t y;
+    asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(y) : "r"(a), "r"(b));
+    return y;
+}
+
+// Two fp32 values in one 64-bit register pair: lo in bits 0..31.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi)
+{
+    uint64_t y;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(y) : "f"(lo), "f"(hi));
+    return y;
+}
+
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b)
+{
+    uint64_t y;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(y) : "l"(a), "l"(b));
+    return y;
+}
+
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b)
+{
+    uint64_t y;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(y) : "l"(a), "l"(b));
+    return y;
+}
+
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b)
+{
+    uint64_t y;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(y) : "l"(a), "l"(b));
+    return y;
+}
+
+// 16-byte store into cluster shared memory completing `bytes` on the
+// destination CTA's mbarrier (both addresses from mapa).
+__device__ __forceinline__ void st_async_v4(uint32_t addr, float4 v, uint32_t mbar)
+{
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];"
+        ::"r"(addr), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(mbar) : "memory");
+}
+
+__device__ __forceinline__ void st_async_s32(uint32_t addr, int v, uint32_t mbar)
+{
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];"
+                 ::"r"(addr), "r"(v), "r"(mbar) : "memory");
 }
 
 __device__ __forceinline__ uint8_t ld_cg_u8(const uint8_t* p)

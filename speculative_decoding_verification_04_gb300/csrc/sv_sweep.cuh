@@ -1,30 +1,38 @@
 // sv_sweep.cuh -- the persistent vocabulary-sweep kernel.
 //
 // A grid of thread-block clusters (C CTAs each, as many as the device holds at
-// once) works through the batch.  Each CTA owns `ncpc` contiguous vocabulary
-// chunks of every row and keeps `nslot` shared-memory stages of that slice
-// (target and draft), filled by 1-D bulk copies (cp.async.bulk, one mbarrier
-// per chunk and stage).
+// once) works through the batch one row (sequence b, position i) at a time per
+// cluster.  CTA r of a cluster owns the vocabulary chunks [r*ncpc, (r+1)*ncpc)
+// of every row; warp w of the CTA owns every nw-th of those chunks and streams
+// them through its own ring of R shared-memory stages (target and draft chunk
+// per stage), filled by 1-D bulk copies (cp.async.bulk) that complete on one
+// mbarrier per stage.  No two warps share a stage, so the steady state has no
+// CTA-wide barrier at all.
 //
-// Schedule: every cluster runs `nslot` sequence slots round-robin, slot s
-// using stage s.  A slot walks one sequence's positions in order.  As soon as
-// row i is decided, the slot knows its next row exactly -- row i+1 when x_i was
-// accepted, otherwise a fresh sequence (the rows after a rejection are never
-// read: the method's own early exit, with no speculative traffic) -- and its
-// bulk copies run while the cluster reduces the other slots' rows.  Fresh
-// sequences come from one atomic claim per sequence (longest K first), made a
-// whole row ahead by a scheduler warp.  When there are fewer sequences than
-// clusters, slots claim single rows instead (all positions in parallel).
+// Schedule: a cluster walks one sequence's positions in order.  Row i+1 is
+// read only once x_i has been accepted (the method's own early exit: rows after
+// the first rejection are never read).  Fresh sequences come from one atomic
+// claim per sequence (longest K first), made a row ahead by rank 0 and handed
+// to the cluster with that row's exchange.  When there are fewer sequences
+// than clusters, clusters claim single rows instead (all positions at once).
 //
-// Per row, with the slice resident in shared memory:
-//   pass 1  per-warp NaN-propagating max of the target (and draft) logits;
-//   pass 2  sampling rows: per-chunk sums of exp2((l - m_w) log2(e)/T) relative
-//           to the warp max; greedy rows: lowest index of the warp max;
-//   exchange  one cluster all-reduce through distributed shared memory of
-//           (max, rescaled sum, argmax) per CTA;
-//   decide  u q(x) < p(x) (sampling) or x == argmax (greedy);
-//   pass 3  rejected rows (every tested row in verify-all mode): per-chunk
-//           residual mass sum max(0, p - q) from the resident slice.
+// Per row, each warp makes one pass over its chunks, from the stage straight
+// into registers:
+//   greedy row       lane max (packed bf16x2 / three-input fp32 max) and the
+//                    lowest index holding it;
+//   tested sampling  lane-online max and sum of exp2((l - m) log2(e)/T) of the
+//   row              target and the draft row (rescaled when the lane max
+//                    grows), in packed two-lane fp32 arithmetic;
+//   bonus row        per-chunk (max, sum) of the target, kept for the draw.
+// exchange  every warp pushes a 16-byte partial to every CTA of the cluster
+//           with st.async, completing on the receiver's exchange mbarrier
+//           (double-buffered by row parity);
+// decide    every warp combines all C*nw partials (identical arithmetic, so
+//           identical results) and decides u q(x) < p(x), or x == argmax at
+//           temperature 0;
+// residual  rejected rows (every tested row in verify-all mode): per-chunk
+//           sums of max(0, p - q) and of p from the ring -- still resident
+//           when the warp's chunks fit in it, read again through it otherwise.
 // Results go to the workspace; sv_finalize draws the tokens.
 #pragma once
 
@@ -32,89 +40,113 @@
 
 namespace sv {
 
-constexpr int kMaxSlots = 3;
+constexpr int kMaxRing = 8;    // ring stages per warp
+constexpr int kMaxParts = 32;  // C * nw partials per row: one per lane in the combine
 
-// Row flags.  Schedule flags come from the sequence's K_b and T alone; the
-// decision flag needs the proposed token and its uniform.
+// Dynamic shared memory of one CTA (host and device compute it alike).
+struct SweepLayout {
+    size_t stage_bytes;   // one stage: target chunk + draft chunk
+    size_t bars;          // [nw][R] stage mbarriers
+    size_t xbar;          // [2] exchange mbarriers
+    size_t xbuf;          // [2][kMaxParts] float4 partials
+    size_t xclaim;        // [2] int: unit claimed by rank 0 during the row
+    size_t first;         // [2] int: first unit of the cluster (one used)
+    size_t stats;         // [nw][kw] float2: per-chunk (max, sum) of bonus rows
+    size_t total;
+};
+
+__host__ __device__ inline SweepLayout sweep_layout(int nw, int R, int chunk_bytes, int kw)
+{
+    SweepLayout L;
+    L.stage_bytes = 2 * (size_t)chunk_bytes;
+    L.bars = (size_t)nw * R * L.stage_bytes;
+    L.xbar = L.bars + (size_t)nw * R * 8;
+    L.xbuf = (L.xbar + 16 + 15) & ~(size_t)15;
+    L.xclaim = L.xbuf + 2 * kMaxParts * 16;
+    L.first = L.xclaim + 8;
+    L.stats = L.first + 8;
+    L.total = L.stats + (size_t)nw * kw * 8;
+    return L;
+}
+
+// Row flags, from the sequence's K_b and T alone.
 enum : int {
     kFGreedy = 1,   // T == 0
     kFTest = 2,     // i < K_b: a proposal is tested at this row
     kFDraft = 4,    // the draft row is read (tested sampling row)
-    kFUsable = 8,   // temperature usable and, if needed, draft logits supplied
-    kFOk = 16       // everything the decision needs is usable (set by describe)
+    kFUsable = 8    // temperature usable and, if needed, draft logits supplied
 };
 
-// One row as every CTA of the cluster sees it (all fields derive from the
-// same global reads, so every CTA takes the same branches).  Integer fields
-// only: the struct lives in shared memory, shared by the CTA's threads.
-struct Item {
+struct Row {
     int i, b, Kb;
     float T;
-    int sflags;         // kFGreedy | kFTest | kFDraft | kFUsable
-    int x;
-    float u;
-    float lt_x, ld_x;   // target / draft logit at the proposed token (prefetched)
-    int dflags;         // kFOk
+    int flags;
 };
 
-// The row's schedule fields, from the sequence's cached K_b and T.
-__device__ __forceinline__ Item schedule(const Args& a, int i, int b, int Kb, float T)
+__device__ __forceinline__ Row make_row(const Args& a, int i, int b, int Kb, float T)
 {
-    Item it;
-    it.i = i;
-    it.b = b;
-    it.Kb = Kb;
-    it.T = T;
+    Row r;
+    r.i = i;
+    r.b = b;
+    r.Kb = Kb;
+    r.T = T;
     const int greedy = T == 0.0f ? kFGreedy : 0;
     const int test = i < Kb ? kFTest : 0;
     const int draft = (test && !greedy) ? kFDraft : 0;
     const int usable = (temperature_usable(T) && (!draft || a.has_draft != 0)) ? kFUsable : 0;
-    it.sflags = greedy | test | draft | usable;
-    it.x = 0;
-    it.u = it.lt_x = it.ld_x = 0.0f;
-    it.dflags = 0;
-    return it;
+    r.flags = greedy | test | draft | usable;
+    return r;
 }
 
-// Everything else the row's decision needs: the proposed token, its uniform
-// and the two logits at the token (one thread; writes only x, u, lt_x, ld_x
-// and dflags).  Called right after the row's bulk copies are issued, a full
-// row ahead of the decision.
+// What the decision needs besides the sums: the proposed token, its uniform
+// and the two logits at the token.  Loaded by one lane a row ahead.
+struct Tok {
+    int x;
+    float u, lt, ld;
+    int ok;
+};
+
 template <typename T>
-__device__ __forceinline__ void describe(const Args& a, Item& it)
+__device__ __forceinline__ Tok describe(const Args& a, const Row& r)
 {
-    const int f = it.sflags;
-    if (!(f & kFUsable)) {
-        it.dflags = 0;
-        return;
+    Tok t{0, 0.0f, 0.0f, 0.0f, 0};
+    if (!(r.flags & kFUsable))
+        return t;
+    if (!(r.flags & kFTest)) {
+        t.ok = 1;
+        return t;
     }
-    if (!(f & kFTest)) {
-        it.dflags = kFOk;
-        return;
-    }
-    const int x = __ldg(a.tok + (size_t)it.b * a.Kmax + it.i);
+    const int x = __ldg(a.tok + (size_t)r.b * a.Kmax + r.i);
     bool ok = x >= 0 && x < a.V;
-    float u = 0.0f, lt = 0.0f, ld = 0.0f;
-    if (!(f & kFGreedy)) {
-        u = __ldg(a.uni + (size_t)it.b * (a.Kmax + 1) + it.i);
-        ok = ok && u >= 0.0f && u < 1.0f;
+    if (!(r.flags & kFGreedy)) {
+        t.u = __ldg(a.uni + (size_t)r.b * (a.Kmax + 1) + r.i);
+        ok = ok && t.u >= 0.0f && t.u < 1.0f;
     }
     if (ok) {
-        const size_t trow = (size_t)it.b * (a.Kmax + 1) + it.i;
-        lt = Elem<T>::load(static_cast<const T*>(a.tgt) + trow * (size_t)a.V + x);
-        if ((f & kFDraft) && a.has_draft)
-            ld = Elem<T>::load(static_cast<const T*>(a.drf) +
-                               ((size_t)it.b * a.Kmax + it.i) * (size_t)a.V + x);
+        const size_t trow = (size_t)r.b * (a.Kmax + 1) + r.i;
+        t.lt = Elem<T>::load(static_cast<const T*>(a.tgt) + trow * (size_t)a.V + x);
+        if (r.flags & kFDraft)
+            t.ld = Elem<T>::load(static_cast<const T*>(a.drf) +
+                                 ((size_t)r.b * a.Kmax + r.i) * (size_t)a.V + x);
     }
-    it.x = x;
-    it.u = u;
-    it.lt_x = lt;
-    it.ld_x = ld;
-    it.dflags = ok ? kFOk : 0;
+    t.x = x;
+    t.ok = ok ? 1 : 0;
+    return t;
+}
+
+__device__ __forceinline__ Tok shfl_tok(const Tok& t)
+{
+    Tok o;
+    o.x = __shfl_sync(kFull, t.x, 0);
+    o.u = __shfl_sync(kFull, t.u, 0);
+    o.lt = __shfl_sync(kFull, t.lt, 0);
+    o.ld = __shfl_sync(kFull, t.ld, 0);
+    o.ok = __shfl_sync(kFull, t.ok, 0);
+    return o;
 }
 
 // Claim the next unit of work (one thread): a sequence id in claim order, or
-// a live row index i * B + b when slots claim single rows.  -1: none left.
+// a live row index i * B + b when clusters claim single rows.  -1: none left.
 // Anything outside the unit range also reads as -1, so a unit id can never
 // index past the batch.
 __device__ __forceinline__ int claim_unit(const Args& a)
@@ -138,520 +170,662 @@ __device__ __forceinline__ bool unit_valid(const Args& a, int u)
     return u >= 0 && u < (a.per_row ? a.n_units : a.B);
 }
 
-// First row of a claimed unit.
-__device__ __forceinline__ void unit_row(const Args& a, int unit, int* i, int* b)
-{
-    if (a.per_row) {
-        *i = unit / a.B;
-        *b = unit - *i * a.B;
-    } else {
-        *i = 0;
-        *b = unit;
-    }
-}
-
-template <typename T, int NV>
-struct SweepSmem {
-    static constexpr int E = Elem<T>::E;
-    static constexpr int CH = 32 * NV * E;
-    T* base;
-    uint64_t* mbar;   // [nslot][ncpc]
-    int ncpc;
-    __device__ T* tchunk(int s, int lc) const { return base + ((size_t)s * 2 * ncpc + lc) * CH; }
-    __device__ T* dchunk(int s, int lc) const { return base + ((size_t)s * 2 * ncpc + ncpc + lc) * CH; }
-    __device__ uint32_t bar(int s, int lc) const { return smem_addr(&mbar[s * ncpc + lc]); }
-};
-
-// Stage this CTA's chunks of row `d` into stage `s` (compute warps only): the
-// 16-byte-aligned body of each chunk by bulk copy, the ragged tail (or the
-// whole chunk when rows are not 16-byte aligned) by element loads.  Every
-// owned chunk's barrier receives exactly one arrival per use.
-template <typename T, int NV>
-__device__ __forceinline__ void issue_row(const Args& a, const SweepSmem<T, NV>& sm, const Item& d,
-                                          int s, int c0, int nck, int cw, int nwc, int lane,
-                                          bool poisoned)
-{
-    using EL = Elem<T>;
-    constexpr int CH = SweepSmem<T, NV>::CH;
-    const bool load_t = (d.sflags & kFUsable) && !poisoned;
-    const bool load_d = load_t && (d.sflags & kFDraft) && a.has_draft != 0;
-    const T* tg = static_cast<const T*>(a.tgt) + ((size_t)d.b * (a.Kmax + 1) + d.i) * (size_t)a.V;
-    const T* dg = load_d ? static_cast<const T*>(a.drf) + ((size_t)d.b * a.Kmax + d.i) * (size_t)a.V
-                         : nullptr;
-    for (int lc = cw; lc < nck; lc += nwc) {
-        const int e0 = (c0 + lc) * CH;
-        const int n = min(CH, a.V - e0);
-        const int nb = a.aligned ? ((n * (int)sizeof(T)) & ~15) / (int)sizeof(T) : 0;
-        T* dt = sm.tchunk(s, lc);
-        T* dd = sm.dchunk(s, lc);
-        if (lane == 0) {
-            const uint32_t mb = sm.bar(s, lc);
-            const uint32_t bytes = (uint32_t)nb * (uint32_t)sizeof(T);
-            const uint32_t tx = (load_t ? bytes : 0u) + (load_d ? bytes : 0u);
-            if (tx) {
-                fence_proxy_async();
-                mbar_arrive_expect_tx(mb, tx);
-                bulk_copy_g2s(smem_addr(dt), tg + e0, bytes, mb);
-                if (load_d)
-                    bulk_copy_g2s(smem_addr(dd), dg + e0, bytes, mb);
-            } else {
-                mbar_arrive(mb);
-            }
-        }
-        if (load_t)
-            for (int j = nb + lane; j < n; j += 32) {
-                EL::copy(dt + j, tg + e0 + j);
-                if (load_d)
-                    EL::copy(dd + j, dg + e0 + j);
-            }
-    }
-}
-
-// A part's sum of exp2((l - m_part) c) rescaled to a common max m.  Parts
-// whose max is -inf hold no mass.
-__device__ __forceinline__ float rescaled(float s_part, float m_part, float m, float c)
-{
-    return m_part == -INFINITY ? 0.0f : s_part * weight(m_part, m, c);
-}
-
-// (max, sum, argmax) over up to 32 parts held one per lane, identical in every
-// lane: NaN-propagating max, compensated sum of the rescaled part sums, lowest
-// index among the parts holding the max.
-__device__ __forceinline__ void combine_parts(float m_part, float s_part, int i_part, float c,
-                                              float& m, float& S, int& idx)
-{
-    m = warp_max_nan(m_part);
-    S = warp_sum_comp(rescaled(s_part, m_part, m, c));
-    idx = __reduce_min_sync(kFull, m_part == m ? i_part : INT_MAX);
-}
-
-// Per-row result broadcast from warp 0 to the CTA.
-struct RowResult {
-    float m_t, m_d, inv_st, inv_sd;
-    int dec;
-    int resid;   // pass 3 wanted
-};
-
-// A sequence (or, in per-row mode, a row) held by a slot: the row it is at and
-// the sequence's K_b and temperature, cached for its later rows.
-struct SlotPos {
+// First row of a claimed (valid) unit, with its sequence's K_b and T loaded
+// but not yet used (the flags are made when the unit starts).
+struct UnitPos {
     int i, b, Kb;
     float T;
 };
 
-__device__ __forceinline__ SlotPos unit_pos(const Args& a, int unit)
+__device__ __forceinline__ UnitPos unit_pos(const Args& a, int unit)
 {
-    SlotPos p;
-    unit_row(a, unit, &p.i, &p.b);
+    UnitPos p;
+    p.i = 0;
+    p.b = unit;
+    if (a.per_row) {
+        p.i = unit / a.B;
+        p.b = unit - p.i * a.B;
+    }
     p.Kb = __ldg(a.K + p.b);
     p.T = __ldg(a.temp + p.b);
     return p;
 }
 
+__device__ __forceinline__ Row unit_row(const Args& a, int unit)
+{
+    const UnitPos p = unit_pos(a, unit);
+    return make_row(a, p.i, p.b, p.Kb, p.T);
+}
+
+// ---------------------------------------------------------------------------
+// per-lane chunk arithmetic on registers.  A lane holds NV 16-byte vectors of
+// a chunk: elements (k * 32 + lane) * E .. + E - 1 for vector k.
+// ---------------------------------------------------------------------------
+template <typename T, int NV> struct Lane;
+
+template <int NV> struct Lane<__nv_bfloat16, NV> {
+    static constexpr int E = 8;
+    // NaN-propagating max of the lane's 8 * NV elements
+    __device__ static __forceinline__ float max(const uint4 (&v)[NV])
+    {
+        uint32_t m0 = bmax2_nan(v[0].x, v[0].y), m1 = bmax2_nan(v[0].z, v[0].w);
+#pragma unroll
+        for (int k = 1; k < NV; ++k) {
+            m0 = bmax2_nan(m0, bmax2_nan(v[k].x, v[k].y));
+            m1 = bmax2_nan(m1, bmax2_nan(v[k].z, v[k].w));
+        }
+        const uint32_t m = bmax2_nan(m0, m1);
+        return max_nan(__uint_as_float(m << 16), __uint_as_float(m & 0xffff0000u));
+    }
+    // the two elements of a bf16 pair as fp32 (lower index in the low lane)
+    __device__ static __forceinline__ uint64_t pair(uint32_t w)
+    {
+        return f2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+    }
+    // sum of exp2((l - m) c) over the lane's elements
+    __device__ static __forceinline__ float exp_sum(const uint4 (&v)[NV], float m, float c)
+    {
+        const uint64_t M = f2_pack(m, m), Cc = f2_pack(c, c);
+        uint64_t acc0 = f2_pack(0.0f, 0.0f), acc1 = acc0;
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            const uint32_t wv[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                float d0, d1;
+                f2_unpack(f2_mul(f2_sub(pair(wv[h]), M), Cc), d0, d1);
+                const uint64_t e = f2_pack(ex2_approx(d0), ex2_approx(d1));
+                if (h & 1)
+                    acc1 = f2_add(acc1, e);
+                else
+                    acc0 = f2_add(acc0, e);
+            }
+        }
+        float a0, a1, b0, b1;
+        f2_unpack(acc0, a0, a1);
+        f2_unpack(acc1, b0, b1);
+        return (a0 + a1) + (b0 + b1);
+    }
+    // element j (0 .. 8 * NV - 1, in index order) of the lane's slice
+    __device__ static __forceinline__ float elem(const uint4 (&v)[NV], int j)
+    {
+        const uint4 q = v[j >> 3];
+        const int h = (j >> 1) & 3;
+        const uint32_t wd = h == 0 ? q.x : h == 1 ? q.y : h == 2 ? q.z : q.w;
+        return (j & 1) ? __uint_as_float(wd & 0xffff0000u) : __uint_as_float(wd << 16);
+    }
+    // sums of the residual terms max(0, p - q) and of the weights of p
+    __device__ static __forceinline__ void resid_sums(const uint4 (&t)[NV], const uint4 (&d)[NV],
+                                                      float mt, float ist, float md, float isd,
+                                                      float c, float& rs, float& ps)
+    {
+        const uint64_t MT = f2_pack(mt, mt), MD = f2_pack(md, md), Cc = f2_pack(c, c);
+        const uint64_t IT = f2_pack(ist, ist), ID = f2_pack(isd, isd);
+        uint64_t racc = f2_pack(0.0f, 0.0f), pacc = racc;
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            const uint32_t wt[4] = {t[k].x, t[k].y, t[k].z, t[k].w};
+            const uint32_t wd[4] = {d[k].x, d[k].y, d[k].z, d[k].w};
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                float a0, a1, b0, b1;
+                f2_unpack(f2_mul(f2_sub(pair(wt[h]), MT), Cc), a0, a1);
+                f2_unpack(f2_mul(f2_sub(pair(wd[h]), MD), Cc), b0, b1);
+                const uint64_t et = f2_pack(ex2_approx(a0), ex2_approx(a1));
+                const uint64_t ed = f2_pack(ex2_approx(b0), ex2_approx(b1));
+                float r0, r1;
+                f2_unpack(f2_sub(f2_mul(et, IT), f2_mul(ed, ID)), r0, r1);
+                racc = f2_add(racc, f2_pack(fmaxf(r0, 0.0f), fmaxf(r1, 0.0f)));
+                pacc = f2_add(pacc, et);
+            }
+        }
+        float x0, x1, y0, y1;
+        f2_unpack(racc, x0, x1);
+        f2_unpack(pacc, y0, y1);
+        rs = x0 + x1;
+        ps = y0 + y1;
+    }
+};
+
+template <int NV> struct Lane<float, NV> {
+    static constexpr int E = 4;
+    __device__ static __forceinline__ float max(const uint4 (&v)[NV])
+    {
+        float m = max_nan(__uint_as_float(v[0].x), __uint_as_float(v[0].y));
+        m = max3_nan(m, __uint_as_float(v[0].z), __uint_as_float(v[0].w));
+#pragma unroll
+        for (int k = 1; k < NV; ++k) {
+            m = max3_nan(m, __uint_as_float(v[k].x), __uint_as_float(v[k].y));
+            m = max3_nan(m, __uint_as_float(v[k].z), __uint_as_float(v[k].w));
+        }
+        return m;
+    }
+    __device__ static __forceinline__ float exp_sum(const uint4 (&v)[NV], float m, float c)
+    {
+        const uint64_t M = f2_pack(m, m), Cc = f2_pack(c, c);
+        uint64_t acc0 = f2_pack(0.0f, 0.0f), acc1 = acc0;
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            float d0, d1, d2, d3;
+            f2_unpack(f2_mul(f2_sub(f2_pack(__uint_as_float(v[k].x), __uint_as_float(v[k].y)), M),
+                             Cc), d0, d1);
+            f2_unpack(f2_mul(f2_sub(f2_pack(__uint_as_float(v[k].z), __uint_as_float(v[k].w)), M),
+                             Cc), d2, d3);
+            acc0 = f2_add(acc0, f2_pack(ex2_approx(d0), ex2_approx(d1)));
+            acc1 = f2_add(acc1, f2_pack(ex2_approx(d2), ex2_approx(d3)));
+        }
+        float a0, a1, b0, b1;
+        f2_unpack(acc0, a0, a1);
+        f2_unpack(acc1, b0, b1);
+        return (a0 + a1) + (b0 + b1);
+    }
+    __device__ static __forceinline__ float elem(const uint4 (&v)[NV], int j)
+    {
+        const uint4 q = v[j >> 2];
+        const int h = j & 3;
+        return __uint_as_float(h == 0 ? q.x : h == 1 ? q.y : h == 2 ? q.z : q.w);
+    }
+    __device__ static __forceinline__ void resid_sums(const uint4 (&t)[NV], const uint4 (&d)[NV],
+                                                      float mt, float ist, float md, float isd,
+                                                      float c, float& rs, float& ps)
+    {
+        const uint64_t MT = f2_pack(mt, mt), MD = f2_pack(md, md), Cc = f2_pack(c, c);
+        const uint64_t IT = f2_pack(ist, ist), ID = f2_pack(isd, isd);
+        uint64_t racc = f2_pack(0.0f, 0.0f), pacc = racc;
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            const uint32_t wt[4] = {t[k].x, t[k].y, t[k].z, t[k].w};
+            const uint32_t wd[4] = {d[k].x, d[k].y, d[k].z, d[k].w};
+#pragma unroll
+            for (int h = 0; h < 4; h += 2) {
+                float a0, a1, b0, b1;
+                f2_unpack(f2_mul(f2_sub(f2_pack(__uint_as_float(wt[h]), __uint_as_float(wt[h + 1])),
+                                        MT), Cc), a0, a1);
+                f2_unpack(f2_mul(f2_sub(f2_pack(__uint_as_float(wd[h]), __uint_as_float(wd[h + 1])),
+                                        MD), Cc), b0, b1);
+                const uint64_t et = f2_pack(ex2_approx(a0), ex2_approx(a1));
+                const uint64_t ed = f2_pack(ex2_approx(b0), ex2_approx(b1));
+                float r0, r1;
+                f2_unpack(f2_sub(f2_mul(et, IT), f2_mul(ed, ID)), r0, r1);
+                racc = f2_add(racc, f2_pack(fmaxf(r0, 0.0f), fmaxf(r1, 0.0f)));
+                pacc = f2_add(pacc, et);
+            }
+        }
+        float x0, x1, y0, y1;
+        f2_unpack(racc, x0, x1);
+        f2_unpack(pacc, y0, y1);
+        rs = x0 + x1;
+        ps = y0 + y1;
+    }
+};
+
+// ---------------------------------------------------------------------------
+// one warp's ring of stages
+// ---------------------------------------------------------------------------
 template <typename T, int NV>
-__global__ void __launch_bounds__(kMaxWarps * 32, 1) sv_sweep_kernel(const Args a, const int nslot)
+struct Ring {
+    static constexpr int CH = 32 * NV * Elem<T>::E;
+    T* base;          // this warp's R stages
+    uint64_t* bars;   // this warp's R mbarriers
+    int R;
+    __device__ T* tst(int s) const { return base + (size_t)s * 2 * CH; }
+    __device__ T* dst(int s) const { return base + (size_t)s * 2 * CH + CH; }
+    __device__ uint32_t bar(int s) const { return smem_addr(&bars[s]); }
+};
+
+// Copy number q (stage q % R) brings global chunk gc of a row: the
+// 16-byte-aligned body by bulk copy, the ragged tail (or the whole chunk when
+// rows are not 16-byte aligned) by element loads, -inf past V.  The stage's
+// previous contents have been consumed by this warp (whole warp calls).
+template <typename T, int NV>
+__device__ __forceinline__ void issue_chunk(const Args& a, const Ring<T, NV>& rg, uint32_t q,
+                                            int gc, const T* trow, const T* drow, bool load_d,
+                                            int lane)
 {
     using EL = Elem<T>;
+    constexpr int CH = Ring<T, NV>::CH;
+    const int s = (int)(q % (uint32_t)rg.R);
+    const int e0 = gc * CH;
+    const int n = min(CH, a.V - e0);
+    const int nb = a.aligned ? ((n * (int)sizeof(T)) & ~15) / (int)sizeof(T) : 0;
+    T* dt = rg.tst(s);
+    T* dd = rg.dst(s);
+    if (lane == 0) {
+        const uint32_t bytes = (uint32_t)nb * (uint32_t)sizeof(T);
+        const uint32_t tx = bytes * (load_d ? 2u : 1u);
+        if (tx) {
+            fence_proxy_async();
+            mbar_arrive_expect_tx(rg.bar(s), tx);
+            bulk_copy_g2s(smem_addr(dt), trow + e0, bytes, rg.bar(s));
+            if (load_d)
+                bulk_copy_g2s(smem_addr(dd), drow + e0, bytes, rg.bar(s));
+        } else {
+            mbar_arrive(rg.bar(s));
+        }
+    }
+    for (int j = nb + lane; j < n; j += 32) {
+        EL::copy(dt + j, trow + e0 + j);
+        if (load_d)
+            EL::copy(dd + j, drow + e0 + j);
+    }
+    for (int j = n + lane; j < CH; j += 32) {
+        EL::set_neg_inf(dt + j);
+        if (load_d)
+            EL::set_neg_inf(dd + j);
+    }
+}
+
+template <typename T, int NV>
+__device__ __forceinline__ void load_stage(const T* p, int lane, uint4 (&v)[NV])
+{
+    const uint4* q = reinterpret_cast<const uint4*>(p);
+#pragma unroll
+    for (int k = 0; k < NV; ++k)
+        v[k] = q[k * 32 + lane];
+}
+
+// Combine (max, sum relative to that max) parts held one per lane; the sum
+// is compensated.  Every lane gets the same result.
+__device__ __forceinline__ void combine_ms(float m_part, float s_part, float c, float& m, float& S)
+{
+    m = warp_max_nan(m_part);
+    S = warp_sum_comp(m_part == -INFINITY ? 0.0f : s_part * weight(m_part, m, c));
+}
+
+template <typename T, int NV>
+__global__ void __launch_bounds__(kMaxWarps * 32) sv_sweep_kernel(const Args a)
+{
+    using EL = Elem<T>;
+    using LN = Lane<T, NV>;
     constexpr int E = EL::E;
     constexpr int CH = 32 * NV * E;
+    extern __shared__ __align__(128) unsigned char dsm[];
 
-    extern __shared__ __align__(128) unsigned char dsmem[];
-    __shared__ float s_wm[kMaxWarps][2];     // per compute warp: max (target, draft)
-    __shared__ float s_ws[kMaxWarps][2];     // per compute warp: sum relative to its max
-    __shared__ int s_wi[kMaxWarps];          // per compute warp: lowest index of its max
-    // Exchange slots, double-buffered by row parity: a CTA can push row k+1's
-    // partials while a peer still reads row k's; row k+2's push needs the row
-    // k+1 barrier, which the peer reaches only after its reads.
-    __shared__ float s_cm[2][kMaxCluster][2];   // per cluster rank, pushed: CTA max
-    __shared__ float s_cs[2][kMaxCluster][2];   // per cluster rank, pushed: CTA sum
-    __shared__ int s_ci[2][kMaxCluster];        // per cluster rank, pushed: CTA argmax
-    __shared__ int s_claim[2];                  // unit claimed during the row, from rank 0
-    __shared__ int s_units[kMaxSlots + 1];      // first units, pushed by rank 0
-    __shared__ int s_bad;                       // a bounded copy wait gave up in this CTA
-    __shared__ RowResult s_res;
-    // Slot state, written by thread 0 (descriptors' decision fields by compute
-    // warp 0, lane 0) between barriers and read by every thread.
-    __shared__ Item s_desc[kMaxSlots];
-    __shared__ int s_active[kMaxSlots];
-    __shared__ int s_uses[kMaxSlots];
-
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int nwc = (int)(blockDim.x >> 5) - 1;   // compute warps; warp 0 schedules
-    const int cw = warp - 1;                       // compute-warp index (-1: scheduler)
-    const int C = a.C, V = a.V, Kmax = a.Kmax;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int nw = (int)(blockDim.x >> 5);
+    const int C = a.C, V = a.V, Kmax = a.Kmax, R = a.ring;
+    const int P = C * nw;   // partials per row
     const uint32_t rank = cluster_ctarank();
     const int c0 = (int)rank * a.ncpc;
     const int nck = max(0, min(a.ncpc, a.nchunks - c0));
-    SweepSmem<T, NV> sm;
-    sm.base = reinterpret_cast<T*>(dsmem);
-    sm.ncpc = a.ncpc;
-    sm.mbar = reinterpret_cast<uint64_t*>(dsmem + (size_t)nslot * 2 * a.ncpc * CH * sizeof(T));
-    float* s_pc = reinterpret_cast<float*>(sm.mbar + (size_t)nslot * a.ncpc);   // [ncpc]
+    const int kw = w < nck ? (nck - w + nw - 1) / nw : 0;   // chunks of this warp
+    const bool resident = kw <= R;                          // residual pass needs no re-read
+    const SweepLayout L = sweep_layout(nw, R, CH * (int)sizeof(T), a.kw);
 
-    // ---- one-time set-up: barriers, -inf padding past V (never overwritten) ----
-    if (cw >= 0) {
-        for (int lc = cw; lc < nck; lc += nwc) {
-            if (lane == 0) {
-                for (int s = 0; s < nslot; ++s)
-                    mbar_init(sm.bar(s, lc), 1);
-                fence_mbar_init();
-            }
-            const int n = min(CH, V - (c0 + lc) * CH);
-            for (int s = 0; s < nslot; ++s)
-                for (int j = n + lane; j < CH; j += 32) {
-                    EL::set_neg_inf(sm.tchunk(s, lc) + j);
-                    EL::set_neg_inf(sm.dchunk(s, lc) + j);
-                }
+    Ring<T, NV> rg;
+    rg.base = reinterpret_cast<T*>(dsm) + (size_t)w * R * 2 * CH;
+    rg.bars = reinterpret_cast<uint64_t*>(dsm + L.bars) + (size_t)w * R;
+    rg.R = R;
+    uint64_t* xbar = reinterpret_cast<uint64_t*>(dsm + L.xbar);
+    float4* xbuf = reinterpret_cast<float4*>(dsm + L.xbuf);   // [2][kMaxParts]
+    int* xclaim = reinterpret_cast<int*>(dsm + L.xclaim);     // [2]
+    int* first = reinterpret_cast<int*>(dsm + L.first);       // [2]
+    float2* stats = reinterpret_cast<float2*>(dsm + L.stats) + (size_t)w * a.kw;
+
+    // ---- set-up: barriers, then the first unit from rank 0 (one per cluster:
+    // taking a spare here as well would leave clusters idle when there are
+    // fewer than twice as many units as clusters) ----
+    if (lane == 0) {
+        for (int s = 0; s < R; ++s)
+            mbar_init(rg.bar(s), 1);
+        if (w == 0) {
+            mbar_init(smem_addr(&xbar[0]), 1);
+            mbar_init(smem_addr(&xbar[1]), 1);
         }
+        fence_mbar_init();
     }
-    if (tid == 0)
-        s_bad = 0;
     __syncthreads();
-
-    // ---- first units: one per slot plus a spare (all CTAs started first) ----
-    // The claims stay in warp 0's registers (lane 0 claims, a shuffle hands
-    // them to the pushing lanes): nothing is read back from shared memory
-    // that another thread wrote after its cluster arrive.
-    cluster_arrive();
-    int first[kMaxSlots + 1] = {-1, -1, -1, -1};
-    if (rank == 0 && warp == 0) {
+    cluster_arrive();   // every CTA's barriers exist before any peer signals them
+    int f0 = -1;
+    if (rank == 0 && w == 0) {
         if (lane == 0)
-            for (int s = 0; s <= nslot; ++s)
-                first[s] = claim_unit(a);
-#pragma unroll
-        for (int s = 0; s <= kMaxSlots; ++s)
-            first[s] = __shfl_sync(kFull, first[s], 0);
+            f0 = claim_unit(a);
+        f0 = __shfl_sync(kFull, f0, 0);
     }
     cluster_wait();
-    if (rank == 0 && tid < C) {
-        const uint32_t dst = map_to_rank(smem_addr(&s_units[0]), (uint32_t)tid);
-        for (int s = 0; s <= nslot; ++s)
-            st_cluster_s32(dst + 4 * s, first[s]);
+    if (rank == 0 && w == 0 && lane < C) {
+        const uint32_t dst = map_to_rank(smem_addr(first), (uint32_t)lane);
+        st_cluster_s32(dst, f0);
     }
     cluster_arrive();
     cluster_wait();
 
-    // Slot state: the same in every CTA of the cluster (it derives from the
-    // pushed units and from decisions every CTA computes identically).
-    if (tid == 0) {
-        for (int s = 0; s < kMaxSlots; ++s) {
-            const int u = s < nslot ? s_units[s] : -1;
-            s_uses[s] = 0;
-            s_active[s] = unit_valid(a, u) ? 1 : 0;
-            if (s_active[s]) {
-                const SlotPos p = unit_pos(a, u);
-                s_desc[s] = schedule(a, p.i, p.b, p.Kb, p.T);
-            }
-        }
-    }
-    __syncthreads();
-    for (int s = 0; s < nslot; ++s) {
-        if (!s_active[s])
-            continue;
-        if (cw >= 0)
-            issue_row<T, NV>(a, sm, s_desc[s], s, c0, nck, cw, nwc, lane, false);
-        if (cw == 0 && lane == 0)
-            describe<T>(a, s_desc[s]);
-    }
-    __syncthreads();
-    int spare = unit_valid(a, s_units[nslot]) ? s_units[nslot] : -1;
-    SlotPos spare_pos{0, 0, 0, 0.0f};
-    if (spare >= 0)
-        spare_pos = unit_pos(a, spare);
-    bool exhausted = spare < 0;
+    // ---- per-warp schedule state (the same in every warp of the cluster) ----
+    bool active = unit_valid(a, first[0]);
+    int spare = -1;   // claimed during the first row
+    UnitPos spare_pos{0, 0, 0, 0.0f};
+    bool exhausted = false;
     bool triggered = false;
-    int xp = 0;   // exchange parity: flips once per processed row
+    bool broken = false;     // a stage wait gave up: no more copies, rows poisoned
+    bool xbroken = false;    // an exchange wait gave up: leave the loop
+    Row row = active ? unit_row(a, first[0]) : make_row(a, 0, 0, 0, 0.0f);
+    Tok tk{0, 0.0f, 0.0f, 0.0f, 0};
+    uint32_t qi = 0;   // copies issued by this warp
+    uint32_t qw = 0;   // copies waited for by this warp
+    // bound on the rows a cluster can process (guards the loop after a timeout)
+    const long long max_rows = (long long)a.n_units * (Kmax + 1) + 2;
 
-    for (int k = 0;; ++k) {
-        const bool any = (s_active[0] | s_active[1] | s_active[2]) != 0;
-        if (!any)
-            break;
+    const T* tgt = static_cast<const T*>(a.tgt);
+    const T* drf = static_cast<const T*>(a.drf);
+    auto row_ptrs = [&](const Row& r, const T*& tr, const T*& dr) {
+        tr = tgt + ((size_t)r.b * (Kmax + 1) + r.i) * (size_t)V;
+        dr = (r.flags & kFDraft) ? drf + ((size_t)r.b * Kmax + r.i) * (size_t)V : nullptr;
+    };
+    // first copies of a pass over a row (copy numbers qi, qi + 1, ...)
+    auto prologue = [&](const Row& r, bool with_d) {
+        const T* tr;
+        const T* dr;
+        row_ptrs(r, tr, dr);
+        const int n = min(R, kw);
+        for (int j = 0; j < n; ++j)
+            issue_chunk<T, NV>(a, rg, qi + (uint32_t)j, c0 + w + j * nw, tr, dr, with_d, lane);
+        qi += (uint32_t)n;
+    };
+    // wait for copy q (whole warp); false if any lane gave up (the copy then
+    // stays outstanding for the wind-down)
+    auto wait_copy = [&](uint32_t q) -> bool {
+        const bool ok = mbar_wait_bounded(rg.bar((int)(q % (uint32_t)R)), (q / (uint32_t)R) & 1u,
+                                          kWaitSpins);
+        const bool all = !__any_sync(kFull, !ok);
+        if (all)
+            qw = q + 1;
+        return all;
+    };
+
+    if (active) {
+        if ((row.flags & kFUsable) && kw > 0)
+            prologue(row, (row.flags & kFDraft) != 0);
+        if (lane == 0)
+            tk = describe<T>(a, row);
+    }
+
+    for (long long k = 0; active && k < max_rows; ++k) {
         if (exhausted && !triggered) {   // the finaliser may start launching
             griddep_launch_dependents();
             triggered = true;
         }
-        const int s = k % nslot;
-        if (!s_active[s])
-            continue;
-        const Item dc = s_desc[s];
-        const bool d_greedy = (dc.sflags & kFGreedy) != 0;
-        const bool d_test = (dc.sflags & kFTest) != 0;
-        const bool d_draft = (dc.sflags & kFDraft) != 0;
-        const bool d_ok = (dc.sflags & kFUsable) && (dc.dflags & kFOk);
-        const uint32_t par = (uint32_t)s_uses[s] & 1u;
+        const int p = (int)(k & 1);
+        const uint32_t xpar = (uint32_t)((k >> 1) & 1);
+        const bool greedy = (row.flags & kFGreedy) != 0;
+        const bool test = (row.flags & kFTest) != 0;
+        const bool draft = (row.flags & kFDraft) != 0;
+        const bool usable = (row.flags & kFUsable) != 0;
+        const bool load = usable && !broken && kw > 0;
+        const float c = (usable && !greedy) ? log2e_over(row.T) : 0.0f;
         const bool want_claim = spare < 0 && !exhausted;
-        const bool poisoned_before = s_bad != 0;
-        const float c = (d_ok && !d_greedy) ? log2e_over(dc.T) : 0.0f;
-        const size_t trow = (size_t)dc.b * (Kmax + 1) + dc.i;
+        if (w == 0 && lane == 0)
+            mbar_arrive_expect_tx(smem_addr(&xbar[p]), (uint32_t)P * 16u + (want_claim ? 4u : 0u));
+        int claimed = -1;
+        if (rank == 0 && w == 0 && lane == 0 && want_claim)
+            claimed = claim_unit(a);
+        const T* tr;
+        const T* dr;
+        row_ptrs(row, tr, dr);
 
-        float wmt = -INFINITY;   // this warp's target max (kept for its chunk sums)
-        if (warp == 0) {
-            // ---- scheduler: claim the next unit concurrently with the passes ----
-            if (rank == 0 && lane == 0 && want_claim)
-                s_claim[xp] = claim_unit(a);
+        // ---- one pass over this warp's chunks ----
+        float4 part = make_float4(-INFINITY, 0.0f, -INFINITY, 0.0f);
+        const uint32_t q0 = qi - (uint32_t)(load ? min(R, kw) : 0);   // this row's first copy
+        if (greedy) {
+            float gm = -INFINITY;
+            int gi = INT_MAX;
+            if (load) {
+                for (int j = 0; j < kw; ++j) {
+                    const uint32_t q = q0 + (uint32_t)j;
+                    if (!broken && !wait_copy(q))
+                        broken = true;
+                    __syncwarp();
+                    uint4 tv[NV];
+                    load_stage<T, NV>(rg.tst((int)(q % (uint32_t)R)), lane, tv);
+                    __syncwarp();
+                    if (j + R < kw && !broken) {
+                        issue_chunk<T, NV>(a, rg, qi, c0 + w + (j + R) * nw, tr, dr, false, lane);
+                        ++qi;
+                    }
+                    const float cm = LN::max(tv);
+                    if (cm > gm) {   // strictly greater: an earlier index keeps a tie
+                        const int gbase = (c0 + w + j * nw) * CH;
+                        int found = INT_MAX;
+#pragma unroll
+                        for (int e = NV * E - 1; e >= 0; --e)   // the lowest match wins
+                            if (LN::elem(tv, e) == cm)
+                                found = gbase + ((e / E) * 32 + lane) * E + (e % E);
+                        gm = cm;
+                        gi = found;
+                    } else if (cm != cm) {
+                        gm = cm;
+                    }
+                }
+            }
+            const float m = warp_max_nan(gm);
+            const int gidx = __reduce_min_sync(kFull, gm == m ? gi : INT_MAX);
+            part = make_float4(broken ? NAN : m, __int_as_float(gidx), -INFINITY, 0.0f);
+        } else if (test) {
+            float mt = -INFINITY, st = 0.0f, md = -INFINITY, sd = 0.0f;
+            if (load) {
+                for (int j = 0; j < kw; ++j) {
+                    const uint32_t q = q0 + (uint32_t)j;
+                    if (!broken && !wait_copy(q))
+                        broken = true;
+                    __syncwarp();
+                    const int s = (int)(q % (uint32_t)R);
+                    uint4 tv[NV], dv[NV];
+                    load_stage<T, NV>(rg.tst(s), lane, tv);
+                    if (draft)
+                        load_stage<T, NV>(rg.dst(s), lane, dv);
+                    __syncwarp();
+                    if (j + R < kw && !broken) {
+                        issue_chunk<T, NV>(a, rg, qi, c0 + w + (j + R) * nw, tr, dr, draft, lane);
+                        ++qi;
+                    }
+                    const float nt = max_nan(mt, LN::max(tv));
+                    if (nt != mt) {   // the lane max grew (or turned NaN): rescale the sum
+                        st = mt == -INFINITY ? 0.0f : st * weight(mt, nt, c);
+                        mt = nt;
+                    }
+                    st += LN::exp_sum(tv, mt == -INFINITY ? 0.0f : mt, c);
+                    if (draft) {
+                        const float nd = max_nan(md, LN::max(dv));
+                        if (nd != md) {
+                            sd = md == -INFINITY ? 0.0f : sd * weight(md, nd, c);
+                            md = nd;
+                        }
+                        sd += LN::exp_sum(dv, md == -INFINITY ? 0.0f : md, c);
+                    }
+                }
+            }
+            float m1, S1, m2, S2;
+            combine_ms(mt, st, c, m1, S1);
+            combine_ms(md, sd, c, m2, S2);
+            part = make_float4(broken ? NAN : m1, S1, m2, S2);
         } else {
-            // ---- pass 1: per-warp maxima over the owned chunks ----
-            float mt[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-            float md[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-            bool timed = false;
-            for (int lc = cw; lc < nck; lc += nwc) {
-                if (!poisoned_before && !mbar_wait_bounded(sm.bar(s, lc), par, kWaitSpins))
-                    timed = true;
-                if (!d_ok)
-                    continue;
-                const uint4* vt = reinterpret_cast<const uint4*>(sm.tchunk(s, lc));
-#pragma unroll
-                for (int v = 0; v < NV; ++v) {
-                    float xs[E];
-                    EL::unpack(vt[v * 32 + lane], xs);
-#pragma unroll
-                    for (int e = 0; e < E; ++e)
-                        mt[e & 3] = max_nan(mt[e & 3], xs[e]);
-                }
-                if (d_draft) {
-                    const uint4* vd = reinterpret_cast<const uint4*>(sm.dchunk(s, lc));
-#pragma unroll
-                    for (int v = 0; v < NV; ++v) {
-                        float xs[E];
-                        EL::unpack(vd[v * 32 + lane], xs);
-#pragma unroll
-                        for (int e = 0; e < E; ++e)
-                            md[e & 3] = max_nan(md[e & 3], xs[e]);
+            // bonus row: per-chunk (max, sum) of the target, kept for the draw
+            if (load) {
+                for (int j = 0; j < kw; ++j) {
+                    const uint32_t q = q0 + (uint32_t)j;
+                    if (!broken && !wait_copy(q))
+                        broken = true;
+                    __syncwarp();
+                    uint4 tv[NV];
+                    load_stage<T, NV>(rg.tst((int)(q % (uint32_t)R)), lane, tv);
+                    __syncwarp();
+                    if (j + R < kw && !broken) {
+                        issue_chunk<T, NV>(a, rg, qi, c0 + w + (j + R) * nw, tr, dr, false, lane);
+                        ++qi;
                     }
-                }
-            }
-            if (__any_sync(kFull, timed) && lane == 0)
-                s_bad = 1;
-            wmt = warp_max_nan(max_nan(max_nan(mt[0], mt[1]), max_nan(mt[2], mt[3])));
-            const float wmd = warp_max_nan(max_nan(max_nan(md[0], md[1]), max_nan(md[2], md[3])));
-            int widx = INT_MAX;
-            float wst = 0.0f, wsd = 0.0f;
-            if (d_ok && d_greedy) {
-                // ---- pass 2 (greedy): lowest index holding this warp's max ----
-                if (isfinite(wmt)) {
-                    for (int lc = cw; lc < nck; lc += nwc) {
-                        const uint4* vt = reinterpret_cast<const uint4*>(sm.tchunk(s, lc));
-                        const int gbase = (c0 + lc) * CH;
-#pragma unroll
-                        for (int v = 0; v < NV; ++v) {
-                            float xs[E];
-                            EL::unpack(vt[v * 32 + lane], xs);
-#pragma unroll
-                            for (int e = 0; e < E; ++e)
-                                if (xs[e] == wmt)
-                                    widx = min(widx, gbase + (v * 32 + lane) * E + e);
-                        }
-                    }
-                }
-                widx = __reduce_min_sync(kFull, widx);
-            } else if (d_ok) {
-                // ---- pass 2 (sampling): per-chunk sums relative to this warp's max ----
-                for (int lc = cw; lc < nck; lc += nwc) {
-                    float pc = 0.0f;
-                    if (wmt != -INFINITY) {
-                        const uint4* vt = reinterpret_cast<const uint4*>(sm.tchunk(s, lc));
-                        float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-                        for (int v = 0; v < NV; ++v) {
-                            float xs[E];
-                            EL::unpack(vt[v * 32 + lane], xs);
-#pragma unroll
-                            for (int e = 0; e < E; ++e)
-                                acc[e & 3] += weight(xs[e], wmt, c);
-                        }
-                        pc = warp_sum((acc[0] + acc[1]) + (acc[2] + acc[3]));
-                    }
+                    const float mc = warp_max_nan(LN::max(tv));
+                    const float sc = mc == -INFINITY ? 0.0f : warp_sum(LN::exp_sum(tv, mc, c));
                     if (lane == 0)
-                        s_pc[lc] = pc;
-                    wst += pc;
-                    if (d_draft && wmd != -INFINITY) {
-                        const uint4* vd = reinterpret_cast<const uint4*>(sm.dchunk(s, lc));
-                        float accd[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-                        for (int v = 0; v < NV; ++v) {
-                            float xs[E];
-                            EL::unpack(vd[v * 32 + lane], xs);
-#pragma unroll
-                            for (int e = 0; e < E; ++e)
-                                accd[e & 3] += weight(xs[e], wmd, c);
-                        }
-                        wsd += warp_sum((accd[0] + accd[1]) + (accd[2] + accd[3]));
-                    }
+                        stats[j] = make_float2(mc, sc);
                 }
+                __syncwarp();
             }
-            if (lane == 0) {
-                s_wm[cw][0] = wmt;
-                s_wm[cw][1] = wmd;
-                s_ws[cw][0] = wst;
-                s_ws[cw][1] = wsd;
-                s_wi[cw] = widx;
+            // combine this warp's chunk stats, 32 at a time
+            const int nst = load ? kw : 0;
+            float mm = -INFINITY;
+            for (int j = lane; j < nst; j += 32)
+                mm = max_nan(mm, stats[j].x);
+            const float mw = warp_max_nan(mm);
+            float sacc = 0.0f, scmp = 0.0f;
+            for (int j0 = 0; j0 < nst; j0 += 32) {
+                const int j = j0 + lane;
+                const float2 sj = j < nst ? stats[j] : make_float2(-INFINITY, 0.0f);
+                const float v = warp_sum_comp(sj.x == -INFINITY ? 0.0f : sj.y * weight(sj.x, mw, c));
+                float t, e;
+                two_sum(sacc, v, t, e);
+                sacc = t;
+                scmp += e;
             }
+            part = make_float4(broken ? NAN : mw, sacc + scmp, -INFINITY, 0.0f);
         }
-        __syncthreads();
-        // ---- warp 0: this CTA's partial (lane w = compute warp w), pushed to every rank ----
-        if (warp == 0) {
-            const bool has = lane < nwc;
-            float m0, m1, S0, S1;
-            int i0, i1;
-            combine_parts(has ? s_wm[lane][0] : -INFINITY, has ? s_ws[lane][0] : 0.0f,
-                          has ? s_wi[lane] : INT_MAX, c, m0, S0, i0);
-            combine_parts(has ? s_wm[lane][1] : -INFINITY, has ? s_ws[lane][1] : 0.0f, INT_MAX, c,
-                          m1, S1, i1);
-            if (s_bad) {   // poison this row in every CTA of the cluster
-                m0 = NAN;
-                m1 = NAN;
-            }
-            if (lane < C) {
-                const uint32_t dm = map_to_rank(smem_addr(&s_cm[xp][rank][0]), (uint32_t)lane);
-                st_cluster_f32(dm, m0);
-                st_cluster_f32(dm + 4, m1);
-                const uint32_t ds = map_to_rank(smem_addr(&s_cs[xp][rank][0]), (uint32_t)lane);
-                st_cluster_f32(ds, S0);
-                st_cluster_f32(ds + 4, S1);
-                st_cluster_s32(map_to_rank(smem_addr(&s_ci[xp][rank]), (uint32_t)lane), i0);
-                if (rank == 0 && want_claim) {
-                    const int cl = s_claim[xp];
-                    st_cluster_s32(map_to_rank(smem_addr(&s_claim[xp]), (uint32_t)lane), cl);
-                }
-                fence_cluster();   // the pushes above are released to the peers
-            }
-        }
-        cluster_arrive_relaxed();
-        cluster_wait();   // the one cluster exchange of this row (acquire)
 
-        // ---- warp 0: cluster combine (lane r = rank r) and the decision ----
-        if (warp == 0) {
-            const bool has = lane < C;
-            float m_t, m_d, St, Sd;
-            int g, unused;
-            combine_parts(has ? s_cm[xp][lane][0] : -INFINITY, has ? s_cs[xp][lane][0] : 0.0f,
-                          has ? s_ci[xp][lane] : INT_MAX, c, m_t, St, g);
-            combine_parts(has ? s_cm[xp][lane][1] : -INFINITY, has ? s_cs[xp][lane][1] : 0.0f,
-                          INT_MAX, c, m_d, Sd, unused);
-            if (lane == 0) {
-                const bool ok_t = isfinite(m_t);
-                const bool ok_d = !d_draft || isfinite(m_d);
-                RowResult res{m_t, m_d, 0.0f, 0.0f, kDecInvalid, 0};
-                if (d_greedy) {
-                    const bool row_ok = d_ok && ok_t && g < V;
-                    res.dec = !row_ok ? kDecInvalid
-                                      : (d_test ? (dc.x == g ? kDecAccept : kDecReject)
-                                                    : kDecBonus);
-                    if (rank == 0) {
-                        a.dec[trow] = (uint8_t)res.dec;
-                        a.argmax[trow] = row_ok ? g : -1;
-                        if (d_test && a.want_pq) {
-                            a.p_x[(size_t)dc.b * Kmax + dc.i] = NAN;
-                            a.q_x[(size_t)dc.b * Kmax + dc.i] = NAN;
-                        }
-                    }
-                } else {
-                    const bool row_ok =
-                        d_ok && ok_t && ok_d && St > 0.0f && (!d_draft || Sd > 0.0f);
-                    res.inv_st = row_ok ? __frcp_rn(St) : 0.0f;
-                    res.inv_sd = row_ok && d_draft ? __frcp_rn(Sd) : 0.0f;
-                    bool accept = false;
-                    float px = NAN, qx = NAN;
-                    if (d_test && row_ok) {
-                        px = __fmul_rn(weight(dc.lt_x, m_t, c), res.inv_st);
-                        qx = __fmul_rn(weight(dc.ld_x, m_d, c), res.inv_sd);
-                        accept = __fmul_rn(dc.u, qx) < px;   // u < min(1, p/q) without a division
-                    }
-                    res.dec = !row_ok ? kDecInvalid
-                                      : (d_test ? (accept ? kDecAccept : kDecReject) : kDecBonus);
-                    res.resid = row_ok && d_draft && (res.dec == kDecReject || !a.early_exit);
-                    if (rank == 0) {
-                        a.dec[trow] = (uint8_t)res.dec;
-                        a.rowstat[trow] = make_float4(m_t, res.inv_st, m_d, res.inv_sd);
-                        if (d_test && a.want_pq) {
-                            a.p_x[(size_t)dc.b * Kmax + dc.i] = px;
-                            a.q_x[(size_t)dc.b * Kmax + dc.i] = qx;
-                        }
-                    }
+        // ---- exchange: this warp's partial to every CTA of the cluster ----
+        const int myslot = (int)rank * nw + w;
+        const int claimed_b = __shfl_sync(kFull, claimed, 0);
+        if (lane < C) {
+            const uint32_t rb = map_to_rank(smem_addr(&xbar[p]), (uint32_t)lane);
+            st_async_v4(map_to_rank(smem_addr(&xbuf[p * kMaxParts + myslot]), (uint32_t)lane), part,
+                        rb);
+            if (rank == 0 && w == 0 && want_claim)
+                st_async_s32(map_to_rank(smem_addr(&xclaim[p]), (uint32_t)lane), claimed_b, rb);
+        }
+        if (!mbar_wait_bounded(smem_addr(&xbar[p]), xpar, kWaitSpins))
+            xbroken = true;
+        if (__any_sync(kFull, xbroken))
+            break;
+
+        // ---- combine all partials and decide (every warp alike) ----
+        const float4 xv = lane < P ? xbuf[p * kMaxParts + lane]
+                                   : make_float4(-INFINITY, __int_as_float(INT_MAX), -INFINITY, 0.0f);
+        const Tok tkb = shfl_tok(tk);
+        const size_t trow = (size_t)row.b * (Kmax + 1) + row.i;
+        const bool writer = rank == 0 && w == 0 && lane == 0;
+        int dec = kDecInvalid;
+        float m_t = 0.0f, m_d = 0.0f, inv_st = 0.0f, inv_sd = 0.0f;
+        bool row_ok = false;
+        if (greedy) {
+            m_t = warp_max_nan(xv.x);
+            const int g =
+                __reduce_min_sync(kFull, (lane < P && xv.x == m_t) ? __float_as_int(xv.y) : INT_MAX);
+            row_ok = usable && tkb.ok && isfinite(m_t) && g < V;
+            dec = !row_ok ? kDecInvalid : (test ? (tkb.x == g ? kDecAccept : kDecReject) : kDecBonus);
+            if (writer) {
+                a.dec[trow] = (uint8_t)dec;
+                a.argmax[trow] = row_ok ? g : -1;
+                if (test && a.want_pq) {
+                    a.p_x[(size_t)row.b * Kmax + row.i] = NAN;
+                    a.q_x[(size_t)row.b * Kmax + row.i] = NAN;
                 }
-                s_res = res;
+            }
+        } else {
+            float St, Sd;
+            combine_ms(xv.x, xv.y, c, m_t, St);
+            combine_ms(xv.z, xv.w, c, m_d, Sd);
+            row_ok = usable && tkb.ok && isfinite(m_t) && St > 0.0f &&
+                     (!draft || (isfinite(m_d) && Sd > 0.0f));
+            inv_st = row_ok ? __frcp_rn(St) : 0.0f;
+            inv_sd = row_ok && draft ? __frcp_rn(Sd) : 0.0f;
+            bool accept = false;
+            float px = NAN, qx = NAN;
+            if (test && row_ok) {
+                px = __fmul_rn(weight(tkb.lt, m_t, c), inv_st);
+                qx = __fmul_rn(weight(tkb.ld, m_d, c), inv_sd);
+                accept = __fmul_rn(tkb.u, qx) < px;   // u < min(1, p/q) without a division
+            }
+            dec = !row_ok ? kDecInvalid : (test ? (accept ? kDecAccept : kDecReject) : kDecBonus);
+            if (writer) {
+                a.dec[trow] = (uint8_t)dec;
+                a.rowstat[trow] = make_float4(m_t, inv_st, m_d, inv_sd);
+                if (test && a.want_pq) {
+                    a.p_x[(size_t)row.b * Kmax + row.i] = px;
+                    a.q_x[(size_t)row.b * Kmax + row.i] = qx;
+                }
             }
         }
-        __syncthreads();
-        const RowResult res = s_res;
-
-        // ---- next row of this slot (same decision in every thread), issued at once ----
         if (want_claim) {
-            spare = unit_valid(a, s_claim[xp]) ? s_claim[xp] : -1;
+            const int cl = xclaim[p];
+            spare = unit_valid(a, cl) ? cl : -1;
             exhausted = spare < 0;
             if (spare >= 0)
-                spare_pos = unit_pos(a, spare);
-        }
-        xp ^= 1;
-        const bool valid = res.dec == kDecAccept || res.dec == kDecReject;
-        const bool cont = !a.per_row && dc.i < dc.Kb &&
-                          (res.dec == kDecAccept || (!a.early_exit && valid));
-        SlotPos np{dc.i + 1, dc.b, dc.Kb, dc.T};
-        bool next_active = true;
-        if (!cont) {
-            if (spare >= 0) {
-                np = spare_pos;
-                spare = -1;
-            } else {
-                next_active = false;
-            }
+                spare_pos = unit_pos(a, spare);   // loads now, used when the unit starts
         }
 
-        if (cw >= 0 && !d_greedy && res.dec != kDecInvalid) {
-            // chunk sums of the weights, rescaled to the row max
-            if (lane == 0)
-                for (int lc = cw; lc < nck; lc += nwc)
-                    a.Pc[trow * a.nchunks + (c0 + lc)] =
-                        wmt == -INFINITY ? 0.0f : s_pc[lc] * weight(wmt, res.m_t, c);
-            // ---- pass 3: residual mass per chunk of rows that may be drawn from ----
-            if (res.resid) {
-                for (int lc = cw; lc < nck; lc += nwc) {
-                    const uint4* vt = reinterpret_cast<const uint4*>(sm.tchunk(s, lc));
-                    const uint4* vd = reinterpret_cast<const uint4*>(sm.dchunk(s, lc));
-                    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-                    for (int v = 0; v < NV; ++v) {
-                        float xt[E], xd[E];
-                        EL::unpack(vt[v * 32 + lane], xt);
-                        EL::unpack(vd[v * 32 + lane], xd);
-#pragma unroll
-                        for (int e = 0; e < E; ++e)
-                            acc[e & 3] += resid_term(weight(xt[e], res.m_t, c), res.inv_st,
-                                                     weight(xd[e], res.m_d, c), res.inv_sd);
-                    }
-                    const float rc = warp_sum((acc[0] + acc[1]) + (acc[2] + acc[3]));
-                    if (lane == 0)
-                        a.Rc[trow * a.nchunks + (c0 + lc)] = rc;
+        // ---- chunk sums of p for the draw (bonus rows) ----
+        if (!greedy && !test && row_ok && load) {
+            for (int j = lane; j < kw; j += 32) {
+                const float2 sj = stats[j];
+                a.Pc[trow * a.nchunks + (c0 + w + j * nw)] =
+                    sj.x == -INFINITY ? 0.0f : sj.y * weight(sj.x, m_t, c);
+            }
+        }
+        // ---- residual pass: rows that may be drawn from ----
+        if (!greedy && test && draft && row_ok && kw > 0 && !broken &&
+            (dec == kDecReject || !a.early_exit)) {
+            uint32_t r0 = q0;
+            if (!resident) {
+                r0 = qi;
+                prologue(row, true);
+            }
+            for (int j = 0; j < kw; ++j) {
+                const uint32_t q = r0 + (uint32_t)j;
+                if (!resident) {
+                    if (!broken && !wait_copy(q))
+                        broken = true;
+                    __syncwarp();
+                }
+                const int s = (int)(q % (uint32_t)R);
+                uint4 tv[NV], dv[NV];
+                load_stage<T, NV>(rg.tst(s), lane, tv);
+                load_stage<T, NV>(rg.dst(s), lane, dv);
+                __syncwarp();
+                if (!resident && j + R < kw && !broken) {
+                    issue_chunk<T, NV>(a, rg, qi, c0 + w + (j + R) * nw, tr, dr, true, lane);
+                    ++qi;
+                }
+                float rs, ps;
+                LN::resid_sums(tv, dv, m_t, inv_st, m_d, inv_sd, c, rs, ps);
+                rs = warp_sum(rs);
+                ps = warp_sum(ps);
+                if (lane == 0) {
+                    const size_t at = trow * a.nchunks + (c0 + w + j * nw);
+                    a.Rc[at] = rs;
+                    a.Pc[at] = ps;
                 }
             }
         }
-        if (tid == 0) {
-            if (s_bad && !poisoned_before)
-                atomicOr(a.err, kErrWaitTimeout);
-            // nobody reads slot s's shared state again before the barrier below
-            s_uses[s] += 1;
-            s_active[s] = next_active ? 1 : 0;
-            if (next_active)
-                s_desc[s] = schedule(a, np.i, np.b, np.Kb, np.T);
+
+        // ---- the cluster's next row (the same decision in every warp) ----
+        const bool valid = dec == kDecAccept || dec == kDecReject;
+        const bool cont = !a.per_row && row.i < row.Kb &&
+                          (dec == kDecAccept || (!a.early_exit && valid));
+        if (cont) {
+            row = make_row(a, row.i + 1, row.b, row.Kb, row.T);
+        } else if (spare >= 0) {
+            row = make_row(a, spare_pos.i, spare_pos.b, spare_pos.Kb, spare_pos.T);
+            spare = -1;
+        } else {
+            break;
         }
-        __syncthreads();   // stage s consumed; s_pc, s_w*, s_res free; slot s rescheduled
-        if (next_active) {
-            if (cw >= 0)
-                issue_row<T, NV>(a, sm, s_desc[s], s, c0, nck, cw, nwc, lane, s_bad != 0);
-            if (cw == 0 && lane == 0)
-                describe<T>(a, s_desc[s]);
-        }
-        // If the next row processed is this slot's again (one slot, or the
-        // other slots idle), its descriptor must be complete before it is read.
-        bool same_next = true;
-        for (int t = 1; t < nslot; ++t)
-            if (s_active[(s + t) % nslot]) {
-                same_next = false;
-                break;
-            }
-        if (same_next)
-            __syncthreads();
+        // copies first: the token loads of describe overlap with them
+        if ((row.flags & kFUsable) && kw > 0 && !broken)
+            prologue(row, (row.flags & kFDraft) != 0);
+        if (lane == 0)
+            tk = describe<T>(a, row);
     }
+
+    // ---- wind-down: copies still in flight (only after a timeout), then
+    // leave together, so that no CTA exits while a peer may still address it ----
+    if (broken || xbroken) {
+        if (lane == 0)
+            atomicOr(a.err, kErrWaitTimeout);
+        for (uint32_t q = qw; q < qi; ++q)
+            (void)mbar_wait_bounded(rg.bar((int)(q % (uint32_t)R)), (q / (uint32_t)R) & 1u,
+                                    kWaitSpins);
+    }
+    if (!triggered)
+        griddep_launch_dependents();
+    __syncwarp();
+    cluster_arrive();
+    cluster_wait();
 }
 
 }  // namespace sv
