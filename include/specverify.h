@@ -97,16 +97,12 @@ typedef struct {
  *                   the diagnostics differ).  0: rows a known earlier
  *                   rejection makes irrelevant are skipped.
  *   chunks_per_cta  0: automatic.  Otherwise the number of vocabulary chunks
- *                   each CTA of a row's cluster sweeps (tuning: sets the
- *                   cluster size, at most 16; SV_ERR_UNSUPPORTED beyond).
+ *                   each CTA of a row's cluster holds (tuning: sets the
+ *                   cluster size, at most 16; SV_ERR_UNSUPPORTED when the
+ *                   row's slice then does not fit in shared memory).
  *   chunks_per_warp 0: automatic.  Otherwise how many of the CTA's chunks
- *                   each warp sweeps (tuning: sets the warps per CTA, at most
+ *                   each warp holds (tuning: sets the warps per CTA, at most
  *                   16 and at most 32 / cluster size).
- *   ring_stages     0: automatic.  Otherwise the shared-memory stages of each
- *                   warp's copy ring (tuning, 1..8; capped by the warp's
- *                   chunks).  A warp whose chunks all fit in its ring keeps
- *                   them for the residual pass; otherwise that pass reads
- *                   them again.
  * Tuning options change only the fp32 summation grouping: results agree
  * with the automatic geometry except within the rounding of those sums.
  */
@@ -115,7 +111,6 @@ typedef struct {
     int32_t verify_all;
     int32_t chunks_per_cta;
     int32_t chunks_per_warp;
-    int32_t ring_stages;
 } sv_options;
 
 /* Human-readable name of a status code (static storage). */
@@ -130,21 +125,20 @@ int32_t sv_max_vocab(sv_dtype dtype);
 /*
  * Launch geometry a call of this shape would use on the current device
  * (diagnostic; queries the device, queues no work).  out8 receives:
- *   [0] cluster size C (CTAs per row), [1] vocabulary chunks per CTA,
- *   [2] ring stages per warp, [3] clusters in the persistent grid,
+ *   [0] cluster size C (CTAs per row), [1] warps per CTA,
+ *   [2] vocabulary chunks per warp, [3] clusters in the persistent grid,
  *   [4] threads per CTA, [5] dynamic shared memory per CTA (bytes),
- *   [6] 1 if work is claimed per row (small batches), 0 per sequence,
- *   [7] vocabulary chunks per row.
+ *   [6] warps whose range holds chunks, [7] vocabulary chunks per row.
  * Zero tuning arguments select the automatic choice (as in sv_options).
  */
 sv_status sv_geometry(int32_t B, int32_t Kmax, int32_t V, sv_dtype dtype, int32_t chunks_per_cta,
-                      int32_t chunks_per_warp, int32_t ring_stages, int32_t* out8);
+                      int32_t chunks_per_warp, int32_t* out8);
 
 /*
  * Bytes of device workspace spec_verify_ws / spec_verify_ex need for this
- * shape (0 on invalid arguments).  The workspace holds per-row statistics,
- * per-chunk partial sums, per-sequence counters and the uploaded K; each call
- * re-initialises what it uses, so the buffer needs no clearing.
+ * shape (0 on invalid arguments).  The workspace holds the per-call header:
+ * the error word, the claim counter, K and the order in which sequences are
+ * claimed; each call uploads it afresh, so the buffer needs no clearing.
  */
 size_t sv_workspace_size(int32_t B, int32_t Kmax, int32_t V, sv_dtype dtype);
 

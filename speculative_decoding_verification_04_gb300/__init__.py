@@ -49,8 +49,7 @@ class SVDiag(ctypes.Structure):
 
 class SVOptions(ctypes.Structure):
     _fields_ = [("diag", SVDiag), ("verify_all", ctypes.c_int32),
-                ("chunks_per_cta", ctypes.c_int32), ("chunks_per_warp", ctypes.c_int32),
-                ("ring_stages", ctypes.c_int32)]
+                ("chunks_per_cta", ctypes.c_int32), ("chunks_per_warp", ctypes.c_int32)]
 
 
 def _load():
@@ -82,7 +81,7 @@ def _load():
     lib.sv_abi_version.restype = i32
     lib.sv_workspace_errors.argtypes = [P, ctypes.POINTER(ctypes.c_uint32), P]
     lib.sv_workspace_errors.restype = ctypes.c_int
-    lib.sv_geometry.argtypes = [i32, i32, i32, ctypes.c_int, i32, i32, i32, P]
+    lib.sv_geometry.argtypes = [i32, i32, i32, ctypes.c_int, i32, i32, P]
     lib.sv_geometry.restype = ctypes.c_int
     _lib = lib
     return lib
@@ -105,16 +104,16 @@ def sv_max_vocab(dtype: int) -> int:
     return int(_load().sv_max_vocab(int(dtype)))
 
 
-GEOMETRY_FIELDS = ("cluster_ctas", "chunks_per_cta", "ring_stages", "clusters", "threads",
-                   "smem_bytes", "per_row", "chunks")
+GEOMETRY_FIELDS = ("cluster_ctas", "warps", "chunks_per_warp", "clusters", "threads",
+                   "smem_bytes", "warp_ranges", "chunks")
 
 
 def sv_geometry(B: int, Kmax: int, V: int, dtype: int, chunks_per_cta: int = 0,
-                chunks_per_warp: int = 0, ring_stages: int = 0) -> dict:
+                chunks_per_warp: int = 0) -> dict:
     """Launch geometry a call of this shape would use on the current device."""
     out = (ctypes.c_int32 * 8)()
     st = _load().sv_geometry(int(B), int(Kmax), int(V), int(dtype), int(chunks_per_cta),
-                             int(chunks_per_warp), int(ring_stages), out)
+                             int(chunks_per_warp), out)
     _check(st, "sv_geometry")
     return dict(zip(GEOMETRY_FIELDS, [int(v) for v in out]))
 
@@ -270,7 +269,7 @@ def spec_verify_ws(target, draft, draft_tokens, uniforms, temperature, K, worksp
 
 def spec_verify_ex(target, draft, draft_tokens, uniforms, temperature, K, workspace: Workspace,
                    diag: dict | None = None, verify_all: bool = False, chunks_per_cta: int = 0,
-                   chunks_per_warp: int = 0, ring_stages: int = 0, out_tokens=None,
+                   chunks_per_warp: int = 0, out_tokens=None,
                    out_num_accepted=None, stream=None):
     """spec_verify_ex; ``diag`` maps p_x / q_x / resid_mass / final_row to tensors."""
     k, kp, B, Kmax, V = _common(target, draft, draft_tokens, uniforms, temperature, K)
@@ -285,7 +284,6 @@ def spec_verify_ex(target, draft, draft_tokens, uniforms, temperature, K, worksp
     opt.verify_all = 1 if verify_all else 0
     opt.chunks_per_cta = int(chunks_per_cta)
     opt.chunks_per_warp = int(chunks_per_warp)
-    opt.ring_stages = int(ring_stages)
     sp, _ = _stream(stream)
     st = _load().spec_verify_ex(_dptr(target), _dptr(draft), _dtype_code(target),
                                 _dptr(draft_tokens), _dptr(uniforms), _dptr(temperature), B, kp, V,

@@ -13,10 +13,9 @@
 //  * issoh.co.jp "Speculative Decoding（投機的デコーディング）とは？…", section
 //    受理・棄却の規則と出力分布が変わらない理由, steps 1-5.
 //
-// One call = one small host-to-device copy (zeroed counters and the per-
-// sequence K) + the persistent cluster sweep (sv_sweep.cuh) + the warp-per-
-// sequence finalisation (sv_finalize.cuh), launched back to back on the
-// caller's stream with programmatic dependent launch.
+// One call = one small host-to-device copy (zeroed counters, the per-sequence
+// K and the claim order) + one launch of the persistent cluster kernel
+// (sv_sweep.cuh), which also draws the tokens and writes the outputs.
 #include <cuda_runtime.h>
 #include <string.h>
 
@@ -27,7 +26,6 @@
 #include <vector>
 
 #include "../../include/specverify.h"
-#include "sv_finalize.cuh"
 #include "sv_sweep.cuh"
 
 namespace sv {
@@ -36,20 +34,17 @@ namespace sv {
 // host side
 // ---------------------------------------------------------------------------
 constexpr int kSmemPerCtaMax = 227 * 1024;   // opt-in dynamic shared memory limit
-constexpr int kMaxVocab = 1 << 22;           // vocabulary limit of the ABI (int32 indices stay small)
-constexpr int kAutoRing = 4;                 // default stages per warp
-constexpr int kAutoWarps = 4;                // default warps per CTA
-constexpr int kAutoCluster = 8;              // default CTAs per row
+// A row (target and draft) must fit, resident, in the shared memory of one
+// cluster of 16 CTAs: these limits leave room for the slices' rounding.
+constexpr int kMaxVocabBf16 = 786432;
+constexpr int kMaxVocabF32 = 393216;
 
 struct Geom {
     int s = 0, nv = 0, ch = 0, nchunks = 0;
-    int ncpc = 0;       // chunks per CTA
     int C = 0;          // CTAs per cluster (per row)
     int nw = 0;         // warps per CTA
-    int R = 0;          // ring stages per warp
-    int kw = 0;         // most chunks of one warp
+    int kw = 0;         // chunks per warp (one contiguous range)
     int clusters = 0;   // persistent grid size (clusters)
-    int per_row = 0;    // clusters claim rows (small batches) instead of sequences
     size_t smem = 0;
 };
 
@@ -74,9 +69,9 @@ static int n_chunks(int V, int s)
     return (V + ch - 1) / ch;
 }
 
-// ---- workspace layout ----
+// ---- workspace layout: the per-call header, uploaded by every call ----
 struct WsLayout {
-    size_t err, next_unit, dec, K, order, header_end, argmax, rowstat, Pc, Rc, total;
+    size_t err, next_unit, K, order, header_end, total;
 };
 
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -85,20 +80,15 @@ static bool ws_layout(int B, int Kmax, int V, sv_dtype dt, WsLayout* L)
 {
     if (B < 0 || Kmax < 0 || Kmax > SV_K_MAX || V < 1)
         return false;
-    const size_t R = (size_t)B * (size_t)(Kmax + 1);
-    const size_t nch = (size_t)n_chunks(V, elem_size(dt));
+    (void)V;
+    (void)dt;
     size_t o = 0;
     L->err = o;
     L->next_unit = o + 4;
     o = align256(o + 16);
-    L->dec = o;      o = align256(o + R);
     L->K = o;        o = align256(o + (size_t)B * 4);
     L->order = o;    o = align256(o + (size_t)B * 4);
     L->header_end = o;
-    L->argmax = o;   o = align256(o + R * 4);
-    L->rowstat = o;  o = align256(o + R * 16);
-    L->Pc = o;       o = align256(o + R * nch * 4);
-    L->Rc = o;       o = align256(o + R * nch * 4);
     L->total = o;
     return true;
 }
@@ -200,23 +190,24 @@ static cudaError_t capacity_nv(const Geom& g, int dev, int* n)
     }
 }
 
-// Geometry for a cluster size C (balanced chunks per CTA), nw warps per CTA
-// and R stages per warp; false if it does not fit.
-static bool shape_geometry(int V, sv_dtype dt, int C, int nw, int R, Geom* g)
+// Geometry for C CTAs of nw warps per row: P = C * nw warp ranges of kw
+// chunks each; false if it does not fit.
+static bool shape_geometry(int V, sv_dtype dt, int C, int nw, Geom* g)
 {
     const int s = elem_size(dt);
     g->s = s;
     g->nv = pick_nv(V, s);
     g->ch = 32 * g->nv * (16 / s);
     g->nchunks = (V + g->ch - 1) / g->ch;
-    C = std::max(1, std::min(C, std::min(kMaxCluster, g->nchunks)));
-    g->ncpc = (g->nchunks + C - 1) / C;
-    g->C = (g->nchunks + g->ncpc - 1) / g->ncpc;   // no CTA without chunks
-    nw = std::max(1, std::min(nw, std::min(kMaxWarps, kMaxParts / g->C)));
-    g->nw = std::min(nw, g->ncpc);
-    g->kw = (g->ncpc + g->nw - 1) / g->nw;
-    g->R = std::max(1, std::min(R, std::min(kMaxRing, g->kw)));
-    g->smem = sweep_layout(g->nw, g->R, g->ch * s, g->kw).total;
+    if (C < 1 || C > kMaxCluster || nw < 1 || nw > kMaxWarps || C * nw > kMaxParts)
+        return false;
+    g->C = C;
+    g->nw = nw;
+    g->kw = (g->nchunks + C * nw - 1) / (C * nw);
+    // no CTA without chunks
+    if ((long long)(C - 1) * nw * g->kw >= g->nchunks)
+        return false;
+    g->smem = sweep_layout(nw, g->kw, g->ch * s).total;
     return g->smem <= (size_t)kSmemPerCtaMax;
 }
 
@@ -227,13 +218,16 @@ static sv_status capacity_of(const Geom& g, sv_dtype dt, int dev, int* cap)
     return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
-// Pick the geometry of one launch (cached per shape).  Tuning overrides:
-// chunks per CTA (sets C), chunks per warp (sets nw), ring stages.
+// Pick the geometry of one launch (cached per shape).  Every cluster size and
+// warp count that fits is considered; a row's slice stays resident from its
+// copy to its decision, so the device holds as many rows at once as clusters
+// fit.  Score: rows in flight (resident clusters, up to B), then more warps
+// per row (shorter passes), then larger clusters.  Tuning overrides: chunks
+// per CTA (sets C), chunks per warp (sets the warps per CTA).
 static sv_status pick_geometry(int V, sv_dtype dt, int B, int Kmax, int override_ncpc,
-                               int want_cpw, int want_ring, int dev, Geom* g)
+                               int want_cpw, int dev, Geom* g)
 {
-    const auto key = std::make_tuple(dev, V, (int)dt, B, Kmax, override_ncpc * 64 + want_ring,
-                                     want_cpw);
+    const auto key = std::make_tuple(dev, V, (int)dt, B, Kmax, override_ncpc, want_cpw);
     {
         std::lock_guard<std::mutex> lk(g_mu);
         auto it = g_pick.find(key);
@@ -244,37 +238,45 @@ static sv_status pick_geometry(int V, sv_dtype dt, int B, int Kmax, int override
     }
     const int s = elem_size(dt);
     const int nch = n_chunks(V, s);
-    int C = kAutoCluster;
-    if (override_ncpc > 0)
-        C = (nch + override_ncpc - 1) / override_ncpc;
-    int nw = kAutoWarps;
-    if (want_cpw > 0) {
-        const int ncpc = (nch + std::min(C, nch) - 1) / std::min(C, nch);
-        nw = (ncpc + want_cpw - 1) / want_cpw;
+    Geom best;
+    long long best_score = -1;
+    for (int C = 1; C <= kMaxCluster; ++C) {
+        if (override_ncpc > 0 && C != (nch + override_ncpc - 1) / override_ncpc)
+            continue;
+        for (int nw = 1; nw <= kMaxWarps && C * nw <= kMaxParts; ++nw) {
+            if (want_cpw > 0) {
+                const int ncpc = (nch + C - 1) / C;
+                if (nw != std::min((ncpc + want_cpw - 1) / want_cpw, kMaxParts / C))
+                    continue;
+            }
+            Geom t;
+            if (!shape_geometry(V, dt, C, nw, &t))
+                continue;
+            int cap = 0;
+            const sv_status st = capacity_of(t, dt, dev, &cap);
+            if (st != SV_OK)
+                return st;
+            if (cap <= 0)
+                continue;
+            t.clusters = std::min(cap, std::max(1, B));
+            const long long score = ((long long)t.clusters * 64 + C * nw) * 32 + C;
+            if (score > best_score) {
+                best_score = score;
+                best = t;
+            }
+        }
     }
-    const int R = want_ring > 0 ? want_ring : kAutoRing;
-    Geom t;
-    if (C > kMaxCluster || !shape_geometry(V, dt, C, nw, R, &t))
+    (void)Kmax;
+    if (best_score < 0)
         return SV_ERR_UNSUPPORTED;
-    int cap = 0;
-    const sv_status st = capacity_of(t, dt, dev, &cap);
-    if (st != SV_OK)
-        return st;
-    if (cap <= 0)
-        return SV_ERR_UNSUPPORTED;
-    // sequences are the units unless there are fewer of them than clusters
-    const long long rows = (long long)B * (Kmax + 1);
-    t.per_row = B < cap ? 1 : 0;
-    const long long units = t.per_row ? rows : (long long)B;
-    t.clusters = (int)std::min<long long>(cap, std::max<long long>(1, units));
     std::lock_guard<std::mutex> lk(g_mu);
-    g_pick[key] = t;
-    *g = t;
+    g_pick[key] = best;
+    *g = best;
     return SV_OK;
 }
 
 template <typename T, int NV>
-static cudaError_t launch_pair(const Args& a, const Geom& g, cudaStream_t st, int dev)
+static cudaError_t launch_sweep(const Args& a, const Geom& g, cudaStream_t st, int dev)
 {
     cudaError_t e = prepare_kernels<T, NV>(dev);
     if (e != cudaSuccess)
@@ -282,29 +284,16 @@ static cudaError_t launch_pair(const Args& a, const Geom& g, cudaStream_t st, in
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[1];
     sweep_config(&cfg, attr, g, g.clusters, st);
-    e = cudaLaunchKernelEx(&cfg, sv_sweep_kernel<T, NV>, a);
-    if (e != cudaSuccess)
-        return e;
-    cudaLaunchConfig_t fcfg = {};
-    fcfg.gridDim = dim3((unsigned)((a.B + kFinalizeWarps - 1) / kFinalizeWarps), 1, 1);
-    fcfg.blockDim = dim3(kFinalizeWarps * 32, 1, 1);
-    fcfg.dynamicSmemBytes = 0;
-    fcfg.stream = st;
-    cudaLaunchAttribute fattr[1];
-    fattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    fattr[0].val.programmaticStreamSerializationAllowed = 1;
-    fcfg.attrs = fattr;
-    fcfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&fcfg, sv_finalize_kernel<T, NV>, a);
+    return cudaLaunchKernelEx(&cfg, sv_sweep_kernel<T, NV>, a);
 }
 
 template <typename T>
 static cudaError_t launch_nv(const Args& a, const Geom& g, cudaStream_t st, int dev)
 {
     switch (g.nv) {
-    case 1: return launch_pair<T, 1>(a, g, st, dev);
-    case 2: return launch_pair<T, 2>(a, g, st, dev);
-    default: return launch_pair<T, 4>(a, g, st, dev);
+    case 1: return launch_sweep<T, 1>(a, g, st, dev);
+    case 2: return launch_sweep<T, 2>(a, g, st, dev);
+    default: return launch_sweep<T, 4>(a, g, st, dev);
     }
 }
 
@@ -472,7 +461,7 @@ static sv_status run(const Call& c, int kmax, const sv_options* opt, void* ws, s
         return SV_ERR_INVALID_ARG;
     Geom g;
     st = pick_geometry(c.V, c.dtype, c.B, kmax, opt ? opt->chunks_per_cta : 0,
-                       opt ? opt->chunks_per_warp : 0, opt ? opt->ring_stages : 0, dev, &g);
+                       opt ? opt->chunks_per_warp : 0, dev, &g);
     if (st != SV_OK)
         return st;
     if ((long long)g.clusters * g.C > 0x7fffffffLL)
@@ -533,12 +522,8 @@ static sv_status run(const Call& c, int kmax, const sv_options* opt, void* ws, s
     a.B = c.B;
     a.Kmax = kmax;
     a.V = c.V;
-    a.per_row = g.per_row;
-    a.n_units = g.per_row ? c.B * (kmax + 1) : c.B;
     a.nchunks = g.nchunks;
-    a.ncpc = g.ncpc;
     a.C = g.C;
-    a.ring = g.R;
     a.kw = g.kw;
     a.early_exit = (want_diag || (opt && opt->verify_all)) ? 0 : 1;
     a.has_draft = c.drf != nullptr ? 1 : 0;
@@ -546,13 +531,8 @@ static sv_status run(const Call& c, int kmax, const sv_options* opt, void* ws, s
     a.aligned = ((al & 15) == 0) && (((size_t)c.V * g.s) % 16 == 0);
     a.err = reinterpret_cast<uint32_t*>(base + L.err);
     a.next_unit = reinterpret_cast<int*>(base + L.next_unit);
-    a.dec = base + L.dec;
     a.K = reinterpret_cast<const int32_t*>(base + L.K);
     a.order = reinterpret_cast<const int32_t*>(base + L.order);
-    a.argmax = reinterpret_cast<int32_t*>(base + L.argmax);
-    a.rowstat = reinterpret_cast<float4*>(base + L.rowstat);
-    a.Pc = reinterpret_cast<float*>(base + L.Pc);
-    a.Rc = reinterpret_cast<float*>(base + L.Rc);
     a.p_x = want_diag ? dg->p_x : nullptr;
     a.q_x = want_diag ? dg->q_x : nullptr;
     a.resid = want_diag ? dg->resid_mass : nullptr;
@@ -567,7 +547,7 @@ static sv_status run(const Call& c, int kmax, const sv_options* opt, void* ws, s
 }
 
 // Launch geometry a call would use (for reports and tests).
-static sv_status geometry_of(int B, int Kmax, int V, sv_dtype dt, int ncpc, int cpw, int ring,
+static sv_status geometry_of(int B, int Kmax, int V, sv_dtype dt, int ncpc, int cpw,
                              int32_t* out)
 {
     int dev = 0, nsm = 0;
@@ -575,16 +555,16 @@ static sv_status geometry_of(int B, int Kmax, int V, sv_dtype dt, int ncpc, int 
     if (st != SV_OK)
         return st;
     Geom g;
-    st = pick_geometry(V, dt, B, Kmax, ncpc, cpw, ring, dev, &g);
+    st = pick_geometry(V, dt, B, Kmax, ncpc, cpw, dev, &g);
     if (st != SV_OK)
         return st;
     out[0] = g.C;
-    out[1] = g.ncpc;
-    out[2] = g.R;
+    out[1] = g.nw;
+    out[2] = g.kw;
     out[3] = g.clusters;
     out[4] = 32 * g.nw;
     out[5] = (int32_t)g.smem;
-    out[6] = g.per_row;
+    out[6] = (g.nchunks + g.kw - 1) / g.kw;   // warp ranges holding chunks
     out[7] = g.nchunks;
     return SV_OK;
 }
@@ -615,19 +595,19 @@ int32_t sv_max_vocab(sv_dtype dtype)
 {
     if (dtype != SV_DTYPE_F32 && dtype != SV_DTYPE_BF16)
         return 0;
-    return sv::kMaxVocab;
+    return dtype == SV_DTYPE_BF16 ? sv::kMaxVocabBf16 : sv::kMaxVocabF32;
 }
 
 sv_status sv_geometry(int32_t B, int32_t Kmax, int32_t V, sv_dtype dtype, int32_t chunks_per_cta,
-                      int32_t chunks_per_warp, int32_t ring_stages, int32_t* out8)
+                      int32_t chunks_per_warp, int32_t* out8)
 {
     if (!out8 || B < 1 || Kmax < 0 || Kmax > SV_K_MAX || V < 1 || chunks_per_cta < 0 ||
-        chunks_per_warp < 0 || ring_stages < 0 ||
+        chunks_per_warp < 0 ||
         (dtype != SV_DTYPE_F32 && dtype != SV_DTYPE_BF16))
         return SV_ERR_INVALID_ARG;
     if (V > sv_max_vocab(dtype))
         return SV_ERR_UNSUPPORTED;
-    return sv::geometry_of(B, Kmax, V, dtype, chunks_per_cta, chunks_per_warp, ring_stages, out8);
+    return sv::geometry_of(B, Kmax, V, dtype, chunks_per_cta, chunks_per_warp, out8);
 }
 
 size_t sv_workspace_size(int32_t B, int32_t Kmax, int32_t V, sv_dtype dtype)
@@ -653,8 +633,7 @@ sv_status spec_verify_ex(const void* target_logits, const void* draft_logits, sv
     const sv_status st = sv::check_args(c, &kmax);
     if (st != SV_OK)
         return st;
-    if (options && (options->chunks_per_cta < 0 || options->ring_stages < 0 ||
-                    options->chunks_per_warp < 0))
+    if (options && (options->chunks_per_cta < 0 || options->chunks_per_warp < 0))
         return SV_ERR_INVALID_ARG;
     return sv::run(c, kmax, options, workspace, workspace_bytes, stream);
 }

@@ -17,12 +17,8 @@ constexpr unsigned kFull = 0xffffffffu;
 constexpr int kMaxWarps = 16;
 constexpr int kMaxCluster = 16;
 constexpr uint32_t kWaitSpins = 1u << 22;   // bounded mbarrier polls (a few seconds)
-constexpr double kLog2e = 1.4426950408889634;
-constexpr int kFinalizeWarps = 4;           // sequences per finalize CTA
-
-// Per-row decision written by the sweep and read by the finaliser.
-enum : uint8_t {
-    kDecNone = 0,      // row not evaluated in this call
+// Decision of one row.
+enum : int {
     kDecAccept = 1,
     kDecReject = 2,
     kDecInvalid = 3,   // unusable input on this row
@@ -40,11 +36,9 @@ struct Args {
     int32_t* out_tok;
     int32_t* out_n;
     int B, Kmax, V;
-    int per_row;           // 1: clusters claim single rows; 0: whole sequences
-    int n_units;           // claimable units: B sequences, or B * (Kmax + 1) rows
-    int nchunks, ncpc, C;  // chunks per row, chunks per CTA, CTAs per cluster
-    int ring;              // shared-memory stages per warp
-    int kw;                // most chunks any warp owns (stride of its chunk statistics)
+    int nchunks;           // vocabulary chunks per row
+    int C;                 // CTAs per cluster (one row at a time per cluster)
+    int kw;                // chunks per warp (a contiguous range)
     int early_exit, aligned;
     // Which optional buffers were supplied.  Decided on the host: device code
     // never branches on a pointer's null-ness.
@@ -55,13 +49,8 @@ struct Args {
     // workspace
     uint32_t* err;
     int* next_unit;        // claim counter of the persistent sweep
-    uint8_t* dec;          // per row decision
     const int32_t* K;
     const int32_t* order;  // sequences in claim order (longest K first)
-    int32_t* argmax;       // per row (greedy)
-    float4* rowstat;       // per row: m_t, 1/S_t, m_d, 1/S_d
-    float* Pc;             // per (row, chunk): sum of exp2((l - m_t) c)
-    float* Rc;             // per (row, chunk): sum of max(0, p - q)
     // diagnostics (nullable)
     float* p_x;
     float* q_x;
@@ -185,15 +174,23 @@ struct CompSum {
     __device__ __forceinline__ float value() const { return s + c; }
 };
 
-__device__ __forceinline__ double warp_incl_scan(double v, int lane)
+// Compensated inclusive prefix sum across the warp (lane order): lane l gets
+// s + c ~ v_0 + ... + v_l, with the rounding error of the additions kept in c.
+__device__ __forceinline__ void warp_incl_scan_comp(float v, int lane, float& s, float& c)
 {
+    s = v;
+    c = 0.0f;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const double y = __shfl_up_sync(kFull, v, o);
-        if (lane >= o)
-            v += y;
+        const float so = __shfl_up_sync(kFull, s, o);
+        const float co = __shfl_up_sync(kFull, c, o);
+        if (lane >= o) {
+            float t, e;
+            two_sum(so, s, t, e);
+            s = t;
+            c = (co + c) + e;
+        }
     }
-    return v;
 }
 
 __device__ __forceinline__ bool temperature_usable(float T)

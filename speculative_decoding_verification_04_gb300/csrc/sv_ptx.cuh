@@ -229,6 +229,13 @@ __device__ __forceinline__ void st_async_v4(uint32_t addr, float4 v, uint32_t mb
         ::"r"(addr), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(mbar) : "memory");
 }
 
+__device__ __forceinline__ void st_async_v2(uint32_t addr, float2 v, uint32_t mbar)
+{
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];"
+        ::"r"(addr), "f"(v.x), "f"(v.y), "r"(mbar) : "memory");
+}
+
 __device__ __forceinline__ void st_async_s32(uint32_t addr, int v, uint32_t mbar)
 {
     asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];"

@@ -1,23 +1,22 @@
-// sv_sweep.cuh -- the persistent vocabulary-sweep kernel.
+// sv_sweep.cuh -- the persistent verification kernel.
 //
-// A grid of thread-block clusters (C CTAs each, as many as the device holds at
-// once) works through the batch one row (sequence b, position i) at a time per
-// cluster.  CTA r of a cluster owns the vocabulary chunks [r*ncpc, (r+1)*ncpc)
-// of every row; warp w of the CTA owns every nw-th of those chunks and streams
-// them through its own ring of R shared-memory stages (target and draft chunk
-// per stage), filled by 1-D bulk copies (cp.async.bulk) that complete on one
-// mbarrier per stage.  No two warps share a stage, so the steady state has no
-// CTA-wide barrier at all.
+// A grid of thread-block clusters (C CTAs of nw warps each, as many as the
+// device holds at once) works through the batch one row (sequence b, position
+// i) at a time per cluster.  The row's vocabulary is cut into P = C * nw
+// contiguous ranges of kw chunks; warp g = rank * nw + w owns range g and
+// keeps its slice of the row (target and draft) resident in its own slot of
+// shared memory, filled by one 1-D bulk copy (cp.async.bulk) per array that
+// completes on the slot's mbarrier.  No two warps share data, so the steady
+// state has no CTA-wide barrier at all.
 //
 // Schedule: a cluster walks one sequence's positions in order.  Row i+1 is
 // read only once x_i has been accepted (the method's own early exit: rows after
 // the first rejection are never read).  Fresh sequences come from one atomic
 // claim per sequence (longest K first), made a row ahead by rank 0 and handed
-// to the cluster with that row's exchange.  When there are fewer sequences
-// than clusters, clusters claim single rows instead (all positions at once).
+// to the cluster with that row's exchange.
 //
-// Per row, each warp makes one pass over its chunks, from the stage straight
-// into registers:
+// Per row, each warp makes one pass over its slice, from shared memory
+// straight into registers:
 //   greedy row       lane max (packed bf16x2 / three-input fp32 max) and the
 //                    lowest index holding it;
 //   tested sampling  lane-online max and sum of exp2((l - m) log2(e)/T) of the
@@ -27,45 +26,61 @@
 // exchange  every warp pushes a 16-byte partial to every CTA of the cluster
 //           with st.async, completing on the receiver's exchange mbarrier
 //           (double-buffered by row parity);
-// decide    every warp combines all C*nw partials (identical arithmetic, so
+// decide    every warp combines all P partials (identical arithmetic, so
 //           identical results) and decides u q(x) < p(x), or x == argmax at
 //           temperature 0;
-// residual  rejected rows (every tested row in verify-all mode): per-chunk
-//           sums of max(0, p - q) and of p from the ring -- still resident
-//           when the warp's chunks fit in it, read again through it otherwise.
-// Results go to the workspace; sv_finalize draws the tokens.
+// residual  rejected rows (every tested row in verify-all mode): per-chunk sums
+//           of max(0, p - q) and of p from the resident slice, and a second
+//           exchange of the per-warp totals;
+// draw      at the sequence's final row the warp whose range holds u * S (a
+//           compensated prefix over the warps, then over its chunks, then
+//           over lane spans of one chunk) picks the token by inverse CDF from
+//           its resident slice and writes the sequence's outputs.
 #pragma once
 
 #include "sv_common.cuh"
 
 namespace sv {
 
-constexpr int kMaxRing = 8;    // ring stages per warp
-constexpr int kMaxParts = 32;  // C * nw partials per row: one per lane in the combine
+constexpr int kMaxParts = 32;   // warps per cluster: one per lane in the combines
 
 // Dynamic shared memory of one CTA (host and device compute it alike).
 struct SweepLayout {
-    size_t stage_bytes;   // one stage: target chunk + draft chunk
-    size_t bars;          // [nw][R] stage mbarriers
-    size_t xbar;          // [2] exchange mbarriers
-    size_t xbuf;          // [2][kMaxParts] float4 partials
-    size_t xclaim;        // [2] int: unit claimed by rank 0 during the row
-    size_t first;         // [2] int: first unit of the cluster (one used)
-    size_t stats;         // [nw][kw] float2: per-chunk (max, sum) of bonus rows
+    size_t slot_bytes;   // one warp's resident slice: kw target chunks, kw draft chunks
+    size_t bars;         // [nw] slot mbarriers
+    size_t xbar;         // [2] exchange mbarriers: row partials
+    size_t xbar2;        // [2] exchange mbarriers: residual totals
+    size_t xbuf;         // [2][kMaxParts] float4 row partials
+    size_t xbuf2;        // [2][kMaxParts] float2 residual totals
+    size_t xclaim;       // [2] int: unit claimed by rank 0 during the row
+    size_t first;        // int: the cluster's first unit
+    size_t stats;        // [nw][kw] float2: per-chunk statistics for the draw
     size_t total;
 };
 
-__host__ __device__ inline SweepLayout sweep_layout(int nw, int R, int chunk_bytes, int kw)
+__host__ __device__ inline SweepLayout sweep_layout(int nw, int kw, int chunk_bytes)
 {
     SweepLayout L;
-    L.stage_bytes = 2 * (size_t)chunk_bytes;
-    L.bars = (size_t)nw * R * L.stage_bytes;
-    L.xbar = L.bars + (size_t)nw * R * 8;
-    L.xbuf = (L.xbar + 16 + 15) & ~(size_t)15;
-    L.xclaim = L.xbuf + 2 * kMaxParts * 16;
-    L.first = L.xclaim + 8;
-    L.stats = L.first + 8;
-    L.total = L.stats + (size_t)nw * kw * 8;
+    L.slot_bytes = 2 * (size_t)kw * (size_t)chunk_bytes;
+    size_t o = (size_t)nw * L.slot_bytes;
+    L.bars = o;
+    o += (size_t)nw * 8;
+    L.xbar = o;
+    o += 16;
+    L.xbar2 = o;
+    o += 16;
+    o = (o + 15) & ~(size_t)15;
+    L.xbuf = o;
+    o += 2 * kMaxParts * 16;
+    L.xbuf2 = o;
+    o += 2 * kMaxParts * 8;
+    L.xclaim = o;
+    o += 8;
+    L.first = o;
+    o += 8;
+    L.stats = o;
+    o += (size_t)nw * kw * 8;
+    L.total = o;
     return L;
 }
 
@@ -98,16 +113,16 @@ __device__ __forceinline__ Row make_row(const Args& a, int i, int b, int Kb, flo
     return r;
 }
 
-// What the decision needs besides the sums: the proposed token, its uniform
-// and the two logits at the token.  Loaded by one lane a row ahead.
+// The row's proposal, held by lane 0 of every warp: token and uniform (loaded
+// when the row's copies are issued) and the two logits at the token (loaded
+// once the slice has arrived, so from L2).
 struct Tok {
     int x;
     float u, lt, ld;
     int ok;
 };
 
-template <typename T>
-__device__ __forceinline__ Tok describe(const Args& a, const Row& r)
+__device__ __forceinline__ Tok tok_of(const Args& a, const Row& r)
 {
     Tok t{0, 0.0f, 0.0f, 0.0f, 0};
     if (!(r.flags & kFUsable))
@@ -116,22 +131,26 @@ __device__ __forceinline__ Tok describe(const Args& a, const Row& r)
         t.ok = 1;
         return t;
     }
-    const int x = __ldg(a.tok + (size_t)r.b * a.Kmax + r.i);
-    bool ok = x >= 0 && x < a.V;
+    t.x = __ldg(a.tok + (size_t)r.b * a.Kmax + r.i);
+    bool ok = t.x >= 0 && t.x < a.V;
     if (!(r.flags & kFGreedy)) {
         t.u = __ldg(a.uni + (size_t)r.b * (a.Kmax + 1) + r.i);
         ok = ok && t.u >= 0.0f && t.u < 1.0f;
     }
-    if (ok) {
-        const size_t trow = (size_t)r.b * (a.Kmax + 1) + r.i;
-        t.lt = Elem<T>::load(static_cast<const T*>(a.tgt) + trow * (size_t)a.V + x);
-        if (r.flags & kFDraft)
-            t.ld = Elem<T>::load(static_cast<const T*>(a.drf) +
-                                 ((size_t)r.b * a.Kmax + r.i) * (size_t)a.V + x);
-    }
-    t.x = x;
     t.ok = ok ? 1 : 0;
     return t;
+}
+
+template <typename T>
+__device__ __forceinline__ void tok_logits(const Args& a, const Row& r, Tok& t)
+{
+    if (!t.ok || !(r.flags & kFTest))
+        return;
+    const size_t trow = (size_t)r.b * (a.Kmax + 1) + r.i;
+    t.lt = Elem<T>::load(static_cast<const T*>(a.tgt) + trow * (size_t)a.V + t.x);
+    if (r.flags & kFDraft)
+        t.ld = Elem<T>::load(static_cast<const T*>(a.drf) +
+                             ((size_t)r.b * a.Kmax + r.i) * (size_t)a.V + t.x);
 }
 
 __device__ __forceinline__ Tok shfl_tok(const Tok& t)
@@ -145,56 +164,36 @@ __device__ __forceinline__ Tok shfl_tok(const Tok& t)
     return o;
 }
 
-// Claim the next unit of work (one thread): a sequence id in claim order, or
-// a live row index i * B + b when clusters claim single rows.  -1: none left.
-// Anything outside the unit range also reads as -1, so a unit id can never
-// index past the batch.
-__device__ __forceinline__ int claim_unit(const Args& a)
+// Claims (one thread): a ticket now, its sequence later (the ticket's value
+// is not waited for until the sequence is needed).  Tickets past the batch,
+// or anything out of range, read as -1.
+__device__ __forceinline__ int claim_ticket(const Args& a) { return atomicAdd(a.next_unit, 1); }
+
+__device__ __forceinline__ int ticket_unit(const Args& a, int t)
 {
-    for (;;) {
-        const int u = atomicAdd(a.next_unit, 1);
-        if (u < 0 || u >= a.n_units)
-            return -1;
-        if (!a.per_row) {
-            const int b = __ldg(a.order + u);
-            return (b >= 0 && b < a.B) ? b : -1;
-        }
-        const int i = u / a.B;
-        if (i <= __ldg(a.K + (u - i * a.B)))
-            return u;
-    }
+    if (t < 0 || t >= a.B)
+        return -1;
+    const int b = __ldg(a.order + t);
+    return (b >= 0 && b < a.B) ? b : -1;
 }
 
-__device__ __forceinline__ bool unit_valid(const Args& a, int u)
-{
-    return u >= 0 && u < (a.per_row ? a.n_units : a.B);
-}
-
-// First row of a claimed (valid) unit, with its sequence's K_b and T loaded
-// but not yet used (the flags are made when the unit starts).
+// A sequence's first row: K_b and T loaded at claim time, used when it starts.
 struct UnitPos {
-    int i, b, Kb;
+    int b, Kb;
     float T;
 };
 
-__device__ __forceinline__ UnitPos unit_pos(const Args& a, int unit)
+__device__ __forceinline__ UnitPos unit_pos(const Args& a, int b)
 {
-    UnitPos p;
-    p.i = 0;
-    p.b = unit;
-    if (a.per_row) {
-        p.i = unit / a.B;
-        p.b = unit - p.i * a.B;
-    }
-    p.Kb = __ldg(a.K + p.b);
-    p.T = __ldg(a.temp + p.b);
-    return p;
+    return UnitPos{b, __ldg(a.K + b), __ldg(a.temp + b)};
 }
 
-__device__ __forceinline__ Row unit_row(const Args& a, int unit)
+// The sequence's final-draw uniform (slot K_b), sampling sequences only.
+__device__ __forceinline__ float final_uniform(const Args& a, const Row& r)
 {
-    const UnitPos p = unit_pos(a, unit);
-    return make_row(a, p.i, p.b, p.Kb, p.T);
+    if ((r.flags & kFGreedy) || !(r.flags & kFUsable))
+        return 0.0f;
+    return __ldg(a.uni + (size_t)r.b * (a.Kmax + 1) + r.Kb);
 }
 
 // ---------------------------------------------------------------------------
@@ -359,64 +358,15 @@ template <int NV> struct Lane<float, NV> {
     }
 };
 
-// ---------------------------------------------------------------------------
-// one warp's ring of stages
-// ---------------------------------------------------------------------------
-template <typename T, int NV>
-struct Ring {
-    static constexpr int CH = 32 * NV * Elem<T>::E;
-    T* base;          // this warp's R stages
-    uint64_t* bars;   // this warp's R mbarriers
-    int R;
-    __device__ T* tst(int s) const { return base + (size_t)s * 2 * CH; }
-    __device__ T* dst(int s) const { return base + (size_t)s * 2 * CH + CH; }
-    __device__ uint32_t bar(int s) const { return smem_addr(&bars[s]); }
-};
-
-// Copy number q (stage q % R) brings global chunk gc of a row: the
-// 16-byte-aligned body by bulk copy, the ragged tail (or the whole chunk when
-// rows are not 16-byte aligned) by element loads, -inf past V.  The stage's
-// previous contents have been consumed by this warp (whole warp calls).
-template <typename T, int NV>
-__device__ __forceinline__ void issue_chunk(const Args& a, const Ring<T, NV>& rg, uint32_t q,
-                                            int gc, const T* trow, const T* drow, bool load_d,
-                                            int lane)
+// one element of a slice in shared memory, as fp32
+__device__ __forceinline__ float sm_elem(const float* p) { return *p; }
+__device__ __forceinline__ float sm_elem(const __nv_bfloat16* p)
 {
-    using EL = Elem<T>;
-    constexpr int CH = Ring<T, NV>::CH;
-    const int s = (int)(q % (uint32_t)rg.R);
-    const int e0 = gc * CH;
-    const int n = min(CH, a.V - e0);
-    const int nb = a.aligned ? ((n * (int)sizeof(T)) & ~15) / (int)sizeof(T) : 0;
-    T* dt = rg.tst(s);
-    T* dd = rg.dst(s);
-    if (lane == 0) {
-        const uint32_t bytes = (uint32_t)nb * (uint32_t)sizeof(T);
-        const uint32_t tx = bytes * (load_d ? 2u : 1u);
-        if (tx) {
-            fence_proxy_async();
-            mbar_arrive_expect_tx(rg.bar(s), tx);
-            bulk_copy_g2s(smem_addr(dt), trow + e0, bytes, rg.bar(s));
-            if (load_d)
-                bulk_copy_g2s(smem_addr(dd), drow + e0, bytes, rg.bar(s));
-        } else {
-            mbar_arrive(rg.bar(s));
-        }
-    }
-    for (int j = nb + lane; j < n; j += 32) {
-        EL::copy(dt + j, trow + e0 + j);
-        if (load_d)
-            EL::copy(dd + j, drow + e0 + j);
-    }
-    for (int j = n + lane; j < CH; j += 32) {
-        EL::set_neg_inf(dt + j);
-        if (load_d)
-            EL::set_neg_inf(dd + j);
-    }
+    return __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const unsigned short*>(p)) << 16);
 }
 
 template <typename T, int NV>
-__device__ __forceinline__ void load_stage(const T* p, int lane, uint4 (&v)[NV])
+__device__ __forceinline__ void load_chunk(const T* p, int lane, uint4 (&v)[NV])
 {
     const uint4* q = reinterpret_cast<const uint4*>(p);
 #pragma unroll
@@ -432,6 +382,50 @@ __device__ __forceinline__ void combine_ms(float m_part, float s_part, float c, 
     S = warp_sum_comp(m_part == -INFINITY ? 0.0f : s_part * weight(m_part, m, c));
 }
 
+// Inverse-CDF selection over `n` non-negative masses D(0..n-1), one warp:
+// the smallest j with t < D(0) + ... + D(j), sums compensated, 32 at a time.
+// `t` is reduced to the mass left inside the selected entry.  If t lies beyond
+// the total (rounding), the last positive entry is taken and *beyond is set.
+// Returns -1 if no entry is positive.  Every lane gets the same result.
+template <typename F>
+__device__ __forceinline__ int select_cdf(int n, F D, float& t, bool& beyond, int lane)
+{
+    int last_pos = -1;
+    if (!beyond) {
+        float base_s = 0.0f, base_c = 0.0f;   // compensated mass of earlier groups
+        for (int j0 = 0; j0 < n; j0 += 32) {
+            const int j = j0 + lane;
+            const float d = j < n ? D(j) : 0.0f;
+            if (d > 0.0f)
+                last_pos = j;
+            float s, c;
+            warp_incl_scan_comp(d, lane, s, c);
+            const float rel = (t - base_s) - base_c;   // mass left after earlier groups
+            const unsigned hit = __ballot_sync(kFull, j < n && rel < s + c);
+            if (hit) {
+                const int src = __ffs(hit) - 1;
+                const float ex_s = __shfl_sync(kFull, s, src), ex_c = __shfl_sync(kFull, c, src);
+                const float dd = __shfl_sync(kFull, d, src);
+                t = rel - ((ex_s - dd) + ex_c);   // mass left inside the entry
+                return j0 + src;
+            }
+            const float gs = __shfl_sync(kFull, s, 31), gc = __shfl_sync(kFull, c, 31);
+            float ts, te;
+            two_sum(base_s, gs, ts, te);
+            base_s = ts;
+            base_c += gc + te;
+        }
+    } else {
+        for (int j0 = 0; j0 < n; j0 += 32) {
+            const int j = j0 + lane;
+            if (j < n && D(j) > 0.0f)
+                last_pos = j;
+        }
+    }
+    beyond = true;
+    return __reduce_max_sync(kFull, last_pos);
+}
+
 template <typename T, int NV>
 __global__ void __launch_bounds__(kMaxWarps * 32) sv_sweep_kernel(const Args a)
 {
@@ -439,151 +433,187 @@ __global__ void __launch_bounds__(kMaxWarps * 32) sv_sweep_kernel(const Args a)
     using LN = Lane<T, NV>;
     constexpr int E = EL::E;
     constexpr int CH = 32 * NV * E;
+    constexpr int SPAN = CH / 32;   // contiguous elements per lane in the draw
     extern __shared__ __align__(128) unsigned char dsm[];
 
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const int nw = (int)(blockDim.x >> 5);
-    const int C = a.C, V = a.V, Kmax = a.Kmax, R = a.ring;
-    const int P = C * nw;   // partials per row
+    const int C = a.C, V = a.V, Kmax = a.Kmax, KW = a.kw;
+    const int P = C * nw;   // warps per row
     const uint32_t rank = cluster_ctarank();
-    const int c0 = (int)rank * a.ncpc;
-    const int nck = max(0, min(a.ncpc, a.nchunks - c0));
-    const int kw = w < nck ? (nck - w + nw - 1) / nw : 0;   // chunks of this warp
-    const bool resident = kw <= R;                          // residual pass needs no re-read
-    const SweepLayout L = sweep_layout(nw, R, CH * (int)sizeof(T), a.kw);
+    const int g = (int)rank * nw + w;   // this warp's range of the row
+    const int c_lo = min(g * KW, a.nchunks);
+    const int kwm = min(c_lo + KW, a.nchunks) - c_lo;   // chunks in range (0..KW)
+    const int e0 = c_lo * CH;                           // first element of the range
+    const int n_el = max(0, min(e0 + kwm * CH, V) - e0);
+    const SweepLayout L = sweep_layout(nw, KW, CH * (int)sizeof(T));
 
-    Ring<T, NV> rg;
-    rg.base = reinterpret_cast<T*>(dsm) + (size_t)w * R * 2 * CH;
-    rg.bars = reinterpret_cast<uint64_t*>(dsm + L.bars) + (size_t)w * R;
-    rg.R = R;
+    T* slot_t = reinterpret_cast<T*>(dsm + (size_t)w * L.slot_bytes);
+    T* slot_d = slot_t + (size_t)KW * CH;
+    const uint32_t bar = smem_addr(dsm + L.bars + 8 * (size_t)w);
     uint64_t* xbar = reinterpret_cast<uint64_t*>(dsm + L.xbar);
-    float4* xbuf = reinterpret_cast<float4*>(dsm + L.xbuf);   // [2][kMaxParts]
-    int* xclaim = reinterpret_cast<int*>(dsm + L.xclaim);     // [2]
-    int* first = reinterpret_cast<int*>(dsm + L.first);       // [2]
-    float2* stats = reinterpret_cast<float2*>(dsm + L.stats) + (size_t)w * a.kw;
+    uint64_t* xbar2 = reinterpret_cast<uint64_t*>(dsm + L.xbar2);
+    float4* xbuf = reinterpret_cast<float4*>(dsm + L.xbuf);    // [2][kMaxParts]
+    float2* xbuf2 = reinterpret_cast<float2*>(dsm + L.xbuf2);  // [2][kMaxParts]
+    int* xclaim = reinterpret_cast<int*>(dsm + L.xclaim);      // [2]
+    int* first = reinterpret_cast<int*>(dsm + L.first);
+    float2* stats = reinterpret_cast<float2*>(dsm + L.stats) + (size_t)w * KW;
 
-    // ---- set-up: barriers, then the first unit from rank 0 (one per cluster:
-    // taking a spare here as well would leave clusters idle when there are
-    // fewer than twice as many units as clusters) ----
+    // ---- set-up: barriers; -inf past V in this warp's range (copies never
+    // write there); the cluster's first unit from rank 0 ----
     if (lane == 0) {
-        for (int s = 0; s < R; ++s)
-            mbar_init(rg.bar(s), 1);
+        mbar_init(bar, 1);
         if (w == 0) {
             mbar_init(smem_addr(&xbar[0]), 1);
             mbar_init(smem_addr(&xbar[1]), 1);
+            mbar_init(smem_addr(&xbar2[0]), 1);
+            mbar_init(smem_addr(&xbar2[1]), 1);
         }
         fence_mbar_init();
+    }
+    for (int j = n_el + lane; j < kwm * CH; j += 32) {
+        EL::set_neg_inf(slot_t + j);
+        EL::set_neg_inf(slot_d + j);
     }
     __syncthreads();
     cluster_arrive();   // every CTA's barriers exist before any peer signals them
     int f0 = -1;
     if (rank == 0 && w == 0) {
         if (lane == 0)
-            f0 = claim_unit(a);
+            f0 = ticket_unit(a, claim_ticket(a));
         f0 = __shfl_sync(kFull, f0, 0);
     }
     cluster_wait();
-    if (rank == 0 && w == 0 && lane < C) {
-        const uint32_t dst = map_to_rank(smem_addr(first), (uint32_t)lane);
-        st_cluster_s32(dst, f0);
-    }
+    if (rank == 0 && w == 0 && lane < C)
+        st_cluster_s32(map_to_rank(smem_addr(first), (uint32_t)lane), f0);
     cluster_arrive();
     cluster_wait();
 
     // ---- per-warp schedule state (the same in every warp of the cluster) ----
-    bool active = unit_valid(a, first[0]);
-    int spare = -1;   // claimed during the first row
-    UnitPos spare_pos{0, 0, 0, 0.0f};
+    const int u0 = first[0];
+    bool active = u0 >= 0 && u0 < a.B;
+    int spare = -1;
+    UnitPos spare_pos{0, 0, 0.0f};
     bool exhausted = false;
-    bool triggered = false;
-    bool broken = false;     // a stage wait gave up: no more copies, rows poisoned
+    bool broken = false;     // a slot wait gave up: no more copies, rows poisoned
     bool xbroken = false;    // an exchange wait gave up: leave the loop
-    Row row = active ? unit_row(a, first[0]) : make_row(a, 0, 0, 0, 0.0f);
-    Tok tk{0, 0.0f, 0.0f, 0.0f, 0};
-    uint32_t qi = 0;   // copies issued by this warp
-    uint32_t qw = 0;   // copies waited for by this warp
-    // bound on the rows a cluster can process (guards the loop after a timeout)
-    const long long max_rows = (long long)a.n_units * (Kmax + 1) + 2;
+    bool drawn = false;      // the current sequence's outputs are written
+    Row row = make_row(a, 0, 0, 0, 0.0f);
+    if (active) {
+        const UnitPos p0 = unit_pos(a, u0);
+        row = make_row(a, 0, p0.b, p0.Kb, p0.T);
+    }
+    Tok tk{0, 0.0f, 0.0f, 0.0f, 0};   // lane 0
+    float uf = 0.0f;                  // lane 0: the sequence's final uniform
+    int ticket = -1;                  // rank 0, warp 0, lane 0
+    uint32_t uses = 0;                // completed slot fills (mbarrier phase)
+    bool pending = false;             // a slot fill is in flight
+    uint32_t k2 = 0;                  // residual exchanges so far
+    const long long max_rows = (long long)a.B * (Kmax + 1) + 2;
 
     const T* tgt = static_cast<const T*>(a.tgt);
     const T* drf = static_cast<const T*>(a.drf);
-    auto row_ptrs = [&](const Row& r, const T*& tr, const T*& dr) {
-        tr = tgt + ((size_t)r.b * (Kmax + 1) + r.i) * (size_t)V;
-        dr = (r.flags & kFDraft) ? drf + ((size_t)r.b * Kmax + r.i) * (size_t)V : nullptr;
+    const bool writer = rank == 0 && w == 0;   // writes per-row results and short outputs
+
+    // copies of this warp's range of row r into the slot (whole warp)
+    auto issue = [&](const Row& r) {
+        if (!(r.flags & kFUsable) || broken || n_el <= 0)
+            return;
+        const bool ld = (r.flags & kFDraft) != 0;
+        const T* tr = tgt + ((size_t)r.b * (Kmax + 1) + r.i) * (size_t)V + e0;
+        const T* dr = ld ? drf + ((size_t)r.b * Kmax + r.i) * (size_t)V + e0 : nullptr;
+        const int nb = a.aligned ? ((n_el * (int)sizeof(T)) & ~15) / (int)sizeof(T) : 0;
+        if (lane == 0) {
+            const uint32_t bytes = (uint32_t)nb * (uint32_t)sizeof(T);
+            const uint32_t tx = bytes * (ld ? 2u : 1u);
+            if (tx) {
+                fence_proxy_async();
+                mbar_arrive_expect_tx(bar, tx);
+                bulk_copy_g2s(smem_addr(slot_t), tr, bytes, bar);
+                if (ld)
+                    bulk_copy_g2s(smem_addr(slot_d), dr, bytes, bar);
+            } else {
+                mbar_arrive(bar);
+            }
+        }
+        for (int j = nb + lane; j < n_el; j += 32) {
+            EL::copy(slot_t + j, tr + j);
+            if (ld)
+                EL::copy(slot_d + j, dr + j);
+        }
+        pending = true;
     };
-    // first copies of a pass over a row (copy numbers qi, qi + 1, ...)
-    auto prologue = [&](const Row& r, bool with_d) {
-        const T* tr;
-        const T* dr;
-        row_ptrs(r, tr, dr);
-        const int n = min(R, kw);
-        for (int j = 0; j < n; ++j)
-            issue_chunk<T, NV>(a, rg, qi + (uint32_t)j, c0 + w + j * nw, tr, dr, with_d, lane);
-        qi += (uint32_t)n;
-    };
-    // wait for copy q (whole warp); false if any lane gave up (the copy then
-    // stays outstanding for the wind-down)
-    auto wait_copy = [&](uint32_t q) -> bool {
-        const bool ok = mbar_wait_bounded(rg.bar((int)(q % (uint32_t)R)), (q / (uint32_t)R) & 1u,
-                                          kWaitSpins);
+    // wait for the slot fill (whole warp); false if any lane gave up
+    auto wait_slot = [&]() -> bool {
+        const bool ok = mbar_wait_bounded(bar, uses & 1u, kWaitSpins);
         const bool all = !__any_sync(kFull, !ok);
-        if (all)
-            qw = q + 1;
+        if (all) {
+            pending = false;
+            ++uses;
+        }
+        __syncwarp();
         return all;
+    };
+    // outputs of sequence b: draft tokens before n, `token` at n, -1 after
+    auto write_outputs = [&](int b, int n, int token) {
+        const bool bad = token < 0;
+        int32_t* orow = a.out_tok + (size_t)b * (Kmax + 1);
+        for (int j = lane; j <= Kmax; j += 32)
+            orow[j] = bad ? -1 : (j < n ? __ldg(a.tok + (size_t)b * Kmax + j) : (j == n ? token : -1));
+        if (lane == 0) {
+            a.out_n[b] = bad ? -1 : n;
+            if (a.want_final)
+                a.final_row[b] = bad ? -1 : n;
+        }
     };
 
     if (active) {
-        if ((row.flags & kFUsable) && kw > 0)
-            prologue(row, (row.flags & kFDraft) != 0);
-        if (lane == 0)
-            tk = describe<T>(a, row);
+        issue(row);
+        if (lane == 0) {
+            tk = tok_of(a, row);
+            uf = final_uniform(a, row);
+        }
     }
 
     for (long long k = 0; active && k < max_rows; ++k) {
-        if (exhausted && !triggered) {   // the finaliser may start launching
-            griddep_launch_dependents();
-            triggered = true;
-        }
         const int p = (int)(k & 1);
         const uint32_t xpar = (uint32_t)((k >> 1) & 1);
         const bool greedy = (row.flags & kFGreedy) != 0;
         const bool test = (row.flags & kFTest) != 0;
         const bool draft = (row.flags & kFDraft) != 0;
         const bool usable = (row.flags & kFUsable) != 0;
-        const bool load = usable && !broken && kw > 0;
         const float c = (usable && !greedy) ? log2e_over(row.T) : 0.0f;
         const bool want_claim = spare < 0 && !exhausted;
         if (w == 0 && lane == 0)
             mbar_arrive_expect_tx(smem_addr(&xbar[p]), (uint32_t)P * 16u + (want_claim ? 4u : 0u));
-        int claimed = -1;
-        if (rank == 0 && w == 0 && lane == 0 && want_claim)
-            claimed = claim_unit(a);
-        const T* tr;
-        const T* dr;
-        row_ptrs(row, tr, dr);
+        if (writer && lane == 0 && want_claim)
+            ticket = claim_ticket(a);
 
-        // ---- one pass over this warp's chunks ----
-        float4 part = make_float4(-INFINITY, 0.0f, -INFINITY, 0.0f);
-        const uint32_t q0 = qi - (uint32_t)(load ? min(R, kw) : 0);   // this row's first copy
+        // ---- the slice, then the proposal's logits and the claim's sequence ----
+        bool have = false;
+        if (pending) {
+            have = wait_slot();
+            if (!have)
+                broken = true;
+        }
+        if (lane == 0)
+            tok_logits<T>(a, row, tk);
+        int claimed = -1;
+        if (writer && lane == 0 && want_claim)
+            claimed = ticket_unit(a, ticket);
+
+        // ---- one pass over this warp's slice ----
+        float4 part = make_float4(-INFINITY, __int_as_float(INT_MAX), -INFINITY, 0.0f);
         if (greedy) {
             float gm = -INFINITY;
             int gi = INT_MAX;
-            if (load) {
-                for (int j = 0; j < kw; ++j) {
-                    const uint32_t q = q0 + (uint32_t)j;
-                    if (!broken && !wait_copy(q))
-                        broken = true;
-                    __syncwarp();
+            if (have) {
+                for (int j = 0; j < kwm; ++j) {
                     uint4 tv[NV];
-                    load_stage<T, NV>(rg.tst((int)(q % (uint32_t)R)), lane, tv);
-                    __syncwarp();
-                    if (j + R < kw && !broken) {
-                        issue_chunk<T, NV>(a, rg, qi, c0 + w + (j + R) * nw, tr, dr, false, lane);
-                        ++qi;
-                    }
+                    load_chunk<T, NV>(slot_t + (size_t)j * CH, lane, tv);
                     const float cm = LN::max(tv);
                     if (cm > gm) {   // strictly greater: an earlier index keeps a tie
-                        const int gbase = (c0 + w + j * nw) * CH;
+                        const int gbase = e0 + j * CH;
                         int found = INT_MAX;
 #pragma unroll
                         for (int e = NV * E - 1; e >= 0; --e)   // the lowest match wins
@@ -598,94 +628,69 @@ __global__ void __launch_bounds__(kMaxWarps * 32) sv_sweep_kernel(const Args a)
             }
             const float m = warp_max_nan(gm);
             const int gidx = __reduce_min_sync(kFull, gm == m ? gi : INT_MAX);
-            part = make_float4(broken ? NAN : m, __int_as_float(gidx), -INFINITY, 0.0f);
+            part = make_float4(m, __int_as_float(gidx), -INFINITY, 0.0f);
         } else if (test) {
             float mt = -INFINITY, st = 0.0f, md = -INFINITY, sd = 0.0f;
-            if (load) {
-                for (int j = 0; j < kw; ++j) {
-                    const uint32_t q = q0 + (uint32_t)j;
-                    if (!broken && !wait_copy(q))
-                        broken = true;
-                    __syncwarp();
-                    const int s = (int)(q % (uint32_t)R);
+            if (have) {
+                for (int j = 0; j < kwm; ++j) {
                     uint4 tv[NV], dv[NV];
-                    load_stage<T, NV>(rg.tst(s), lane, tv);
-                    if (draft)
-                        load_stage<T, NV>(rg.dst(s), lane, dv);
-                    __syncwarp();
-                    if (j + R < kw && !broken) {
-                        issue_chunk<T, NV>(a, rg, qi, c0 + w + (j + R) * nw, tr, dr, draft, lane);
-                        ++qi;
-                    }
+                    load_chunk<T, NV>(slot_t + (size_t)j * CH, lane, tv);
+                    load_chunk<T, NV>(slot_d + (size_t)j * CH, lane, dv);
                     const float nt = max_nan(mt, LN::max(tv));
                     if (nt != mt) {   // the lane max grew (or turned NaN): rescale the sum
                         st = mt == -INFINITY ? 0.0f : st * weight(mt, nt, c);
                         mt = nt;
                     }
                     st += LN::exp_sum(tv, mt == -INFINITY ? 0.0f : mt, c);
-                    if (draft) {
-                        const float nd = max_nan(md, LN::max(dv));
-                        if (nd != md) {
-                            sd = md == -INFINITY ? 0.0f : sd * weight(md, nd, c);
-                            md = nd;
-                        }
-                        sd += LN::exp_sum(dv, md == -INFINITY ? 0.0f : md, c);
+                    const float nd = max_nan(md, LN::max(dv));
+                    if (nd != md) {
+                        sd = md == -INFINITY ? 0.0f : sd * weight(md, nd, c);
+                        md = nd;
                     }
+                    sd += LN::exp_sum(dv, md == -INFINITY ? 0.0f : md, c);
                 }
             }
             float m1, S1, m2, S2;
             combine_ms(mt, st, c, m1, S1);
             combine_ms(md, sd, c, m2, S2);
-            part = make_float4(broken ? NAN : m1, S1, m2, S2);
+            part = make_float4(m1, S1, m2, S2);
         } else {
             // bonus row: per-chunk (max, sum) of the target, kept for the draw
-            if (load) {
-                for (int j = 0; j < kw; ++j) {
-                    const uint32_t q = q0 + (uint32_t)j;
-                    if (!broken && !wait_copy(q))
-                        broken = true;
-                    __syncwarp();
+            float mm = -INFINITY;
+            if (have) {
+                for (int j = 0; j < kwm; ++j) {
                     uint4 tv[NV];
-                    load_stage<T, NV>(rg.tst((int)(q % (uint32_t)R)), lane, tv);
-                    __syncwarp();
-                    if (j + R < kw && !broken) {
-                        issue_chunk<T, NV>(a, rg, qi, c0 + w + (j + R) * nw, tr, dr, false, lane);
-                        ++qi;
-                    }
+                    load_chunk<T, NV>(slot_t + (size_t)j * CH, lane, tv);
                     const float mc = warp_max_nan(LN::max(tv));
                     const float sc = mc == -INFINITY ? 0.0f : warp_sum(LN::exp_sum(tv, mc, c));
                     if (lane == 0)
                         stats[j] = make_float2(mc, sc);
+                    mm = max_nan(mm, mc);
                 }
                 __syncwarp();
             }
-            // combine this warp's chunk stats, 32 at a time
-            const int nst = load ? kw : 0;
-            float mm = -INFINITY;
-            for (int j = lane; j < nst; j += 32)
-                mm = max_nan(mm, stats[j].x);
-            const float mw = warp_max_nan(mm);
+            // this warp's total, compensated over its chunks, 32 at a time
             float sacc = 0.0f, scmp = 0.0f;
-            for (int j0 = 0; j0 < nst; j0 += 32) {
+            for (int j0 = 0; j0 < (have ? kwm : 0); j0 += 32) {
                 const int j = j0 + lane;
-                const float2 sj = j < nst ? stats[j] : make_float2(-INFINITY, 0.0f);
-                const float v = warp_sum_comp(sj.x == -INFINITY ? 0.0f : sj.y * weight(sj.x, mw, c));
+                const float2 sj = j < kwm ? stats[j] : make_float2(-INFINITY, 0.0f);
+                const float v = warp_sum_comp(sj.x == -INFINITY ? 0.0f : sj.y * weight(sj.x, mm, c));
                 float t, e;
                 two_sum(sacc, v, t, e);
                 sacc = t;
                 scmp += e;
             }
-            part = make_float4(broken ? NAN : mw, sacc + scmp, -INFINITY, 0.0f);
+            part = make_float4(mm, sacc + scmp, -INFINITY, 0.0f);
         }
+        if (broken)
+            part.x = NAN;   // poisons the row in every warp of the cluster
 
         // ---- exchange: this warp's partial to every CTA of the cluster ----
-        const int myslot = (int)rank * nw + w;
         const int claimed_b = __shfl_sync(kFull, claimed, 0);
         if (lane < C) {
             const uint32_t rb = map_to_rank(smem_addr(&xbar[p]), (uint32_t)lane);
-            st_async_v4(map_to_rank(smem_addr(&xbuf[p * kMaxParts + myslot]), (uint32_t)lane), part,
-                        rb);
-            if (rank == 0 && w == 0 && want_claim)
+            st_async_v4(map_to_rank(smem_addr(&xbuf[p * kMaxParts + g]), (uint32_t)lane), part, rb);
+            if (writer && want_claim)
                 st_async_s32(map_to_rank(smem_addr(&xclaim[p]), (uint32_t)lane), claimed_b, rb);
         }
         if (!mbar_wait_bounded(smem_addr(&xbar[p]), xpar, kWaitSpins))
@@ -697,24 +702,19 @@ __global__ void __launch_bounds__(kMaxWarps * 32) sv_sweep_kernel(const Args a)
         const float4 xv = lane < P ? xbuf[p * kMaxParts + lane]
                                    : make_float4(-INFINITY, __int_as_float(INT_MAX), -INFINITY, 0.0f);
         const Tok tkb = shfl_tok(tk);
-        const size_t trow = (size_t)row.b * (Kmax + 1) + row.i;
-        const bool writer = rank == 0 && w == 0 && lane == 0;
+        const size_t pos = (size_t)row.b * Kmax + row.i;   // diagnostics index (test rows)
         int dec = kDecInvalid;
+        int gtok = -1;
         float m_t = 0.0f, m_d = 0.0f, inv_st = 0.0f, inv_sd = 0.0f;
         bool row_ok = false;
         if (greedy) {
             m_t = warp_max_nan(xv.x);
-            const int g =
-                __reduce_min_sync(kFull, (lane < P && xv.x == m_t) ? __float_as_int(xv.y) : INT_MAX);
-            row_ok = usable && tkb.ok && isfinite(m_t) && g < V;
-            dec = !row_ok ? kDecInvalid : (test ? (tkb.x == g ? kDecAccept : kDecReject) : kDecBonus);
-            if (writer) {
-                a.dec[trow] = (uint8_t)dec;
-                a.argmax[trow] = row_ok ? g : -1;
-                if (test && a.want_pq) {
-                    a.p_x[(size_t)row.b * Kmax + row.i] = NAN;
-                    a.q_x[(size_t)row.b * Kmax + row.i] = NAN;
-                }
+            gtok = __reduce_min_sync(kFull, (lane < P && xv.x == m_t) ? __float_as_int(xv.y) : INT_MAX);
+            row_ok = usable && tkb.ok && isfinite(m_t) && gtok < V;
+            dec = !row_ok ? kDecInvalid : (test ? (tkb.x == gtok ? kDecAccept : kDecReject) : kDecBonus);
+            if (writer && lane == 0 && test && a.want_pq) {
+                a.p_x[pos] = NAN;
+                a.q_x[pos] = NAN;
             }
         } else {
             float St, Sd;
@@ -732,97 +732,215 @@ __global__ void __launch_bounds__(kMaxWarps * 32) sv_sweep_kernel(const Args a)
                 accept = __fmul_rn(tkb.u, qx) < px;   // u < min(1, p/q) without a division
             }
             dec = !row_ok ? kDecInvalid : (test ? (accept ? kDecAccept : kDecReject) : kDecBonus);
-            if (writer) {
-                a.dec[trow] = (uint8_t)dec;
-                a.rowstat[trow] = make_float4(m_t, inv_st, m_d, inv_sd);
-                if (test && a.want_pq) {
-                    a.p_x[(size_t)row.b * Kmax + row.i] = px;
-                    a.q_x[(size_t)row.b * Kmax + row.i] = qx;
-                }
+            if (writer && lane == 0 && test && a.want_pq) {
+                a.p_x[pos] = px;
+                a.q_x[pos] = qx;
             }
         }
         if (want_claim) {
             const int cl = xclaim[p];
-            spare = unit_valid(a, cl) ? cl : -1;
+            spare = (cl >= 0 && cl < a.B) ? cl : -1;
             exhausted = spare < 0;
             if (spare >= 0)
                 spare_pos = unit_pos(a, spare);   // loads now, used when the unit starts
         }
 
-        // ---- chunk sums of p for the draw (bonus rows) ----
-        if (!greedy && !test && row_ok && load) {
-            for (int j = lane; j < kw; j += 32) {
-                const float2 sj = stats[j];
-                a.Pc[trow * a.nchunks + (c0 + w + j * nw)] =
-                    sj.x == -INFINITY ? 0.0f : sj.y * weight(sj.x, m_t, c);
-            }
-        }
-        // ---- residual pass: rows that may be drawn from ----
-        if (!greedy && test && draft && row_ok && kw > 0 && !broken &&
-            (dec == kDecReject || !a.early_exit)) {
-            uint32_t r0 = q0;
-            if (!resident) {
-                r0 = qi;
-                prologue(row, true);
-            }
-            for (int j = 0; j < kw; ++j) {
-                const uint32_t q = r0 + (uint32_t)j;
-                if (!resident) {
-                    if (!broken && !wait_copy(q))
-                        broken = true;
-                    __syncwarp();
-                }
-                const int s = (int)(q % (uint32_t)R);
+        // ---- residual pass: rows that may be drawn from (resident slice) ----
+        const bool resid_pass = !greedy && test && draft && row_ok && !broken &&
+                                (dec == kDecReject || !a.early_exit);
+        float S_R = 0.0f;
+        float2 wtot = make_float2(0.0f, 0.0f);   // lane j: warp j's (residual, p) totals
+        if (resid_pass) {
+            float rs_s = 0.0f, rs_c = 0.0f, ps_s = 0.0f, ps_c = 0.0f;
+            for (int j = 0; j < kwm; ++j) {
                 uint4 tv[NV], dv[NV];
-                load_stage<T, NV>(rg.tst(s), lane, tv);
-                load_stage<T, NV>(rg.dst(s), lane, dv);
-                __syncwarp();
-                if (!resident && j + R < kw && !broken) {
-                    issue_chunk<T, NV>(a, rg, qi, c0 + w + (j + R) * nw, tr, dr, true, lane);
-                    ++qi;
-                }
+                load_chunk<T, NV>(slot_t + (size_t)j * CH, lane, tv);
+                load_chunk<T, NV>(slot_d + (size_t)j * CH, lane, dv);
                 float rs, ps;
                 LN::resid_sums(tv, dv, m_t, inv_st, m_d, inv_sd, c, rs, ps);
                 rs = warp_sum(rs);
                 ps = warp_sum(ps);
-                if (lane == 0) {
-                    const size_t at = trow * a.nchunks + (c0 + w + j * nw);
-                    a.Rc[at] = rs;
-                    a.Pc[at] = ps;
+                if (lane == 0)
+                    stats[j] = make_float2(rs, ps);
+                float t, e;
+                two_sum(rs_s, rs, t, e);
+                rs_s = t;
+                rs_c += e;
+                two_sum(ps_s, ps, t, e);
+                ps_s = t;
+                ps_c += e;
+            }
+            __syncwarp();
+            const int p2 = (int)(k2 & 1);
+            const uint32_t par2 = (k2 >> 1) & 1u;
+            ++k2;
+            if (w == 0 && lane == 0)
+                mbar_arrive_expect_tx(smem_addr(&xbar2[p2]), (uint32_t)P * 8u);
+            if (lane < C) {
+                const uint32_t rb = map_to_rank(smem_addr(&xbar2[p2]), (uint32_t)lane);
+                const uint32_t dst = map_to_rank(smem_addr(&xbuf2[p2 * kMaxParts + g]), (uint32_t)lane);
+                st_async_v2(dst, make_float2(rs_s + rs_c, ps_s + ps_c), rb);
+            }
+            if (!mbar_wait_bounded(smem_addr(&xbar2[p2]), par2, kWaitSpins))
+                xbroken = true;
+            if (__any_sync(kFull, xbroken))
+                break;
+            wtot = lane < P ? xbuf2[p2 * kMaxParts + lane] : make_float2(0.0f, 0.0f);
+            S_R = warp_sum_comp(wtot.x);
+        }
+        if (writer && lane == 0 && test && a.want_resid)
+            a.resid[pos] = resid_pass ? S_R : NAN;
+
+        // ---- the sequence's final row: its token and outputs ----
+        if (!drawn && dec != kDecAccept) {
+            drawn = true;
+            const int n = row.i;
+            const float ufb = __shfl_sync(kFull, uf, 0);
+            if (dec == kDecInvalid || (!greedy && !(ufb >= 0.0f && ufb < 1.0f))) {
+                if (writer)
+                    write_outputs(row.b, n, -1);
+            } else if (greedy) {
+                if (writer)
+                    write_outputs(row.b, n, gtok);
+            } else {
+                // per-warp masses of the distribution drawn from: the residual
+                // (zero residual mass: p of the same row), or p at the bonus row
+                const bool bonus = dec == kDecBonus;
+                const bool use_r = !bonus && S_R > 0.0f;
+                float Wj = 0.0f;
+                if (lane < P)
+                    Wj = bonus ? (xv.x == -INFINITY ? 0.0f : xv.y * weight(xv.x, m_t, c))
+                               : (use_r ? wtot.x : wtot.y);
+                // the warp whose range holds u * S (lane j holds warp j's mass)
+                float t = 0.0f;
+                bool beyond = false;
+                int owner = -1;
+                {
+                    float s, cc;
+                    warp_incl_scan_comp(Wj, lane, s, cc);
+                    const float S = __shfl_sync(kFull, s, 31) + __shfl_sync(kFull, cc, 31);
+                    if (S > 0.0f && isfinite(S)) {
+                        t = ufb * S;
+                        const unsigned hit = __ballot_sync(kFull, lane < P && t < s + cc);
+                        if (hit) {
+                            owner = __ffs(hit) - 1;
+                            const float os = __shfl_sync(kFull, s, owner);
+                            const float oc = __shfl_sync(kFull, cc, owner);
+                            const float ow = __shfl_sync(kFull, Wj, owner);
+                            t = t - ((os - ow) + oc);
+                        } else {
+                            const unsigned posm = __ballot_sync(kFull, lane < P && Wj > 0.0f);
+                            owner = posm ? 31 - __clz(posm) : -1;
+                            beyond = true;
+                        }
+                    }
+                }
+                if (owner < 0) {
+                    if (writer)
+                        write_outputs(row.b, n, -1);
+                } else if (owner == g) {
+                    // this warp holds the token: its chunk, then the element
+                    auto chunk_mass = [&](int j) -> float {
+                        const float2 sj = stats[j];
+                        if (bonus)
+                            return sj.x == -INFINITY ? 0.0f : sj.y * weight(sj.x, m_t, c);
+                        return use_r ? sj.x : sj.y;
+                    };
+                    float tc = t;
+                    const int jc = select_cdf(kwm, chunk_mass, tc, beyond, lane);
+                    int token = -1;
+                    if (jc >= 0) {
+                        const T* ct = slot_t + (size_t)jc * CH + lane * SPAN;
+                        const T* cd = slot_d + (size_t)jc * CH + lane * SPAN;
+                        auto term = [&](int e) -> float {
+                            const float et = weight(sm_elem(ct + e), m_t, c);
+                            if (!use_r)
+                                return et;
+                            return resid_term(et, inv_st, weight(sm_elem(cd + e), m_d, c), inv_sd);
+                        };
+                        CompSum span;
+                        int lastpos = -1;
+                        for (int e = 0; e < SPAN; ++e) {
+                            const float v = term(e);
+                            span.add(v);
+                            if (v > 0.0f)
+                                lastpos = e;
+                        }
+                        float s, cc;
+                        warp_incl_scan_comp(span.value(), lane, s, cc);
+                        int cand = INT_MAX;
+                        const unsigned hit = beyond ? 0u : __ballot_sync(kFull, tc < s + cc);
+                        if (hit) {
+                            const int src = __ffs(hit) - 1;
+                            if (lane == src) {
+                                float tl = tc - ((s - span.value()) + cc);
+                                CompSum cum;
+                                for (int e = 0; e < SPAN; ++e) {
+                                    cum.add(term(e));
+                                    if (tl < cum.value()) {
+                                        cand = e;
+                                        break;
+                                    }
+                                }
+                                if (cand == INT_MAX)
+                                    cand = lastpos >= 0 ? lastpos : INT_MAX;
+                                if (cand != INT_MAX)
+                                    cand += lane * SPAN;
+                            }
+                            cand = __reduce_min_sync(kFull, cand);
+                        }
+                        if (cand == INT_MAX) {   // beyond the mass (rounding): last positive element
+                            const int lp = __reduce_max_sync(kFull, lastpos >= 0 ? lane * SPAN + lastpos : -1);
+                            cand = lp >= 0 ? lp : INT_MAX;
+                        }
+                        if (cand != INT_MAX)
+                            token = e0 + jc * CH + cand;
+                    }
+                    write_outputs(row.b, n, (token >= 0 && token < V) ? token : -1);
                 }
             }
         }
 
         // ---- the cluster's next row (the same decision in every warp) ----
         const bool valid = dec == kDecAccept || dec == kDecReject;
-        const bool cont = !a.per_row && row.i < row.Kb &&
-                          (dec == kDecAccept || (!a.early_exit && valid));
+        const bool cont = row.i < row.Kb && (dec == kDecAccept || (!a.early_exit && valid));
+        if (!cont && writer && (a.want_pq || a.want_resid)) {
+            // positions this sequence does not reach carry NaN diagnostics
+            for (int i = (test ? row.i + 1 : row.i) + lane; i < Kmax; i += 32) {
+                const size_t q = (size_t)row.b * Kmax + i;
+                if (a.want_pq) {
+                    a.p_x[q] = NAN;
+                    a.q_x[q] = NAN;
+                }
+                if (a.want_resid)
+                    a.resid[q] = NAN;
+            }
+        }
         if (cont) {
             row = make_row(a, row.i + 1, row.b, row.Kb, row.T);
         } else if (spare >= 0) {
-            row = make_row(a, spare_pos.i, spare_pos.b, spare_pos.Kb, spare_pos.T);
+            row = make_row(a, 0, spare_pos.b, spare_pos.Kb, spare_pos.T);
             spare = -1;
+            drawn = false;
         } else {
             break;
         }
-        // copies first: the token loads of describe overlap with them
-        if ((row.flags & kFUsable) && kw > 0 && !broken)
-            prologue(row, (row.flags & kFDraft) != 0);
-        if (lane == 0)
-            tk = describe<T>(a, row);
+        issue(row);   // copies first: the token loads overlap with them
+        if (lane == 0) {
+            tk = tok_of(a, row);
+            if (!cont)
+                uf = final_uniform(a, row);
+        }
     }
 
-    // ---- wind-down: copies still in flight (only after a timeout), then
+    // ---- wind-down: a fill still in flight (only after a timeout), then
     // leave together, so that no CTA exits while a peer may still address it ----
     if (broken || xbroken) {
         if (lane == 0)
             atomicOr(a.err, kErrWaitTimeout);
-        for (uint32_t q = qw; q < qi; ++q)
-            (void)mbar_wait_bounded(rg.bar((int)(q % (uint32_t)R)), (q / (uint32_t)R) & 1u,
-                                    kWaitSpins);
+        if (pending)
+            (void)mbar_wait_bounded(bar, uses & 1u, kWaitSpins);
     }
-    if (!triggered)
-        griddep_launch_dependents();
     __syncwarp();
     cluster_arrive();
     cluster_wait();

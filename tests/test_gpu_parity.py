@@ -190,10 +190,10 @@ def test_verify_all_gives_identical_outputs(dev, mixed):
 
 
 GEOMETRIES = [dict(chunks_per_cta=1), dict(chunks_per_cta=2), dict(chunks_per_cta=5),
-              dict(chunks_per_cta=3, chunks_per_warp=2), dict(chunks_per_cta=4, chunks_per_warp=4),
-              dict(chunks_per_cta=2, ring_stages=1), dict(chunks_per_cta=5, ring_stages=2),
-              dict(chunks_per_cta=1, chunks_per_warp=1, ring_stages=1),
-              dict(verify_all=True, chunks_per_cta=3, chunks_per_warp=3)]
+              dict(chunks_per_cta=13), dict(chunks_per_cta=4, chunks_per_warp=4),
+              dict(chunks_per_cta=13, chunks_per_warp=1), dict(chunks_per_cta=3, chunks_per_warp=3),
+              dict(chunks_per_cta=8, chunks_per_warp=2),
+              dict(verify_all=True, chunks_per_cta=5, chunks_per_warp=2)]
 
 
 @pytest.mark.parametrize("kw", GEOMETRIES, ids=[str(sorted(g.items())) for g in GEOMETRIES])
@@ -208,20 +208,20 @@ def test_launch_geometries_match_oracle(dev, mixed, kw):
     assert np.array_equal(got[0], again[0]) and np.array_equal(got[1], again[1])
 
 
-# chunks per CTA, chunks per warp, ring stages: resident and streamed slices,
-# one to sixteen CTAs per row
-LARGE_GEOMETRIES = [("bf16", 128256, 16, 4, 4), ("bf16", 128256, 9, 3, 2), ("bf16", 128256, 126, 8, 2),
-                    ("bf16", 128256, 8, 8, 1), ("f32", 151936, 19, 5, 4), ("f32", 151936, 25, 3, 3),
-                    ("f32", 151936, 297, 40, 4), ("f32", 151936, 20, 20, 2)]
+# chunks per CTA, chunks per warp: one to sixteen CTAs per row, one to five
+# warps per CTA, four to twenty chunks per warp
+LARGE_GEOMETRIES = [("bf16", 128256, 16, 4), ("bf16", 128256, 8, 2), ("bf16", 128256, 21, 2),
+                    ("bf16", 128256, 32, 8), ("bf16", 128256, 20, 20), ("f32", 151936, 21, 2),
+                    ("f32", 151936, 38, 10), ("f32", 151936, 20, 20)]
 
 
-@pytest.mark.parametrize("dtype,V,ncpc,cpw,ring", LARGE_GEOMETRIES)
-def test_large_vocab_geometries_match_oracle(dev, dtype, V, ncpc, cpw, ring):
+@pytest.mark.parametrize("dtype,V,ncpc,cpw", LARGE_GEOMETRIES)
+def test_large_vocab_geometries_match_oracle(dev, dtype, V, ncpc, cpw):
     B = 12
     inp = W.make_host(B, W.configs.ragged_k(7, B), V, dtype, 2.0, 1.0,
-                      np.where(np.arange(B) % 2 == 0, 0.0, 1.0).astype(np.float32), seed=ncpc * 31 + cpw + ring)
+                      np.where(np.arange(B) % 2 == 0, 0.0, 1.0).astype(np.float32), seed=ncpc * 31 + cpw)
     ref = oracle_ref(inp)
-    got = run_gpu(to_device(inp, dev), "ex", chunks_per_cta=ncpc, chunks_per_warp=cpw, ring_stages=ring)
+    got = run_gpu(to_device(inp, dev), "ex", chunks_per_cta=ncpc, chunks_per_warp=cpw)
     compare(ref, *got)
 
 

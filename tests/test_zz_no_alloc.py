@@ -17,13 +17,13 @@ from helpers import compare, oracle_ref, to_device
 def test_shape_beyond_static_scratch_is_rejected():
     """A shape needing more than SV_STATIC_SCRATCH_BYTES of scratch returns
     SV_ERR_NO_MEMORY before any CUDA call (so this runs without a GPU)."""
-    B, V = 4096, 128256
-    K = (ctypes.c_int32 * B)(*([8] * B))
-    need = sv.sv_workspace_size(B, 8, V, sv.SV_DTYPE_BF16)
+    B, V = 4 << 20, 128256
+    K = np.full(B, 2, np.int32)
+    need = sv.sv_workspace_size(B, 2, V, sv.SV_DTYPE_BF16)
     assert need > sv.SV_STATIC_SCRATCH_BYTES
     dummy = ctypes.c_void_p(256)
     st = sv.library().spec_verify_noalloc(dummy, dummy, sv.SV_DTYPE_BF16, dummy, dummy, dummy, B,
-                                          K, V, dummy, dummy, None)
+                                          K.ctypes.data_as(ctypes.c_void_p), V, dummy, dummy, None)
     assert st == sv.SV_ERR_NO_MEMORY
 
 
