@@ -22,7 +22,8 @@ enum : int {
     kDecAccept = 1,
     kDecReject = 2,
     kDecInvalid = 3,   // unusable input on this row
-    kDecBonus = 4      // position K_b evaluated and usable
+    kDecBonus = 4,     // position K_b evaluated and usable
+    kDecRedo = 5       // weigh the row again against its maxima
 };
 
 enum : uint32_t { kErrWaitTimeout = 1u };
@@ -107,11 +108,21 @@ __device__ __forceinline__ float log2e_over(float T)
     return __fdiv_rn(1.44269504088896341f, T);
 }
 
-// exp2((l - m) * c): the unnormalised softmax weight, in one fixed rounding
-// sequence shared by the sweep and the finaliser.
+// The unnormalised softmax weight exp2((l - m) c) relative to a reference
+// logit m, as exp2(fma(l, c, -r)) with r = m c rounded once: one fused
+// multiply-add per element, and every weight of a row carries the same
+// rounding of r, which cancels in the ratios p = e / S.  The packed loops
+// compute exactly this per element.
+__device__ __forceinline__ float ref_of(float m, float c) { return __fmul_rn(m, c); }
+
+__device__ __forceinline__ float weight_r(float l, float r, float c)
+{
+    return ex2_approx(__fmaf_rn(l, c, -r));
+}
+
 __device__ __forceinline__ float weight(float l, float m, float c)
 {
-    return ex2_approx(__fmul_rn(__fsub_rn(l, m), c));
+    return weight_r(l, ref_of(m, c), c);
 }
 
 // max(0, p - q) with p = e_t / S_t and q = e_d / S_d, fixed rounding sequence.

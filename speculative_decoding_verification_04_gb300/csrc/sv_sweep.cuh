@@ -89,7 +89,9 @@ enum : int {
     kFGreedy = 1,   // T == 0
     kFTest = 2,     // i < K_b: a proposal is tested at this row
     kFDraft = 4,    // the draft row is read (tested sampling row)
-    kFUsable = 8    // temperature usable and, if needed, draft logits supplied
+    kFUsable = 8,   // temperature usable and, if needed, draft logits supplied
+    kFMaxRef = 16   // tested row weighed against the row maxima (its weights
+                    // against the proposal's logits overflowed)
 };
 
 struct Row {
@@ -141,6 +143,8 @@ __device__ __forceinline__ Tok tok_of(const Args& a, const Row& r)
     return t;
 }
 
+// The logits at the proposed token: the decision needs them, and a tested
+// row's pass weighs its logits against them.
 template <typename T>
 __device__ __forceinline__ void tok_logits(const Args& a, const Row& r, Tok& t)
 {
@@ -221,10 +225,11 @@ template <int NV> struct Lane<__nv_bfloat16, NV> {
     {
         return f2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
     }
-    // sum of exp2((l - m) c) over the lane's elements
+    // sum of weight(l, m, c) over the lane's elements
     __device__ static __forceinline__ float exp_sum(const uint4 (&v)[NV], float m, float c)
     {
-        const uint64_t M = f2_pack(m, m), Cc = f2_pack(c, c);
+        const float r = ref_of(m, c);
+        const uint64_t Cc = f2_pack(c, c), NR = f2_pack(-r, -r);
         uint64_t acc0 = f2_pack(0.0f, 0.0f), acc1 = acc0;
 #pragma unroll
         for (int k = 0; k < NV; ++k) {
@@ -232,7 +237,7 @@ template <int NV> struct Lane<__nv_bfloat16, NV> {
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
                 float d0, d1;
-                f2_unpack(f2_mul(f2_sub(pair(wv[h]), M), Cc), d0, d1);
+                f2_unpack(f2_fma(pair(wv[h]), Cc, NR), d0, d1);
                 const uint64_t e = f2_pack(ex2_approx(d0), ex2_approx(d1));
                 if (h & 1)
                     acc1 = f2_add(acc1, e);
@@ -253,36 +258,35 @@ template <int NV> struct Lane<__nv_bfloat16, NV> {
         const uint32_t wd = h == 0 ? q.x : h == 1 ? q.y : h == 2 ? q.z : q.w;
         return (j & 1) ? __uint_as_float(wd & 0xffff0000u) : __uint_as_float(wd << 16);
     }
-    // sums of the residual terms max(0, p - q) and of the weights of p
+    // sums of the residual terms max(0, p - q) and of the weights of p; the
+    // target and draft weights of one element share a packed fma and multiply
     __device__ static __forceinline__ void resid_sums(const uint4 (&t)[NV], const uint4 (&d)[NV],
                                                       float mt, float ist, float md, float isd,
                                                       float c, float& rs, float& ps)
     {
-        const uint64_t MT = f2_pack(mt, mt), MD = f2_pack(md, md), Cc = f2_pack(c, c);
-        const uint64_t IT = f2_pack(ist, ist), ID = f2_pack(isd, isd);
-        uint64_t racc = f2_pack(0.0f, 0.0f), pacc = racc;
+        const uint64_t Cc = f2_pack(c, c), NR = f2_pack(-ref_of(mt, c), -ref_of(md, c));
+        const uint64_t IS = f2_pack(ist, isd);
+        uint64_t acc = f2_pack(0.0f, 0.0f);   // (residual, p)
 #pragma unroll
         for (int k = 0; k < NV; ++k) {
             const uint32_t wt[4] = {t[k].x, t[k].y, t[k].z, t[k].w};
             const uint32_t wd[4] = {d[k].x, d[k].y, d[k].z, d[k].w};
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
-                float a0, a1, b0, b1;
-                f2_unpack(f2_mul(f2_sub(pair(wt[h]), MT), Cc), a0, a1);
-                f2_unpack(f2_mul(f2_sub(pair(wd[h]), MD), Cc), b0, b1);
-                const uint64_t et = f2_pack(ex2_approx(a0), ex2_approx(a1));
-                const uint64_t ed = f2_pack(ex2_approx(b0), ex2_approx(b1));
-                float r0, r1;
-                f2_unpack(f2_sub(f2_mul(et, IT), f2_mul(ed, ID)), r0, r1);
-                racc = f2_add(racc, f2_pack(fmaxf(r0, 0.0f), fmaxf(r1, 0.0f)));
-                pacc = f2_add(pacc, et);
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    const float lt = half ? __uint_as_float(wt[h] & 0xffff0000u) : __uint_as_float(wt[h] << 16);
+                    const float ld = half ? __uint_as_float(wd[h] & 0xffff0000u) : __uint_as_float(wd[h] << 16);
+                    float a0, a1;
+                    f2_unpack(f2_fma(f2_pack(lt, ld), Cc, NR), a0, a1);
+                    const float et = ex2_approx(a0);
+                    float p, q;
+                    f2_unpack(f2_mul(f2_pack(et, ex2_approx(a1)), IS), p, q);
+                    acc = f2_add(acc, f2_pack(fmaxf(__fsub_rn(p, q), 0.0f), et));
+                }
             }
         }
-        float x0, x1, y0, y1;
-        f2_unpack(racc, x0, x1);
-        f2_unpack(pacc, y0, y1);
-        rs = x0 + x1;
-        ps = y0 + y1;
+        f2_unpack(acc, rs, ps);
     }
 };
 
@@ -301,15 +305,14 @@ template <int NV> struct Lane<float, NV> {
     }
     __device__ static __forceinline__ float exp_sum(const uint4 (&v)[NV], float m, float c)
     {
-        const uint64_t M = f2_pack(m, m), Cc = f2_pack(c, c);
+        const float r = ref_of(m, c);
+        const uint64_t Cc = f2_pack(c, c), NR = f2_pack(-r, -r);
         uint64_t acc0 = f2_pack(0.0f, 0.0f), acc1 = acc0;
 #pragma unroll
         for (int k = 0; k < NV; ++k) {
             float d0, d1, d2, d3;
-            f2_unpack(f2_mul(f2_sub(f2_pack(__uint_as_float(v[k].x), __uint_as_float(v[k].y)), M),
-                             Cc), d0, d1);
-            f2_unpack(f2_mul(f2_sub(f2_pack(__uint_as_float(v[k].z), __uint_as_float(v[k].w)), M),
-                             Cc), d2, d3);
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(v[k].x), __uint_as_float(v[k].y)), Cc, NR), d0, d1);
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(v[k].z), __uint_as_float(v[k].w)), Cc, NR), d2, d3);
             acc0 = f2_add(acc0, f2_pack(ex2_approx(d0), ex2_approx(d1)));
             acc1 = f2_add(acc1, f2_pack(ex2_approx(d2), ex2_approx(d3)));
         }
@@ -328,33 +331,24 @@ template <int NV> struct Lane<float, NV> {
                                                       float mt, float ist, float md, float isd,
                                                       float c, float& rs, float& ps)
     {
-        const uint64_t MT = f2_pack(mt, mt), MD = f2_pack(md, md), Cc = f2_pack(c, c);
-        const uint64_t IT = f2_pack(ist, ist), ID = f2_pack(isd, isd);
-        uint64_t racc = f2_pack(0.0f, 0.0f), pacc = racc;
+        const uint64_t Cc = f2_pack(c, c), NR = f2_pack(-ref_of(mt, c), -ref_of(md, c));
+        const uint64_t IS = f2_pack(ist, isd);
+        uint64_t acc = f2_pack(0.0f, 0.0f);   // (residual, p)
 #pragma unroll
         for (int k = 0; k < NV; ++k) {
             const uint32_t wt[4] = {t[k].x, t[k].y, t[k].z, t[k].w};
             const uint32_t wd[4] = {d[k].x, d[k].y, d[k].z, d[k].w};
 #pragma unroll
-            for (int h = 0; h < 4; h += 2) {
-                float a0, a1, b0, b1;
-                f2_unpack(f2_mul(f2_sub(f2_pack(__uint_as_float(wt[h]), __uint_as_float(wt[h + 1])),
-                                        MT), Cc), a0, a1);
-                f2_unpack(f2_mul(f2_sub(f2_pack(__uint_as_float(wd[h]), __uint_as_float(wd[h + 1])),
-                                        MD), Cc), b0, b1);
-                const uint64_t et = f2_pack(ex2_approx(a0), ex2_approx(a1));
-                const uint64_t ed = f2_pack(ex2_approx(b0), ex2_approx(b1));
-                float r0, r1;
-                f2_unpack(f2_sub(f2_mul(et, IT), f2_mul(ed, ID)), r0, r1);
-                racc = f2_add(racc, f2_pack(fmaxf(r0, 0.0f), fmaxf(r1, 0.0f)));
-                pacc = f2_add(pacc, et);
+            for (int h = 0; h < 4; ++h) {
+                float a0, a1;
+                f2_unpack(f2_fma(f2_pack(__uint_as_float(wt[h]), __uint_as_float(wd[h])), Cc, NR), a0, a1);
+                const float et = ex2_approx(a0);
+                float p, q;
+                f2_unpack(f2_mul(f2_pack(et, ex2_approx(a1)), IS), p, q);
+                acc = f2_add(acc, f2_pack(fmaxf(__fsub_rn(p, q), 0.0f), et));
             }
         }
-        float x0, x1, y0, y1;
-        f2_unpack(racc, x0, x1);
-        f2_unpack(pacc, y0, y1);
-        rs = x0 + x1;
-        ps = y0 + y1;
+        f2_unpack(acc, rs, ps);
     }
 };
 
@@ -374,12 +368,24 @@ __device__ __forceinline__ void load_chunk(const T* p, int lane, uint4 (&v)[NV])
         v[k] = q[k * 32 + lane];
 }
 
+// Warp sum of non-negative lane sums, compensated; +inf if a lane overflowed
+// (and no lane is NaN), NaN if a lane is NaN.
+__device__ __forceinline__ float sum_or_special(float v)
+{
+    if (__any_sync(kFull, isnan(v)))
+        return NAN;
+    if (__any_sync(kFull, isinf(v)))
+        return INFINITY;
+    return warp_sum_comp(v);
+}
+
 // Combine (max, sum relative to that max) parts held one per lane; the sum
 // is compensated.  Every lane gets the same result.
 __device__ __forceinline__ void combine_ms(float m_part, float s_part, float c, float& m, float& S)
 {
     m = warp_max_nan(m_part);
-    S = warp_sum_comp(m_part == -INFINITY ? 0.0f : s_part * weight(m_part, m, c));
+    S = warp_sum_comp(m_part == -INFINITY ? 0.0f
+                                          : (m_part == m ? s_part : s_part * weight(m_part, m, c)));
 }
 
 // Inverse-CDF selection over `n` non-negative masses D(0..n-1), one warp:
@@ -571,6 +577,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32) sv_sweep_kernel(const Args a)
         issue(row);
         if (lane == 0) {
             tk = tok_of(a, row);
+            tok_logits<T>(a, row, tk);
             uf = final_uniform(a, row);
         }
     }
@@ -596,13 +603,14 @@ __global__ void __launch_bounds__(kMaxWarps * 32) sv_sweep_kernel(const Args a)
             if (!have)
                 broken = true;
         }
-        if (lane == 0)
-            tok_logits<T>(a, row, tk);
         int claimed = -1;
         if (writer && lane == 0 && want_claim)
             claimed = ticket_unit(a, ticket);
 
         // ---- one pass over this warp's slice ----
+        const float ref_t = __shfl_sync(kFull, tk.lt, 0);
+        const float ref_d = __shfl_sync(kFull, tk.ld, 0);
+        const bool ref_ok = __shfl_sync(kFull, tk.ok, 0) && isfinite(ref_t) && isfinite(ref_d);
         float4 part = make_float4(-INFINITY, __int_as_float(INT_MAX), -INFINITY, 0.0f);
         if (greedy) {
             float gm = -INFINITY;
@@ -629,7 +637,25 @@ __global__ void __launch_bounds__(kMaxWarps * 32) sv_sweep_kernel(const Args a)
             const float m = warp_max_nan(gm);
             const int gidx = __reduce_min_sync(kFull, gm == m ? gi : INT_MAX);
             part = make_float4(m, __int_as_float(gidx), -INFINITY, 0.0f);
+        } else if (test && !(row.flags & kFMaxRef) && ref_ok) {
+            // weights against the proposal's logits: one sweep, and every
+            // warp's sums share the reference, so the partials simply add
+            float st = 0.0f, sd = 0.0f;
+            if (have) {
+#pragma unroll 2
+                for (int j = 0; j < kwm; ++j) {
+                    uint4 v[NV];
+                    load_chunk<T, NV>(slot_t + (size_t)j * CH, lane, v);
+                    st += LN::exp_sum(v, ref_t, c);
+                    load_chunk<T, NV>(slot_d + (size_t)j * CH, lane, v);
+                    sd += LN::exp_sum(v, ref_d, c);
+                }
+            }
+            // an overflowed weight makes the warp's sum +inf (the compensated
+            // sum would turn it into NaN, which means unusable input)
+            part = make_float4(ref_t, sum_or_special(st), ref_d, sum_or_special(sd));
         } else if (test) {
+            // weights against the running lane maxima
             float mt = -INFINITY, st = 0.0f, md = -INFINITY, sd = 0.0f;
             if (have) {
                 for (int j = 0; j < kwm; ++j) {
@@ -704,6 +730,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32) sv_sweep_kernel(const Args a)
         const Tok tkb = shfl_tok(tk);
         const size_t pos = (size_t)row.b * Kmax + row.i;   // diagnostics index (test rows)
         int dec = kDecInvalid;
+        bool redo = false;
         int gtok = -1;
         float m_t = 0.0f, m_d = 0.0f, inv_st = 0.0f, inv_sd = 0.0f;
         bool row_ok = false;
@@ -718,10 +745,17 @@ __global__ void __launch_bounds__(kMaxWarps * 32) sv_sweep_kernel(const Args a)
             }
         } else {
             float St, Sd;
+            // weights against the proposal's logits that overflowed: the row
+            // is weighed again against its maxima (same data, same result)
+            const bool has = lane < P;
+            const bool any_inf = __any_sync(kFull, has && (isinf(xv.y) || isinf(xv.w)));
+            const bool any_nan =
+                __any_sync(kFull, has && (isnan(xv.x) || isnan(xv.y) || isnan(xv.z) || isnan(xv.w)));
+            redo = test && !(row.flags & kFMaxRef) && ref_ok && !broken && any_inf && !any_nan;
             combine_ms(xv.x, xv.y, c, m_t, St);
             combine_ms(xv.z, xv.w, c, m_d, Sd);
-            row_ok = usable && tkb.ok && isfinite(m_t) && St > 0.0f &&
-                     (!draft || (isfinite(m_d) && Sd > 0.0f));
+            row_ok = !redo && usable && tkb.ok && isfinite(m_t) && St > 0.0f && isfinite(St) &&
+                     (!draft || (isfinite(m_d) && Sd > 0.0f && isfinite(Sd)));
             inv_st = row_ok ? __frcp_rn(St) : 0.0f;
             inv_sd = row_ok && draft ? __frcp_rn(Sd) : 0.0f;
             bool accept = false;
@@ -731,8 +765,9 @@ __global__ void __launch_bounds__(kMaxWarps * 32) sv_sweep_kernel(const Args a)
                 qx = __fmul_rn(weight(tkb.ld, m_d, c), inv_sd);
                 accept = __fmul_rn(tkb.u, qx) < px;   // u < min(1, p/q) without a division
             }
-            dec = !row_ok ? kDecInvalid : (test ? (accept ? kDecAccept : kDecReject) : kDecBonus);
-            if (writer && lane == 0 && test && a.want_pq) {
+            dec = redo ? kDecRedo
+                       : (!row_ok ? kDecInvalid : (test ? (accept ? kDecAccept : kDecReject) : kDecBonus));
+            if (writer && lane == 0 && test && a.want_pq && !redo) {
                 a.p_x[pos] = px;
                 a.q_x[pos] = qx;
             }
@@ -788,11 +823,11 @@ __global__ void __launch_bounds__(kMaxWarps * 32) sv_sweep_kernel(const Args a)
             wtot = lane < P ? xbuf2[p2 * kMaxParts + lane] : make_float2(0.0f, 0.0f);
             S_R = warp_sum_comp(wtot.x);
         }
-        if (writer && lane == 0 && test && a.want_resid)
+        if (writer && lane == 0 && test && a.want_resid && !redo)
             a.resid[pos] = resid_pass ? S_R : NAN;
 
         // ---- the sequence's final row: its token and outputs ----
-        if (!drawn && dec != kDecAccept) {
+        if (!drawn && dec != kDecAccept && !redo) {
             drawn = true;
             const int n = row.i;
             const float ufb = __shfl_sync(kFull, uf, 0);
@@ -903,7 +938,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32) sv_sweep_kernel(const Args a)
 
         // ---- the cluster's next row (the same decision in every warp) ----
         const bool valid = dec == kDecAccept || dec == kDecReject;
-        const bool cont = row.i < row.Kb && (dec == kDecAccept || (!a.early_exit && valid));
+        const bool cont = redo || (row.i < row.Kb && (dec == kDecAccept || (!a.early_exit && valid)));
         if (!cont && writer && (a.want_pq || a.want_resid)) {
             // positions this sequence does not reach carry NaN diagnostics
             for (int i = (test ? row.i + 1 : row.i) + lane; i < Kmax; i += 32) {
@@ -916,7 +951,9 @@ __global__ void __launch_bounds__(kMaxWarps * 32) sv_sweep_kernel(const Args a)
                     a.resid[q] = NAN;
             }
         }
-        if (cont) {
+        if (redo) {
+            row.flags |= kFMaxRef;   // the same row again
+        } else if (cont) {
             row = make_row(a, row.i + 1, row.b, row.Kb, row.T);
         } else if (spare >= 0) {
             row = make_row(a, 0, spare_pos.b, spare_pos.Kb, spare_pos.T);
@@ -928,6 +965,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32) sv_sweep_kernel(const Args a)
         issue(row);   // copies first: the token loads overlap with them
         if (lane == 0) {
             tk = tok_of(a, row);
+            tok_logits<T>(a, row, tk);
             if (!cont)
                 uf = final_uniform(a, row);
         }

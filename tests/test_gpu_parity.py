@@ -101,6 +101,32 @@ def test_special_uniforms(dev):
     _check(inp, dev)
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_proposals_far_below_the_row_max(dev, dtype):
+    """Weights taken against the proposal's own logit overflow when that logit
+    lies far below the row's maximum (or is -inf); such rows are weighed again
+    against their maxima and must still match the oracle."""
+    B, K, V = 24, 3, 3000
+    inp = W.make_host(B, K, V, "f32", 2.0, 1.0, 1.0, seed=21)
+    tgt, drf, tok = inp["target"], inp["draft"], inp["tokens"]
+    for b in range(B):
+        for i in range(K):
+            x = tok[b, i]
+            if b % 4 == 0:    # target logit at x 200 below a spike: exp2 of ~288 overflows
+                tgt[b, i, (x + 7) % V] = 150.0
+                tgt[b, i, x] = -50.0
+            elif b % 4 == 1:  # draft logit at x far below its own spike
+                drf[b, i, (x + 11) % V] = 150.0
+                drf[b, i, x] = -60.0
+            elif b % 4 == 2:  # -inf at the proposal in the target row: p(x) = 0
+                tgt[b, i, x] = -np.inf
+    if dtype == "bf16":
+        for k in ("target", "draft"):
+            inp[k] = W.configs.f32_to_bf16_bits(inp[k])
+        inp["dtype"] = "bf16"
+    _check(inp, dev)
+
+
 def test_workload1_full_size(dev):
     _check(W.make_spec_host(1), dev)
 
