@@ -38,6 +38,8 @@ import workloads as W  # noqa: E402
 METRIC = "verified draft positions/sec and achieved HBM GB/s (% of GB300 peak), 1 GPU"
 UNIT = "positions/s"
 KERNEL_SOURCES = ["speculative_decoding_verification_04_gb300/csrc/spec_verify.cu",
+                  "speculative_decoding_verification_04_gb300/csrc/sv_sweep.cuh",
+                  "speculative_decoding_verification_04_gb300/csrc/sv_common.cuh",
                   "speculative_decoding_verification_04_gb300/csrc/sv_ptx.cuh"]
 WORKLOAD_TEXT = {
     0: "B=64 K=4 V=5 fp32 N(0,1) draft+N(0,1) T=1",
@@ -214,7 +216,7 @@ def run_ours(args):
     torch.cuda.set_device(dev)
     widx = args.workload
 
-    d = W.make_device(widx, dev)
+    d = W.make_device(widx, dev, B=args.sequences)
     B, Kmax, V = d["B"], d["Kmax"], d["V"]
     K = np.asarray(d["K"], np.int32)
     dcode = sv.SV_DTYPE_BF16 if d["dtype"] == "bf16" else sv.SV_DTYPE_F32
@@ -287,11 +289,13 @@ def run_ours(args):
     peaks = _peaks()
     med_ms = statistics.median(times)
     achieved = bytes_need / (med_ms / 1e3) / 1e9
-    traffic = _profile_traffic(widx)
+    traffic = _profile_traffic(widx) if args.sequences is None else None
     roofline = dict(bound="hbm", achieved=round(achieved, 1), peak=peaks["hbm_gbs"], unit="GB/s",
                     frac=round(achieved / peaks["hbm_gbs"], 4), traffic=traffic,
                     bytes_algorithmic=bytes_need, peak_source=peaks["source"],
-                    kernel="sv_verify_kernel")
+                    kernel="sv_sweep_kernel",
+                    duration="CUDA events around each spec_verify_ws call: the 1-kernel step "
+                             "plus its header upload")
 
     # ---- end to end through the host entry point (pinned buffers) ----
     e2e = None
@@ -342,7 +346,9 @@ def run_ours(args):
             metric=METRIC, value=value, unit=UNIT, n_gpus=world, steps=args.steps,
             warmup=args.warmup, ms_per_step=round(ms_per_step, 5), higher_is_better=True,
             scaling="weak", vs_baseline=None, dtype="f32", data="synthetic",
-            config=dict(workload=WORKLOAD_TEXT[widx], bench_workload=widx, logits=d["dtype"],
+            config=dict(workload=WORKLOAD_TEXT[widx] if args.sequences is None
+                        else f"first {B} sequences of: {WORKLOAD_TEXT[widx]}",
+                        bench_workload=widx, logits=d["dtype"],
                         B=B, Kmax=Kmax, V=V, positions_per_step=pos_per_step,
                         l2="flushed before every step (1 GiB write, > 2x L2)", parallelism=f"dp{world}"),
             roofline=roofline, cpu_baseline=cpu, e2e=e2e, gpu_launches=args.steps,
@@ -386,6 +392,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", type=int, default=4, choices=[0, 1, 2, 3, 4])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sequences", type=int, default=None,
+                    help="the workload's first N sequences only (profiling captures)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
