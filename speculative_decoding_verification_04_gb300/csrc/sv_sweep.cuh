@@ -50,15 +50,16 @@ struct SweepLayout {
     size_t bars;         // [nw] slot mbarriers
     size_t xbar;         // [2] exchange mbarriers: row partials
     size_t xbar2;        // [2] exchange mbarriers: residual totals
-    size_t xbuf;         // [2][kMaxParts] float4 row partials
-    size_t xbuf2;        // [2][kMaxParts] float2 residual totals
+    size_t xbuf;         // [2][P] float4 row partials (P = warps per row)
+    size_t xbuf2;        // [2][P] float2 residual totals
     size_t xclaim;       // [2] int: unit claimed by rank 0 during the row
     size_t first;        // int: the cluster's first unit
-    size_t stats;        // [nw][kw] float2: per-chunk statistics for the draw
+    size_t stats;        // [nw][kw][8] float2: per-chunk statistics for the draw,
+                         // as eight partial sums (lanes folded two butterfly levels)
     size_t total;
 };
 
-__host__ __device__ inline SweepLayout sweep_layout(int nw, int kw, int chunk_bytes)
+__host__ __device__ inline SweepLayout sweep_layout(int nw, int kw, int chunk_bytes, int P)
 {
     SweepLayout L;
     L.slot_bytes = 2 * (size_t)kw * (size_t)chunk_bytes;
@@ -71,15 +72,15 @@ __host__ __device__ inline SweepLayout sweep_layout(int nw, int kw, int chunk_by
     o += 16;
     o = (o + 15) & ~(size_t)15;
     L.xbuf = o;
-    o += 2 * kMaxParts * 16;
+    o += 2 * (size_t)P * 16;
     L.xbuf2 = o;
-    o += 2 * kMaxParts * 8;
+    o += 2 * (size_t)P * 8;
     L.xclaim = o;
     o += 8;
     L.first = o;
     o += 8;
     L.stats = o;
-    o += (size_t)nw * kw * 8;
+    o += (size_t)nw * kw * 8 * 8;
     L.total = o;
     return L;
 }
@@ -115,17 +116,38 @@ __device__ __forceinline__ Row make_row(const Args& a, int i, int b, int Kb, flo
     return r;
 }
 
-// The row's proposal, held by lane 0 of every warp: token and uniform (loaded
-// when the row's copies are issued) and the two logits at the token (loaded
-// once the slice has arrived, so from L2).
+// A sequence's draft tokens and uniforms, lane j holding position j
+// (K_max <= 32), loaded once per sequence when it is claimed, so that no row
+// waits on them.
+struct SeqVals {
+    int tok;
+    float u;
+};
+
+__device__ __forceinline__ SeqVals seq_vals(const Args& a, int b, int lane)
+{
+    SeqVals v{0, 0.0f};
+    if (lane < a.Kmax)
+        v.tok = __ldg(a.tok + (size_t)b * a.Kmax + lane);
+    if (lane <= a.Kmax)
+        v.u = __ldg(a.uni + (size_t)b * (a.Kmax + 1) + lane);
+    return v;
+}
+
+// The row's proposal, held by lane 0 of every warp: token and uniform (from
+// the sequence's registers) and the two logits at the token (loaded when the
+// row's copies are issued, first used after the slice has arrived).
 struct Tok {
     int x;
     float u, lt, ld;
     int ok;
 };
 
-__device__ __forceinline__ Tok tok_of(const Args& a, const Row& r)
+// Whole warp (shuffles); the result is meaningful in every lane.
+__device__ __forceinline__ Tok tok_of(const Args& a, const Row& r, const SeqVals& sv)
 {
+    const int x = __shfl_sync(kFull, sv.tok, r.i & 31);
+    const float u = __shfl_sync(kFull, sv.u, r.i & 31);
     Tok t{0, 0.0f, 0.0f, 0.0f, 0};
     if (!(r.flags & kFUsable))
         return t;
@@ -133,11 +155,11 @@ __device__ __forceinline__ Tok tok_of(const Args& a, const Row& r)
         t.ok = 1;
         return t;
     }
-    t.x = __ldg(a.tok + (size_t)r.b * a.Kmax + r.i);
-    bool ok = t.x >= 0 && t.x < a.V;
+    t.x = x;
+    bool ok = x >= 0 && x < a.V;
     if (!(r.flags & kFGreedy)) {
-        t.u = __ldg(a.uni + (size_t)r.b * (a.Kmax + 1) + r.i);
-        ok = ok && t.u >= 0.0f && t.u < 1.0f;
+        t.u = u;
+        ok = ok && u >= 0.0f && u < 1.0f;
     }
     t.ok = ok ? 1 : 0;
     return t;
@@ -179,6 +201,19 @@ __device__ __forceinline__ int ticket_unit(const Args& a, int t)
         return -1;
     const int b = __ldg(a.order + t);
     return (b >= 0 && b < a.B) ? b : -1;
+}
+
+// The same in two steps, so that the order lookup's latency hides behind
+// other work: the load (at a clamped index, always in bounds; B >= 1), then
+// the range checks once its value is needed.
+__device__ __forceinline__ int ticket_load(const Args& a, int t)
+{
+    return __ldg(a.order + min(max(t, 0), a.B - 1));
+}
+
+__device__ __forceinline__ int ticket_check(const Args& a, int t, int b)
+{
+    return (t >= 0 && t < a.B && b >= 0 && b < a.B) ? b : -1;
 }
 
 // A sequence's first row: K_b and T loaded at claim time, used when it starts.
@@ -368,6 +403,15 @@ __device__ __forceinline__ void load_chunk(const T* p, int lane, uint4 (&v)[NV])
         v[k] = q[k * 32 + lane];
 }
 
+// Fold a lane value two butterfly levels: lanes l, l^8, l^16, l^24 end with
+// their four-lane sum, so lanes 0..7 hold eight partials of the warp's sum.
+__device__ __forceinline__ float fold8(float v)
+{
+    v += __shfl_xor_sync(kFull, v, 16);
+    v += __shfl_xor_sync(kFull, v, 8);
+    return v;
+}
+
 // Warp sum of non-negative lane sums, compensated; +inf if a lane overflowed
 // (and no lane is NaN), NaN if a lane is NaN.
 __device__ __forceinline__ float sum_or_special(float v)
@@ -407,7 +451,9 @@ __device__ __forceinline__ int select_cdf(int n, F D, float& t, bool& beyond, in
             float s, c;
             warp_incl_scan_comp(d, lane, s, c);
             const float rel = (t - base_s) - base_c;   // mass left after earlier groups
-            const unsigned hit = __ballot_sync(kFull, j < n && rel < s + c);
+            // an entry without mass is never taken (a remainder that rounded
+            // below zero lands on the first entry with mass)
+            const unsigned hit = __ballot_sync(kFull, j < n && d > 0.0f && rel < s + c);
             if (hit) {
                 const int src = __ffs(hit) - 1;
                 const float ex_s = __shfl_sync(kFull, s, src), ex_c = __shfl_sync(kFull, c, src);
@@ -452,18 +498,18 @@ __global__ void __launch_bounds__(kMaxWarps * 32) sv_sweep_kernel(const Args a)
     const int kwm = min(c_lo + KW, a.nchunks) - c_lo;   // chunks in range (0..KW)
     const int e0 = c_lo * CH;                           // first element of the range
     const int n_el = max(0, min(e0 + kwm * CH, V) - e0);
-    const SweepLayout L = sweep_layout(nw, KW, CH * (int)sizeof(T));
+    const SweepLayout L = sweep_layout(nw, KW, CH * (int)sizeof(T), P);
 
     T* slot_t = reinterpret_cast<T*>(dsm + (size_t)w * L.slot_bytes);
     T* slot_d = slot_t + (size_t)KW * CH;
     const uint32_t bar = smem_addr(dsm + L.bars + 8 * (size_t)w);
     uint64_t* xbar = reinterpret_cast<uint64_t*>(dsm + L.xbar);
     uint64_t* xbar2 = reinterpret_cast<uint64_t*>(dsm + L.xbar2);
-    float4* xbuf = reinterpret_cast<float4*>(dsm + L.xbuf);    // [2][kMaxParts]
-    float2* xbuf2 = reinterpret_cast<float2*>(dsm + L.xbuf2);  // [2][kMaxParts]
+    float4* xbuf = reinterpret_cast<float4*>(dsm + L.xbuf);    // [2][P]
+    float2* xbuf2 = reinterpret_cast<float2*>(dsm + L.xbuf2);  // [2][P]
     int* xclaim = reinterpret_cast<int*>(dsm + L.xclaim);      // [2]
     int* first = reinterpret_cast<int*>(dsm + L.first);
-    float2* stats = reinterpret_cast<float2*>(dsm + L.stats) + (size_t)w * KW;
+    float2* stats = reinterpret_cast<float2*>(dsm + L.stats) + (size_t)w * KW * 8;   // [kw][8]
 
     // ---- set-up: barriers; -inf past V in this warp's range (copies never
     // write there); the cluster's first unit from rank 0 ----
@@ -505,9 +551,11 @@ __global__ void __launch_bounds__(kMaxWarps * 32) sv_sweep_kernel(const Args a)
     bool xbroken = false;    // an exchange wait gave up: leave the loop
     bool drawn = false;      // the current sequence's outputs are written
     Row row = make_row(a, 0, 0, 0, 0.0f);
+    SeqVals cur_sv{0, 0.0f}, spare_sv{0, 0.0f};   // the current and the spare sequence's
     if (active) {
         const UnitPos p0 = unit_pos(a, u0);
         row = make_row(a, 0, p0.b, p0.Kb, p0.T);
+        cur_sv = seq_vals(a, u0, lane);
     }
     Tok tk{0, 0.0f, 0.0f, 0.0f, 0};   // lane 0
     float uf = 0.0f;                  // lane 0: the sequence's final uniform
@@ -560,12 +608,13 @@ __global__ void __launch_bounds__(kMaxWarps * 32) sv_sweep_kernel(const Args a)
         __syncwarp();
         return all;
     };
-    // outputs of sequence b: draft tokens before n, `token` at n, -1 after
+    // outputs of the current sequence b (whole warp): draft tokens before n
+    // (n <= 32, from the sequence's registers), `token` at n, -1 after
     auto write_outputs = [&](int b, int n, int token) {
         const bool bad = token < 0;
         int32_t* orow = a.out_tok + (size_t)b * (Kmax + 1);
         for (int j = lane; j <= Kmax; j += 32)
-            orow[j] = bad ? -1 : (j < n ? __ldg(a.tok + (size_t)b * Kmax + j) : (j == n ? token : -1));
+            orow[j] = bad ? -1 : (j < n ? cur_sv.tok : (j == n ? token : -1));
         if (lane == 0) {
             a.out_n[b] = bad ? -1 : n;
             if (a.want_final)
@@ -575,8 +624,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32) sv_sweep_kernel(const Args a)
 
     if (active) {
         issue(row);
+        tk = tok_of(a, row, cur_sv);
         if (lane == 0) {
-            tk = tok_of(a, row);
             tok_logits<T>(a, row, tk);
             uf = final_uniform(a, row);
         }
@@ -603,9 +652,9 @@ __global__ void __launch_bounds__(kMaxWarps * 32) sv_sweep_kernel(const Args a)
             if (!have)
                 broken = true;
         }
-        int claimed = -1;
+        int claimed = -1;   // the order lookup now, its checks after the pass
         if (writer && lane == 0 && want_claim)
-            claimed = ticket_unit(a, ticket);
+            claimed = ticket_load(a, ticket);
 
         // ---- one pass over this warp's slice ----
         const float ref_t = __shfl_sync(kFull, tk.lt, 0);
@@ -681,41 +730,43 @@ __global__ void __launch_bounds__(kMaxWarps * 32) sv_sweep_kernel(const Args a)
             combine_ms(md, sd, c, m2, S2);
             part = make_float4(m1, S1, m2, S2);
         } else {
-            // bonus row: per-chunk (max, sum) of the target, kept for the draw
-            float mm = -INFINITY;
+            // bonus row: the warp's maximum, then per-chunk sums against it
+            // (kept for the draw as eight partials per chunk)
+            float mm = -INFINITY, acc = 0.0f, cmp = 0.0f;
             if (have) {
+                float lm = -INFINITY;
                 for (int j = 0; j < kwm; ++j) {
                     uint4 tv[NV];
                     load_chunk<T, NV>(slot_t + (size_t)j * CH, lane, tv);
-                    const float mc = warp_max_nan(LN::max(tv));
-                    const float sc = mc == -INFINITY ? 0.0f : warp_sum(LN::exp_sum(tv, mc, c));
-                    if (lane == 0)
-                        stats[j] = make_float2(mc, sc);
-                    mm = max_nan(mm, mc);
+                    lm = max_nan(lm, LN::max(tv));
+                }
+                mm = warp_max_nan(lm);
+                const float mu = mm == -INFINITY ? 0.0f : mm;
+                for (int j = 0; j < kwm; ++j) {
+                    uint4 tv[NV];
+                    load_chunk<T, NV>(slot_t + (size_t)j * CH, lane, tv);
+                    const float v = fold8(LN::exp_sum(tv, mu, c));
+                    if (lane < 8)
+                        stats[j * 8 + lane] = make_float2(v, 0.0f);
+                    float t, e;
+                    two_sum(acc, v, t, e);
+                    acc = t;
+                    cmp += e;
                 }
                 __syncwarp();
             }
-            // this warp's total, compensated over its chunks, 32 at a time
-            float sacc = 0.0f, scmp = 0.0f;
-            for (int j0 = 0; j0 < (have ? kwm : 0); j0 += 32) {
-                const int j = j0 + lane;
-                const float2 sj = j < kwm ? stats[j] : make_float2(-INFINITY, 0.0f);
-                const float v = warp_sum_comp(sj.x == -INFINITY ? 0.0f : sj.y * weight(sj.x, mm, c));
-                float t, e;
-                two_sum(sacc, v, t, e);
-                sacc = t;
-                scmp += e;
-            }
-            part = make_float4(mm, sacc + scmp, -INFINITY, 0.0f);
+            part = make_float4(mm, sum_or_special(lane < 8 ? acc + cmp : 0.0f), -INFINITY, 0.0f);
         }
         if (broken)
             part.x = NAN;   // poisons the row in every warp of the cluster
 
         // ---- exchange: this warp's partial to every CTA of the cluster ----
+        if (writer && lane == 0 && want_claim)
+            claimed = ticket_check(a, ticket, claimed);
         const int claimed_b = __shfl_sync(kFull, claimed, 0);
         if (lane < C) {
             const uint32_t rb = map_to_rank(smem_addr(&xbar[p]), (uint32_t)lane);
-            st_async_v4(map_to_rank(smem_addr(&xbuf[p * kMaxParts + g]), (uint32_t)lane), part, rb);
+            st_async_v4(map_to_rank(smem_addr(&xbuf[p * P + g]), (uint32_t)lane), part, rb);
             if (writer && want_claim)
                 st_async_s32(map_to_rank(smem_addr(&xclaim[p]), (uint32_t)lane), claimed_b, rb);
         }
@@ -725,7 +776,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32) sv_sweep_kernel(const Args a)
             break;
 
         // ---- combine all partials and decide (every warp alike) ----
-        const float4 xv = lane < P ? xbuf[p * kMaxParts + lane]
+        const float4 xv = lane < P ? xbuf[p * P + lane]
                                    : make_float4(-INFINITY, __int_as_float(INT_MAX), -INFINITY, 0.0f);
         const Tok tkb = shfl_tok(tk);
         const size_t pos = (size_t)row.b * Kmax + row.i;   // diagnostics index (test rows)
@@ -776,8 +827,10 @@ __global__ void __launch_bounds__(kMaxWarps * 32) sv_sweep_kernel(const Args a)
             const int cl = xclaim[p];
             spare = (cl >= 0 && cl < a.B) ? cl : -1;
             exhausted = spare < 0;
-            if (spare >= 0)
+            if (spare >= 0) {
                 spare_pos = unit_pos(a, spare);   // loads now, used when the unit starts
+                spare_sv = seq_vals(a, spare, lane);
+            }
         }
 
         // ---- residual pass: rows that may be drawn from (resident slice) ----
@@ -793,10 +846,10 @@ __global__ void __launch_bounds__(kMaxWarps * 32) sv_sweep_kernel(const Args a)
                 load_chunk<T, NV>(slot_d + (size_t)j * CH, lane, dv);
                 float rs, ps;
                 LN::resid_sums(tv, dv, m_t, inv_st, m_d, inv_sd, c, rs, ps);
-                rs = warp_sum(rs);
-                ps = warp_sum(ps);
-                if (lane == 0)
-                    stats[j] = make_float2(rs, ps);
+                rs = fold8(rs);
+                ps = fold8(ps);
+                if (lane < 8)
+                    stats[j * 8 + lane] = make_float2(rs, ps);
                 float t, e;
                 two_sum(rs_s, rs, t, e);
                 rs_s = t;
@@ -806,6 +859,10 @@ __global__ void __launch_bounds__(kMaxWarps * 32) sv_sweep_kernel(const Args a)
                 ps_c += e;
             }
             __syncwarp();
+            rs_s = warp_sum_comp(lane < 8 ? rs_s + rs_c : 0.0f);
+            rs_c = 0.0f;
+            ps_s = warp_sum_comp(lane < 8 ? ps_s + ps_c : 0.0f);
+            ps_c = 0.0f;
             const int p2 = (int)(k2 & 1);
             const uint32_t par2 = (k2 >> 1) & 1u;
             ++k2;
@@ -813,14 +870,14 @@ __global__ void __launch_bounds__(kMaxWarps * 32) sv_sweep_kernel(const Args a)
                 mbar_arrive_expect_tx(smem_addr(&xbar2[p2]), (uint32_t)P * 8u);
             if (lane < C) {
                 const uint32_t rb = map_to_rank(smem_addr(&xbar2[p2]), (uint32_t)lane);
-                const uint32_t dst = map_to_rank(smem_addr(&xbuf2[p2 * kMaxParts + g]), (uint32_t)lane);
+                const uint32_t dst = map_to_rank(smem_addr(&xbuf2[p2 * P + g]), (uint32_t)lane);
                 st_async_v2(dst, make_float2(rs_s + rs_c, ps_s + ps_c), rb);
             }
             if (!mbar_wait_bounded(smem_addr(&xbar2[p2]), par2, kWaitSpins))
                 xbroken = true;
             if (__any_sync(kFull, xbroken))
                 break;
-            wtot = lane < P ? xbuf2[p2 * kMaxParts + lane] : make_float2(0.0f, 0.0f);
+            wtot = lane < P ? xbuf2[p2 * P + lane] : make_float2(0.0f, 0.0f);
             S_R = warp_sum_comp(wtot.x);
         }
         if (writer && lane == 0 && test && a.want_resid && !redo)
@@ -875,11 +932,19 @@ __global__ void __launch_bounds__(kMaxWarps * 32) sv_sweep_kernel(const Args a)
                         write_outputs(row.b, n, -1);
                 } else if (owner == g) {
                     // this warp holds the token: its chunk, then the element
+                    // chunk masses: the sums of the chunk's eight partials (the
+                    // bonus pass summed against this warp's own maximum, the
+                    // max of partial g)
+                    const float own_m = __shfl_sync(kFull, xv.x, g);
+                    const float wscale = bonus ? (own_m == -INFINITY ? 0.0f : weight(own_m, m_t, c)) : 1.0f;
                     auto chunk_mass = [&](int j) -> float {
-                        const float2 sj = stats[j];
-                        if (bonus)
-                            return sj.x == -INFINITY ? 0.0f : sj.y * weight(sj.x, m_t, c);
-                        return use_r ? sj.x : sj.y;
+                        float s8 = 0.0f;
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const float2 sj = stats[j * 8 + e];
+                            s8 += bonus ? sj.x : (use_r ? sj.x : sj.y);
+                        }
+                        return bonus ? s8 * wscale : s8;
                     };
                     float tc = t;
                     const int jc = select_cdf(kwm, chunk_mass, tc, beyond, lane);
@@ -901,28 +966,29 @@ __global__ void __launch_bounds__(kMaxWarps * 32) sv_sweep_kernel(const Args a)
                             if (v > 0.0f)
                                 lastpos = e;
                         }
+                        const float sv_l = span.value();
                         float s, cc;
-                        warp_incl_scan_comp(span.value(), lane, s, cc);
+                        warp_incl_scan_comp(sv_l, lane, s, cc);
                         int cand = INT_MAX;
-                        const unsigned hit = beyond ? 0u : __ballot_sync(kFull, tc < s + cc);
+                        const unsigned hit = beyond ? 0u : __ballot_sync(kFull, sv_l > 0.0f && tc < s + cc);
                         if (hit) {
+                            // the span that holds the point, one element per lane
+                            // (SPAN <= 32), and the point's place within it
                             const int src = __ffs(hit) - 1;
-                            if (lane == src) {
-                                float tl = tc - ((s - span.value()) + cc);
-                                CompSum cum;
-                                for (int e = 0; e < SPAN; ++e) {
-                                    cum.add(term(e));
-                                    if (tl < cum.value()) {
-                                        cand = e;
-                                        break;
-                                    }
-                                }
-                                if (cand == INT_MAX)
-                                    cand = lastpos >= 0 ? lastpos : INT_MAX;
-                                if (cand != INT_MAX)
-                                    cand += lane * SPAN;
+                            const float tl = __shfl_sync(kFull, tc - ((s - sv_l) + cc), src);
+                            const T* hs_t = slot_t + (size_t)jc * CH + src * SPAN + lane;
+                            const T* hs_d = slot_d + (size_t)jc * CH + src * SPAN + lane;
+                            float v = 0.0f;
+                            if (lane < SPAN) {
+                                const float et = weight(sm_elem(hs_t), m_t, c);
+                                v = use_r ? resid_term(et, inv_st, weight(sm_elem(hs_d), m_d, c), inv_sd) : et;
                             }
-                            cand = __reduce_min_sync(kFull, cand);
+                            float s2, c2;
+                            warp_incl_scan_comp(v, lane, s2, c2);
+                            const unsigned h2 = __ballot_sync(kFull, v > 0.0f && tl < s2 + c2);
+                            const int lp = __reduce_max_sync(kFull, v > 0.0f ? lane : -1);
+                            const int e = h2 ? __ffs(h2) - 1 : lp;   // rounding: last element with mass
+                            cand = e >= 0 ? src * SPAN + e : INT_MAX;
                         }
                         if (cand == INT_MAX) {   // beyond the mass (rounding): last positive element
                             const int lp = __reduce_max_sync(kFull, lastpos >= 0 ? lane * SPAN + lastpos : -1);
@@ -957,14 +1023,15 @@ __global__ void __launch_bounds__(kMaxWarps * 32) sv_sweep_kernel(const Args a)
             row = make_row(a, row.i + 1, row.b, row.Kb, row.T);
         } else if (spare >= 0) {
             row = make_row(a, 0, spare_pos.b, spare_pos.Kb, spare_pos.T);
+            cur_sv = spare_sv;
             spare = -1;
             drawn = false;
         } else {
             break;
         }
-        issue(row);   // copies first: the token loads overlap with them
+        issue(row);   // copies first: the logit loads overlap with them
+        tk = tok_of(a, row, cur_sv);
         if (lane == 0) {
-            tk = tok_of(a, row);
             tok_logits<T>(a, row, tk);
             if (!cont)
                 uf = final_uniform(a, row);
