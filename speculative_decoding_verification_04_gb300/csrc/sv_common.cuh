@@ -173,6 +173,41 @@ __device__ __forceinline__ float warp_sum_comp(float v)
     return s + c;
 }
 
+// Two independent compensated butterfly sums, interleaved so that their
+// shuffle latencies overlap; each result equals warp_sum_comp of its input.
+__device__ __forceinline__ void warp_sum_comp2(float& va, float& vb)
+{
+    float sa = va, ca = 0.0f, sb = vb, cb = 0.0f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float soa = __shfl_xor_sync(kFull, sa, o);
+        const float sob = __shfl_xor_sync(kFull, sb, o);
+        const float coa = __shfl_xor_sync(kFull, ca, o);
+        const float cob = __shfl_xor_sync(kFull, cb, o);
+        float ta, ea, tb, eb;
+        two_sum(sa, soa, ta, ea);
+        two_sum(sb, sob, tb, eb);
+        sa = ta;
+        sb = tb;
+        ca = (ca + coa) + ea;
+        cb = (cb + cob) + eb;
+    }
+    va = sa + ca;
+    vb = sb + cb;
+}
+
+// Two NaN-propagating warp maxima, interleaved.
+__device__ __forceinline__ void warp_max_nan2(float& va, float& vb)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float oa = __shfl_xor_sync(kFull, va, o);
+        const float ob = __shfl_xor_sync(kFull, vb, o);
+        va = max_nan(va, oa);
+        vb = max_nan(vb, ob);
+    }
+}
+
 // Compensated (Neumaier) fp32 running sum.
 struct CompSum {
     float s = 0.0f, c = 0.0f;

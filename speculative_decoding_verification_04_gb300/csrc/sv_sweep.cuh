@@ -432,6 +432,28 @@ __device__ __forceinline__ void combine_ms(float m_part, float s_part, float c, 
                                           : (m_part == m ? s_part : s_part * weight(m_part, m, c)));
 }
 
+// sum_or_special of two values, interleaved (each result as the single form).
+__device__ __forceinline__ void sum_or_special2(float& va, float& vb)
+{
+    const bool nan_a = __any_sync(kFull, isnan(va)), nan_b = __any_sync(kFull, isnan(vb));
+    const bool inf_a = __any_sync(kFull, isinf(va)), inf_b = __any_sync(kFull, isinf(vb));
+    warp_sum_comp2(va, vb);
+    va = nan_a ? NAN : (inf_a ? INFINITY : va);
+    vb = nan_b ? NAN : (inf_b ? INFINITY : vb);
+}
+
+// combine_ms of two (max, sum) pairs, interleaved (each result as the single form).
+__device__ __forceinline__ void combine_ms2(float ma_part, float sa_part, float mb_part, float sb_part,
+                                            float c, float& ma, float& Sa, float& mb, float& Sb)
+{
+    ma = ma_part;
+    mb = mb_part;
+    warp_max_nan2(ma, mb);
+    Sa = ma_part == -INFINITY ? 0.0f : (ma_part == ma ? sa_part : sa_part * weight(ma_part, ma, c));
+    Sb = mb_part == -INFINITY ? 0.0f : (mb_part == mb ? sb_part : sb_part * weight(mb_part, mb, c));
+    warp_sum_comp2(Sa, Sb);
+}
+
 // Inverse-CDF selection over `n` non-negative masses D(0..n-1), one warp:
 // the smallest j with t < D(0) + ... + D(j), sums compensated, 32 at a time.
 // `t` is reduced to the mass left inside the selected entry.  If t lies beyond
@@ -485,7 +507,6 @@ __global__ void __launch_bounds__(kMaxWarps * 32) sv_sweep_kernel(const Args a)
     using LN = Lane<T, NV>;
     constexpr int E = EL::E;
     constexpr int CH = 32 * NV * E;
-    constexpr int SPAN = CH / 32;   // contiguous elements per lane in the draw
     extern __shared__ __align__(128) unsigned char dsm[];
 
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -702,7 +723,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32) sv_sweep_kernel(const Args a)
             }
             // an overflowed weight makes the warp's sum +inf (the compensated
             // sum would turn it into NaN, which means unusable input)
-            part = make_float4(ref_t, sum_or_special(st), ref_d, sum_or_special(sd));
+            sum_or_special2(st, sd);
+            part = make_float4(ref_t, st, ref_d, sd);
         } else if (test) {
             // weights against the running lane maxima
             float mt = -INFINITY, st = 0.0f, md = -INFINITY, sd = 0.0f;
@@ -726,8 +748,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32) sv_sweep_kernel(const Args a)
                 }
             }
             float m1, S1, m2, S2;
-            combine_ms(mt, st, c, m1, S1);
-            combine_ms(md, sd, c, m2, S2);
+            combine_ms2(mt, st, md, sd, c, m1, S1, m2, S2);
             part = make_float4(m1, S1, m2, S2);
         } else {
             // bonus row: the warp's maximum, then per-chunk sums against it
@@ -803,8 +824,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32) sv_sweep_kernel(const Args a)
             const bool any_nan =
                 __any_sync(kFull, has && (isnan(xv.x) || isnan(xv.y) || isnan(xv.z) || isnan(xv.w)));
             redo = test && !(row.flags & kFMaxRef) && ref_ok && !broken && any_inf && !any_nan;
-            combine_ms(xv.x, xv.y, c, m_t, St);
-            combine_ms(xv.z, xv.w, c, m_d, Sd);
+            combine_ms2(xv.x, xv.y, xv.z, xv.w, c, m_t, St, m_d, Sd);
             row_ok = !redo && usable && tkb.ok && isfinite(m_t) && St > 0.0f && isfinite(St) &&
                      (!draft || (isfinite(m_d) && Sd > 0.0f && isfinite(Sd)));
             inv_st = row_ok ? __frcp_rn(St) : 0.0f;
@@ -859,9 +879,10 @@ __global__ void __launch_bounds__(kMaxWarps * 32) sv_sweep_kernel(const Args a)
                 ps_c += e;
             }
             __syncwarp();
-            rs_s = warp_sum_comp(lane < 8 ? rs_s + rs_c : 0.0f);
+            rs_s = lane < 8 ? rs_s + rs_c : 0.0f;
+            ps_s = lane < 8 ? ps_s + ps_c : 0.0f;
+            warp_sum_comp2(rs_s, ps_s);
             rs_c = 0.0f;
-            ps_s = warp_sum_comp(lane < 8 ? ps_s + ps_c : 0.0f);
             ps_c = 0.0f;
             const int p2 = (int)(k2 & 1);
             const uint32_t par2 = (k2 >> 1) & 1u;
@@ -950,51 +971,63 @@ __global__ void __launch_bounds__(kMaxWarps * 32) sv_sweep_kernel(const Args a)
                     const int jc = select_cdf(kwm, chunk_mass, tc, beyond, lane);
                     int token = -1;
                     if (jc >= 0) {
-                        const T* ct = slot_t + (size_t)jc * CH + lane * SPAN;
-                        const T* cd = slot_d + (size_t)jc * CH + lane * SPAN;
-                        auto term = [&](int e) -> float {
-                            const float et = weight(sm_elem(ct + e), m_t, c);
-                            if (!use_r)
-                                return et;
-                            return resid_term(et, inv_st, weight(sm_elem(cd + e), m_d, c), inv_sd);
-                        };
-                        CompSum span;
-                        int lastpos = -1;
-                        for (int e = 0; e < SPAN; ++e) {
-                            const float v = term(e);
-                            span.add(v);
-                            if (v > 0.0f)
-                                lastpos = e;
-                        }
-                        const float sv_l = span.value();
-                        float s, cc;
-                        warp_incl_scan_comp(sv_l, lane, s, cc);
-                        int cand = INT_MAX;
-                        const unsigned hit = beyond ? 0u : __ballot_sync(kFull, sv_l > 0.0f && tc < s + cc);
-                        if (hit) {
-                            // the span that holds the point, one element per lane
-                            // (SPAN <= 32), and the point's place within it
-                            const int src = __ffs(hit) - 1;
-                            const float tl = __shfl_sync(kFull, tc - ((s - sv_l) + cc), src);
-                            const T* hs_t = slot_t + (size_t)jc * CH + src * SPAN + lane;
-                            const T* hs_d = slot_d + (size_t)jc * CH + src * SPAN + lane;
-                            float v = 0.0f;
-                            if (lane < SPAN) {
-                                const float et = weight(sm_elem(hs_t), m_t, c);
-                                v = use_r ? resid_term(et, inv_st, weight(sm_elem(hs_d), m_d, c), inv_sd) : et;
+                        // the element, in the chunk's own layout: strip k (vector
+                        // k of every lane) holds elements (k * 32 + lane) * E + e,
+                        // so index order is strip, then lane, then e.  Strip by
+                        // strip: each lane's E terms, a warp scan of their sums,
+                        // the lane that holds the point, then its element.
+                        uint4 tv[NV], dv[NV];
+                        load_chunk<T, NV>(slot_t + (size_t)jc * CH, lane, tv);
+                        if (use_r)
+                            load_chunk<T, NV>(slot_d + (size_t)jc * CH, lane, dv);
+                        float base_s = 0.0f, base_c = 0.0f;   // mass of earlier strips
+                        int cand = -1, lastpos = -1;
+#pragma unroll
+                        for (int k = 0; k < NV; ++k) {
+                            float tm[E];
+                            float ls = 0.0f;
+#pragma unroll
+                            for (int e = 0; e < E; ++e) {
+                                const float et = weight(LN::elem(tv, k * E + e), m_t, c);
+                                tm[e] = use_r ? resid_term(et, inv_st, weight(LN::elem(dv, k * E + e), m_d, c), inv_sd)
+                                              : et;
+                                ls += tm[e];
+                                if (tm[e] > 0.0f)
+                                    lastpos = (k * 32 + lane) * E + e;
                             }
-                            float s2, c2;
-                            warp_incl_scan_comp(v, lane, s2, c2);
-                            const unsigned h2 = __ballot_sync(kFull, v > 0.0f && tl < s2 + c2);
-                            const int lp = __reduce_max_sync(kFull, v > 0.0f ? lane : -1);
-                            const int e = h2 ? __ffs(h2) - 1 : lp;   // rounding: last element with mass
-                            cand = e >= 0 ? src * SPAN + e : INT_MAX;
+                            if (cand >= 0 || beyond)
+                                continue;
+                            float ss, sc;
+                            warp_incl_scan_comp(ls, lane, ss, sc);
+                            const float rel = (tc - base_s) - base_c;   // mass left after earlier strips
+                            const unsigned hit = __ballot_sync(kFull, ls > 0.0f && rel < ss + sc);
+                            if (hit) {
+                                const int src = __ffs(hit) - 1;
+                                const float tl = __shfl_sync(kFull, rel - ((ss - ls) + sc), src);
+                                int ce = -1, lp = -1;
+                                float cum = 0.0f;
+#pragma unroll
+                                for (int e = 0; e < E; ++e) {   // the same sums as ls
+                                    cum += tm[e];
+                                    if (tm[e] > 0.0f) {
+                                        lp = e;
+                                        if (ce < 0 && tl < cum)
+                                            ce = e;
+                                    }
+                                }
+                                ce = ce >= 0 ? ce : lp;   // rounding: the lane's last element with mass
+                                cand = __shfl_sync(kFull, (k * 32 + lane) * E + ce, src);
+                            } else {
+                                const float gs = __shfl_sync(kFull, ss, 31), gc = __shfl_sync(kFull, sc, 31);
+                                float ts, te;
+                                two_sum(base_s, gs, ts, te);
+                                base_s = ts;
+                                base_c += gc + te;
+                            }
                         }
-                        if (cand == INT_MAX) {   // beyond the mass (rounding): last positive element
-                            const int lp = __reduce_max_sync(kFull, lastpos >= 0 ? lane * SPAN + lastpos : -1);
-                            cand = lp >= 0 ? lp : INT_MAX;
-                        }
-                        if (cand != INT_MAX)
+                        if (cand < 0)   // beyond the mass (rounding): the chunk's last element with mass
+                            cand = __reduce_max_sync(kFull, lastpos);
+                        if (cand >= 0)
                             token = e0 + jc * CH + cand;
                     }
                     write_outputs(row.b, n, (token >= 0 && token < V) ? token : -1);
