@@ -102,7 +102,7 @@ typedef struct {
  *                   row's slice then does not fit in shared memory).
  *   chunks_per_warp 0: automatic.  Otherwise how many of the CTA's chunks
  *                   each warp holds (tuning: sets the warps per CTA, at most
- *                   16 and at most 32 / cluster size).
+ *                   8 and at most 32 / cluster size).
  * Tuning options change only the fp32 summation grouping: results agree
  * with the automatic geometry except within the rounding of those sums.
  */

@@ -246,7 +246,7 @@ static sv_status pick_geometry(int V, sv_dtype dt, int B, int Kmax, int override
         for (int nw = 1; nw <= kMaxWarps && C * nw <= kMaxParts; ++nw) {
             if (want_cpw > 0) {
                 const int ncpc = (nch + C - 1) / C;
-                if (nw != std::min((ncpc + want_cpw - 1) / want_cpw, kMaxParts / C))
+                if (nw != std::min({(ncpc + want_cpw - 1) / want_cpw, kMaxParts / C, kMaxWarps}))
                     continue;
             }
             Geom t;

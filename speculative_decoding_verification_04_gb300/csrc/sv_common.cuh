@@ -14,7 +14,11 @@
 namespace sv {
 
 constexpr unsigned kFull = 0xffffffffu;
-constexpr int kMaxWarps = 16;
+constexpr int kMaxWarps = 8;
+// Registers per thread of the sweep: an SM sub-partition's 16K registers
+// then hold three warps (nine to twelve per SM, the geometries the resident
+// row slices lead to).
+constexpr int kMaxRegs = 168;
 constexpr int kMaxCluster = 16;
 constexpr uint32_t kWaitSpins = 1u << 22;   // bounded mbarrier polls (a few seconds)
 // Decision of one row.
@@ -71,6 +75,13 @@ template <> struct Elem<float> {
         x[3] = __uint_as_float(w.w);
     }
     __device__ static __forceinline__ float load(const float* p) { return __ldg(p); }
+    // the element's bits, widened to fp32 by widen() where first used, so
+    // that no instruction right after the load waits for it
+    __device__ static __forceinline__ uint32_t load_raw(const float* p)
+    {
+        return __float_as_uint(__ldg(p));
+    }
+    __device__ static __forceinline__ float widen(uint32_t r) { return __uint_as_float(r); }
     __device__ static __forceinline__ void copy(float* dst, const float* src) { *dst = __ldg(src); }
     __device__ static __forceinline__ void set_neg_inf(float* dst) { *dst = -INFINITY; }
 };
@@ -91,6 +102,13 @@ template <> struct Elem<__nv_bfloat16> {
         const unsigned short h = __ldg(reinterpret_cast<const unsigned short*>(p));
         return __uint_as_float(static_cast<uint32_t>(h) << 16);
     }
+    __device__ static __forceinline__ uint32_t load_raw(const __nv_bfloat16* p)
+    {
+        uint32_t r;   // 16-bit load, zero-extended into the 32-bit register
+        asm("ld.global.nc.u16 %0, [%1];" : "=r"(r) : "l"(p));
+        return r;
+    }
+    __device__ static __forceinline__ float widen(uint32_t r) { return __uint_as_float(r << 16); }
     __device__ static __forceinline__ void copy(__nv_bfloat16* dst, const __nv_bfloat16* src)
     {
         *reinterpret_cast<unsigned short*>(dst) = __ldg(reinterpret_cast<const unsigned short*>(src));

@@ -54,8 +54,8 @@ struct SweepLayout {
     size_t xbuf2;        // [2][P] float2 residual totals
     size_t xclaim;       // [2] int: unit claimed by rank 0 during the row
     size_t first;        // int: the cluster's first unit
-    size_t stats;        // [nw][kw][8] float2: per-chunk statistics for the draw,
-                         // as eight partial sums (lanes folded two butterfly levels)
+    size_t stats;        // [nw][kw][strips][4] float: per-strip partial sums of the
+                         // draw masses (at most 64 bytes a chunk)
     size_t total;
 };
 
@@ -135,11 +135,13 @@ __device__ __forceinline__ SeqVals seq_vals(const Args& a, int b, int lane)
 }
 
 // The row's proposal, held by lane 0 of every warp: token and uniform (from
-// the sequence's registers) and the two logits at the token (loaded when the
-// row's copies are issued, first used after the slice has arrived).
+// the sequence's registers) and the bits of the two logits at the token
+// (loaded when the row's copies are issued, widened to fp32 where first used,
+// after the slice has arrived).
 struct Tok {
     int x;
-    float u, lt, ld;
+    float u;
+    uint32_t lt, ld;
     int ok;
 };
 
@@ -148,7 +150,7 @@ __device__ __forceinline__ Tok tok_of(const Args& a, const Row& r, const SeqVals
 {
     const int x = __shfl_sync(kFull, sv.tok, r.i & 31);
     const float u = __shfl_sync(kFull, sv.u, r.i & 31);
-    Tok t{0, 0.0f, 0.0f, 0.0f, 0};
+    Tok t{0, 0.0f, 0u, 0u, 0};
     if (!(r.flags & kFUsable))
         return t;
     if (!(r.flags & kFTest)) {
@@ -173,19 +175,27 @@ __device__ __forceinline__ void tok_logits(const Args& a, const Row& r, Tok& t)
     if (!t.ok || !(r.flags & kFTest))
         return;
     const size_t trow = (size_t)r.b * (a.Kmax + 1) + r.i;
-    t.lt = Elem<T>::load(static_cast<const T*>(a.tgt) + trow * (size_t)a.V + t.x);
+    t.lt = Elem<T>::load_raw(static_cast<const T*>(a.tgt) + trow * (size_t)a.V + t.x);
     if (r.flags & kFDraft)
-        t.ld = Elem<T>::load(static_cast<const T*>(a.drf) +
-                             ((size_t)r.b * a.Kmax + r.i) * (size_t)a.V + t.x);
+        t.ld = Elem<T>::load_raw(static_cast<const T*>(a.drf) +
+                                 ((size_t)r.b * a.Kmax + r.i) * (size_t)a.V + t.x);
 }
 
-__device__ __forceinline__ Tok shfl_tok(const Tok& t)
+// The proposal as every lane sees it, the logits widened to fp32.
+struct TokF {
+    int x;
+    float u, lt, ld;
+    int ok;
+};
+
+template <typename T>
+__device__ __forceinline__ TokF shfl_tok(const Tok& t)
 {
-    Tok o;
+    TokF o;
     o.x = __shfl_sync(kFull, t.x, 0);
     o.u = __shfl_sync(kFull, t.u, 0);
-    o.lt = __shfl_sync(kFull, t.lt, 0);
-    o.ld = __shfl_sync(kFull, t.ld, 0);
+    o.lt = Elem<T>::widen(__shfl_sync(kFull, t.lt, 0));
+    o.ld = Elem<T>::widen(__shfl_sync(kFull, t.ld, 0));
     o.ok = __shfl_sync(kFull, t.ok, 0);
     return o;
 }
@@ -293,35 +303,93 @@ template <int NV> struct Lane<__nv_bfloat16, NV> {
         const uint32_t wd = h == 0 ? q.x : h == 1 ? q.y : h == 2 ? q.z : q.w;
         return (j & 1) ? __uint_as_float(wd & 0xffff0000u) : __uint_as_float(wd << 16);
     }
-    // sums of the residual terms max(0, p - q) and of the weights of p; the
-    // target and draft weights of one element share a packed fma and multiply
-    __device__ static __forceinline__ void resid_sums(const uint4 (&t)[NV], const uint4 (&d)[NV],
-                                                      float mt, float ist, float md, float isd,
-                                                      float c, float& rs, float& ps)
+    // per strip (vector k: 8 elements), the lane's sum of weight(l, m, c)
+    __device__ static __forceinline__ void exp_strips(const uint4 (&v)[NV], float m, float c, float (&s)[NV])
+    {
+        const float r = ref_of(m, c);
+        const uint64_t Cc = f2_pack(c, c), NR = f2_pack(-r, -r);
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            const uint32_t wv[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+            uint64_t acc0 = f2_pack(0.0f, 0.0f), acc1 = acc0;
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                float d0, d1;
+                f2_unpack(f2_fma(pair(wv[h]), Cc, NR), d0, d1);
+                const uint64_t e = f2_pack(ex2_approx(d0), ex2_approx(d1));
+                if (h & 1)
+                    acc1 = f2_add(acc1, e);
+                else
+                    acc0 = f2_add(acc0, e);
+            }
+            float a0, a1, b0, b1;
+            f2_unpack(acc0, a0, a1);
+            f2_unpack(acc1, b0, b1);
+            s[k] = (a0 + a1) + (b0 + b1);
+        }
+    }
+    // the residual term max(0, p - q) and the weight of p of element e of a
+    // lane vector pair; the target and draft weights share a packed fma and
+    // a packed multiply (the one rounding sequence of every residual term)
+    __device__ static __forceinline__ void resid_term2(uint32_t wt, uint32_t wd, int half, uint64_t Cc,
+                                                       uint64_t NR, uint64_t IS, float& r, float& et)
+    {
+        const float lt = half ? __uint_as_float(wt & 0xffff0000u) : __uint_as_float(wt << 16);
+        const float ld = half ? __uint_as_float(wd & 0xffff0000u) : __uint_as_float(wd << 16);
+        float a0, a1;
+        f2_unpack(f2_fma(f2_pack(lt, ld), Cc, NR), a0, a1);
+        et = ex2_approx(a0);
+        float p, q;
+        f2_unpack(f2_mul(f2_pack(et, ex2_approx(a1)), IS), p, q);
+        r = fmaxf(__fsub_rn(p, q), 0.0f);
+    }
+    // per strip, the lane's sum of residual terms; over all strips, the
+    // lane's sum of the weights of p
+    __device__ static __forceinline__ void resid_strips(const uint4 (&t)[NV], const uint4 (&d)[NV],
+                                                        float mt, float ist, float md, float isd,
+                                                        float c, float (&rs)[NV], float& ps)
     {
         const uint64_t Cc = f2_pack(c, c), NR = f2_pack(-ref_of(mt, c), -ref_of(md, c));
         const uint64_t IS = f2_pack(ist, isd);
-        uint64_t acc = f2_pack(0.0f, 0.0f);   // (residual, p)
+        float p0 = 0.0f, p1 = 0.0f;
 #pragma unroll
         for (int k = 0; k < NV; ++k) {
             const uint32_t wt[4] = {t[k].x, t[k].y, t[k].z, t[k].w};
             const uint32_t wd[4] = {d[k].x, d[k].y, d[k].z, d[k].w};
+            float r0 = 0.0f, r1 = 0.0f;
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
-                    const float lt = half ? __uint_as_float(wt[h] & 0xffff0000u) : __uint_as_float(wt[h] << 16);
-                    const float ld = half ? __uint_as_float(wd[h] & 0xffff0000u) : __uint_as_float(wd[h] << 16);
-                    float a0, a1;
-                    f2_unpack(f2_fma(f2_pack(lt, ld), Cc, NR), a0, a1);
-                    const float et = ex2_approx(a0);
-                    float p, q;
-                    f2_unpack(f2_mul(f2_pack(et, ex2_approx(a1)), IS), p, q);
-                    acc = f2_add(acc, f2_pack(fmaxf(__fsub_rn(p, q), 0.0f), et));
+                    float r, et;
+                    resid_term2(wt[h], wd[h], half, Cc, NR, IS, r, et);
+                    if (half) {
+                        r1 += r;
+                        p1 += et;
+                    } else {
+                        r0 += r;
+                        p0 += et;
+                    }
                 }
             }
+            rs[k] = r0 + r1;
         }
-        f2_unpack(acc, rs, ps);
+        ps = p0 + p1;
+    }
+    __device__ static __forceinline__ void resid_elem(const uint4& t, const uint4& d, int e, uint64_t Cc,
+                                                      uint64_t NR, uint64_t IS, float& r, float& et)
+    {
+        const int h = e >> 1;
+        const uint32_t wt = h == 0 ? t.x : h == 1 ? t.y : h == 2 ? t.z : t.w;
+        const uint32_t wd = h == 0 ? d.x : h == 1 ? d.y : h == 2 ? d.z : d.w;
+        resid_term2(wt, wd, e & 1, Cc, NR, IS, r, et);
+    }
+    // element e (0..7) of a lane vector, as fp32
+    __device__ static __forceinline__ float vec_elem(const uint4& q, int e)
+    {
+        const int h = e >> 1;
+        const uint32_t wd = h == 0 ? q.x : h == 1 ? q.y : h == 2 ? q.z : q.w;
+        return (e & 1) ? __uint_as_float(wd & 0xffff0000u) : __uint_as_float(wd << 16);
     }
 };
 
@@ -362,37 +430,71 @@ template <int NV> struct Lane<float, NV> {
         const int h = j & 3;
         return __uint_as_float(h == 0 ? q.x : h == 1 ? q.y : h == 2 ? q.z : q.w);
     }
-    __device__ static __forceinline__ void resid_sums(const uint4 (&t)[NV], const uint4 (&d)[NV],
-                                                      float mt, float ist, float md, float isd,
-                                                      float c, float& rs, float& ps)
+    __device__ static __forceinline__ void exp_strips(const uint4 (&v)[NV], float m, float c, float (&s)[NV])
+    {
+        const float r = ref_of(m, c);
+        const uint64_t Cc = f2_pack(c, c), NR = f2_pack(-r, -r);
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            float d0, d1, d2, d3;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(v[k].x), __uint_as_float(v[k].y)), Cc, NR), d0, d1);
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(v[k].z), __uint_as_float(v[k].w)), Cc, NR), d2, d3);
+            float a0, a1, b0, b1;
+            f2_unpack(f2_pack(ex2_approx(d0), ex2_approx(d1)), a0, a1);
+            f2_unpack(f2_pack(ex2_approx(d2), ex2_approx(d3)), b0, b1);
+            s[k] = (a0 + a1) + (b0 + b1);
+        }
+    }
+    __device__ static __forceinline__ void resid_term2(uint32_t wt, uint32_t wd, int /*half*/, uint64_t Cc,
+                                                       uint64_t NR, uint64_t IS, float& r, float& et)
+    {
+        float a0, a1;
+        f2_unpack(f2_fma(f2_pack(__uint_as_float(wt), __uint_as_float(wd)), Cc, NR), a0, a1);
+        et = ex2_approx(a0);
+        float p, q;
+        f2_unpack(f2_mul(f2_pack(et, ex2_approx(a1)), IS), p, q);
+        r = fmaxf(__fsub_rn(p, q), 0.0f);
+    }
+    __device__ static __forceinline__ void resid_strips(const uint4 (&t)[NV], const uint4 (&d)[NV],
+                                                        float mt, float ist, float md, float isd,
+                                                        float c, float (&rs)[NV], float& ps)
     {
         const uint64_t Cc = f2_pack(c, c), NR = f2_pack(-ref_of(mt, c), -ref_of(md, c));
         const uint64_t IS = f2_pack(ist, isd);
-        uint64_t acc = f2_pack(0.0f, 0.0f);   // (residual, p)
+        float p0 = 0.0f, p1 = 0.0f;
 #pragma unroll
         for (int k = 0; k < NV; ++k) {
             const uint32_t wt[4] = {t[k].x, t[k].y, t[k].z, t[k].w};
             const uint32_t wd[4] = {d[k].x, d[k].y, d[k].z, d[k].w};
+            float r0 = 0.0f, r1 = 0.0f;
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
-                float a0, a1;
-                f2_unpack(f2_fma(f2_pack(__uint_as_float(wt[h]), __uint_as_float(wd[h])), Cc, NR), a0, a1);
-                const float et = ex2_approx(a0);
-                float p, q;
-                f2_unpack(f2_mul(f2_pack(et, ex2_approx(a1)), IS), p, q);
-                acc = f2_add(acc, f2_pack(fmaxf(__fsub_rn(p, q), 0.0f), et));
+                float r, et;
+                resid_term2(wt[h], wd[h], 0, Cc, NR, IS, r, et);
+                if (h & 1) {
+                    r1 += r;
+                    p1 += et;
+                } else {
+                    r0 += r;
+                    p0 += et;
+                }
             }
+            rs[k] = r0 + r1;
         }
-        f2_unpack(acc, rs, ps);
+        ps = p0 + p1;
+    }
+    __device__ static __forceinline__ void resid_elem(const uint4& t, const uint4& d, int e, uint64_t Cc,
+                                                      uint64_t NR, uint64_t IS, float& r, float& et)
+    {
+        const uint32_t wt = e == 0 ? t.x : e == 1 ? t.y : e == 2 ? t.z : t.w;
+        const uint32_t wd = e == 0 ? d.x : e == 1 ? d.y : e == 2 ? d.z : d.w;
+        resid_term2(wt, wd, 0, Cc, NR, IS, r, et);
+    }
+    __device__ static __forceinline__ float vec_elem(const uint4& q, int e)
+    {
+        return __uint_as_float(e == 0 ? q.x : e == 1 ? q.y : e == 2 ? q.z : q.w);
     }
 };
-
-// one element of a slice in shared memory, as fp32
-__device__ __forceinline__ float sm_elem(const float* p) { return *p; }
-__device__ __forceinline__ float sm_elem(const __nv_bfloat16* p)
-{
-    return __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const unsigned short*>(p)) << 16);
-}
 
 template <typename T, int NV>
 __device__ __forceinline__ void load_chunk(const T* p, int lane, uint4 (&v)[NV])
@@ -403,13 +505,41 @@ __device__ __forceinline__ void load_chunk(const T* p, int lane, uint4 (&v)[NV])
         v[k] = q[k * 32 + lane];
 }
 
-// Fold a lane value two butterfly levels: lanes l, l^8, l^16, l^24 end with
-// their four-lane sum, so lanes 0..7 hold eight partials of the warp's sum.
-__device__ __forceinline__ float fold8(float v)
+// Per-strip partial sums of a chunk for the draw: v[k] is the lane's sum
+// over strip k (vector k of every lane).  Three butterfly levels, halving the
+// values each lane carries while there is more than one (a transpose-reduce:
+// four shuffles for four strips), leave each strip's sum as four partials
+// (partial q over the eight lanes whose lane index is q modulo 4), stored as
+// dst[k * 4 + q].
+template <int NV>
+__device__ __forceinline__ void strip_partials(const float (&v)[NV], int lane, float* dst)
 {
-    v += __shfl_xor_sync(kFull, v, 16);
-    v += __shfl_xor_sync(kFull, v, 8);
-    return v;
+    float x;
+    int k;
+    if constexpr (NV == 4) {
+        const bool b4 = (lane & 16) != 0, b3 = (lane & 8) != 0;
+        // xor 16: the lower half keeps strips 0, 1, the upper half 2, 3
+        const float r0 = __shfl_xor_sync(kFull, b4 ? v[0] : v[2], 16);
+        const float r1 = __shfl_xor_sync(kFull, b4 ? v[1] : v[3], 16);
+        const float k0 = (b4 ? v[2] : v[0]) + r0, k1 = (b4 ? v[3] : v[1]) + r1;
+        // xor 8: each lane keeps one strip, 2 * b4 + b3
+        const float r2 = __shfl_xor_sync(kFull, b3 ? k0 : k1, 8);
+        x = (b3 ? k1 : k0) + r2;
+        k = (b4 ? 2 : 0) + (b3 ? 1 : 0);
+    } else if constexpr (NV == 2) {
+        const bool b4 = (lane & 16) != 0;
+        x = (b4 ? v[1] : v[0]) + __shfl_xor_sync(kFull, b4 ? v[0] : v[1], 16);
+        x += __shfl_xor_sync(kFull, x, 8);
+        k = b4 ? 1 : 0;
+    } else {
+        x = v[0] + __shfl_xor_sync(kFull, v[0], 16);
+        x += __shfl_xor_sync(kFull, x, 8);
+        k = 0;
+    }
+    x += __shfl_xor_sync(kFull, x, 4);
+    const int keep = NV == 4 ? 4 : (NV == 2 ? 12 : 28);   // lanes holding a distinct partial
+    if ((lane & keep) == 0)
+        dst[k * 4 + (lane & 3)] = x;
 }
 
 // Warp sum of non-negative lane sums, compensated; +inf if a lane overflowed
@@ -500,8 +630,71 @@ __device__ __forceinline__ int select_cdf(int n, F D, float& t, bool& beyond, in
     return __reduce_max_sync(kFull, last_pos);
 }
 
+// The element of one strip of a chunk that holds the point tc of the
+// distribution drawn from (one warp; tv / dv: each lane's vector of the strip
+// in the target / draft slice, dv read only for the residual).  The strip's
+// index order is lane, then element, so: each lane's E terms, a compensated
+// warp scan of their sums, the lane that holds the point, then its element.
+// The terms are computed exactly as in the residual pass (or the bonus pass).
+// Returns lane * E + e, or -1 if the strip has no mass; when the point lies
+// beyond the strip's mass (rounding, or `beyond` already set) the last
+// element with mass is taken.
 template <typename T, int NV>
-__global__ void __launch_bounds__(kMaxWarps * 32) sv_sweep_kernel(const Args a)
+__device__ __forceinline__ int pick_in_strip(const uint4& tv, const uint4& dv, bool use_r, float m_t,
+                                             float inv_st, float m_d, float inv_sd, float c, float tc,
+                                             bool beyond, int lane)
+{
+    using LN = Lane<T, NV>;
+    constexpr int E = Elem<T>::E;
+    const float rt = ref_of(m_t, c), rd = ref_of(m_d, c);
+    const uint64_t Cc = f2_pack(c, c), NR = f2_pack(-rt, -rd), IS = f2_pack(inv_st, inv_sd);
+    float tm[E];
+    float ls = 0.0f;
+    int lastpos = -1;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+        float v;
+        if (use_r) {
+            float et;
+            LN::resid_elem(tv, dv, e, Cc, NR, IS, v, et);
+        } else {
+            v = ex2_approx(__fmaf_rn(LN::vec_elem(tv, e), c, -rt));
+        }
+        tm[e] = v;
+        ls += v;
+        if (v > 0.0f)
+            lastpos = lane * E + e;
+    }
+    int cand = -1;
+    if (!beyond) {
+        float ss, sc;
+        warp_incl_scan_comp(ls, lane, ss, sc);
+        const unsigned hit = __ballot_sync(kFull, ls > 0.0f && tc < ss + sc);
+        if (hit) {
+            const int src = __ffs(hit) - 1;
+            const float tl = tc - ((ss - ls) + sc);   // the point's place in the lane (src)
+            int ce = -1, lp = -1;
+            float cum = 0.0f;
+#pragma unroll
+            for (int e = 0; e < E; ++e) {   // the same sums as ls
+                cum += tm[e];
+                if (tm[e] > 0.0f) {
+                    lp = e;
+                    if (ce < 0 && tl < cum)
+                        ce = e;
+                }
+            }
+            ce = ce >= 0 ? ce : lp;   // rounding: the lane's last element with mass
+            cand = __shfl_sync(kFull, lane * E + ce, src);
+        }
+    }
+    if (cand < 0)   // beyond the mass (rounding): the strip's last element with mass
+        cand = __reduce_max_sync(kFull, lastpos);
+    return cand;
+}
+
+template <typename T, int NV>
+__global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
 {
     using EL = Elem<T>;
     using LN = Lane<T, NV>;
@@ -530,7 +723,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32) sv_sweep_kernel(const Args a)
     float2* xbuf2 = reinterpret_cast<float2*>(dsm + L.xbuf2);  // [2][P]
     int* xclaim = reinterpret_cast<int*>(dsm + L.xclaim);      // [2]
     int* first = reinterpret_cast<int*>(dsm + L.first);
-    float2* stats = reinterpret_cast<float2*>(dsm + L.stats) + (size_t)w * KW * 8;   // [kw][8]
+    float* stats = reinterpret_cast<float*>(dsm + L.stats) + (size_t)w * KW * 16;   // [kw][NV][4]
 
     // ---- set-up: barriers; -inf past V in this warp's range (copies never
     // write there); the cluster's first unit from rank 0 ----
@@ -578,7 +771,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32) sv_sweep_kernel(const Args a)
         row = make_row(a, 0, p0.b, p0.Kb, p0.T);
         cur_sv = seq_vals(a, u0, lane);
     }
-    Tok tk{0, 0.0f, 0.0f, 0.0f, 0};   // lane 0
+    Tok tk{0, 0.0f, 0u, 0u, 0};       // lane 0
     float uf = 0.0f;                  // lane 0: the sequence's final uniform
     int ticket = -1;                  // rank 0, warp 0, lane 0
     uint32_t uses = 0;                // completed slot fills (mbarrier phase)
@@ -631,11 +824,11 @@ __global__ void __launch_bounds__(kMaxWarps * 32) sv_sweep_kernel(const Args a)
     };
     // outputs of the current sequence b (whole warp): draft tokens before n
     // (n <= 32, from the sequence's registers), `token` at n, -1 after
-    auto write_outputs = [&](int b, int n, int token) {
+    auto write_outputs = [&](int b, int n, int token, int seq_tok) {
         const bool bad = token < 0;
         int32_t* orow = a.out_tok + (size_t)b * (Kmax + 1);
         for (int j = lane; j <= Kmax; j += 32)
-            orow[j] = bad ? -1 : (j < n ? cur_sv.tok : (j == n ? token : -1));
+            orow[j] = bad ? -1 : (j < n ? seq_tok : (j == n ? token : -1));
         if (lane == 0) {
             a.out_n[b] = bad ? -1 : n;
             if (a.want_final)
@@ -678,8 +871,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32) sv_sweep_kernel(const Args a)
             claimed = ticket_load(a, ticket);
 
         // ---- one pass over this warp's slice ----
-        const float ref_t = __shfl_sync(kFull, tk.lt, 0);
-        const float ref_d = __shfl_sync(kFull, tk.ld, 0);
+        const float ref_t = EL::widen(__shfl_sync(kFull, tk.lt, 0));
+        const float ref_d = EL::widen(__shfl_sync(kFull, tk.ld, 0));
         const bool ref_ok = __shfl_sync(kFull, tk.ok, 0) && isfinite(ref_t) && isfinite(ref_d);
         float4 part = make_float4(-INFINITY, __int_as_float(INT_MAX), -INFINITY, 0.0f);
         if (greedy) {
@@ -751,8 +944,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32) sv_sweep_kernel(const Args a)
             combine_ms2(mt, st, md, sd, c, m1, S1, m2, S2);
             part = make_float4(m1, S1, m2, S2);
         } else {
-            // bonus row: the warp's maximum, then per-chunk sums against it
-            // (kept for the draw as eight partials per chunk)
+            // bonus row: the warp's maximum, then per-strip sums against it
+            // (kept for the draw)
             float mm = -INFINITY, acc = 0.0f, cmp = 0.0f;
             if (have) {
                 float lm = -INFINITY;
@@ -766,9 +959,13 @@ __global__ void __launch_bounds__(kMaxWarps * 32) sv_sweep_kernel(const Args a)
                 for (int j = 0; j < kwm; ++j) {
                     uint4 tv[NV];
                     load_chunk<T, NV>(slot_t + (size_t)j * CH, lane, tv);
-                    const float v = fold8(LN::exp_sum(tv, mu, c));
-                    if (lane < 8)
-                        stats[j * 8 + lane] = make_float2(v, 0.0f);
+                    float sv[NV];
+                    LN::exp_strips(tv, mu, c, sv);
+                    strip_partials<NV>(sv, lane, stats + (size_t)j * NV * 4);
+                    float v = 0.0f;
+#pragma unroll
+                    for (int k = 0; k < NV; ++k)
+                        v += sv[k];
                     float t, e;
                     two_sum(acc, v, t, e);
                     acc = t;
@@ -776,7 +973,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32) sv_sweep_kernel(const Args a)
                 }
                 __syncwarp();
             }
-            part = make_float4(mm, sum_or_special(lane < 8 ? acc + cmp : 0.0f), -INFINITY, 0.0f);
+            part = make_float4(mm, sum_or_special(acc + cmp), -INFINITY, 0.0f);
         }
         if (broken)
             part.x = NAN;   // poisons the row in every warp of the cluster
@@ -799,7 +996,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32) sv_sweep_kernel(const Args a)
         // ---- combine all partials and decide (every warp alike) ----
         const float4 xv = lane < P ? xbuf[p * P + lane]
                                    : make_float4(-INFINITY, __int_as_float(INT_MAX), -INFINITY, 0.0f);
-        const Tok tkb = shfl_tok(tk);
+        const TokF tkb = shfl_tok<T>(tk);
         const size_t pos = (size_t)row.b * Kmax + row.i;   // diagnostics index (test rows)
         int dec = kDecInvalid;
         bool redo = false;
@@ -823,9 +1020,20 @@ __global__ void __launch_bounds__(kMaxWarps * 32) sv_sweep_kernel(const Args a)
             const bool any_inf = __any_sync(kFull, has && (isinf(xv.y) || isinf(xv.w)));
             const bool any_nan =
                 __any_sync(kFull, has && (isnan(xv.x) || isnan(xv.y) || isnan(xv.z) || isnan(xv.w)));
-            redo = test && !(row.flags & kFMaxRef) && ref_ok && !broken && any_inf && !any_nan;
-            combine_ms2(xv.x, xv.y, xv.z, xv.w, c, m_t, St, m_d, Sd);
-            row_ok = !redo && usable && tkb.ok && isfinite(m_t) && St > 0.0f && isfinite(St) &&
+            const bool refmode = test && !(row.flags & kFMaxRef) && ref_ok;
+            redo = refmode && !broken && any_inf && !any_nan;
+            if (refmode) {
+                // every warp weighed against the proposal's logits: the
+                // partials share that reference and simply add
+                m_t = ref_t;
+                m_d = ref_d;
+                St = has ? xv.y : 0.0f;
+                Sd = has ? xv.w : 0.0f;
+                warp_sum_comp2(St, Sd);
+            } else {
+                combine_ms2(xv.x, xv.y, xv.z, xv.w, c, m_t, St, m_d, Sd);
+            }
+            row_ok = !redo && !any_nan && usable && tkb.ok && isfinite(m_t) && St > 0.0f && isfinite(St) &&
                      (!draft || (isfinite(m_d) && Sd > 0.0f && isfinite(Sd)));
             inv_st = row_ok ? __frcp_rn(St) : 0.0f;
             inv_sd = row_ok && draft ? __frcp_rn(Sd) : 0.0f;
@@ -864,12 +1072,13 @@ __global__ void __launch_bounds__(kMaxWarps * 32) sv_sweep_kernel(const Args a)
                 uint4 tv[NV], dv[NV];
                 load_chunk<T, NV>(slot_t + (size_t)j * CH, lane, tv);
                 load_chunk<T, NV>(slot_d + (size_t)j * CH, lane, dv);
-                float rs, ps;
-                LN::resid_sums(tv, dv, m_t, inv_st, m_d, inv_sd, c, rs, ps);
-                rs = fold8(rs);
-                ps = fold8(ps);
-                if (lane < 8)
-                    stats[j * 8 + lane] = make_float2(rs, ps);
+                float rsv[NV], ps;
+                LN::resid_strips(tv, dv, m_t, inv_st, m_d, inv_sd, c, rsv, ps);
+                strip_partials<NV>(rsv, lane, stats + (size_t)j * NV * 4);
+                float rs = 0.0f;
+#pragma unroll
+                for (int k = 0; k < NV; ++k)
+                    rs += rsv[k];
                 float t, e;
                 two_sum(rs_s, rs, t, e);
                 rs_s = t;
@@ -879,8 +1088,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32) sv_sweep_kernel(const Args a)
                 ps_c += e;
             }
             __syncwarp();
-            rs_s = lane < 8 ? rs_s + rs_c : 0.0f;
-            ps_s = lane < 8 ? ps_s + ps_c : 0.0f;
+            rs_s += rs_c;
+            ps_s += ps_c;
             warp_sum_comp2(rs_s, ps_s);
             rs_c = 0.0f;
             ps_c = 0.0f;
@@ -911,10 +1120,10 @@ __global__ void __launch_bounds__(kMaxWarps * 32) sv_sweep_kernel(const Args a)
             const float ufb = __shfl_sync(kFull, uf, 0);
             if (dec == kDecInvalid || (!greedy && !(ufb >= 0.0f && ufb < 1.0f))) {
                 if (writer)
-                    write_outputs(row.b, n, -1);
+                    write_outputs(row.b, n, -1, cur_sv.tok);
             } else if (greedy) {
                 if (writer)
-                    write_outputs(row.b, n, gtok);
+                    write_outputs(row.b, n, gtok, cur_sv.tok);
             } else {
                 // per-warp masses of the distribution drawn from: the residual
                 // (zero residual mass: p of the same row), or p at the bonus row
@@ -950,87 +1159,54 @@ __global__ void __launch_bounds__(kMaxWarps * 32) sv_sweep_kernel(const Args a)
                 }
                 if (owner < 0) {
                     if (writer)
-                        write_outputs(row.b, n, -1);
+                        write_outputs(row.b, n, -1, cur_sv.tok);
                 } else if (owner == g) {
-                    // this warp holds the token: its chunk, then the element
-                    // chunk masses: the sums of the chunk's eight partials (the
-                    // bonus pass summed against this warp's own maximum, the
-                    // max of partial g)
+                    // this warp holds the token: its chunk, the strip, then the
+                    // element.  Zero residual mass: p's strip sums are made
+                    // first (the residual pass kept only p's warp totals).
+                    if (!bonus && !use_r) {
+                        for (int j = 0; j < kwm; ++j) {
+                            uint4 tv[NV];
+                            load_chunk<T, NV>(slot_t + (size_t)j * CH, lane, tv);
+                            float sv[NV];
+                            LN::exp_strips(tv, m_t, c, sv);
+                            strip_partials<NV>(sv, lane, stats + (size_t)j * NV * 4);
+                        }
+                        __syncwarp();
+                    }
+                    // masses: sums of the strips' four partials (the bonus pass
+                    // summed against this warp's own maximum, that of partial g)
                     const float own_m = __shfl_sync(kFull, xv.x, g);
                     const float wscale = bonus ? (own_m == -INFINITY ? 0.0f : weight(own_m, m_t, c)) : 1.0f;
+                    auto strip_mass = [&](int j, int k) -> float {
+                        const float4 q = *reinterpret_cast<const float4*>(stats + ((size_t)j * NV + k) * 4);
+                        return ((q.x + q.y) + (q.z + q.w)) * wscale;
+                    };
                     auto chunk_mass = [&](int j) -> float {
-                        float s8 = 0.0f;
+                        float m = 0.0f;
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            const float2 sj = stats[j * 8 + e];
-                            s8 += bonus ? sj.x : (use_r ? sj.x : sj.y);
-                        }
-                        return bonus ? s8 * wscale : s8;
+                        for (int k = 0; k < NV; ++k)
+                            m += strip_mass(j, k);
+                        return m;
                     };
                     float tc = t;
-                    const int jc = select_cdf(kwm, chunk_mass, tc, beyond, lane);
                     int token = -1;
+                    const int jc = select_cdf(kwm, chunk_mass, tc, beyond, lane);
                     if (jc >= 0) {
-                        // the element, in the chunk's own layout: strip k (vector
-                        // k of every lane) holds elements (k * 32 + lane) * E + e,
-                        // so index order is strip, then lane, then e.  Strip by
-                        // strip: each lane's E terms, a warp scan of their sums,
-                        // the lane that holds the point, then its element.
-                        uint4 tv[NV], dv[NV];
-                        load_chunk<T, NV>(slot_t + (size_t)jc * CH, lane, tv);
-                        if (use_r)
-                            load_chunk<T, NV>(slot_d + (size_t)jc * CH, lane, dv);
-                        float base_s = 0.0f, base_c = 0.0f;   // mass of earlier strips
-                        int cand = -1, lastpos = -1;
-#pragma unroll
-                        for (int k = 0; k < NV; ++k) {
-                            float tm[E];
-                            float ls = 0.0f;
-#pragma unroll
-                            for (int e = 0; e < E; ++e) {
-                                const float et = weight(LN::elem(tv, k * E + e), m_t, c);
-                                tm[e] = use_r ? resid_term(et, inv_st, weight(LN::elem(dv, k * E + e), m_d, c), inv_sd)
-                                              : et;
-                                ls += tm[e];
-                                if (tm[e] > 0.0f)
-                                    lastpos = (k * 32 + lane) * E + e;
-                            }
-                            if (cand >= 0 || beyond)
-                                continue;
-                            float ss, sc;
-                            warp_incl_scan_comp(ls, lane, ss, sc);
-                            const float rel = (tc - base_s) - base_c;   // mass left after earlier strips
-                            const unsigned hit = __ballot_sync(kFull, ls > 0.0f && rel < ss + sc);
-                            if (hit) {
-                                const int src = __ffs(hit) - 1;
-                                const float tl = __shfl_sync(kFull, rel - ((ss - ls) + sc), src);
-                                int ce = -1, lp = -1;
-                                float cum = 0.0f;
-#pragma unroll
-                                for (int e = 0; e < E; ++e) {   // the same sums as ls
-                                    cum += tm[e];
-                                    if (tm[e] > 0.0f) {
-                                        lp = e;
-                                        if (ce < 0 && tl < cum)
-                                            ce = e;
-                                    }
-                                }
-                                ce = ce >= 0 ? ce : lp;   // rounding: the lane's last element with mass
-                                cand = __shfl_sync(kFull, (k * 32 + lane) * E + ce, src);
-                            } else {
-                                const float gs = __shfl_sync(kFull, ss, 31), gc = __shfl_sync(kFull, sc, 31);
-                                float ts, te;
-                                two_sum(base_s, gs, ts, te);
-                                base_s = ts;
-                                base_c += gc + te;
-                            }
+                        const int ks = select_cdf(NV, [&](int k) -> float { return strip_mass(jc, k); }, tc,
+                                                  beyond, lane);
+                        if (ks >= 0) {
+                            const uint4* vt = reinterpret_cast<const uint4*>(slot_t + (size_t)jc * CH);
+                            const uint4* vd = reinterpret_cast<const uint4*>(slot_d + (size_t)jc * CH);
+                            const uint4 tk = vt[ks * 32 + lane];
+                            const uint4 dk = use_r ? vd[ks * 32 + lane] : tk;
+                            const int ce = pick_in_strip<T, NV>(tk, dk, use_r, m_t, inv_st, m_d, inv_sd, c, tc,
+                                                                beyond, lane);
+                            if (ce >= 0)
+                                token = e0 + jc * CH + ks * 32 * E + ce;
                         }
-                        if (cand < 0)   // beyond the mass (rounding): the chunk's last element with mass
-                            cand = __reduce_max_sync(kFull, lastpos);
-                        if (cand >= 0)
-                            token = e0 + jc * CH + cand;
                     }
-                    write_outputs(row.b, n, (token >= 0 && token < V) ? token : -1);
+                    write_outputs(row.b, n, (token >= 0 && token < V) ? token : -1, cur_sv.tok);
                 }
             }
         }
