@@ -351,30 +351,33 @@ template <int NV> struct Lane<__nv_bfloat16, NV> {
     {
         const uint64_t Cc = f2_pack(c, c), NR = f2_pack(-ref_of(mt, c), -ref_of(md, c));
         const uint64_t IS = f2_pack(ist, isd);
-        float p0 = 0.0f, p1 = 0.0f;
+        // (residual, p) pairs accumulated with one packed add per element,
+        // two accumulators per strip; p's sums carried over the strips
+        float p_all = 0.0f;
 #pragma unroll
         for (int k = 0; k < NV; ++k) {
             const uint32_t wt[4] = {t[k].x, t[k].y, t[k].z, t[k].w};
             const uint32_t wd[4] = {d[k].x, d[k].y, d[k].z, d[k].w};
-            float r0 = 0.0f, r1 = 0.0f;
+            uint64_t acc0 = f2_pack(0.0f, 0.0f), acc1 = acc0;
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     float r, et;
                     resid_term2(wt[h], wd[h], half, Cc, NR, IS, r, et);
-                    if (half) {
-                        r1 += r;
-                        p1 += et;
-                    } else {
-                        r0 += r;
-                        p0 += et;
-                    }
+                    if (half)
+                        acc1 = f2_add(acc1, f2_pack(r, et));
+                    else
+                        acc0 = f2_add(acc0, f2_pack(r, et));
                 }
             }
+            float r0, e0, r1, e1;
+            f2_unpack(acc0, r0, e0);
+            f2_unpack(acc1, r1, e1);
             rs[k] = r0 + r1;
+            p_all += e0 + e1;
         }
-        ps = p0 + p1;
+        ps = p_all;
     }
     __device__ static __forceinline__ void resid_elem(const uint4& t, const uint4& d, int e, uint64_t Cc,
                                                       uint64_t NR, uint64_t IS, float& r, float& et)
@@ -461,27 +464,28 @@ template <int NV> struct Lane<float, NV> {
     {
         const uint64_t Cc = f2_pack(c, c), NR = f2_pack(-ref_of(mt, c), -ref_of(md, c));
         const uint64_t IS = f2_pack(ist, isd);
-        float p0 = 0.0f, p1 = 0.0f;
+        float p_all = 0.0f;
 #pragma unroll
         for (int k = 0; k < NV; ++k) {
             const uint32_t wt[4] = {t[k].x, t[k].y, t[k].z, t[k].w};
             const uint32_t wd[4] = {d[k].x, d[k].y, d[k].z, d[k].w};
-            float r0 = 0.0f, r1 = 0.0f;
+            uint64_t acc0 = f2_pack(0.0f, 0.0f), acc1 = acc0;
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
                 float r, et;
                 resid_term2(wt[h], wd[h], 0, Cc, NR, IS, r, et);
-                if (h & 1) {
-                    r1 += r;
-                    p1 += et;
-                } else {
-                    r0 += r;
-                    p0 += et;
-                }
+                if (h & 1)
+                    acc1 = f2_add(acc1, f2_pack(r, et));
+                else
+                    acc0 = f2_add(acc0, f2_pack(r, et));
             }
+            float r0, e0, r1, e1;
+            f2_unpack(acc0, r0, e0);
+            f2_unpack(acc1, r1, e1);
             rs[k] = r0 + r1;
+            p_all += e0 + e1;
         }
-        ps = p0 + p1;
+        ps = p_all;
     }
     __device__ static __forceinline__ void resid_elem(const uint4& t, const uint4& d, int e, uint64_t Cc,
                                                       uint64_t NR, uint64_t IS, float& r, float& et)
@@ -1178,24 +1182,17 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
                     // summed against this warp's own maximum, that of partial g)
                     const float own_m = __shfl_sync(kFull, xv.x, g);
                     const float wscale = bonus ? (own_m == -INFINITY ? 0.0f : weight(own_m, m_t, c)) : 1.0f;
-                    auto strip_mass = [&](int j, int k) -> float {
-                        const float4 q = *reinterpret_cast<const float4*>(stats + ((size_t)j * NV + k) * 4);
-                        return ((q.x + q.y) + (q.z + q.w)) * wscale;
-                    };
-                    auto chunk_mass = [&](int j) -> float {
-                        float m = 0.0f;
-#pragma unroll
-                        for (int k = 0; k < NV; ++k)
-                            m += strip_mass(j, k);
-                        return m;
+                    // strips in index order: chunk j's strip k is entry j * NV + k
+                    auto strip_mass = [&](int q) -> float {
+                        const float4 v = *reinterpret_cast<const float4*>(stats + (size_t)q * 4);
+                        return ((v.x + v.y) + (v.z + v.w)) * wscale;
                     };
                     float tc = t;
                     int token = -1;
-                    const int jc = select_cdf(kwm, chunk_mass, tc, beyond, lane);
-                    if (jc >= 0) {
-                        const int ks = select_cdf(NV, [&](int k) -> float { return strip_mass(jc, k); }, tc,
-                                                  beyond, lane);
-                        if (ks >= 0) {
+                    const int js = select_cdf(kwm * NV, strip_mass, tc, beyond, lane);
+                    if (js >= 0) {
+                        const int jc = js / NV, ks = js % NV;
+                        {
                             const uint4* vt = reinterpret_cast<const uint4*>(slot_t + (size_t)jc * CH);
                             const uint4* vd = reinterpret_cast<const uint4*>(slot_d + (size_t)jc * CH);
                             const uint4 tk = vt[ks * 32 + lane];
