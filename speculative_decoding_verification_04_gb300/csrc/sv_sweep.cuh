@@ -1039,20 +1039,29 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
             }
             row_ok = !redo && !any_nan && usable && tkb.ok && isfinite(m_t) && St > 0.0f && isfinite(St) &&
                      (!draft || (isfinite(m_d) && Sd > 0.0f && isfinite(Sd)));
-            inv_st = row_ok ? __frcp_rn(St) : 0.0f;
-            inv_sd = row_ok && draft ? __frcp_rn(Sd) : 0.0f;
             bool accept = false;
-            float px = NAN, qx = NAN;
             if (test && row_ok) {
-                px = __fmul_rn(weight(tkb.lt, m_t, c), inv_st);
-                qx = __fmul_rn(weight(tkb.ld, m_d, c), inv_sd);
-                accept = __fmul_rn(tkb.u, qx) < px;   // u < min(1, p/q) without a division
+                if (refmode) {
+                    // p(x) = w_t(x) / S_t and q(x) = w_d(x) / S_d, both weights
+                    // taken against themselves (exp2(0) = 1): u < min(1, p/q)
+                    // reads u S_t < S_d, with no exponential or division
+                    accept = __fmul_rn(tkb.u, St) < Sd;
+                } else {
+                    const float px = __fmul_rn(weight(tkb.lt, m_t, c), __frcp_rn(St));
+                    const float qx = __fmul_rn(weight(tkb.ld, m_d, c), __frcp_rn(Sd));
+                    accept = __fmul_rn(tkb.u, qx) < px;   // u < min(1, p/q) without a division
+                }
             }
             dec = redo ? kDecRedo
                        : (!row_ok ? kDecInvalid : (test ? (accept ? kDecAccept : kDecReject) : kDecBonus));
+            // the inverse sums, where the residual pass or the diagnostics need them
+            if (row_ok && (dec == kDecReject || !a.early_exit || a.want_pq)) {
+                inv_st = __frcp_rn(St);
+                inv_sd = draft ? __frcp_rn(Sd) : 0.0f;
+            }
             if (writer && lane == 0 && test && a.want_pq && !redo) {
-                a.p_x[pos] = px;
-                a.q_x[pos] = qx;
+                a.p_x[pos] = row_ok ? __fmul_rn(weight(tkb.lt, m_t, c), inv_st) : NAN;
+                a.q_x[pos] = row_ok ? __fmul_rn(weight(tkb.ld, m_d, c), inv_sd) : NAN;
             }
         }
         if (want_claim) {
