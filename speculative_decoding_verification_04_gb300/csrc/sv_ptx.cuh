@@ -137,6 +137,13 @@ __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uin
         ::"r"(dst), "l"(src), "r"(bytes), "r"(mbar) : "memory");
 }
 
+// Bring [src, src + bytes) into L2 ahead of its bulk copy (16-byte aligned
+// address, size a multiple of 16); no completion is tracked.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // Order this thread's earlier generic-proxy shared-memory accesses before its
 // later bulk-copy (async-proxy) writes into the same buffer.
 __device__ __forceinline__ void fence_proxy_async()

@@ -826,6 +826,21 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
         __syncwarp();
         return all;
     };
+    // The spare sequence's first row is read whatever the current rows
+    // decide, so this warp's range of it is brought into L2 as soon as the
+    // spare is known: its target row at once, its draft row (sampling
+    // sequences with a tested row only) once the spare's K and T have loaded.
+    bool pf_draft = false;   // the spare's draft row is still to prefetch
+    const int nb_pf = a.aligned ? ((n_el * (int)sizeof(T)) & ~15) / (int)sizeof(T) : 0;
+    auto prefetch_target = [&](int b) {
+        if (lane == 0 && nb_pf > 0)
+            bulk_prefetch_l2(tgt + (size_t)b * (Kmax + 1) * (size_t)V + e0, (uint32_t)nb_pf * (uint32_t)sizeof(T));
+    };
+    auto prefetch_draft = [&]() {
+        if (lane == 0 && nb_pf > 0 && spare >= 0 && a.has_draft && spare_pos.Kb > 0 && spare_pos.T != 0.0f)
+            bulk_prefetch_l2(drf + (size_t)spare * Kmax * (size_t)V + e0, (uint32_t)nb_pf * (uint32_t)sizeof(T));
+    };
+
     // outputs of the current sequence b (whole warp): draft tokens before n
     // (n <= 32, from the sequence's registers), `token` at n, -1 after
     auto write_outputs = [&](int b, int n, int token, int seq_tok) {
@@ -992,6 +1007,10 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
             if (writer && want_claim)
                 st_async_s32(map_to_rank(smem_addr(&xclaim[p]), (uint32_t)lane), claimed_b, rb);
         }
+        if (pf_draft) {   // the spare's K and T have long loaded
+            prefetch_draft();
+            pf_draft = false;
+        }
         if (!mbar_wait_bounded(smem_addr(&xbar[p]), xpar, kWaitSpins))
             xbroken = true;
         if (__any_sync(kFull, xbroken))
@@ -1071,6 +1090,8 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
             if (spare >= 0) {
                 spare_pos = unit_pos(a, spare);   // loads now, used when the unit starts
                 spare_sv = seq_vals(a, spare, lane);
+                prefetch_target(spare);
+                pf_draft = true;
             }
         }
 
@@ -1115,6 +1136,10 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
                 const uint32_t rb = map_to_rank(smem_addr(&xbar2[p2]), (uint32_t)lane);
                 const uint32_t dst = map_to_rank(smem_addr(&xbuf2[p2 * P + g]), (uint32_t)lane);
                 st_async_v2(dst, make_float2(rs_s + rs_c, ps_s + ps_c), rb);
+            }
+            if (pf_draft) {
+                prefetch_draft();
+                pf_draft = false;
             }
             if (!mbar_wait_bounded(smem_addr(&xbar2[p2]), par2, kWaitSpins))
                 xbroken = true;
