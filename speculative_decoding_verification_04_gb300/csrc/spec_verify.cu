@@ -207,7 +207,10 @@ static bool shape_geometry(int V, sv_dtype dt, int C, int nw, Geom* g)
     // no CTA without chunks
     if ((long long)(C - 1) * nw * g->kw >= g->nchunks)
         return false;
-    g->smem = sweep_layout(nw, g->kw, g->ch * s, C * nw).total;
+    const SweepLayout L = sweep_layout(nw, g->kw, g->ch * s, C * nw);
+    if (!sweep_layout_aligned(L))   // never launch a layout the kernel cannot address
+        return false;
+    g->smem = L.total;
     return g->smem <= (size_t)kSmemPerCtaMax;
 }
 

@@ -79,10 +79,21 @@ __host__ __device__ inline SweepLayout sweep_layout(int nw, int kw, int chunk_by
     o += 8;
     L.first = o;
     o += 8;
+    o = (o + 15) & ~(size_t)15;   // stats are read as 16-byte vectors
     L.stats = o;
     o += (size_t)nw * kw * 8 * 8;
     L.total = o;
     return L;
+}
+
+// The alignments the kernel's shared-memory accesses rely on: 16-byte
+// vectors (slots, row partials, strip partials), 8-byte mbarriers, residual
+// totals and claims.
+__host__ __device__ inline bool sweep_layout_aligned(const SweepLayout& L)
+{
+    return L.slot_bytes % 16 == 0 && L.bars % 8 == 0 && L.xbar % 8 == 0 && L.xbar2 % 8 == 0 &&
+           L.xbuf % 16 == 0 && L.xbuf2 % 8 == 0 && L.xclaim % 4 == 0 && L.first % 4 == 0 &&
+           L.stats % 16 == 0;
 }
 
 // Row flags, from the sequence's K_b and T alone.
