@@ -129,6 +129,23 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t addr, uint32_t parity
 }
 
 // 1-D bulk copy global -> shared; src, dst 16-byte aligned, bytes % 16 == 0.
+// An L2 cache policy that evicts first what it tags: rows that are read once.
+__device__ __forceinline__ uint64_t l2_evict_first_policy()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// As bulk_copy_g2s, the source lines tagged with an L2 cache policy.
+__device__ __forceinline__ void bulk_copy_g2s_hint(uint32_t dst, const void* src, uint32_t bytes,
+                                                   uint32_t mbar, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
+        ::"r"(dst), "l"(src), "r"(bytes), "r"(mbar), "l"(policy) : "memory");
+}
+
 __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes,
                                               uint32_t mbar)
 {

@@ -812,9 +812,12 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
             if (tx) {
                 fence_proxy_async();
                 mbar_arrive_expect_tx(bar, tx);
-                bulk_copy_g2s(smem_addr(slot_t), tr, bytes, bar);
+                // each row is read once: its lines go first from L2, ahead
+                // of prefetched rows and the small per-row arrays
+                const uint64_t pol = l2_evict_first_policy();
+                bulk_copy_g2s_hint(smem_addr(slot_t), tr, bytes, bar, pol);
                 if (ld)
-                    bulk_copy_g2s(smem_addr(slot_d), dr, bytes, bar);
+                    bulk_copy_g2s_hint(smem_addr(slot_d), dr, bytes, bar, pol);
             } else {
                 mbar_arrive(bar);
             }
