@@ -369,6 +369,60 @@ def run_ours(args):
     return 0
 
 
+def run_sample(args):
+    """The draft-side sampler (spec_sample): one token per row of the
+    workload's row-0 target logits [B, V], L2 flushed before every step.  An
+    auxiliary measurement beside the verification headline."""
+    import torch
+
+    import speculative_decoding_verification_04_gb300 as sv
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    d = W.make_device(args.workload, dev, B=args.sequences)
+    B, V = d["B"], d["V"]
+    code = sv.SV_DTYPE_BF16 if d["dtype"] == "bf16" else sv.SV_DTYPE_F32
+    logits = d["target"][:, 0, :].contiguous()
+    uni = d["uniforms"][:, 0].contiguous()
+    temp = d["temperature"]
+    ws = torch.empty(sv.sv_sample_workspace_size(B, V, code), dtype=torch.uint8, device=dev)
+    out = torch.empty(B, dtype=torch.int32, device=dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 1 << 30), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(max(args.warmup, 3)):
+        flush.fill_(1)
+        sv.spec_sample(logits, uni, temp, workspace=ws, out_tokens=out)
+    torch.cuda.synchronize()
+    evs = []
+    for _ in range(args.steps):
+        flush.fill_(1)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        sv.spec_sample(logits, uni, temp, workspace=ws, out_tokens=out)
+        e1.record(stream)
+        evs.append((e0, e1))
+    torch.cuda.synchronize()
+    times = [a.elapsed_time(b) for a, b in evs]
+    med = statistics.median(times)
+    s_el = 2 if d["dtype"] == "bf16" else 4
+    nbytes = B * V * s_el
+    peaks = _peaks()
+    achieved = nbytes / (med / 1e3) / 1e9
+    line = dict(metric="sampled rows/sec (spec_sample, one draw per row)", value=B / (med / 1e3),
+                unit="rows/s", n_gpus=1, steps=args.steps, warmup=args.warmup, ms_per_step=med,
+                higher_is_better=True, dtype=d["dtype"], data="synthetic",
+                config=dict(workload=f"row 0 of each sequence of: {WORKLOAD_TEXT[args.workload]}",
+                            B=B, V=V, l2="flushed before every step"),
+                roofline=dict(bound="hbm", achieved=round(achieved, 1), peak=peaks["hbm_gbs"],
+                              unit="GB/s", frac=round(achieved / peaks["hbm_gbs"], 4),
+                              bytes_algorithmic=nbytes, kernel="sv_sweep_kernel"),
+                gpu_launches=args.steps)
+    print(json.dumps(line))
+    return 0
+
+
 def _rows_to_host(d, seqs):
     import torch
     idx = torch.as_tensor(np.asarray(seqs), device=d["target"].device, dtype=torch.long)
@@ -394,11 +448,15 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sequences", type=int, default=None,
                     help="the workload's first N sequences only (profiling captures)")
+    ap.add_argument("--op", choices=["verify", "sample"], default="verify",
+                    help="sample: time the draft-side sampler (spec_sample) instead")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.op == "sample":
+        return run_sample(args)
     return run_ours(args)
 
 

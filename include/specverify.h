@@ -58,7 +58,7 @@
 extern "C" {
 #endif
 
-#define SV_ABI_VERSION 1
+#define SV_ABI_VERSION 2
 /* Largest per-sequence draft count: one warp ballot covers the accept bits. */
 #define SV_K_MAX 32
 
@@ -90,6 +90,30 @@ typedef struct {
 } sv_diag;
 
 /*
+ * Per-call counters (device memory, accumulated: zero them before the first
+ * call they should cover).  Only the positions the method walks count: the
+ * tested positions up to and including the first rejection.
+ *   sequences   sequences with valid outputs (n_b >= 0)
+ *   invalid     sequences whose device data was unusable (n_b = -1)
+ *   tested      draft positions tested (accept tests taken)
+ *   accepted    of these, the accepted ones
+ *   committed   tokens committed: sum over valid sequences of n_b + 1
+ *   near_ties   sampling accept tests whose uniform lies within 1e-6 of its
+ *               threshold p/q (the decisions a change of summation order
+ *               could flip)
+ * The acceptance rate is accepted / tested; tokens per round is
+ * committed / sequences.
+ */
+typedef struct {
+    unsigned long long sequences;
+    unsigned long long invalid;
+    unsigned long long tested;
+    unsigned long long accepted;
+    unsigned long long committed;
+    unsigned long long near_ties;
+} sv_stats;
+
+/*
  * Options for spec_verify_ex.  Zero-initialise for defaults.
  *   diag            diagnostics (requesting any forces verify_all).
  *   verify_all      1: sweep every row, including those after the first
@@ -103,6 +127,11 @@ typedef struct {
  *   chunks_per_warp 0: automatic.  Otherwise how many of the CTA's chunks
  *                   each warp holds (tuning: sets the warps per CTA, at most
  *                   8 and at most 32 / cluster size).
+ *   stats           device sv_stats to accumulate into, or NULL.
+ *   kv_len          device [B] int32, or NULL: the caller's KV-cache lengths,
+ *                   updated in place to kv_len[b] + 1 + n_b for every sequence
+ *                   with valid outputs (unchanged when n_b = -1), so that no
+ *                   host round trip is needed to commit the accepted tokens.
  * Tuning options change only the fp32 summation grouping: results agree
  * with the automatic geometry except within the rounding of those sums.
  */
@@ -111,6 +140,8 @@ typedef struct {
     int32_t verify_all;
     int32_t chunks_per_cta;
     int32_t chunks_per_warp;
+    sv_stats* stats;
+    int32_t* kv_len;
 } sv_options;
 
 /* Human-readable name of a status code (static storage). */
@@ -230,6 +261,25 @@ sv_status spec_verify_ex(const void* target_logits, const void* draft_logits, sv
  * bit 0 was set, SV_OK otherwise.
  */
 sv_status sv_workspace_errors(void* workspace, uint32_t* flags, cudaStream_t stream);
+
+/*
+ * spec_sample -- draw one token per row from softmax(logits[b] / T_b) by the
+ * inverse CDF at uniforms[b] (the draft model's own sampling step, with the
+ * machinery of the final draw: a K = 0 verification of every row).
+ *   logits        device, [B][V], dtype.
+ *   uniforms      device, [B] float32 in [0, 1).
+ *   temperature   device, [B] float32 (0 = argmax, lowest index on ties).
+ *   out_tokens    device, [B] int32 (written; -1 for a row with unusable data).
+ *   workspace     device, at least sv_sample_workspace_size(B, V, dtype) bytes,
+ *                 256-byte aligned.
+ * Errors as spec_verify_ws.
+ */
+sv_status spec_sample(const void* logits, sv_dtype dtype, const float* uniforms,
+                      const float* temperature, int32_t B, int32_t V, int32_t* out_tokens,
+                      void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Bytes of device workspace spec_sample needs (0 on invalid arguments). */
+size_t sv_sample_workspace_size(int32_t B, int32_t V, sv_dtype dtype);
 
 /*
  * Bytes of device staging spec_verify_host needs (inputs, outputs and the

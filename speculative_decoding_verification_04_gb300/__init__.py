@@ -7,11 +7,12 @@ the shared library has not been built the import of any entry point raises:
 there is no CPU fallback.
 
 Entry points (same names as the C ABI):
-  spec_verify, spec_verify_ws, spec_verify_ex, spec_verify_host,
-  sv_workspace_size, sv_host_staging_size, sv_max_vocab, sv_status_string,
-  sv_abi_version, sv_workspace_errors
-plus ``Workspace`` (a device buffer of sv_workspace_size bytes) and
-``SVOptions`` / ``SVDiag`` (the ctypes mirrors of sv_options / sv_diag).
+  spec_verify, spec_verify_ws, spec_verify_ex, spec_verify_host, spec_sample,
+  sv_workspace_size, sv_sample_workspace_size, sv_host_staging_size,
+  sv_max_vocab, sv_status_string, sv_abi_version, sv_workspace_errors
+plus ``Workspace`` (a device buffer of sv_workspace_size bytes), ``Stats``
+(a device sv_stats) and ``SVOptions`` / ``SVDiag`` (the ctypes mirrors of
+sv_options / sv_diag).
 """
 from __future__ import annotations
 
@@ -49,7 +50,11 @@ class SVDiag(ctypes.Structure):
 
 class SVOptions(ctypes.Structure):
     _fields_ = [("diag", SVDiag), ("verify_all", ctypes.c_int32),
-                ("chunks_per_cta", ctypes.c_int32), ("chunks_per_warp", ctypes.c_int32)]
+                ("chunks_per_cta", ctypes.c_int32), ("chunks_per_warp", ctypes.c_int32),
+                ("stats", ctypes.c_void_p), ("kv_len", ctypes.c_void_p)]
+
+
+STATS_FIELDS = ("sequences", "invalid", "tested", "accepted", "committed", "near_ties")
 
 
 def _load():
@@ -68,6 +73,10 @@ def _load():
     lib.spec_verify_ws.argtypes = common + [P, sz, P]
     lib.spec_verify_ex.argtypes = common + [ctypes.POINTER(SVOptions), P, sz, P]
     lib.spec_verify_host.argtypes = common + [P, sz, P]
+    lib.spec_sample.argtypes = [P, ctypes.c_int, P, P, i32, i32, P, P, sz, P]
+    lib.spec_sample.restype = ctypes.c_int
+    lib.sv_sample_workspace_size.argtypes = [i32, i32, ctypes.c_int]
+    lib.sv_sample_workspace_size.restype = sz
     for f in (lib.spec_verify, lib.spec_verify_ws, lib.spec_verify_ex, lib.spec_verify_host):
         f.restype = ctypes.c_int
     lib.sv_workspace_size.argtypes = [i32, i32, i32, ctypes.c_int]
@@ -207,6 +216,33 @@ class Workspace:
         return ctypes.c_void_p(self.buffer.data_ptr())
 
 
+class Stats:
+    """A device sv_stats (six 64-bit counters), zeroed; calls accumulate into it."""
+
+    def __init__(self, device="cuda"):
+        import torch
+        self.buffer = torch.zeros(len(STATS_FIELDS), dtype=torch.int64, device=device)
+
+    @property
+    def ptr(self):
+        return self.buffer.data_ptr()
+
+    def zero(self):
+        self.buffer.zero_()
+
+    def read(self) -> dict:
+        """The counters (synchronises), plus the acceptance rate and tokens per round."""
+        v = [int(x) for x in self.buffer.cpu().tolist()]
+        d = dict(zip(STATS_FIELDS, v))
+        d["alpha"] = d["accepted"] / d["tested"] if d["tested"] else float("nan")
+        d["tokens_per_round"] = d["committed"] / d["sequences"] if d["sequences"] else float("nan")
+        return d
+
+
+def sv_sample_workspace_size(B: int, V: int, dtype: int) -> int:
+    return int(_load().sv_sample_workspace_size(int(B), int(V), int(dtype)))
+
+
 # ---------------------------------------------------------------------------
 # entry points
 # ---------------------------------------------------------------------------
@@ -270,8 +306,11 @@ def spec_verify_ws(target, draft, draft_tokens, uniforms, temperature, K, worksp
 def spec_verify_ex(target, draft, draft_tokens, uniforms, temperature, K, workspace: Workspace,
                    diag: dict | None = None, verify_all: bool = False, chunks_per_cta: int = 0,
                    chunks_per_warp: int = 0, out_tokens=None,
-                   out_num_accepted=None, stream=None):
-    """spec_verify_ex; ``diag`` maps p_x / q_x / resid_mass / final_row to tensors."""
+                   out_num_accepted=None, stream=None, stats: "Stats | None" = None,
+                   kv_len=None):
+    """spec_verify_ex; ``diag`` maps p_x / q_x / resid_mass / final_row to tensors,
+    ``stats`` accumulates the call's counters, ``kv_len`` (int32 [B] CUDA
+    tensor) is advanced in place by 1 + n_b for every valid sequence."""
     k, kp, B, Kmax, V = _common(target, draft, draft_tokens, uniforms, temperature, K)
     out_tokens, out_num_accepted = _outputs(B, Kmax, target.device, out_tokens, out_num_accepted)
     opt = SVOptions()
@@ -284,6 +323,11 @@ def spec_verify_ex(target, draft, draft_tokens, uniforms, temperature, K, worksp
     opt.verify_all = 1 if verify_all else 0
     opt.chunks_per_cta = int(chunks_per_cta)
     opt.chunks_per_warp = int(chunks_per_warp)
+    if stats is not None:
+        opt.stats = stats.ptr
+    if kv_len is not None:
+        _require(kv_len, "kv_len")
+        opt.kv_len = kv_len.data_ptr()
     sp, _ = _stream(stream)
     st = _load().spec_verify_ex(_dptr(target), _dptr(draft), _dtype_code(target),
                                 _dptr(draft_tokens), _dptr(uniforms), _dptr(temperature), B, kp, V,
@@ -291,6 +335,31 @@ def spec_verify_ex(target, draft, draft_tokens, uniforms, temperature, K, worksp
                                 workspace.ptr, workspace.nbytes, sp)
     _check(st, "spec_verify_ex")
     return out_tokens, out_num_accepted
+
+
+def spec_sample(logits, uniforms, temperature, workspace=None, out_tokens=None, stream=None):
+    """spec_sample on torch CUDA tensors: one token per row of ``logits`` [B, V]
+    from softmax(logits / T) at ``uniforms`` [B] (argmax where T == 0); -1 for
+    a row with unusable data.  ``workspace``: a uint8 CUDA tensor of at least
+    sv_sample_workspace_size bytes (allocated here when omitted)."""
+    import torch
+    if logits.dim() != 2:
+        raise ValueError("logits must be [B, V]")
+    B, V = int(logits.shape[0]), int(logits.shape[1])
+    code = _dtype_code(logits)
+    for t, n in ((logits, "logits"), (uniforms, "uniforms"), (temperature, "temperature")):
+        _require(t, n)
+    if out_tokens is None:
+        out_tokens = torch.empty(B, dtype=torch.int32, device=logits.device)
+    if workspace is None:
+        workspace = torch.empty(max(1, sv_sample_workspace_size(B, V, code)), dtype=torch.uint8,
+                                device=logits.device)
+    sp, _ = _stream(stream)
+    st = _load().spec_sample(_dptr(logits), code, _dptr(uniforms), _dptr(temperature), B, V,
+                             _dptr(out_tokens), ctypes.c_void_p(workspace.data_ptr()),
+                             workspace.numel(), sp)
+    _check(st, "spec_sample")
+    return out_tokens
 
 
 def spec_verify_host(target, draft, draft_tokens, uniforms, temperature, K, staging,

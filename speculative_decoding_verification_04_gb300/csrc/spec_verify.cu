@@ -543,6 +543,10 @@ static sv_status run(const Call& c, int kmax, const sv_options* opt, void* ws, s
     a.want_pq = a.p_x != nullptr ? 1 : 0;
     a.want_resid = a.resid != nullptr ? 1 : 0;
     a.want_final = a.final_row != nullptr ? 1 : 0;
+    a.want_stats = (opt && opt->stats) ? 1 : 0;
+    a.stats = a.want_stats ? reinterpret_cast<unsigned long long*>(opt->stats) : nullptr;
+    a.want_kv = (opt && opt->kv_len) ? 1 : 0;
+    a.kv_len = a.want_kv ? opt->kv_len : nullptr;
 
     const cudaError_t e = c.dtype == SV_DTYPE_BF16 ? launch_nv<__nv_bfloat16>(a, g, stream, dev)
                                                    : launch_nv<float>(a, g, stream, dev);
@@ -638,7 +642,42 @@ sv_status spec_verify_ex(const void* target_logits, const void* draft_logits, sv
         return st;
     if (options && (options->chunks_per_cta < 0 || options->chunks_per_warp < 0))
         return SV_ERR_INVALID_ARG;
+    if (options && ((((uintptr_t)options->stats) & 7) || (((uintptr_t)options->kv_len) & 3)))
+        return SV_ERR_INVALID_ARG;   // 64-bit counters, 32-bit lengths
     return sv::run(c, kmax, options, workspace, workspace_bytes, stream);
+}
+
+size_t sv_sample_workspace_size(int32_t B, int32_t V, sv_dtype dtype)
+{
+    const size_t ws = sv_workspace_size(B, 0, V, dtype);
+    if (!ws)
+        return 0;
+    return ws + sv::align256((size_t)(B > 0 ? B : 1) * 4);   // + the per-row validity words
+}
+
+sv_status spec_sample(const void* logits, sv_dtype dtype, const float* uniforms,
+                      const float* temperature, int32_t B, int32_t V, int32_t* out_tokens,
+                      void* workspace, size_t workspace_bytes, cudaStream_t stream)
+{
+    if (B < 0)
+        return SV_ERR_INVALID_ARG;
+    // a K = 0 verification of every row: row 0 is the final draw, from p
+    thread_local std::vector<int32_t> zeros;
+    zeros.assign((size_t)B, 0);
+    const size_t ws_bytes = sv_workspace_size(B, 0, V, dtype);
+    int32_t* out_n = (workspace && ws_bytes) ? reinterpret_cast<int32_t*>(
+                                                   static_cast<unsigned char*>(workspace) + ws_bytes)
+                                             : nullptr;
+    const sv::Call c{logits, nullptr, dtype, nullptr, uniforms, temperature,
+                     B, zeros.data(), V, out_tokens, out_n ? out_n : out_tokens};
+    int kmax = 0;
+    const sv_status st = sv::check_args(c, &kmax);
+    if (st != SV_OK || B == 0)
+        return st;
+    const size_t need = sv_sample_workspace_size(B, V, dtype);
+    if (!workspace || !need || workspace_bytes < need || ((uintptr_t)workspace & 255))
+        return SV_ERR_NO_MEMORY;
+    return sv::run(c, 0, nullptr, workspace, ws_bytes, stream);
 }
 
 sv_status spec_verify_ws(const void* target_logits, const void* draft_logits, sv_dtype dtype,

@@ -56,6 +56,10 @@ struct Args {
     int* next_unit;        // claim counter of the persistent sweep
     const int32_t* K;
     const int32_t* order;  // sequences in claim order (longest K first)
+    // per-call counters and the caller's KV lengths (used only if flagged)
+    int want_stats, want_kv;
+    unsigned long long* stats;   // sv_stats: sequences, invalid, tested, accepted, committed, near_ties
+    int32_t* kv_len;
     // diagnostics (nullable)
     float* p_x;
     float* q_x;

@@ -855,8 +855,13 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
             bulk_prefetch_l2(drf + (size_t)spare * Kmax * (size_t)V + e0, (uint32_t)nb_pf * (uint32_t)sizeof(T));
     };
 
+    // per-warp counters (lane 0), added to the call's sv_stats at exit
+    uint32_t c_seq = 0, c_inv = 0, c_test = 0, c_acc = 0, c_commit = 0, c_tie = 0;
+
     // outputs of the current sequence b (whole warp): draft tokens before n
-    // (n <= 32, from the sequence's registers), `token` at n, -1 after
+    // (n <= 32, from the sequence's registers), `token` at n, -1 after.  Each
+    // sequence's outputs are written exactly once, so its KV length is
+    // committed here too.
     auto write_outputs = [&](int b, int n, int token, int seq_tok) {
         const bool bad = token < 0;
         int32_t* orow = a.out_tok + (size_t)b * (Kmax + 1);
@@ -866,6 +871,14 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
             a.out_n[b] = bad ? -1 : n;
             if (a.want_final)
                 a.final_row[b] = bad ? -1 : n;
+            if (a.want_kv && !bad)
+                a.kv_len[b] += n + 1;
+            if (bad) {
+                ++c_inv;
+            } else {
+                ++c_seq;
+                c_commit += (uint32_t)n + 1u;
+            }
         }
     };
 
@@ -1037,6 +1050,7 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
         const size_t pos = (size_t)row.b * Kmax + row.i;   // diagnostics index (test rows)
         int dec = kDecInvalid;
         bool redo = false;
+        bool near_tie = false;   // the uniform within 1e-6 of p/q (sampling tests)
         int gtok = -1;
         float m_t = 0.0f, m_d = 0.0f, inv_st = 0.0f, inv_sd = 0.0f;
         bool row_ok = false;
@@ -1079,10 +1093,12 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
                     // taken against themselves (exp2(0) = 1): u < min(1, p/q)
                     // reads u S_t < S_d, with no exponential or division
                     accept = __fmul_rn(tkb.u, St) < Sd;
+                    near_tie = fabsf(__fmaf_rn(tkb.u, St, -Sd)) < 1e-6f * St;
                 } else {
                     const float px = __fmul_rn(weight(tkb.lt, m_t, c), __frcp_rn(St));
                     const float qx = __fmul_rn(weight(tkb.ld, m_d, c), __frcp_rn(Sd));
                     accept = __fmul_rn(tkb.u, qx) < px;   // u < min(1, p/q) without a division
+                    near_tie = fabsf(__fmaf_rn(tkb.u, qx, -px)) < 1e-6f * qx;
                 }
             }
             dec = redo ? kDecRedo
@@ -1096,6 +1112,12 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
                 a.p_x[pos] = row_ok ? __fmul_rn(weight(tkb.lt, m_t, c), inv_st) : NAN;
                 a.q_x[pos] = row_ok ? __fmul_rn(weight(tkb.ld, m_d, c), inv_sd) : NAN;
             }
+        }
+        // counters: the tested positions the method walks (up to the stop)
+        if (writer && lane == 0 && a.want_stats && test && !drawn && (dec == kDecAccept || dec == kDecReject)) {
+            ++c_test;
+            c_acc += dec == kDecAccept ? 1u : 0u;
+            c_tie += near_tie ? 1u : 0u;
         }
         if (want_claim) {
             const int cl = xclaim[p];
@@ -1290,6 +1312,15 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
             if (!cont)
                 uf = final_uniform(a, row);
         }
+    }
+
+    // ---- this warp's counters into the call's sv_stats ----
+    if (a.want_stats && lane == 0) {
+        const uint32_t cs[6] = {c_seq, c_inv, c_test, c_acc, c_commit, c_tie};
+#pragma unroll
+        for (int k = 0; k < 6; ++k)
+            if (cs[k])
+                atomicAdd(a.stats + k, (unsigned long long)cs[k]);
     }
 
     // ---- wind-down: a fill still in flight (only after a timeout), then

@@ -40,7 +40,7 @@ def test_status_strings_and_version():
                        (3, "SV_ERR_UNSUPPORTED"), (4, "SV_ERR_NO_MEMORY"), (5, "SV_ERR_TIMEOUT")]:
         assert sv.sv_status_string(code) == name
     assert sv.sv_status_string(99) == "SV_UNKNOWN_STATUS"
-    assert sv.sv_abi_version() == 1
+    assert sv.sv_abi_version() == 2
 
 
 def test_limits_and_workspace_sizes():
@@ -106,3 +106,43 @@ def test_python_binding_refuses_cpu_tensors():
     with pytest.raises(ValueError):
         sv.spec_verify(t, t[:, :1], torch.zeros((1, 1), dtype=torch.int32),
                        torch.zeros((1, 2)), torch.ones(1), [1])
+
+
+def test_sample_entry_validation():
+    """spec_sample rejects bad arguments on the host (fake, never dereferenced
+    pointers), and its workspace size follows from B, V and dtype."""
+    lib = sv.library()
+    P = lambda f: ctypes.c_void_p(0x1000) if f else None  # noqa: E731
+
+    def call(B=4, V=10, dtype=0, lg=1, uni=1, tmp=1, out=1, ws=1, nbytes=1 << 20):
+        w = ctypes.c_void_p(0x100000) if ws else None
+        return lib.spec_sample(P(lg), dtype, P(uni), P(tmp), B, V, P(out), w, nbytes, None)
+
+    assert call(B=0) == sv.SV_OK
+    assert call(B=-1) == sv.SV_ERR_INVALID_ARG
+    assert call(V=0) == sv.SV_ERR_INVALID_ARG
+    assert call(dtype=3) == sv.SV_ERR_INVALID_ARG
+    assert call(lg=0) == sv.SV_ERR_INVALID_ARG
+    assert call(uni=0) == sv.SV_ERR_INVALID_ARG
+    assert call(tmp=0) == sv.SV_ERR_INVALID_ARG
+    assert call(out=0) == sv.SV_ERR_INVALID_ARG
+    assert call(ws=0) == sv.SV_ERR_NO_MEMORY
+    assert call(nbytes=16) == sv.SV_ERR_NO_MEMORY
+    n = sv.sv_sample_workspace_size(64, 128256, sv.SV_DTYPE_BF16)
+    assert n > sv.sv_workspace_size(64, 0, 128256, sv.SV_DTYPE_BF16) and n % 256 == 0
+    assert sv.sv_sample_workspace_size(-1, 10, 0) == 0
+    assert sv.sv_sample_workspace_size(4, 0, 0) == 0
+
+
+def test_option_pointer_alignment_is_checked():
+    """sv_stats holds 64-bit counters and kv_len 32-bit lengths: misaligned
+    option pointers are refused before any work."""
+    lib = sv.library()
+    P = lambda: ctypes.c_void_p(0x1000)  # noqa: E731
+    k = np.asarray([1, 2], np.int32)
+    for field, addr in (("stats", 0x1004), ("kv_len", 0x1002)):
+        opt = sv.SVOptions()
+        setattr(opt, field, addr)
+        st = lib.spec_verify_ex(P(), P(), 0, P(), P(), P(), 2, k.ctypes.data_as(ctypes.c_void_p), 10,
+                                P(), P(), ctypes.byref(opt), ctypes.c_void_p(0x100000), 1 << 20, None)
+        assert st == sv.SV_ERR_INVALID_ARG, field

@@ -1,0 +1,109 @@
+"""GPU tests of the entry points beside verification: the draft-side sampler
+(spec_sample), the per-call counters (sv_stats) and the on-device KV-length
+commit (kv_len).  Each is checked against the oracle or against what the
+verified outputs imply."""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import speculative_decoding_verification_04_gb300 as sv  # noqa: E402
+import workloads as W  # noqa: E402
+from helpers import compare, dtype_code, oracle_ref, run_gpu, to_device  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    d = torch.device("cuda:0")
+    torch.cuda.set_device(d)
+    return d
+
+
+@pytest.mark.parametrize("dtype,V,B", [("bf16", 9000, 64), ("f32", 7001, 40), ("bf16", 128256, 48),
+                                       ("f32", 151936, 16), ("bf16", 3, 32)])
+def test_spec_sample_is_the_oracles_draw_from_p(dev, dtype, V, B):
+    """One token per row from softmax(l / T) (argmax at T = 0): the final draw
+    of a K = 0 verification, which the oracle defines; bit-exact outside the
+    oracle's tie band."""
+    temps = np.where(np.arange(B) % 4 == 0, 0.0, np.where(np.arange(B) % 4 == 1, 0.7, 1.0))
+    inp = W.make_host(B, 0, V, dtype, 2.0, 1.0, temps.astype(np.float32), seed=V % 1000 + B)
+    ref = oracle_ref(inp)
+    d = to_device(inp, dev)
+    logits = d["target"].view(B, V)
+    out = sv.spec_sample(logits, d["uniforms"].view(B), d["temperature"])
+    got = out.cpu().numpy().astype(np.int32)
+    compare(ref, got.reshape(B, 1), np.zeros(B, np.int32))
+
+
+def test_spec_sample_marks_unusable_rows(dev):
+    """A NaN logit or a uniform outside [0, 1) gives -1 for that row only."""
+    import torch
+    B, V = 8, 4000
+    inp = W.make_host(B, 0, V, "f32", 2.0, 1.0, 1.0, seed=11)
+    ref = oracle_ref(inp)
+    d = to_device(inp, dev)
+    logits = d["target"].view(B, V).clone()
+    logits[2, 17] = float("nan")
+    uni = d["uniforms"].view(B).clone()
+    uni[5] = 1.0
+    got = sv.spec_sample(logits, uni, d["temperature"]).cpu().numpy()
+    assert got[2] == -1 and got[5] == -1
+    keep = [b for b in range(B) if b not in (2, 5)]
+    ok = ~ref["tie"][keep]
+    assert np.array_equal(got[keep][ok], ref["out_tokens"][keep, 0][ok])
+
+
+def _implied_counts(K, n):
+    valid = n >= 0
+    tested = np.where(valid, n + (n < K), 0)
+    return dict(sequences=int(valid.sum()), invalid=int((~valid).sum()), tested=int(tested.sum()),
+                accepted=int(np.where(valid, n, 0).sum()), committed=int(np.where(valid, n + 1, 0).sum()))
+
+
+def test_stats_count_the_walked_positions(dev):
+    """The counters agree with what the outputs imply (tested = n_b, plus the
+    rejected position when n_b < K_b; committed = n_b + 1), are the same
+    under verify_all (rows after the stop are not counted), and accumulate."""
+    B = 40
+    inp = W.make_host(B, W.configs.ragged_k(5, B), 6000, "bf16", 2.0, 0.6,
+                      np.where(np.arange(B) % 3 == 0, 0.0, 1.0).astype(np.float32), seed=17)
+    d = to_device(inp, dev)
+    ws = sv.Workspace(B, int(inp["Kmax"]), 6000, dtype_code("bf16"), dev)
+    st = sv.Stats(dev)
+    t, n = run_gpu(d, "ex", workspace=ws, stats=st)
+    got = st.read()
+    want = _implied_counts(np.asarray(inp["K"]), n)
+    for k, v in want.items():
+        assert got[k] == v, (k, got[k], v)
+    assert 0 <= got["near_ties"] <= got["tested"]
+    st_all = sv.Stats(dev)
+    t2, n2 = run_gpu(d, "ex", workspace=ws, stats=st_all, verify_all=True)
+    assert np.array_equal(n, n2) and st_all.read() == got
+    run_gpu(d, "ex", workspace=ws, stats=st)   # accumulates
+    again = st.read()
+    for k in want:
+        assert again[k] == 2 * got[k]
+
+
+def test_kv_len_advances_by_committed_tokens(dev):
+    """kv_len[b] += 1 + n_b for valid sequences, unchanged for invalid ones."""
+    import torch
+    B = 24
+    inp = W.make_host(B, 4, 5000, "f32", 2.0, 0.5, 1.0, seed=23)
+    inp["target"][3, 0, 10] = np.nan          # sequence 3 is invalid
+    d = to_device(inp, dev)
+    base = torch.arange(B, dtype=torch.int32, device=dev) * 100
+    kv = base.clone()
+    st = sv.Stats(dev)
+    t, n = run_gpu(d, "ex", kv_len=kv, stats=st)
+    kvh, bh = kv.cpu().numpy(), base.cpu().numpy()
+    assert n[3] == -1 and kvh[3] == bh[3]
+    valid = n >= 0
+    assert np.array_equal(kvh[valid], bh[valid] + 1 + n[valid])
+    assert st.read()["invalid"] == 1
+    compare(oracle_ref(inp), t, n)
