@@ -132,6 +132,12 @@ typedef struct {
  *                   updated in place to kv_len[b] + 1 + n_b for every sequence
  *                   with valid outputs (unchanged when n_b = -1), so that no
  *                   host round trip is needed to commit the accepted tokens.
+ *   packed_logits   0: the padded layouts above.  1: the logits of ragged
+ *                   batches packed by K: target_logits [sum_b (K[b]+1)][V]
+ *                   with sequence b's rows from row sum_{c<b} (K[c]+1), and
+ *                   draft_logits [sum_b K[b]][V] with sequence b's rows from
+ *                   row sum_{c<b} K[c].  Tokens, uniforms and outputs keep
+ *                   their padded layouts.
  * Tuning options change only the fp32 summation grouping: results agree
  * with the automatic geometry except within the rounding of those sums.
  */
@@ -142,6 +148,7 @@ typedef struct {
     int32_t chunks_per_warp;
     sv_stats* stats;
     int32_t* kv_len;
+    int32_t packed_logits;
 } sv_options;
 
 /* Human-readable name of a status code (static storage). */
@@ -167,9 +174,13 @@ sv_status sv_geometry(int32_t B, int32_t Kmax, int32_t V, sv_dtype dtype, int32_
 
 /*
  * Bytes of device workspace spec_verify_ws / spec_verify_ex need for this
- * shape (0 on invalid arguments).  The workspace holds the per-call header:
- * the error word, the claim counter, K and the order in which sequences are
- * claimed; each call uploads it afresh, so the buffer needs no clearing.
+ * shape (0 on invalid arguments).  The workspace holds the error word and
+ * the claim counter, reset by every call on its stream; the rest of the
+ * per-call header (K, the order in which sequences are claimed, the packed
+ * row starts) is read by the kernel from a pinned, device-mapped host buffer
+ * of the library's, or, where pinned memory is unavailable or the caller's
+ * own host staging is used (spec_verify_noalloc), uploaded into the
+ * workspace.  The buffer needs no clearing.
  */
 size_t sv_workspace_size(int32_t B, int32_t Kmax, int32_t V, sv_dtype dtype);
 

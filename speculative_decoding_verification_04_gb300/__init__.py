@@ -51,7 +51,8 @@ class SVDiag(ctypes.Structure):
 class SVOptions(ctypes.Structure):
     _fields_ = [("diag", SVDiag), ("verify_all", ctypes.c_int32),
                 ("chunks_per_cta", ctypes.c_int32), ("chunks_per_warp", ctypes.c_int32),
-                ("stats", ctypes.c_void_p), ("kv_len", ctypes.c_void_p)]
+                ("stats", ctypes.c_void_p), ("kv_len", ctypes.c_void_p),
+                ("packed_logits", ctypes.c_int32)]
 
 
 STATS_FIELDS = ("sequences", "invalid", "tested", "accepted", "committed", "near_ties")
@@ -307,10 +308,11 @@ def spec_verify_ex(target, draft, draft_tokens, uniforms, temperature, K, worksp
                    diag: dict | None = None, verify_all: bool = False, chunks_per_cta: int = 0,
                    chunks_per_warp: int = 0, out_tokens=None,
                    out_num_accepted=None, stream=None, stats: "Stats | None" = None,
-                   kv_len=None):
+                   kv_len=None, packed: bool = False):
     """spec_verify_ex; ``diag`` maps p_x / q_x / resid_mass / final_row to tensors,
     ``stats`` accumulates the call's counters, ``kv_len`` (int32 [B] CUDA
-    tensor) is advanced in place by 1 + n_b for every valid sequence."""
+    tensor) is advanced in place by 1 + n_b for every valid sequence; ``packed``
+    takes target [sum(K+1), V] and draft [sum(K), V] packed by K."""
     k, kp, B, Kmax, V = _common(target, draft, draft_tokens, uniforms, temperature, K)
     out_tokens, out_num_accepted = _outputs(B, Kmax, target.device, out_tokens, out_num_accepted)
     opt = SVOptions()
@@ -328,6 +330,7 @@ def spec_verify_ex(target, draft, draft_tokens, uniforms, temperature, K, worksp
     if kv_len is not None:
         _require(kv_len, "kv_len")
         opt.kv_len = kv_len.data_ptr()
+    opt.packed_logits = 1 if packed else 0
     sp, _ = _stream(stream)
     st = _load().spec_verify_ex(_dptr(target), _dptr(draft), _dtype_code(target),
                                 _dptr(draft_tokens), _dptr(uniforms), _dptr(temperature), B, kp, V,

@@ -71,7 +71,7 @@ static int n_chunks(int V, int s)
 
 // ---- workspace layout: the per-call header, uploaded by every call ----
 struct WsLayout {
-    size_t err, next_unit, K, order, header_end, total;
+    size_t err, next_unit, K, order, seq_end, cu_t, cu_d, header_end, total;
 };
 
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -88,6 +88,9 @@ static bool ws_layout(int B, int Kmax, int V, sv_dtype dt, WsLayout* L)
     o = align256(o + 16);
     L->K = o;        o = align256(o + (size_t)B * 4);
     L->order = o;    o = align256(o + (size_t)B * 4);
+    L->seq_end = o;   // the header every call uploads ends here
+    L->cu_t = o;     o = align256(o + (size_t)B * 4);
+    L->cu_d = o;     o = align256(o + (size_t)B * 4);
     L->header_end = o;
     L->total = o;
     return true;
@@ -383,15 +386,19 @@ static sv_status check_args(const Call& c, int* kmax_out)
     return SV_OK;
 }
 
-// Per host thread and device: pinned buffers the per-call header is staged in,
-// used round-robin.  An event recorded after each upload guards a buffer's
-// reuse, so a call blocks only if the GPU is kHeaderSlots calls behind.
-// Pinned staging keeps the upload asynchronous (a pageable source would make
-// the copy wait for the stream's earlier work).  The buffers live as long as
-// the thread (they are small: the header is B * (Kmax + 9) bytes and up).
-constexpr int kHeaderSlots = 4;
+// Per host thread and device: pinned, device-mapped buffers the per-call
+// header (K, the claim order, the packed row starts) is written to, used
+// round-robin.  The kernel reads the header straight from the buffer (zero
+// copy): a host-to-device copy on the copy engine, with the launch waiting on
+// it, cost more than the few kilobytes warrant.  Only the 16 bytes of error
+// word and claim counter are reset on the device, by a memset on the
+// stream.  An event recorded after each launch guards a buffer's reuse, so a
+// call blocks only if the GPU is kHeaderSlots calls behind.  The buffers live
+// as long as the thread (they are small: the header is B * 16 bytes and up).
+constexpr int kHeaderSlots = 16;
 struct HeaderSlot {
     unsigned char* buf = nullptr;
+    unsigned char* dbuf = nullptr;   // its device address
     size_t cap = 0;
     cudaEvent_t done = nullptr;
     bool used = false;
@@ -428,10 +435,17 @@ static HeaderSlot* header_slot(int dev, size_t need, sv_status* st)
         sl.buf = nullptr;
         sl.cap = 0;
         const size_t cap = std::max(need, (size_t)4096);
-        if (cudaHostAlloc(reinterpret_cast<void**>(&sl.buf), cap, cudaHostAllocDefault) !=
+        if (cudaHostAlloc(reinterpret_cast<void**>(&sl.buf), cap, cudaHostAllocMapped) !=
             cudaSuccess) {
             (void)cudaGetLastError();
             sl.buf = nullptr;
+            return nullptr;
+        }
+        if (cudaHostGetDevicePointer(reinterpret_cast<void**>(&sl.dbuf), sl.buf, 0) != cudaSuccess) {
+            (void)cudaGetLastError();
+            (void)cudaFreeHost(sl.buf);
+            sl.buf = nullptr;
+            sl.dbuf = nullptr;
             return nullptr;
         }
         sl.cap = cap;
@@ -492,7 +506,9 @@ static sv_status run(const Call& c, int kmax, const sv_options* opt, void* ws, s
             hdr = hdr_tls.data();
         }
     }
-    memset(hdr, 0, L.header_end);
+    const bool packed = opt && opt->packed_logits;
+    const size_t up_bytes = packed ? L.header_end : L.seq_end;   // row starts only when packed
+    memset(hdr, 0, up_bytes);
     memcpy(hdr + L.K, c.K, (size_t)c.B * 4);
     {
         int32_t* ord = reinterpret_cast<int32_t*>(hdr + L.order);
@@ -504,14 +520,29 @@ static sv_status run(const Call& c, int kmax, const sv_options* opt, void* ws, s
         for (int b = 0; b < c.B; ++b)
             ord[cnt[SV_K_MAX - c.K[b]]++] = b;
     }
+    if (packed) {
+        int32_t* ct = reinterpret_cast<int32_t*>(hdr + L.cu_t);
+        int32_t* cd = reinterpret_cast<int32_t*>(hdr + L.cu_d);
+        long long rt = 0, rd = 0;
+        for (int b = 0; b < c.B; ++b) {
+            ct[b] = (int32_t)rt;
+            cd[b] = (int32_t)rd;
+            rt += c.K[b] + 1;
+            rd += c.K[b];
+        }
+    }
     unsigned char* base = static_cast<unsigned char*>(ws);
-    if (cudaMemcpyAsync(base, hdr, L.header_end, cudaMemcpyHostToDevice, stream) !=
-        cudaSuccess)
-        return SV_ERR_CUDA;
+    // where the kernel reads the header: the mapped slot itself (only the
+    // error word and the claim counter live in the workspace), or the
+    // workspace after an upload (pageable staging)
+    const unsigned char* hbase = base;
     if (slot) {
-        if (cudaEventRecord(slot->done, stream) != cudaSuccess)
+        if (cudaMemsetAsync(base, 0, 16, stream) != cudaSuccess)
             return SV_ERR_CUDA;
-        slot->used = true;
+        hbase = slot->dbuf;
+    } else if (cudaMemcpyAsync(base, hdr, up_bytes, cudaMemcpyHostToDevice, stream) !=
+               cudaSuccess) {
+        return SV_ERR_CUDA;
     }
 
     Args a;
@@ -534,8 +565,8 @@ static sv_status run(const Call& c, int kmax, const sv_options* opt, void* ws, s
     a.aligned = ((al & 15) == 0) && (((size_t)c.V * g.s) % 16 == 0);
     a.err = reinterpret_cast<uint32_t*>(base + L.err);
     a.next_unit = reinterpret_cast<int*>(base + L.next_unit);
-    a.K = reinterpret_cast<const int32_t*>(base + L.K);
-    a.order = reinterpret_cast<const int32_t*>(base + L.order);
+    a.K = reinterpret_cast<const int32_t*>(hbase + L.K);
+    a.order = reinterpret_cast<const int32_t*>(hbase + L.order);
     a.p_x = want_diag ? dg->p_x : nullptr;
     a.q_x = want_diag ? dg->q_x : nullptr;
     a.resid = want_diag ? dg->resid_mass : nullptr;
@@ -543,6 +574,9 @@ static sv_status run(const Call& c, int kmax, const sv_options* opt, void* ws, s
     a.want_pq = a.p_x != nullptr ? 1 : 0;
     a.want_resid = a.resid != nullptr ? 1 : 0;
     a.want_final = a.final_row != nullptr ? 1 : 0;
+    a.packed = packed ? 1 : 0;
+    a.cu_t = reinterpret_cast<const int32_t*>(hbase + L.cu_t);
+    a.cu_d = reinterpret_cast<const int32_t*>(hbase + L.cu_d);
     a.want_stats = (opt && opt->stats) ? 1 : 0;
     a.stats = a.want_stats ? reinterpret_cast<unsigned long long*>(opt->stats) : nullptr;
     a.want_kv = (opt && opt->kv_len) ? 1 : 0;
@@ -550,6 +584,11 @@ static sv_status run(const Call& c, int kmax, const sv_options* opt, void* ws, s
 
     const cudaError_t e = c.dtype == SV_DTYPE_BF16 ? launch_nv<__nv_bfloat16>(a, g, stream, dev)
                                                    : launch_nv<float>(a, g, stream, dev);
+    if (slot) {   // the kernel reads the slot: it is free again once the kernel is done
+        if (cudaEventRecord(slot->done, stream) != cudaSuccess)
+            return SV_ERR_CUDA;
+        slot->used = true;
+    }
     return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
@@ -644,6 +683,15 @@ sv_status spec_verify_ex(const void* target_logits, const void* draft_logits, sv
         return SV_ERR_INVALID_ARG;
     if (options && ((((uintptr_t)options->stats) & 7) || (((uintptr_t)options->kv_len) & 3)))
         return SV_ERR_INVALID_ARG;   // 64-bit counters, 32-bit lengths
+    if (options && (options->packed_logits < 0 || options->packed_logits > 1))
+        return SV_ERR_INVALID_ARG;
+    if (options && options->packed_logits) {
+        long long rows = 0;   // row indices of the packed arrays must fit 32 bits
+        for (int b = 0; b < B; ++b)
+            rows += (long long)K[b] + 1;
+        if (rows > 0x7fffffffLL)
+            return SV_ERR_UNSUPPORTED;
+    }
     return sv::run(c, kmax, options, workspace, workspace_bytes, stream);
 }
 

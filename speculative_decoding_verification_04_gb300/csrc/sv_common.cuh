@@ -56,6 +56,12 @@ struct Args {
     int* next_unit;        // claim counter of the persistent sweep
     const int32_t* K;
     const int32_t* order;  // sequences in claim order (longest K first)
+    // logit layout: padded ([B][Kmax+1][V], [B][Kmax][V]) or packed by K
+    // (sequence b's rows start at row cu_t[b] of the target and cu_d[b] of the
+    // draft array)
+    int packed;
+    const int32_t* cu_t;
+    const int32_t* cu_d;
     // per-call counters and the caller's KV lengths (used only if flagged)
     int want_stats, want_kv;
     unsigned long long* stats;   // sv_stats: sequences, invalid, tested, accepted, committed, near_ties

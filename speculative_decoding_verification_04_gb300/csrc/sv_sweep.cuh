@@ -110,15 +110,18 @@ struct Row {
     int i, b, Kb;
     float T;
     int flags;
+    int tb, db;   // rows of position 0 of sequence b in the target / draft arrays
 };
 
-__device__ __forceinline__ Row make_row(const Args& a, int i, int b, int Kb, float T)
+__device__ __forceinline__ Row make_row(const Args& a, int i, int b, int Kb, float T, int tb, int db)
 {
     Row r;
     r.i = i;
     r.b = b;
     r.Kb = Kb;
     r.T = T;
+    r.tb = tb;
+    r.db = db;
     const int greedy = T == 0.0f ? kFGreedy : 0;
     const int test = i < Kb ? kFTest : 0;
     const int draft = (test && !greedy) ? kFDraft : 0;
@@ -185,11 +188,11 @@ __device__ __forceinline__ void tok_logits(const Args& a, const Row& r, Tok& t)
 {
     if (!t.ok || !(r.flags & kFTest))
         return;
-    const size_t trow = (size_t)r.b * (a.Kmax + 1) + r.i;
+    const size_t trow = (size_t)r.tb + r.i;
     t.lt = Elem<T>::load_raw(static_cast<const T*>(a.tgt) + trow * (size_t)a.V + t.x);
     if (r.flags & kFDraft)
         t.ld = Elem<T>::load_raw(static_cast<const T*>(a.drf) +
-                                 ((size_t)r.b * a.Kmax + r.i) * (size_t)a.V + t.x);
+                                 ((size_t)r.db + r.i) * (size_t)a.V + t.x);
 }
 
 // The proposal as every lane sees it, the logits widened to fp32.
@@ -241,11 +244,24 @@ __device__ __forceinline__ int ticket_check(const Args& a, int t, int b)
 struct UnitPos {
     int b, Kb;
     float T;
+    int tb, db;
 };
+
+// The rows of position 0 of sequence b: computed for the padded layout,
+// loaded for the packed one.
+__device__ __forceinline__ int seq_trow(const Args& a, int b)
+{
+    return a.packed ? __ldg(a.cu_t + b) : b * (a.Kmax + 1);
+}
+
+__device__ __forceinline__ int seq_drow(const Args& a, int b)
+{
+    return a.packed ? __ldg(a.cu_d + b) : b * a.Kmax;
+}
 
 __device__ __forceinline__ UnitPos unit_pos(const Args& a, int b)
 {
-    return UnitPos{b, __ldg(a.K + b), __ldg(a.temp + b)};
+    return UnitPos{b, __ldg(a.K + b), __ldg(a.temp + b), seq_trow(a, b), seq_drow(a, b)};
 }
 
 // The sequence's final-draw uniform (slot K_b), sampling sequences only.
@@ -779,11 +795,11 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
     bool broken = false;     // a slot wait gave up: no more copies, rows poisoned
     bool xbroken = false;    // an exchange wait gave up: leave the loop
     bool drawn = false;      // the current sequence's outputs are written
-    Row row = make_row(a, 0, 0, 0, 0.0f);
+    Row row = make_row(a, 0, 0, 0, 0.0f, 0, 0);
     SeqVals cur_sv{0, 0.0f}, spare_sv{0, 0.0f};   // the current and the spare sequence's
     if (active) {
         const UnitPos p0 = unit_pos(a, u0);
-        row = make_row(a, 0, p0.b, p0.Kb, p0.T);
+        row = make_row(a, 0, p0.b, p0.Kb, p0.T, p0.tb, p0.db);
         cur_sv = seq_vals(a, u0, lane);
     }
     Tok tk{0, 0.0f, 0u, 0u, 0};       // lane 0
@@ -803,8 +819,8 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
         if (!(r.flags & kFUsable) || broken || n_el <= 0)
             return;
         const bool ld = (r.flags & kFDraft) != 0;
-        const T* tr = tgt + ((size_t)r.b * (Kmax + 1) + r.i) * (size_t)V + e0;
-        const T* dr = ld ? drf + ((size_t)r.b * Kmax + r.i) * (size_t)V + e0 : nullptr;
+        const T* tr = tgt + ((size_t)r.tb + r.i) * (size_t)V + e0;
+        const T* dr = ld ? drf + ((size_t)r.db + r.i) * (size_t)V + e0 : nullptr;
         const int nb = a.aligned ? ((n_el * (int)sizeof(T)) & ~15) / (int)sizeof(T) : 0;
         if (lane == 0) {
             const uint32_t bytes = (uint32_t)nb * (uint32_t)sizeof(T);
@@ -846,13 +862,17 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
     // sequences with a tested row only) once the spare's K and T have loaded.
     bool pf_draft = false;   // the spare's draft row is still to prefetch
     const int nb_pf = a.aligned ? ((n_el * (int)sizeof(T)) & ~15) / (int)sizeof(T) : 0;
-    auto prefetch_target = [&](int b) {
+    auto prefetch_target = [&](int trow) {
         if (lane == 0 && nb_pf > 0)
-            bulk_prefetch_l2(tgt + (size_t)b * (Kmax + 1) * (size_t)V + e0, (uint32_t)nb_pf * (uint32_t)sizeof(T));
+            bulk_prefetch_l2(tgt + (size_t)trow * (size_t)V + e0, (uint32_t)nb_pf * (uint32_t)sizeof(T));
     };
-    auto prefetch_draft = [&]() {
-        if (lane == 0 && nb_pf > 0 && spare >= 0 && a.has_draft && spare_pos.Kb > 0 && spare_pos.T != 0.0f)
-            bulk_prefetch_l2(drf + (size_t)spare * Kmax * (size_t)V + e0, (uint32_t)nb_pf * (uint32_t)sizeof(T));
+    auto prefetch_draft = [&]() {   // (and the target's, packed: its row had to load)
+        if (spare < 0)
+            return;
+        if (a.packed)
+            prefetch_target(spare_pos.tb);
+        if (lane == 0 && nb_pf > 0 && a.has_draft && spare_pos.Kb > 0 && spare_pos.T != 0.0f)
+            bulk_prefetch_l2(drf + (size_t)spare_pos.db * (size_t)V + e0, (uint32_t)nb_pf * (uint32_t)sizeof(T));
     };
 
     // per-warp counters (lane 0), added to the call's sv_stats at exit
@@ -1126,7 +1146,8 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
             if (spare >= 0) {
                 spare_pos = unit_pos(a, spare);   // loads now, used when the unit starts
                 spare_sv = seq_vals(a, spare, lane);
-                prefetch_target(spare);
+                if (!a.packed)
+                    prefetch_target(spare * (Kmax + 1));
                 pf_draft = true;
             }
         }
@@ -1296,9 +1317,9 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
         if (redo) {
             row.flags |= kFMaxRef;   // the same row again
         } else if (cont) {
-            row = make_row(a, row.i + 1, row.b, row.Kb, row.T);
+            row = make_row(a, row.i + 1, row.b, row.Kb, row.T, row.tb, row.db);
         } else if (spare >= 0) {
-            row = make_row(a, 0, spare_pos.b, spare_pos.Kb, spare_pos.T);
+            row = make_row(a, 0, spare_pos.b, spare_pos.Kb, spare_pos.T, spare_pos.tb, spare_pos.db);
             cur_sv = spare_sv;
             spare = -1;
             drawn = false;

@@ -107,3 +107,26 @@ def test_kv_len_advances_by_committed_tokens(dev):
     assert np.array_equal(kvh[valid], bh[valid] + 1 + n[valid])
     assert st.read()["invalid"] == 1
     compare(oracle_ref(inp), t, n)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_packed_logits_give_the_padded_results(dev, dtype):
+    """Logits packed by K (sequence b's rows from row sum_{c<b}(K_c + 1) of the
+    target and sum_{c<b} K_c of the draft) verify exactly as the padded
+    layout, and match the oracle."""
+    B, V = 30, 7000
+    K = W.configs.ragged_k(6, B)
+    inp = W.make_host(B, K, V, dtype, 2.0, 0.7,
+                      np.where(np.arange(B) % 4 == 0, 0.0, 0.9).astype(np.float32), seed=31)
+    d = to_device(inp, dev)
+    k = np.asarray(inp["K"])
+    tp = torch.cat([d["target"][b, : k[b] + 1] for b in range(B)]).contiguous()
+    dp = torch.cat([d["draft"][b, : k[b]] for b in range(B)]).contiguous()
+    assert tp.shape[0] == int((k + 1).sum()) and dp.shape[0] == int(k.sum())
+    ws = sv.Workspace(B, int(k.max()), V, dtype_code(dtype), dev)
+    args = (d["tokens"], d["uniforms"], d["temperature"], k)
+    t1, n1 = sv.spec_verify_ex(tp, dp, *args, ws, packed=True)
+    t0, n0 = sv.spec_verify_ex(d["target"], d["draft"], *args, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(t1, t0) and torch.equal(n1, n0)
+    compare(oracle_ref(inp), t1.cpu().numpy(), n1.cpu().numpy())
