@@ -295,7 +295,7 @@ def run_ours(args):
                     bytes_algorithmic=bytes_need, peak_source=peaks["source"],
                     kernel="sv_sweep_kernel",
                     duration="CUDA events around each spec_verify_ws call: the 1-kernel step "
-                             "plus its header upload")
+                             "plus its 16-byte counter reset")
 
     # ---- end to end through the host entry point (pinned buffers) ----
     e2e = None
