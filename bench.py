@@ -137,6 +137,23 @@ def _dist():
     return ws, rank, local
 
 
+def _max_over_ranks(dist, value: float, device) -> float:
+    """The largest of every rank's value (the job takes as long as its slowest
+    rank); the value itself on a single rank."""
+    if dist is None:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _whole_job_rate(world: int, units_per_rank_step: int, steps: int, seconds: float) -> float:
+    """Units all ranks processed per second: every rank verifies its own batch
+    of the same shape (replicas, weak scaling), timed by the slowest rank."""
+    return world * units_per_rank_step * steps / seconds
+
+
 # ---------------------------------------------------------------------------
 # CPU oracle timing (baseline leg and reference arm)
 # ---------------------------------------------------------------------------
@@ -273,13 +290,9 @@ def run_ours(args):
     if dist:
         dist.barrier()
     clk = clocks.stop() if clocks else None
-    total_ms = float(sum(times))
-    if dist:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = _max_over_ranks(dist, float(sum(times)), dev)
     ms_per_step = total_ms / args.steps
-    value = world * pos_per_step * args.steps / (total_ms / 1e3)
+    value = _whole_job_rate(world, pos_per_step, args.steps, total_ms / 1e3)
     errs = sv.sv_workspace_errors(ws)
 
     # verify-every-row variant of the same step (same outputs, all bytes read)
@@ -317,15 +330,11 @@ def run_ours(args):
         t0 = time.perf_counter()
         for _ in range(n_e2e):
             sv.spec_verify_host(*host_args, out_tokens=h_ot, out_num_accepted=h_on)
-        e2e_s = (time.perf_counter() - t0) / n_e2e
-        if dist:
-            t = torch.tensor([e2e_s], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_s = float(t.item())
+        e2e_s = _max_over_ranks(dist, (time.perf_counter() - t0) / n_e2e, dev)
         same = bool(np.array_equal(h_on.numpy(), nacc))
         h2d = sum(x.numel() * x.element_size() for x in (h_t, h_d, h_tok, h_uni, h_tmp))
         d2h = h_ot.numel() * 4 + h_on.numel() * 4
-        e2e = dict(value=world * pos_per_step / e2e_s, unit=UNIT, h2d_bytes_per_step=h2d,
+        e2e = dict(value=_whole_job_rate(world, pos_per_step, 1, e2e_s), unit=UNIT, h2d_bytes_per_step=h2d,
                    d2h_bytes_per_step=d2h, ms_per_step=round(e2e_s * 1e3, 3),
                    matches_device_run=same, api="spec_verify_host")
         del h_t, h_d, staging
