@@ -50,10 +50,12 @@ struct SweepLayout {
     size_t bars;         // [nw] slot mbarriers
     size_t xbar;         // [2] exchange mbarriers: row partials
     size_t xbar2;        // [2] exchange mbarriers: residual totals
+    size_t xbarc;        // mbarrier of a claim made between sequences
     size_t xbuf;         // [2][P] float4 row partials (P = warps per row)
     size_t xbuf2;        // [2][P] float2 residual totals
-    size_t xclaim;       // [2] int: unit claimed by rank 0 during the row
-    size_t first;        // int: the cluster's first unit
+    size_t xclaim;       // [2] int2: (sequence, ticket) claimed by rank 0 during the row
+    size_t first;        // int2: (sequence, ticket) of the cluster's first unit, or of a
+                         // claim made between sequences
     size_t stats;        // [nw][kw][strips][4] float: per-strip partial sums of the
                          // draw masses (at most 64 bytes a chunk)
     size_t total;
@@ -70,13 +72,15 @@ __host__ __device__ inline SweepLayout sweep_layout(int nw, int kw, int chunk_by
     o += 16;
     L.xbar2 = o;
     o += 16;
+    L.xbarc = o;
+    o += 8;
     o = (o + 15) & ~(size_t)15;
     L.xbuf = o;
     o += 2 * (size_t)P * 16;
     L.xbuf2 = o;
     o += 2 * (size_t)P * 8;
     L.xclaim = o;
-    o += 8;
+    o += 16;
     L.first = o;
     o += 8;
     o = (o + 15) & ~(size_t)15;   // stats are read as 16-byte vectors
@@ -92,7 +96,8 @@ __host__ __device__ inline SweepLayout sweep_layout(int nw, int kw, int chunk_by
 __host__ __device__ inline bool sweep_layout_aligned(const SweepLayout& L)
 {
     return L.slot_bytes % 16 == 0 && L.bars % 8 == 0 && L.xbar % 8 == 0 && L.xbar2 % 8 == 0 &&
-           L.xbuf % 16 == 0 && L.xbuf2 % 8 == 0 && L.xclaim % 4 == 0 && L.first % 4 == 0 &&
+           L.xbarc % 8 == 0 && L.xbuf % 16 == 0 && L.xbuf2 % 8 == 0 && L.xclaim % 8 == 0 &&
+           L.first % 8 == 0 &&
            L.stats % 16 == 0;
 }
 
@@ -752,7 +757,8 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
     uint64_t* xbar2 = reinterpret_cast<uint64_t*>(dsm + L.xbar2);
     float4* xbuf = reinterpret_cast<float4*>(dsm + L.xbuf);    // [2][P]
     float2* xbuf2 = reinterpret_cast<float2*>(dsm + L.xbuf2);  // [2][P]
-    int* xclaim = reinterpret_cast<int*>(dsm + L.xclaim);      // [2]
+    int2* xclaim = reinterpret_cast<int2*>(dsm + L.xclaim);    // [2]
+    const uint32_t xbarc = smem_addr(dsm + L.xbarc);
     int* first = reinterpret_cast<int*>(dsm + L.first);
     float* stats = reinterpret_cast<float*>(dsm + L.stats) + (size_t)w * KW * 16;   // [kw][NV][4]
 
@@ -765,6 +771,7 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
             mbar_init(smem_addr(&xbar[1]), 1);
             mbar_init(smem_addr(&xbar2[0]), 1);
             mbar_init(smem_addr(&xbar2[1]), 1);
+            mbar_init(xbarc, 1);
         }
         fence_mbar_init();
     }
@@ -774,15 +781,20 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
     }
     __syncthreads();
     cluster_arrive();   // every CTA's barriers exist before any peer signals them
-    int f0 = -1;
+    int f0 = -1, t0 = -1;
     if (rank == 0 && w == 0) {
-        if (lane == 0)
-            f0 = ticket_unit(a, claim_ticket(a));
+        if (lane == 0) {
+            t0 = claim_ticket(a);
+            f0 = ticket_unit(a, t0);
+        }
         f0 = __shfl_sync(kFull, f0, 0);
+        t0 = __shfl_sync(kFull, t0, 0);
     }
     cluster_wait();
-    if (rank == 0 && w == 0 && lane < C)
+    if (rank == 0 && w == 0 && lane < C) {
         st_cluster_s32(map_to_rank(smem_addr(first), (uint32_t)lane), f0);
+        st_cluster_s32(map_to_rank(smem_addr(first + 1), (uint32_t)lane), t0);
+    }
     cluster_arrive();
     cluster_wait();
 
@@ -792,6 +804,13 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
     int spare = -1;
     UnitPos spare_pos{0, 0, 0.0f};
     bool exhausted = false;
+    // A cluster claims its next sequence a row ahead (hiding the claim's
+    // latency) only while at least two waves of tickets remain; nearer the
+    // end it claims when it finishes a sequence, so that the last sequences
+    // go to the clusters that are free first.
+    const int n_clusters = (int)(gridDim.x / (unsigned)C);
+    int last_t = first[1];   // the ticket of the cluster's latest claim
+    uint32_t kc = 0;         // claims made between sequences (xbarc phase)
     bool broken = false;     // a slot wait gave up: no more copies, rows poisoned
     bool xbroken = false;    // an exchange wait gave up: leave the loop
     bool drawn = false;      // the current sequence's outputs are written
@@ -919,9 +938,9 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
         const bool draft = (row.flags & kFDraft) != 0;
         const bool usable = (row.flags & kFUsable) != 0;
         const float c = (usable && !greedy) ? log2e_over(row.T) : 0.0f;
-        const bool want_claim = spare < 0 && !exhausted;
+        const bool want_claim = spare < 0 && !exhausted && (long long)last_t + 2LL * n_clusters < (long long)a.B;
         if (w == 0 && lane == 0)
-            mbar_arrive_expect_tx(smem_addr(&xbar[p]), (uint32_t)P * 16u + (want_claim ? 4u : 0u));
+            mbar_arrive_expect_tx(smem_addr(&xbar[p]), (uint32_t)P * 16u + (want_claim ? 8u : 0u));
         if (writer && lane == 0 && want_claim)
             ticket = claim_ticket(a);
 
@@ -1048,11 +1067,13 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
         if (writer && lane == 0 && want_claim)
             claimed = ticket_check(a, ticket, claimed);
         const int claimed_b = __shfl_sync(kFull, claimed, 0);
+        const int claimed_t = __shfl_sync(kFull, ticket, 0);
         if (lane < C) {
             const uint32_t rb = map_to_rank(smem_addr(&xbar[p]), (uint32_t)lane);
             st_async_v4(map_to_rank(smem_addr(&xbuf[p * P + g]), (uint32_t)lane), part, rb);
             if (writer && want_claim)
-                st_async_s32(map_to_rank(smem_addr(&xclaim[p]), (uint32_t)lane), claimed_b, rb);
+                st_async_v2(map_to_rank(smem_addr(&xclaim[p]), (uint32_t)lane),
+                            make_float2(__int_as_float(claimed_b), __int_as_float(claimed_t)), rb);
         }
         if (pf_draft) {   // the spare's K and T have long loaded
             prefetch_draft();
@@ -1140,9 +1161,12 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
             c_tie += near_tie ? 1u : 0u;
         }
         if (want_claim) {
-            const int cl = xclaim[p];
+            const int2 clv = xclaim[p];
+            const int cl = clv.x;
             spare = (cl >= 0 && cl < a.B) ? cl : -1;
             exhausted = spare < 0;
+            if (spare >= 0)
+                last_t = clv.y;
             if (spare >= 0) {
                 spare_pos = unit_pos(a, spare);   // loads now, used when the unit starts
                 spare_sv = seq_vals(a, spare, lane);
@@ -1318,13 +1342,45 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
             row.flags |= kFMaxRef;   // the same row again
         } else if (cont) {
             row = make_row(a, row.i + 1, row.b, row.Kb, row.T, row.tb, row.db);
-        } else if (spare >= 0) {
+        } else {
+            if (spare < 0 && !exhausted) {
+                // claim now: rank 0's writer takes a ticket and sends the
+                // sequence to every CTA (st.async onto each CTA's claim
+                // mbarrier, bounded wait, as the row exchange)
+                if (w == 0 && lane == 0)
+                    mbar_arrive_expect_tx(xbarc, 8u);
+                int cb = -1, ct = -1;
+                if (writer && lane == 0) {
+                    ct = claim_ticket(a);
+                    cb = ticket_unit(a, ct);
+                }
+                cb = __shfl_sync(kFull, cb, 0);
+                ct = __shfl_sync(kFull, ct, 0);
+                if (writer && lane < C)
+                    st_async_v2(map_to_rank(smem_addr(first), (uint32_t)lane),
+                                make_float2(__int_as_float(cb), __int_as_float(ct)),
+                                map_to_rank(xbarc, (uint32_t)lane));
+                if (!mbar_wait_bounded(xbarc, kc & 1u, kWaitSpins))
+                    xbroken = true;
+                ++kc;
+                if (__any_sync(kFull, xbroken))
+                    break;
+                const int nb = first[0];
+                if (nb >= 0 && nb < a.B) {
+                    spare = nb;
+                    last_t = first[1];
+                    spare_pos = unit_pos(a, nb);
+                    spare_sv = seq_vals(a, nb, lane);
+                } else {
+                    exhausted = true;
+                }
+            }
+            if (spare < 0)
+                break;
             row = make_row(a, 0, spare_pos.b, spare_pos.Kb, spare_pos.T, spare_pos.tb, spare_pos.db);
             cur_sv = spare_sv;
             spare = -1;
             drawn = false;
-        } else {
-            break;
         }
         issue(row);   // copies first: the logit loads overlap with them
         tk = tok_of(a, row, cur_sv);
