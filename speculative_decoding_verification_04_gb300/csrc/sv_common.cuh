@@ -1,6 +1,6 @@
 // sv_common.cuh -- shared device definitions of libspecverify: kernel
-// arguments, element access, the fixed-rounding softmax weight and residual
-// term, warp reductions and the per-row decision codes.
+// arguments, element access, the fixed-rounding softmax weight, warp
+// reductions and the per-row decision codes.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -153,26 +153,11 @@ __device__ __forceinline__ float weight(float l, float m, float c)
     return weight_r(l, ref_of(m, c), c);
 }
 
-// max(0, p - q) with p = e_t / S_t and q = e_d / S_d, fixed rounding sequence.
-__device__ __forceinline__ float resid_term(float et, float inv_st, float ed, float inv_sd)
-{
-    return fmaxf(__fsub_rn(__fmul_rn(et, inv_st), __fmul_rn(ed, inv_sd)), 0.0f);
-}
-
 __device__ __forceinline__ float warp_max_nan(float v)
 {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1)
         v = max_nan(v, __shfl_xor_sync(kFull, v, o));
-    return v;
-}
-
-// Butterfly sum: every lane ends with the same value (IEEE addition commutes).
-__device__ __forceinline__ float warp_sum(float v)
-{
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-        v += __shfl_xor_sync(kFull, v, o);
     return v;
 }
 

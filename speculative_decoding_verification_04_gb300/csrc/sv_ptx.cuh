@@ -2,14 +2,15 @@
 // (sm_90+ instructions; the library is built for sm_103a only).
 //
 //  * cluster rank, cluster barrier (arrive.release / wait.acquire) and
-//    distributed-shared-memory loads/stores (mapa + ld/st.shared::cluster);
+//    distributed-shared-memory stores (mapa + st.shared::cluster);
 //  * mbarrier init / arrive.expect_tx / bounded try_wait;
 //  * the non-tensor bulk copy global -> shared (cp.async.bulk, the 1-D TMA
-//    path), completing on an mbarrier transaction count;
+//    path), completing on an mbarrier transaction count, with an L2
+//    evict-first hint, and the bulk prefetch into L2;
 //  * st.async: a store into another cluster CTA's shared memory that
 //    completes on that CTA's mbarrier transaction count;
 //  * ex2.approx, the NaN-propagating max (scalar, three-input and bf16x2) and
-//    the packed two-lane fp32 arithmetic of sm_100+ (add/sub/mul/fma .f32x2,
+//    the packed two-lane fp32 arithmetic of sm_100+ (add/mul/fma .f32x2,
 //    each lane rounded to nearest like its scalar form).
 #pragma once
 
@@ -35,19 +36,6 @@ __device__ __forceinline__ void cluster_arrive()
     asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 }
 
-// Arrive without release semantics (threads that publish nothing to peers).
-__device__ __forceinline__ void cluster_arrive_relaxed()
-{
-    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
-}
-
-// Release this thread's earlier writes (distributed shared memory stores) at
-// cluster scope; used before a relaxed arrive by the threads that publish.
-__device__ __forceinline__ void fence_cluster()
-{
-    asm volatile("fence.acq_rel.cluster;" ::: "memory");
-}
-
 __device__ __forceinline__ void cluster_wait()
 {
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -61,26 +49,9 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t local_addr, uint32_t ra
     return out;
 }
 
-__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v)
-{
-    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
-}
-
-__device__ __forceinline__ void st_cluster_f64(uint32_t addr, double v)
-{
-    asm volatile("st.shared::cluster.f64 [%0], %1;" ::"r"(addr), "d"(v) : "memory");
-}
-
 __device__ __forceinline__ void st_cluster_s32(uint32_t addr, int v)
 {
     asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
-
-__device__ __forceinline__ int ld_cluster_s32(uint32_t addr)
-{
-    int v;
-    asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
-    return v;
 }
 
 __device__ __forceinline__ void mbar_init(uint32_t addr, uint32_t count)
@@ -168,18 +139,6 @@ __device__ __forceinline__ void fence_proxy_async()
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// Programmatic dependent launch: let the next kernel in the stream start
-// launching / wait until the previous kernel has completed and flushed.
-__device__ __forceinline__ void griddep_launch_dependents()
-{
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
-__device__ __forceinline__ void griddep_wait()
-{
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-}
-
 __device__ __forceinline__ float ex2_approx(float x)
 {
     float y;
@@ -230,13 +189,6 @@ __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b)
     return y;
 }
 
-__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b)
-{
-    uint64_t y;
-    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(y) : "l"(a), "l"(b));
-    return y;
-}
-
 __device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b)
 {
     uint64_t y;
@@ -265,26 +217,6 @@ __device__ __forceinline__ void st_async_v2(uint32_t addr, float2 v, uint32_t mb
     asm volatile(
         "st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];"
         ::"r"(addr), "f"(v.x), "f"(v.y), "r"(mbar) : "memory");
-}
-
-__device__ __forceinline__ void st_async_s32(uint32_t addr, int v, uint32_t mbar)
-{
-    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];"
-                 ::"r"(addr), "r"(v), "r"(mbar) : "memory");
-}
-
-__device__ __forceinline__ uint8_t ld_cg_u8(const uint8_t* p)
-{
-    unsigned short v;
-    asm volatile("ld.global.cg.u8 %0, [%1];" : "=h"(v) : "l"(p));
-    return static_cast<uint8_t>(v);
-}
-
-__device__ __forceinline__ uint32_t ld_volatile_u32(const uint32_t* p)
-{
-    uint32_t v;
-    asm volatile("ld.volatile.global.u32 %0, [%1];" : "=r"(v) : "l"(p));
-    return v;
 }
 
 }  // namespace sv

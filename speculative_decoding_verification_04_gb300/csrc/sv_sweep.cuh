@@ -589,15 +589,6 @@ __device__ __forceinline__ float sum_or_special(float v)
     return warp_sum_comp(v);
 }
 
-// Combine (max, sum relative to that max) parts held one per lane; the sum
-// is compensated.  Every lane gets the same result.
-__device__ __forceinline__ void combine_ms(float m_part, float s_part, float c, float& m, float& S)
-{
-    m = warp_max_nan(m_part);
-    S = warp_sum_comp(m_part == -INFINITY ? 0.0f
-                                          : (m_part == m ? s_part : s_part * weight(m_part, m, c)));
-}
-
 // sum_or_special of two values, interleaved (each result as the single form).
 __device__ __forceinline__ void sum_or_special2(float& va, float& vb)
 {
@@ -608,7 +599,9 @@ __device__ __forceinline__ void sum_or_special2(float& va, float& vb)
     vb = nan_b ? NAN : (inf_b ? INFINITY : vb);
 }
 
-// combine_ms of two (max, sum) pairs, interleaved (each result as the single form).
+// Combine two sets of (max, sum relative to that max) parts held one per
+// lane, interleaved so that their shuffle latencies overlap; the sums are
+// compensated.  Every lane gets the same results.
 __device__ __forceinline__ void combine_ms2(float ma_part, float sa_part, float mb_part, float sb_part,
                                             float c, float& ma, float& Sa, float& mb, float& Sb)
 {
