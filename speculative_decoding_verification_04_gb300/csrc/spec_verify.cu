@@ -43,7 +43,8 @@ struct Geom {
     int s = 0, nv = 0, ch = 0, nchunks = 0;
     int C = 0;          // CTAs per cluster (per row)
     int nw = 0;         // warps per CTA
-    int kw = 0;         // chunks per warp (one contiguous range)
+    int kw = 0;         // chunks of the longest warp range
+    int kc = 0;         // chunks of the longest CTA span
     int clusters = 0;   // persistent grid size (clusters)
     size_t smem = 0;
 };
@@ -193,8 +194,8 @@ static cudaError_t capacity_nv(const Geom& g, int dev, int* n)
     }
 }
 
-// Geometry for C CTAs of nw warps per row: P = C * nw warp ranges of kw
-// chunks each; false if it does not fit.
+// Geometry for C CTAs of nw warps per row: P = C * nw warp ranges of whole
+// chunks (lengths differ by at most one); false if it does not fit.
 static bool shape_geometry(int V, sv_dtype dt, int C, int nw, Geom* g)
 {
     const int s = elem_size(dt);
@@ -204,13 +205,13 @@ static bool shape_geometry(int V, sv_dtype dt, int C, int nw, Geom* g)
     g->nchunks = (V + g->ch - 1) / g->ch;
     if (C < 1 || C > kMaxCluster || nw < 1 || nw > kMaxWarps || C * nw > kMaxParts)
         return false;
+    if (C > g->nchunks)   // no CTA without chunks
+        return false;
     g->C = C;
     g->nw = nw;
     g->kw = (g->nchunks + C * nw - 1) / (C * nw);
-    // no CTA without chunks
-    if ((long long)(C - 1) * nw * g->kw >= g->nchunks)
-        return false;
-    const SweepLayout L = sweep_layout(nw, g->kw, g->ch * s, C * nw);
+    g->kc = cta_chunks(g->nchunks, C);
+    const SweepLayout L = sweep_layout(nw, g->kc, g->kw, g->ch * s, C * nw);
     if (!sweep_layout_aligned(L))   // never launch a layout the kernel cannot address
         return false;
     g->smem = L.total;
@@ -255,6 +256,9 @@ static sv_status pick_geometry(int V, sv_dtype dt, int B, int Kmax, int override
                 if (nw != std::min({(ncpc + want_cpw - 1) / want_cpw, kMaxParts / C, kMaxWarps}))
                     continue;
             }
+            // without overrides, every warp range holds a chunk
+            if (override_ncpc <= 0 && want_cpw <= 0 && C * nw > nch)
+                continue;
             Geom t;
             if (!shape_geometry(V, dt, C, nw, &t))
                 continue;
@@ -610,7 +614,7 @@ static sv_status geometry_of(int B, int Kmax, int V, sv_dtype dt, int ncpc, int 
     out[3] = g.clusters;
     out[4] = 32 * g.nw;
     out[5] = (int32_t)g.smem;
-    out[6] = (g.nchunks + g.kw - 1) / g.kw;   // warp ranges holding chunks
+    out[6] = std::min(g.C * g.nw, g.nchunks);   // warp ranges holding chunks
     out[7] = g.nchunks;
     return SV_OK;
 }

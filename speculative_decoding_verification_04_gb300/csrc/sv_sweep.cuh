@@ -3,11 +3,12 @@
 // A grid of thread-block clusters (C CTAs of nw warps each, as many as the
 // device holds at once) works through the batch one row (sequence b, position
 // i) at a time per cluster.  The row's vocabulary is cut into P = C * nw
-// contiguous ranges of kw chunks; warp g = rank * nw + w owns range g and
-// keeps its slice of the row (target and draft) resident in its own slot of
-// shared memory, filled by one 1-D bulk copy (cp.async.bulk) per array that
-// completes on the slot's mbarrier.  No two warps share data, so the steady
-// state has no CTA-wide barrier at all.
+// contiguous ranges of whole chunks whose lengths differ by at most one; warp
+// g = rank * nw + w owns range g and keeps its slice of the row (target and
+// draft) resident in its own part of the CTA's shared memory, filled by one
+// 1-D bulk copy (cp.async.bulk) per array that completes on the warp's
+// mbarrier.  No two warps share data, so the steady state has no CTA-wide
+// barrier at all.
 //
 // Schedule: a cluster walks one sequence's positions in order.  Row i+1 is
 // read only once x_i has been accepted (the method's own early exit: rows after
@@ -44,28 +45,39 @@ namespace sv {
 
 constexpr int kMaxParts = 32;   // warps per cluster: one per lane in the combines
 
+// Warp range g of a row of `nchunks` chunks cut into P ranges is chunks
+// [range_lo(g), range_lo(g + 1)): lengths floor or ceil of nchunks / P.  The
+// nw ranges of CTA r are contiguous and span at most cta_chunks() chunks.
+__host__ __device__ inline int range_lo(int g, int nchunks, int P)
+{
+    return (int)(((long long)g * nchunks) / P);
+}
+
+__host__ __device__ inline int cta_chunks(int nchunks, int C) { return (nchunks + C - 1) / C; }
+
 // Dynamic shared memory of one CTA (host and device compute it alike).
 struct SweepLayout {
-    size_t slot_bytes;   // one warp's resident slice: kw target chunks, kw draft chunks
-    size_t bars;         // [nw] slot mbarriers
-    size_t xbar;         // [2] exchange mbarriers: row partials
-    size_t xbar2;        // [2] exchange mbarriers: residual totals
-    size_t xbarc;        // mbarrier of a claim made between sequences
-    size_t xbuf;         // [2][P] float4 row partials (P = warps per row)
-    size_t xbuf2;        // [2][P] float2 residual totals
-    size_t xclaim;       // [2] int2: (sequence, ticket) claimed by rank 0 during the row
-    size_t first;        // int2: (sequence, ticket) of the cluster's first unit, or of a
-                         // claim made between sequences
-    size_t stats;        // [nw][kw][strips][4] float: per-strip partial sums of the
-                         // draw masses (at most 64 bytes a chunk)
+    size_t region_bytes;   // the CTA's span of target chunks (kc of them); the draft
+                           // chunks follow in a second region of the same size
+    size_t bars;           // [nw] slot mbarriers
+    size_t xbar;           // [2] exchange mbarriers: row partials
+    size_t xbar2;          // [2] exchange mbarriers: residual totals
+    size_t xbarc;          // mbarrier of a claim made between sequences
+    size_t xbuf;           // [2][P] float4 row partials (P = warps per row)
+    size_t xbuf2;          // [2][P] float2 residual totals
+    size_t xclaim;         // [2] int2: (sequence, ticket) claimed by rank 0 during the row
+    size_t first;          // int2: (sequence, ticket) of the cluster's first unit, or of a
+                           // claim made between sequences
+    size_t stats;          // [nw][kw][strips][4] float: per-strip partial sums of the
+                           // draw masses (at most 64 bytes a chunk; kw = longest range)
     size_t total;
 };
 
-__host__ __device__ inline SweepLayout sweep_layout(int nw, int kw, int chunk_bytes, int P)
+__host__ __device__ inline SweepLayout sweep_layout(int nw, int kc, int kw, int chunk_bytes, int P)
 {
     SweepLayout L;
-    L.slot_bytes = 2 * (size_t)kw * (size_t)chunk_bytes;
-    size_t o = (size_t)nw * L.slot_bytes;
+    L.region_bytes = (size_t)kc * (size_t)chunk_bytes;
+    size_t o = 2 * L.region_bytes;
     L.bars = o;
     o += (size_t)nw * 8;
     L.xbar = o;
@@ -91,11 +103,12 @@ __host__ __device__ inline SweepLayout sweep_layout(int nw, int kw, int chunk_by
 }
 
 // The alignments the kernel's shared-memory accesses rely on: 16-byte
-// vectors (slots, row partials, strip partials), 8-byte mbarriers, residual
-// totals and claims.
+// vectors (slices, row partials, strip partials), 8-byte mbarriers, residual
+// totals and claims.  Chunks are whole multiples of 16 bytes, so every
+// warp's slice starts 16-byte aligned inside its region.
 __host__ __device__ inline bool sweep_layout_aligned(const SweepLayout& L)
 {
-    return L.slot_bytes % 16 == 0 && L.bars % 8 == 0 && L.xbar % 8 == 0 && L.xbar2 % 8 == 0 &&
+    return L.region_bytes % 16 == 0 && L.bars % 8 == 0 && L.xbar % 8 == 0 && L.xbar2 % 8 == 0 &&
            L.xbarc % 8 == 0 && L.xbuf % 16 == 0 && L.xbuf2 % 8 == 0 && L.xclaim % 8 == 0 &&
            L.first % 8 == 0 &&
            L.stats % 16 == 0;
@@ -737,14 +750,16 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
     const int P = C * nw;   // warps per row
     const uint32_t rank = cluster_ctarank();
     const int g = (int)rank * nw + w;   // this warp's range of the row
-    const int c_lo = min(g * KW, a.nchunks);
-    const int kwm = min(c_lo + KW, a.nchunks) - c_lo;   // chunks in range (0..KW)
-    const int e0 = c_lo * CH;                           // first element of the range
+    const int c_lo = range_lo(g, a.nchunks, P);
+    const int kwm = range_lo(g + 1, a.nchunks, P) - c_lo;   // chunks in range (0..KW)
+    const int e0 = c_lo * CH;                               // first element of the range
     const int n_el = max(0, min(e0 + kwm * CH, V) - e0);
-    const SweepLayout L = sweep_layout(nw, KW, CH * (int)sizeof(T), P);
+    const SweepLayout L = sweep_layout(nw, cta_chunks(a.nchunks, C), KW, CH * (int)sizeof(T), P);
 
-    T* slot_t = reinterpret_cast<T*>(dsm + (size_t)w * L.slot_bytes);
-    T* slot_d = slot_t + (size_t)KW * CH;
+    // the slice's place in the CTA's target and draft regions
+    const size_t off = (size_t)(c_lo - range_lo((int)rank * nw, a.nchunks, P)) * CH;
+    T* slot_t = reinterpret_cast<T*>(dsm) + off;
+    T* slot_d = reinterpret_cast<T*>(dsm + L.region_bytes) + off;
     const uint32_t bar = smem_addr(dsm + L.bars + 8 * (size_t)w);
     uint64_t* xbar = reinterpret_cast<uint64_t*>(dsm + L.xbar);
     uint64_t* xbar2 = reinterpret_cast<uint64_t*>(dsm + L.xbar2);
