@@ -117,14 +117,14 @@ static std::map<std::tuple<int, int, int, int, size_t>, int> g_fit;
 // chosen geometry per (device, V, dtype, B, Kmax, tuning overrides)
 static std::map<std::tuple<int, int, int, int, int, int, int>, Geom> g_pick;
 
-template <typename T, int NV>
+template <typename T, int NV, bool WIDE>
 static cudaError_t prepare_kernels(int dev)
 {
     const int ti = sizeof(T) == 2 ? 1 : 0;
-    const int ni = NV == 1 ? 0 : NV == 2 ? 1 : 2;
+    const int ni = NV == 1 ? 0 : NV == 2 ? 1 : (WIDE ? 3 : 2);
     std::lock_guard<std::mutex> lk(g_mu);
     if (!g_dev[dev].attrs_set[ti][ni]) {
-        auto kern = sv_sweep_kernel<T, NV>;
+        auto kern = sv_sweep_kernel<T, NV, WIDE>;
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              kSmemPerCtaMax);
         if (e != cudaSuccess)
@@ -154,10 +154,10 @@ static void sweep_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, con
 }
 
 // How many clusters of this shape the device holds at once (0: cannot launch).
-template <typename T, int NV>
+template <typename T, int NV, bool WIDE>
 static cudaError_t cluster_capacity(const Geom& g, int dev, int* n)
 {
-    cudaError_t e = prepare_kernels<T, NV>(dev);
+    cudaError_t e = prepare_kernels<T, NV, WIDE>(dev);
     if (e != cudaSuccess)
         return e;
     const auto key = std::make_tuple(dev, (int)sizeof(T) * 16 + NV, g.C, g.nw, g.smem);
@@ -173,7 +173,7 @@ static cudaError_t cluster_capacity(const Geom& g, int dev, int* n)
     cudaLaunchAttribute attr[1];
     sweep_config(&cfg, attr, g, 1, 0);
     int v = 0;
-    e = cudaOccupancyMaxActiveClusters(&v, sv_sweep_kernel<T, NV>, &cfg);
+    e = cudaOccupancyMaxActiveClusters(&v, sv_sweep_kernel<T, NV, WIDE>, &cfg);
     if (e != cudaSuccess) {
         (void)cudaGetLastError();
         v = 0;
@@ -188,9 +188,11 @@ template <typename T>
 static cudaError_t capacity_nv(const Geom& g, int dev, int* n)
 {
     switch (g.nv) {
-    case 1: return cluster_capacity<T, 1>(g, dev, n);
-    case 2: return cluster_capacity<T, 2>(g, dev, n);
-    default: return cluster_capacity<T, 4>(g, dev, n);
+    case 1: return cluster_capacity<T, 1, false>(g, dev, n);
+    case 2: return cluster_capacity<T, 2, false>(g, dev, n);
+    default:
+        return g.C * g.nw > 32 ? cluster_capacity<T, 4, true>(g, dev, n)
+                               : cluster_capacity<T, 4, false>(g, dev, n);
     }
 }
 
@@ -206,6 +208,8 @@ static bool shape_geometry(int V, sv_dtype dt, int C, int nw, Geom* g)
     if (C < 1 || C > kMaxCluster || nw < 1 || nw > kMaxWarps || C * nw > kMaxParts)
         return false;
     if (C > g->nchunks)   // no CTA without chunks
+        return false;
+    if (C * nw > 32 && g->nv != 4)   // more than 32 ranges: large vocabularies only
         return false;
     g->C = C;
     g->nw = nw;
@@ -285,25 +289,27 @@ static sv_status pick_geometry(int V, sv_dtype dt, int B, int Kmax, int override
     return SV_OK;
 }
 
-template <typename T, int NV>
+template <typename T, int NV, bool WIDE>
 static cudaError_t launch_sweep(const Args& a, const Geom& g, cudaStream_t st, int dev)
 {
-    cudaError_t e = prepare_kernels<T, NV>(dev);
+    cudaError_t e = prepare_kernels<T, NV, WIDE>(dev);
     if (e != cudaSuccess)
         return e;
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[1];
     sweep_config(&cfg, attr, g, g.clusters, st);
-    return cudaLaunchKernelEx(&cfg, sv_sweep_kernel<T, NV>, a);
+    return cudaLaunchKernelEx(&cfg, sv_sweep_kernel<T, NV, WIDE>, a);
 }
 
 template <typename T>
 static cudaError_t launch_nv(const Args& a, const Geom& g, cudaStream_t st, int dev)
 {
     switch (g.nv) {
-    case 1: return launch_sweep<T, 1>(a, g, st, dev);
-    case 2: return launch_sweep<T, 2>(a, g, st, dev);
-    default: return launch_sweep<T, 4>(a, g, st, dev);
+    case 1: return launch_sweep<T, 1, false>(a, g, st, dev);
+    case 2: return launch_sweep<T, 2, false>(a, g, st, dev);
+    default:
+        return g.C * g.nw > 32 ? launch_sweep<T, 4, true>(a, g, st, dev)
+                               : launch_sweep<T, 4, false>(a, g, st, dev);
     }
 }
 

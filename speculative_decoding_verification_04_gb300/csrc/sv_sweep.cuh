@@ -43,7 +43,7 @@
 
 namespace sv {
 
-constexpr int kMaxParts = 32;   // warps per cluster: one per lane in the combines
+constexpr int kMaxParts = 64;   // warps per row: lanes j and j + 32 hold partials j, j + 32 in the combines
 
 // Warp range g of a row of `nchunks` chunks cut into P ranges is chunks
 // [range_lo(g), range_lo(g + 1)): lengths floor or ceil of nchunks / P.  The
@@ -612,6 +612,17 @@ __device__ __forceinline__ void sum_or_special2(float& va, float& vb)
     vb = nan_b ? NAN : (inf_b ? INFINITY : vb);
 }
 
+// Merge part (m2, s2) into (m, s): the larger maximum, both sums taken
+// against it (a part at -inf holds no mass).
+__device__ __forceinline__ void merge_ms(float& m, float& s, float m2, float s2, float c)
+{
+    const float M = max_nan(m, m2);
+    const float a = m == -INFINITY ? 0.0f : (m == M ? s : s * weight(m, M, c));
+    const float b = m2 == -INFINITY ? 0.0f : (m2 == M ? s2 : s2 * weight(m2, M, c));
+    m = M;
+    s = a + b;
+}
+
 // Combine two sets of (max, sum relative to that max) parts held one per
 // lane, interleaved so that their shuffle latencies overlap; the sums are
 // compensated.  Every lane gets the same results.
@@ -735,7 +746,9 @@ __device__ __forceinline__ int pick_in_strip(const uint4& tv, const uint4& dv, b
     return cand;
 }
 
-template <typename T, int NV>
+// WIDE: more than 32 warp ranges per row (lanes hold two partials each in
+// the combines); the host launches it for exactly those geometries.
+template <typename T, int NV, bool WIDE>
 __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
 {
     using EL = Elem<T>;
@@ -1093,8 +1106,11 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
             break;
 
         // ---- combine all partials and decide (every warp alike) ----
-        const float4 xv = lane < P ? xbuf[p * P + lane]
-                                   : make_float4(-INFINITY, __int_as_float(INT_MAX), -INFINITY, 0.0f);
+        // lane j holds the partials of warps j and j + 32
+        const float4 xnone = make_float4(-INFINITY, __int_as_float(INT_MAX), -INFINITY, 0.0f);
+        const bool has = lane < P, has2 = WIDE && lane + 32 < P;
+        const float4 xv = has ? xbuf[p * P + lane] : xnone;
+        const float4 xw = has2 ? xbuf[p * P + lane + 32] : xnone;
         const TokF tkb = shfl_tok<T>(tk);
         const size_t pos = (size_t)row.b * Kmax + row.i;   // diagnostics index (test rows)
         int dec = kDecInvalid;
@@ -1104,8 +1120,10 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
         float m_t = 0.0f, m_d = 0.0f, inv_st = 0.0f, inv_sd = 0.0f;
         bool row_ok = false;
         if (greedy) {
-            m_t = warp_max_nan(xv.x);
-            gtok = __reduce_min_sync(kFull, (lane < P && xv.x == m_t) ? __float_as_int(xv.y) : INT_MAX);
+            m_t = warp_max_nan(WIDE ? max_nan(xv.x, xw.x) : xv.x);
+            const int i1 = (has && xv.x == m_t) ? __float_as_int(xv.y) : INT_MAX;
+            const int i2 = (has2 && xw.x == m_t) ? __float_as_int(xw.y) : INT_MAX;
+            gtok = __reduce_min_sync(kFull, min(i1, i2));
             row_ok = usable && tkb.ok && isfinite(m_t) && gtok < V;
             dec = !row_ok ? kDecInvalid : (test ? (tkb.x == gtok ? kDecAccept : kDecReject) : kDecBonus);
             if (writer && lane == 0 && test && a.want_pq) {
@@ -1116,10 +1134,11 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
             float St, Sd;
             // weights against the proposal's logits that overflowed: the row
             // is weighed again against its maxima (same data, same result)
-            const bool has = lane < P;
-            const bool any_inf = __any_sync(kFull, has && (isinf(xv.y) || isinf(xv.w)));
+            const bool any_inf = __any_sync(kFull, (has && (isinf(xv.y) || isinf(xv.w))) ||
+                                                       (has2 && (isinf(xw.y) || isinf(xw.w))));
             const bool any_nan =
-                __any_sync(kFull, has && (isnan(xv.x) || isnan(xv.y) || isnan(xv.z) || isnan(xv.w)));
+                __any_sync(kFull, (has && (isnan(xv.x) || isnan(xv.y) || isnan(xv.z) || isnan(xv.w))) ||
+                                      (has2 && (isnan(xw.x) || isnan(xw.y) || isnan(xw.z) || isnan(xw.w))));
             const bool refmode = test && !(row.flags & kFMaxRef) && ref_ok;
             redo = refmode && !broken && any_inf && !any_nan;
             if (refmode) {
@@ -1129,9 +1148,18 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
                 m_d = ref_d;
                 St = has ? xv.y : 0.0f;
                 Sd = has ? xv.w : 0.0f;
+                if (has2) {
+                    St += xw.y;
+                    Sd += xw.w;
+                }
                 warp_sum_comp2(St, Sd);
             } else {
-                combine_ms2(xv.x, xv.y, xv.z, xv.w, c, m_t, St, m_d, Sd);
+                float ma = xv.x, sa = xv.y, mb = xv.z, sb = xv.w;
+                if (has2) {
+                    merge_ms(ma, sa, xw.x, xw.y, c);
+                    merge_ms(mb, sb, xw.z, xw.w, c);
+                }
+                combine_ms2(ma, sa, mb, sb, c, m_t, St, m_d, Sd);
             }
             row_ok = !redo && !any_nan && usable && tkb.ok && isfinite(m_t) && St > 0.0f && isfinite(St) &&
                      (!draft || (isfinite(m_d) && Sd > 0.0f && isfinite(Sd)));
@@ -1188,7 +1216,8 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
         const bool resid_pass = !greedy && test && draft && row_ok && !broken &&
                                 (dec == kDecReject || !a.early_exit);
         float S_R = 0.0f;
-        float2 wtot = make_float2(0.0f, 0.0f);   // lane j: warp j's (residual, p) totals
+        float2 wtot = make_float2(0.0f, 0.0f);    // lane j: warp j's (residual, p) totals
+        float2 wtot2 = make_float2(0.0f, 0.0f);   // and warp j + 32's
         if (resid_pass) {
             float rs_s = 0.0f, rs_c = 0.0f, ps_s = 0.0f, ps_c = 0.0f;
             for (int j = 0; j < kwm; ++j) {
@@ -1234,8 +1263,9 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
                 xbroken = true;
             if (__any_sync(kFull, xbroken))
                 break;
-            wtot = lane < P ? xbuf2[p2 * P + lane] : make_float2(0.0f, 0.0f);
-            S_R = warp_sum_comp(wtot.x);
+            wtot = has ? xbuf2[p2 * P + lane] : make_float2(0.0f, 0.0f);
+            wtot2 = has2 ? xbuf2[p2 * P + lane + 32] : make_float2(0.0f, 0.0f);
+            S_R = warp_sum_comp(WIDE ? wtot.x + wtot2.x : wtot.x);
         }
         if (writer && lane == 0 && test && a.want_resid && !redo)
             a.resid[pos] = resid_pass ? S_R : NAN;
@@ -1256,21 +1286,30 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
                 // (zero residual mass: p of the same row), or p at the bonus row
                 const bool bonus = dec == kDecBonus;
                 const bool use_r = !bonus && S_R > 0.0f;
-                float Wj = 0.0f;
-                if (lane < P)
+                float Wj = 0.0f, Wj2 = 0.0f;   // lane j: the masses of warps j and j + 32
+                if (has)
                     Wj = bonus ? (xv.x == -INFINITY ? 0.0f : xv.y * weight(xv.x, m_t, c))
                                : (use_r ? wtot.x : wtot.y);
-                // the warp whose range holds u * S (lane j holds warp j's mass)
+                if (has2)
+                    Wj2 = bonus ? (xw.x == -INFINITY ? 0.0f : xw.y * weight(xw.x, m_t, c))
+                                : (use_r ? wtot2.x : wtot2.y);
+                // the warp whose range holds u * S, and the mass left inside it
                 float t = 0.0f;
                 bool beyond = false;
                 int owner = -1;
-                {
+                if constexpr (WIDE) {
+                    const float S = warp_sum_comp(Wj + Wj2);
+                    if (S > 0.0f && isfinite(S)) {
+                        t = ufb * S;
+                        owner = select_cdf(P, [&](int j) { return j < 32 ? Wj : Wj2; }, t, beyond, lane);
+                    }
+                } else {   // one mass per lane: one compensated scan
                     float s, cc;
                     warp_incl_scan_comp(Wj, lane, s, cc);
                     const float S = __shfl_sync(kFull, s, 31) + __shfl_sync(kFull, cc, 31);
                     if (S > 0.0f && isfinite(S)) {
                         t = ufb * S;
-                        const unsigned hit = __ballot_sync(kFull, lane < P && t < s + cc);
+                        const unsigned hit = __ballot_sync(kFull, lane < P && Wj > 0.0f && t < s + cc);
                         if (hit) {
                             owner = __ffs(hit) - 1;
                             const float os = __shfl_sync(kFull, s, owner);
@@ -1303,7 +1342,7 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
                     }
                     // masses: sums of the strips' four partials (the bonus pass
                     // summed against this warp's own maximum, that of partial g)
-                    const float own_m = __shfl_sync(kFull, xv.x, g);
+                    const float own_m = __shfl_sync(kFull, (WIDE && g >= 32) ? xw.x : xv.x, g & 31);
                     const float wscale = bonus ? (own_m == -INFINITY ? 0.0f : weight(own_m, m_t, c)) : 1.0f;
                     // strips in index order: chunk j's strip k is entry j * NV + k
                     auto strip_mass = [&](int q) -> float {

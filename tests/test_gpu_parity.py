@@ -234,11 +234,13 @@ def test_launch_geometries_match_oracle(dev, mixed, kw):
     assert np.array_equal(got[0], again[0]) and np.array_equal(got[1], again[1])
 
 
-# chunks per CTA, chunks per warp: one to sixteen CTAs per row, one to five
-# warps per CTA, four to twenty chunks per warp
+# chunks per CTA, chunks per warp: one to sixteen CTAs per row, one to eight
+# warps per CTA, one to twenty chunks per warp, up to 64 warp ranges per row
+# (two partials per lane in the combines)
 LARGE_GEOMETRIES = [("bf16", 128256, 16, 4), ("bf16", 128256, 8, 2), ("bf16", 128256, 21, 2),
                     ("bf16", 128256, 32, 8), ("bf16", 128256, 20, 20), ("f32", 151936, 21, 2),
-                    ("f32", 151936, 38, 10), ("f32", 151936, 20, 20)]
+                    ("f32", 151936, 38, 10), ("f32", 151936, 20, 20),
+                    ("bf16", 128256, 16, 2), ("bf16", 128256, 9, 1), ("f32", 151936, 50, 7)]
 
 
 @pytest.mark.parametrize("dtype,V,ncpc,cpw", LARGE_GEOMETRIES)
@@ -321,3 +323,12 @@ def test_full_size_workloads_sampled(dev, idx):
         seqs = np.unique(np.concatenate([seqs, [0, 511, 512, 1023]]))
     ref = oracle.verify_inputs(rows_to_host(d, seqs))
     compare(ref, got_t, got_n, seqs)
+
+
+@pytest.mark.parametrize("dtype,V,ncpc,cpw,parts", [("bf16", 128256, 16, 2, 64), ("bf16", 128256, 9, 1, 56),
+                                                     ("f32", 151936, 50, 7, 48)])
+def test_wide_geometries_use_more_than_32_ranges(dev, dtype, V, ncpc, cpw, parts):
+    """The overrides above really cut a row into more than 32 warp ranges."""
+    code = sv.SV_DTYPE_BF16 if dtype == "bf16" else sv.SV_DTYPE_F32
+    g = sv.sv_geometry(12, 7, V, code, ncpc, cpw)
+    assert g["cluster_ctas"] * g["warps"] == parts == g["warp_ranges"]
