@@ -577,6 +577,14 @@ static sv_status run(const Call& c, int kmax, const sv_options* opt, void* ws, s
     a.next_unit = reinterpret_cast<int*>(base + L.next_unit);
     a.K = reinterpret_cast<const int32_t*>(hbase + L.K);
     a.order = reinterpret_cast<const int32_t*>(hbase + L.order);
+    {
+        const int32_t* ord = reinterpret_cast<const int32_t*>(hdr + L.order);
+        const int nf = std::min(g.clusters, kFirstUnits);   // clusters <= B
+        for (int k = 0; k < nf; ++k) {
+            a.first_b[k] = ord[k];
+            a.first_K[k] = c.K[ord[k]];
+        }
+    }
     a.p_x = want_diag ? dg->p_x : nullptr;
     a.q_x = want_diag ? dg->q_x : nullptr;
     a.resid = want_diag ? dg->resid_mass : nullptr;

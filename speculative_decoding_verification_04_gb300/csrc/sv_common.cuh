@@ -21,6 +21,9 @@ constexpr int kMaxWarps = 8;
 constexpr int kMaxRegs = 168;
 constexpr int kMaxCluster = 16;
 constexpr uint32_t kWaitSpins = 1u << 22;   // bounded mbarrier polls (a few seconds)
+// Clusters whose first sequence comes with the launch arguments (cluster c
+// starts with ticket c; the tickets after the first wave are claimed).
+constexpr int kFirstUnits = 256;
 // Decision of one row.
 enum : int {
     kDecAccept = 1,
@@ -56,6 +59,10 @@ struct Args {
     int* next_unit;        // claim counter of the persistent sweep
     const int32_t* K;
     const int32_t* order;  // sequences in claim order (longest K first)
+    // ticket c's sequence and its K, c < min(clusters, kFirstUnits): the first
+    // wave starts without a claim or a header read
+    int32_t first_b[kFirstUnits];
+    int32_t first_K[kFirstUnits];
     // logit layout: padded ([B][Kmax+1][V], [B][Kmax][V]) or packed by K
     // (sequence b's rows start at row cu_t[b] of the target and cu_d[b] of the
     // draft array)

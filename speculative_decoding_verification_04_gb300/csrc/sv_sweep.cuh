@@ -66,8 +66,7 @@ struct SweepLayout {
     size_t xbuf;           // [2][P] float4 row partials (P = warps per row)
     size_t xbuf2;          // [2][P] float2 residual totals
     size_t xclaim;         // [2] int2: (sequence, ticket) claimed by rank 0 during the row
-    size_t first;          // int2: (sequence, ticket) of the cluster's first unit, or of a
-                           // claim made between sequences
+    size_t first;          // int2: (sequence, ticket) of a claim made between sequences
     size_t stats;          // [nw][kw][strips][4] float: per-strip partial sums of the
                            // draw masses (at most 64 bytes a chunk; kw = longest range)
     size_t total;
@@ -233,9 +232,13 @@ __device__ __forceinline__ TokF shfl_tok(const Tok& t)
 }
 
 // Claims (one thread): a ticket now, its sequence later (the ticket's value
-// is not waited for until the sequence is needed).  Tickets past the batch,
-// or anything out of range, read as -1.
-__device__ __forceinline__ int claim_ticket(const Args& a) { return atomicAdd(a.next_unit, 1); }
+// is not waited for until the sequence is needed).  The first wave's tickets
+// 0 .. n_clusters - 1 are the clusters' own; the counter hands out the rest.
+// Tickets past the batch, or anything out of range, read as -1.
+__device__ __forceinline__ int claim_ticket(const Args& a, int n_clusters)
+{
+    return atomicAdd(a.next_unit, 1) + n_clusters;
+}
 
 __device__ __forceinline__ int ticket_unit(const Args& a, int t)
 {
@@ -280,6 +283,15 @@ __device__ __forceinline__ int seq_drow(const Args& a, int b)
 __device__ __forceinline__ UnitPos unit_pos(const Args& a, int b)
 {
     return UnitPos{b, __ldg(a.K + b), __ldg(a.temp + b), seq_trow(a, b), seq_drow(a, b)};
+}
+
+// The first sequence of cluster `cid` (ticket cid): from the launch
+// arguments for the first kFirstUnits clusters, else from the header.
+__device__ __forceinline__ UnitPos first_unit_pos(const Args& a, int cid, int b)
+{
+    if (cid < kFirstUnits)
+        return UnitPos{b, a.first_K[cid], __ldg(a.temp + b), seq_trow(a, b), seq_drow(a, b)};
+    return unit_pos(a, b);
 }
 
 // The sequence's final-draw uniform (slot K_b), sampling sequences only.
@@ -802,25 +814,12 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
     }
     __syncthreads();
     cluster_arrive();   // every CTA's barriers exist before any peer signals them
-    int f0 = -1, t0 = -1;
-    if (rank == 0 && w == 0) {
-        if (lane == 0) {
-            t0 = claim_ticket(a);
-            f0 = ticket_unit(a, t0);
-        }
-        f0 = __shfl_sync(kFull, f0, 0);
-        t0 = __shfl_sync(kFull, t0, 0);
-    }
-    cluster_wait();
-    if (rank == 0 && w == 0 && lane < C) {
-        st_cluster_s32(map_to_rank(smem_addr(first), (uint32_t)lane), f0);
-        st_cluster_s32(map_to_rank(smem_addr(first + 1), (uint32_t)lane), t0);
-    }
-    cluster_arrive();
     cluster_wait();
 
     // ---- per-warp schedule state (the same in every warp of the cluster) ----
-    const int u0 = first[0];
+    const int n_clusters = (int)(gridDim.x / (unsigned)C);
+    const int cid = (int)(blockIdx.x / (unsigned)C);   // this cluster: ticket cid first
+    const int u0 = cid < kFirstUnits ? a.first_b[cid] : ticket_unit(a, cid);
     bool active = u0 >= 0 && u0 < a.B;
     int spare = -1;
     UnitPos spare_pos{0, 0, 0.0f};
@@ -829,8 +828,7 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
     // latency) only while at least two waves of tickets remain; nearer the
     // end it claims when it finishes a sequence, so that the last sequences
     // go to the clusters that are free first.
-    const int n_clusters = (int)(gridDim.x / (unsigned)C);
-    int last_t = first[1];   // the ticket of the cluster's latest claim
+    int last_t = cid;        // the ticket of the cluster's latest claim
     uint32_t kc = 0;         // claims made between sequences (xbarc phase)
     bool broken = false;     // a slot wait gave up: no more copies, rows poisoned
     bool xbroken = false;    // an exchange wait gave up: leave the loop
@@ -838,7 +836,7 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
     Row row = make_row(a, 0, 0, 0, 0.0f, 0, 0);
     SeqVals cur_sv{0, 0.0f}, spare_sv{0, 0.0f};   // the current and the spare sequence's
     if (active) {
-        const UnitPos p0 = unit_pos(a, u0);
+        const UnitPos p0 = first_unit_pos(a, cid, u0);
         row = make_row(a, 0, p0.b, p0.Kb, p0.T, p0.tb, p0.db);
         cur_sv = seq_vals(a, u0, lane);
     }
@@ -963,7 +961,7 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
         if (w == 0 && lane == 0)
             mbar_arrive_expect_tx(smem_addr(&xbar[p]), (uint32_t)P * 16u + (want_claim ? 8u : 0u));
         if (writer && lane == 0 && want_claim)
-            ticket = claim_ticket(a);
+            ticket = claim_ticket(a, n_clusters);
 
         // ---- the slice, then the proposal's logits and the claim's sequence ----
         bool have = false;
@@ -1398,7 +1396,7 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
                     mbar_arrive_expect_tx(xbarc, 8u);
                 int cb = -1, ct = -1;
                 if (writer && lane == 0) {
-                    ct = claim_ticket(a);
+                    ct = claim_ticket(a, n_clusters);
                     cb = ticket_unit(a, ct);
                 }
                 cb = __shfl_sync(kFull, cb, 0);
