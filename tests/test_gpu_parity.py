@@ -271,7 +271,9 @@ def test_no_device_errors_recorded(dev, mixed):
 # ---------------------------------------------------------------------------
 # per-position probabilities (diagnostics) within 1e-5 relative
 # ---------------------------------------------------------------------------
-@pytest.mark.parametrize("dtype,V,T", [("f32", 7001, 0.7), ("bf16", 12345, 1.0), ("f32", 5, 1.0)])
+# the last case runs the kernel variant with more than 32 warp ranges per row
+@pytest.mark.parametrize("dtype,V,T", [("f32", 7001, 0.7), ("bf16", 12345, 1.0), ("f32", 5, 1.0),
+                                       ("f32", 151936, 0.7)])
 def test_position_probabilities(dev, dtype, V, T):
     B, K = 16, 5
     inp = W.make_host(B, K, V, dtype, 2.0, 1.0, T, seed=V)
