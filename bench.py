@@ -332,11 +332,16 @@ def run_ours(args):
             sv.spec_verify_host(*host_args, out_tokens=h_ot, out_num_accepted=h_on)
         e2e_s = _max_over_ranks(dist, (time.perf_counter() - t0) / n_e2e, dev)
         same = bool(np.array_equal(h_on.numpy(), nacc))
-        h2d = sum(x.numel() * x.element_size() for x in (h_t, h_d, h_tok, h_uni, h_tmp))
+        # page-locked logits are read in place by the kernel over the host
+        # link: the logit rows the method reaches (bytes_need) cross it; the
+        # tokens, uniforms and temperatures are copied
+        h2d = bytes_need + sum(x.numel() * x.element_size() for x in (h_tok, h_uni, h_tmp))
         d2h = h_ot.numel() * 4 + h_on.numel() * 4
         e2e = dict(value=_whole_job_rate(world, pos_per_step, 1, e2e_s), unit=UNIT, h2d_bytes_per_step=h2d,
                    d2h_bytes_per_step=d2h, ms_per_step=round(e2e_s * 1e3, 3),
-                   matches_device_run=same, api="spec_verify_host")
+                   matches_device_run=same, api="spec_verify_host",
+                   logits="page-locked host memory, read in place by the kernel (the rows the method "
+                          "reaches); the other inputs copied, outputs copied back, every step")
         del h_t, h_d, staging
 
     # ---- CPU oracle baseline on a bounded sample (rank 0, N=1 only) ----

@@ -300,10 +300,16 @@ size_t sv_host_staging_size(int32_t B, int32_t Kmax, int32_t V, sv_dtype dtype);
 
 /*
  * spec_verify_host -- the same operation on HOST arrays (same layouts as
- * above; pinned memory gives asynchronous copies, pageable memory works).
- * Copies the inputs into `device_staging` (>= sv_host_staging_size bytes,
- * 256-byte aligned), verifies, copies out_tokens / out_num_accepted back to
- * the host arrays and synchronises `stream` before returning.
+ * above).  `device_staging` is >= sv_host_staging_size bytes, 256-byte
+ * aligned.  Logits in page-locked host memory that is mapped into the
+ * device's address space (cudaHostAlloc / cudaHostRegister memory on a
+ * system with unified addressing) are read in place by the kernel: only the
+ * rows the method reaches cross the host link (on a Grace-Blackwell node,
+ * NVLink-C2C).  Other logits (pageable memory) are first copied into the
+ * staging.  Tokens, uniforms and temperatures are copied into the staging;
+ * out_tokens / out_num_accepted are copied back to the host arrays, and
+ * `stream` is synchronised before returning (the host arrays must not change
+ * while the call runs).
  */
 sv_status spec_verify_host(const void* h_target_logits, const void* h_draft_logits,
                            sv_dtype dtype, const int32_t* h_draft_tokens,

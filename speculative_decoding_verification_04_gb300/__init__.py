@@ -367,7 +367,9 @@ def spec_sample(logits, uniforms, temperature, workspace=None, out_tokens=None, 
 
 def spec_verify_host(target, draft, draft_tokens, uniforms, temperature, K, staging,
                      out_tokens=None, out_num_accepted=None, stream=None):
-    """spec_verify_host on HOST tensors (pinned CPU tensors give async copies).
+    """spec_verify_host on HOST tensors: pinned (page-locked, device-mapped)
+    logits are read in place by the kernel, only the rows the method reaches;
+    pageable logits are copied into ``staging`` first.
 
     ``staging`` is a uint8 CUDA tensor of at least sv_host_staging_size bytes.
     Returns (out_tokens, out_num_accepted) as CPU tensors.

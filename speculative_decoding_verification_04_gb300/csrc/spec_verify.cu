@@ -465,8 +465,9 @@ static HeaderSlot* header_slot(int dev, size_t need, sv_status* st)
 
 // host_header: where the per-call header is assembled before its upload
 // (nullptr: a pinned per-thread slot, else a pageable per-thread buffer).
+// host_rows: the logits are device-mapped host memory (read in place).
 static sv_status run(const Call& c, int kmax, const sv_options* opt, void* ws, size_t ws_bytes,
-                     cudaStream_t stream, unsigned char* host_header = nullptr)
+                     cudaStream_t stream, unsigned char* host_header = nullptr, bool host_rows = false)
 {
     if (c.B == 0)
         return SV_OK;
@@ -479,13 +480,15 @@ static sv_status run(const Call& c, int kmax, const sv_options* opt, void* ws, s
     sv_status st = device_sms(&dev, &nsm);
     if (st != SV_OK)
         return st;
-    cudaPointerAttributes pa;
-    if (cudaPointerGetAttributes(&pa, c.tgt) != cudaSuccess)
-        return SV_ERR_CUDA;
-    if (pa.type != cudaMemoryTypeDevice && pa.type != cudaMemoryTypeManaged)
-        return SV_ERR_INVALID_ARG;
-    if (pa.type == cudaMemoryTypeDevice && pa.device != dev)
-        return SV_ERR_INVALID_ARG;
+    if (!host_rows) {
+        cudaPointerAttributes pa;
+        if (cudaPointerGetAttributes(&pa, c.tgt) != cudaSuccess)
+            return SV_ERR_CUDA;
+        if (pa.type != cudaMemoryTypeDevice && pa.type != cudaMemoryTypeManaged)
+            return SV_ERR_INVALID_ARG;
+        if (pa.type == cudaMemoryTypeDevice && pa.device != dev)
+            return SV_ERR_INVALID_ARG;
+    }
     Geom g;
     st = pick_geometry(c.V, c.dtype, c.B, kmax, opt ? opt->chunks_per_cta : 0,
                        opt ? opt->chunks_per_warp : 0, dev, &g);
@@ -573,6 +576,7 @@ static sv_status run(const Call& c, int kmax, const sv_options* opt, void* ws, s
     a.has_draft = c.drf != nullptr ? 1 : 0;
     const uintptr_t al = (uintptr_t)c.tgt | (c.drf ? (uintptr_t)c.drf : 0);
     a.aligned = ((al & 15) == 0) && (((size_t)c.V * g.s) % 16 == 0);
+    a.host_rows = host_rows ? 1 : 0;
     a.err = reinterpret_cast<uint32_t*>(base + L.err);
     a.next_unit = reinterpret_cast<int*>(base + L.next_unit);
     a.K = reinterpret_cast<const int32_t*>(hbase + L.K);
@@ -608,6 +612,18 @@ static sv_status run(const Call& c, int kmax, const sv_options* opt, void* ws, s
         slot->used = true;
     }
     return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
+// The device's view of page-locked host memory mapped into its address space
+// (nullptr for any other pointer).
+static const void* mapped_host(const void* p)
+{
+    cudaPointerAttributes pa;
+    if (cudaPointerGetAttributes(&pa, p) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return nullptr;
+    }
+    return (pa.type == cudaMemoryTypeHost && pa.devicePointer) ? pa.devicePointer : nullptr;
 }
 
 // Launch geometry a call would use (for reports and tests).
@@ -861,17 +877,27 @@ sv_status spec_verify_host(const void* h_target_logits, const void* h_draft_logi
     void* ws = p;
     const size_t ws_bytes = staging_bytes - (size_t)(p - static_cast<unsigned char*>(device_staging));
     const bool has_drf = h_draft_logits && n_drf;
-    if (cudaMemcpyAsync(d_tgt, h_target_logits, n_tgt, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
-        (has_drf && cudaMemcpyAsync(d_drf, h_draft_logits, n_drf, cudaMemcpyHostToDevice, stream) != cudaSuccess) ||
+    // page-locked logits mapped into the device's address space are read in
+    // place by the kernel, only the rows the method reaches; others are
+    // copied into the staging first
+    const void* m_tgt = sv::mapped_host(h_target_logits);
+    const void* m_drf = has_drf ? sv::mapped_host(h_draft_logits) : nullptr;
+    const bool in_place = m_tgt && (!has_drf || m_drf);
+    if ((!in_place &&
+         (cudaMemcpyAsync(d_tgt, h_target_logits, n_tgt, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
+          (has_drf && cudaMemcpyAsync(d_drf, h_draft_logits, n_drf, cudaMemcpyHostToDevice, stream) !=
+                          cudaSuccess))) ||
         (n_tok && cudaMemcpyAsync(d_tok, h_draft_tokens, n_tok, cudaMemcpyHostToDevice, stream) != cudaSuccess) ||
         cudaMemcpyAsync(d_uni, h_uniforms, n_uni, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
         cudaMemcpyAsync(d_tmp, h_temperature, n_tmp, cudaMemcpyHostToDevice, stream) != cudaSuccess)
         return SV_ERR_CUDA;
-    const sv::Call dc{d_tgt, has_drf ? d_drf : nullptr, dtype,
+    const void* tgt = in_place ? m_tgt : d_tgt;
+    const void* drf = has_drf ? (in_place ? m_drf : d_drf) : nullptr;
+    const sv::Call dc{tgt, drf, dtype,
                       n_tok ? reinterpret_cast<const int32_t*>(d_tok) : nullptr,
                       reinterpret_cast<const float*>(d_uni), reinterpret_cast<const float*>(d_tmp),
                       B, K, V, reinterpret_cast<int32_t*>(d_otok), reinterpret_cast<int32_t*>(d_on)};
-    st = sv::run(dc, kmax, nullptr, ws, ws_bytes, stream);
+    st = sv::run(dc, kmax, nullptr, ws, ws_bytes, stream, nullptr, in_place);
     if (st != SV_OK)
         return st;
     if (cudaMemcpyAsync(h_out_tokens, d_otok, n_otok, cudaMemcpyDeviceToHost, stream) != cudaSuccess ||

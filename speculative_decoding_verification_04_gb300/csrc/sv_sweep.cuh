@@ -860,6 +860,43 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
         const T* tr = tgt + ((size_t)r.tb + r.i) * (size_t)V + e0;
         const T* dr = ld ? drf + ((size_t)r.db + r.i) * (size_t)V + e0 : nullptr;
         const int nb = a.aligned ? ((n_el * (int)sizeof(T)) & ~15) / (int)sizeof(T) : 0;
+        if (a.host_rows) {
+            // logits in device-mapped host memory: 16-byte loads (the bulk-copy
+            // engine is not used on host memory), eight in flight per lane,
+            // stored to the slot (lane l stores the vectors it reads in the
+            // pass); the rest one element at a time; then a plain arrival on
+            // the slot barrier
+            const int nvec = nb * (int)sizeof(T) / 16;
+            for (int arr = 0; arr < (ld ? 2 : 1); ++arr) {
+                const uint4* src = reinterpret_cast<const uint4*>(arr ? dr : tr);
+                uint4* dst = reinterpret_cast<uint4*>(arr ? slot_d : slot_t);
+                for (int j0 = 0; j0 < nvec; j0 += 8 * 32) {
+                    uint4 x[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const int j = j0 + u * 32 + lane;
+                        if (j < nvec)
+                            x[u] = src[j];
+                    }
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const int j = j0 + u * 32 + lane;
+                        if (j < nvec)
+                            dst[j] = x[u];
+                    }
+                }
+            }
+            for (int j = nb + lane; j < n_el; j += 32) {
+                EL::copy(slot_t + j, tr + j);
+                if (ld)
+                    EL::copy(slot_d + j, dr + j);
+            }
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(bar);
+            pending = true;
+            return;
+        }
         if (lane == 0) {
             const uint32_t bytes = (uint32_t)nb * (uint32_t)sizeof(T);
             const uint32_t tx = bytes * (ld ? 2u : 1u);
@@ -901,7 +938,7 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
     bool pf_draft = false;   // the spare's draft row is still to prefetch
     const int nb_pf = a.aligned ? ((n_el * (int)sizeof(T)) & ~15) / (int)sizeof(T) : 0;
     auto prefetch_target = [&](int trow) {
-        if (lane == 0 && nb_pf > 0)
+        if (lane == 0 && nb_pf > 0 && !a.host_rows)
             bulk_prefetch_l2(tgt + (size_t)trow * (size_t)V + e0, (uint32_t)nb_pf * (uint32_t)sizeof(T));
     };
     auto prefetch_draft = [&]() {   // (and the target's, packed: its row had to load)
@@ -909,7 +946,7 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
             return;
         if (a.packed)
             prefetch_target(spare_pos.tb);
-        if (lane == 0 && nb_pf > 0 && a.has_draft && spare_pos.Kb > 0 && spare_pos.T != 0.0f)
+        if (lane == 0 && nb_pf > 0 && !a.host_rows && a.has_draft && spare_pos.Kb > 0 && spare_pos.T != 0.0f)
             bulk_prefetch_l2(drf + (size_t)spare_pos.db * (size_t)V + e0, (uint32_t)nb_pf * (uint32_t)sizeof(T));
     };
 

@@ -206,6 +206,26 @@ def test_entry_points_agree(dev, mixed):
                                torch.from_numpy(inp["uniforms"]),
                                torch.from_numpy(inp["temperature"]), inp["K"], staging)
     assert np.array_equal(t.numpy(), base[0]) and np.array_equal(n.numpy(), base[1])
+    # page-locked logits are read in place by the kernel: the same results
+    t, n = sv.spec_verify_host(ht.pin_memory(), hd.pin_memory(), torch.from_numpy(inp["tokens"]),
+                               torch.from_numpy(inp["uniforms"]),
+                               torch.from_numpy(inp["temperature"]), inp["K"], staging)
+    assert np.array_equal(t.numpy(), base[0]) and np.array_equal(n.numpy(), base[1])
+
+
+@pytest.mark.parametrize("idx", [3, 4])
+def test_host_logits_read_in_place_full_size(dev, idx):
+    """Full-size workloads from page-locked host logits (read in place over
+    the host link, bf16 and fp32, greedy and sampling rows): the device
+    results, bit for bit."""
+    d = W.make_device(idx, dev)
+    B, Kmax, V = d["B"], d["Kmax"], d["V"]
+    base = run_gpu(d, "ws")
+    code = dtype_code(d["dtype"])
+    staging = torch.empty(sv.sv_host_staging_size(B, Kmax, V, code), dtype=torch.uint8, device=dev)
+    host = [d[k].cpu().pin_memory() for k in ("target", "draft", "tokens", "uniforms", "temperature")]
+    t, n = sv.spec_verify_host(*host, d["K"], staging)
+    assert np.array_equal(t.numpy(), base[0]) and np.array_equal(n.numpy(), base[1])
 
 
 def test_verify_all_gives_identical_outputs(dev, mixed):
