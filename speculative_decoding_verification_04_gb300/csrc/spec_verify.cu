@@ -99,7 +99,7 @@ static bool ws_layout(int B, int Kmax, int V, sv_dtype dt, WsLayout* L)
 
 struct DeviceInfo {
     int nsm = 0;
-    bool attrs_set[2][4] = {};
+    bool attrs_set[2][6] = {};
     void* static_scratch = nullptr;   // device address of g_static_scratch on this device
 };
 
@@ -115,16 +115,16 @@ static DeviceInfo g_dev[64];
 // cudaOccupancyMaxActiveClusters per (device, kernel, cluster size, warps, smem)
 static std::map<std::tuple<int, int, int, int, size_t>, int> g_fit;
 // chosen geometry per (device, V, dtype, B, Kmax, tuning overrides)
-static std::map<std::tuple<int, int, int, int, int, int, int>, Geom> g_pick;
+static std::map<std::tuple<int, int, int, int, int, int, int, int>, Geom> g_pick;
 
-template <typename T, int NV, bool WIDE>
+template <typename T, int NV, bool WIDE, bool HOST>
 static cudaError_t prepare_kernels(int dev)
 {
     const int ti = sizeof(T) == 2 ? 1 : 0;
-    const int ni = NV == 1 ? 0 : NV == 2 ? 1 : (WIDE ? 3 : 2);
+    const int ni = NV == 1 ? 0 : NV == 2 ? 1 : (WIDE ? 3 : 2) + (HOST ? 2 : 0);
     std::lock_guard<std::mutex> lk(g_mu);
     if (!g_dev[dev].attrs_set[ti][ni]) {
-        auto kern = sv_sweep_kernel<T, NV, WIDE>;
+        auto kern = sv_sweep_kernel<T, NV, WIDE, HOST>;
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              kSmemPerCtaMax);
         if (e != cudaSuccess)
@@ -154,13 +154,13 @@ static void sweep_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, con
 }
 
 // How many clusters of this shape the device holds at once (0: cannot launch).
-template <typename T, int NV, bool WIDE>
+template <typename T, int NV, bool WIDE, bool HOST>
 static cudaError_t cluster_capacity(const Geom& g, int dev, int* n)
 {
-    cudaError_t e = prepare_kernels<T, NV, WIDE>(dev);
+    cudaError_t e = prepare_kernels<T, NV, WIDE, HOST>(dev);
     if (e != cudaSuccess)
         return e;
-    const auto key = std::make_tuple(dev, (int)sizeof(T) * 16 + NV, g.C, g.nw, g.smem);
+    const auto key = std::make_tuple(dev, (int)sizeof(T) * 16 + NV + (HOST ? 256 : 0), g.C, g.nw, g.smem);
     {
         std::lock_guard<std::mutex> lk(g_mu);
         auto it = g_fit.find(key);
@@ -173,7 +173,7 @@ static cudaError_t cluster_capacity(const Geom& g, int dev, int* n)
     cudaLaunchAttribute attr[1];
     sweep_config(&cfg, attr, g, 1, 0);
     int v = 0;
-    e = cudaOccupancyMaxActiveClusters(&v, sv_sweep_kernel<T, NV, WIDE>, &cfg);
+    e = cudaOccupancyMaxActiveClusters(&v, sv_sweep_kernel<T, NV, WIDE, HOST>, &cfg);
     if (e != cudaSuccess) {
         (void)cudaGetLastError();
         v = 0;
@@ -184,15 +184,21 @@ static cudaError_t cluster_capacity(const Geom& g, int dev, int* n)
     return cudaSuccess;
 }
 
+// host: the logits are device-mapped host memory (16-byte vectors only: the
+// host path exists for NV = 4)
 template <typename T>
-static cudaError_t capacity_nv(const Geom& g, int dev, int* n)
+static cudaError_t capacity_nv(const Geom& g, bool host, int dev, int* n)
 {
+    const bool wide = g.C * g.nw > 32;
     switch (g.nv) {
-    case 1: return cluster_capacity<T, 1, false>(g, dev, n);
-    case 2: return cluster_capacity<T, 2, false>(g, dev, n);
+    case 1: return cluster_capacity<T, 1, false, false>(g, dev, n);
+    case 2: return cluster_capacity<T, 2, false, false>(g, dev, n);
     default:
-        return g.C * g.nw > 32 ? cluster_capacity<T, 4, true>(g, dev, n)
-                               : cluster_capacity<T, 4, false>(g, dev, n);
+        if (host)
+            return wide ? cluster_capacity<T, 4, true, true>(g, dev, n)
+                        : cluster_capacity<T, 4, false, true>(g, dev, n);
+        return wide ? cluster_capacity<T, 4, true, false>(g, dev, n)
+                    : cluster_capacity<T, 4, false, false>(g, dev, n);
     }
 }
 
@@ -222,10 +228,10 @@ static bool shape_geometry(int V, sv_dtype dt, int C, int nw, Geom* g)
     return g->smem <= (size_t)kSmemPerCtaMax;
 }
 
-static sv_status capacity_of(const Geom& g, sv_dtype dt, int dev, int* cap)
+static sv_status capacity_of(const Geom& g, sv_dtype dt, bool host, int dev, int* cap)
 {
-    const cudaError_t e = dt == SV_DTYPE_BF16 ? capacity_nv<__nv_bfloat16>(g, dev, cap)
-                                              : capacity_nv<float>(g, dev, cap);
+    const cudaError_t e = dt == SV_DTYPE_BF16 ? capacity_nv<__nv_bfloat16>(g, host, dev, cap)
+                                              : capacity_nv<float>(g, host, dev, cap);
     return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
@@ -236,9 +242,9 @@ static sv_status capacity_of(const Geom& g, sv_dtype dt, int dev, int* cap)
 // per row (shorter passes), then larger clusters.  Tuning overrides: chunks
 // per CTA (sets C), chunks per warp (sets the warps per CTA).
 static sv_status pick_geometry(int V, sv_dtype dt, int B, int Kmax, int override_ncpc,
-                               int want_cpw, int dev, Geom* g)
+                               int want_cpw, int dev, bool host, Geom* g)
 {
-    const auto key = std::make_tuple(dev, V, (int)dt, B, Kmax, override_ncpc, want_cpw);
+    const auto key = std::make_tuple(dev, V, (int)dt, B, Kmax, override_ncpc, want_cpw, host ? 1 : 0);
     {
         std::lock_guard<std::mutex> lk(g_mu);
         auto it = g_pick.find(key);
@@ -267,7 +273,7 @@ static sv_status pick_geometry(int V, sv_dtype dt, int B, int Kmax, int override
             if (!shape_geometry(V, dt, C, nw, &t))
                 continue;
             int cap = 0;
-            const sv_status st = capacity_of(t, dt, dev, &cap);
+            const sv_status st = capacity_of(t, dt, host, dev, &cap);
             if (st != SV_OK)
                 return st;
             if (cap <= 0)
@@ -289,27 +295,31 @@ static sv_status pick_geometry(int V, sv_dtype dt, int B, int Kmax, int override
     return SV_OK;
 }
 
-template <typename T, int NV, bool WIDE>
+template <typename T, int NV, bool WIDE, bool HOST>
 static cudaError_t launch_sweep(const Args& a, const Geom& g, cudaStream_t st, int dev)
 {
-    cudaError_t e = prepare_kernels<T, NV, WIDE>(dev);
+    cudaError_t e = prepare_kernels<T, NV, WIDE, HOST>(dev);
     if (e != cudaSuccess)
         return e;
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[1];
     sweep_config(&cfg, attr, g, g.clusters, st);
-    return cudaLaunchKernelEx(&cfg, sv_sweep_kernel<T, NV, WIDE>, a);
+    return cudaLaunchKernelEx(&cfg, sv_sweep_kernel<T, NV, WIDE, HOST>, a);
 }
 
 template <typename T>
-static cudaError_t launch_nv(const Args& a, const Geom& g, cudaStream_t st, int dev)
+static cudaError_t launch_nv(const Args& a, const Geom& g, bool host, cudaStream_t st, int dev)
 {
+    const bool wide = g.C * g.nw > 32;
     switch (g.nv) {
-    case 1: return launch_sweep<T, 1, false>(a, g, st, dev);
-    case 2: return launch_sweep<T, 2, false>(a, g, st, dev);
+    case 1: return launch_sweep<T, 1, false, false>(a, g, st, dev);
+    case 2: return launch_sweep<T, 2, false, false>(a, g, st, dev);
     default:
-        return g.C * g.nw > 32 ? launch_sweep<T, 4, true>(a, g, st, dev)
-                               : launch_sweep<T, 4, false>(a, g, st, dev);
+        if (host)
+            return wide ? launch_sweep<T, 4, true, true>(a, g, st, dev)
+                        : launch_sweep<T, 4, false, true>(a, g, st, dev);
+        return wide ? launch_sweep<T, 4, true, false>(a, g, st, dev)
+                    : launch_sweep<T, 4, false, false>(a, g, st, dev);
     }
 }
 
@@ -491,7 +501,11 @@ static sv_status run(const Call& c, int kmax, const sv_options* opt, void* ws, s
     }
     Geom g;
     st = pick_geometry(c.V, c.dtype, c.B, kmax, opt ? opt->chunks_per_cta : 0,
-                       opt ? opt->chunks_per_warp : 0, dev, &g);
+                       opt ? opt->chunks_per_warp : 0, dev, host_rows, &g);
+    if (st != SV_OK)
+        return st;
+    if (host_rows && g.nv != 4)   // the in-place path reads 16-byte vectors
+        return SV_ERR_UNSUPPORTED;
     if (st != SV_OK)
         return st;
     if ((long long)g.clusters * g.C > 0x7fffffffLL)
@@ -576,7 +590,6 @@ static sv_status run(const Call& c, int kmax, const sv_options* opt, void* ws, s
     a.has_draft = c.drf != nullptr ? 1 : 0;
     const uintptr_t al = (uintptr_t)c.tgt | (c.drf ? (uintptr_t)c.drf : 0);
     a.aligned = ((al & 15) == 0) && (((size_t)c.V * g.s) % 16 == 0);
-    a.host_rows = host_rows ? 1 : 0;
     a.err = reinterpret_cast<uint32_t*>(base + L.err);
     a.next_unit = reinterpret_cast<int*>(base + L.next_unit);
     a.K = reinterpret_cast<const int32_t*>(hbase + L.K);
@@ -604,8 +617,8 @@ static sv_status run(const Call& c, int kmax, const sv_options* opt, void* ws, s
     a.want_kv = (opt && opt->kv_len) ? 1 : 0;
     a.kv_len = a.want_kv ? opt->kv_len : nullptr;
 
-    const cudaError_t e = c.dtype == SV_DTYPE_BF16 ? launch_nv<__nv_bfloat16>(a, g, stream, dev)
-                                                   : launch_nv<float>(a, g, stream, dev);
+    const cudaError_t e = c.dtype == SV_DTYPE_BF16 ? launch_nv<__nv_bfloat16>(a, g, host_rows, stream, dev)
+                                                   : launch_nv<float>(a, g, host_rows, stream, dev);
     if (slot) {   // the kernel reads the slot: it is free again once the kernel is done
         if (cudaEventRecord(slot->done, stream) != cudaSuccess)
             return SV_ERR_CUDA;
@@ -635,7 +648,7 @@ static sv_status geometry_of(int B, int Kmax, int V, sv_dtype dt, int ncpc, int 
     if (st != SV_OK)
         return st;
     Geom g;
-    st = pick_geometry(V, dt, B, Kmax, ncpc, cpw, dev, &g);
+    st = pick_geometry(V, dt, B, Kmax, ncpc, cpw, dev, false, &g);
     if (st != SV_OK)
         return st;
     out[0] = g.C;
@@ -882,7 +895,7 @@ sv_status spec_verify_host(const void* h_target_logits, const void* h_draft_logi
     // copied into the staging first
     const void* m_tgt = sv::mapped_host(h_target_logits);
     const void* m_drf = has_drf ? sv::mapped_host(h_draft_logits) : nullptr;
-    const bool in_place = m_tgt && (!has_drf || m_drf);
+    const bool in_place = m_tgt && (!has_drf || m_drf) && sv::pick_nv(V, (int)s) == 4;
     if ((!in_place &&
          (cudaMemcpyAsync(d_tgt, h_target_logits, n_tgt, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
           (has_drf && cudaMemcpyAsync(d_drf, h_draft_logits, n_drf, cudaMemcpyHostToDevice, stream) !=

@@ -48,7 +48,6 @@ struct Args {
     int C;                 // CTAs per cluster (one row at a time per cluster)
     int kw;                // chunks per warp (a contiguous range)
     int early_exit, aligned;
-    int host_rows;         // logits in device-mapped host memory: read with loads, not bulk copies
     // Which optional buffers were supplied.  Decided on the host: device code
     // never branches on a pointer's null-ness.
     int has_draft;         // draft logits

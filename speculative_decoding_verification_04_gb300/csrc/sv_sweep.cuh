@@ -759,8 +759,10 @@ __device__ __forceinline__ int pick_in_strip(const uint4& tv, const uint4& dv, b
 }
 
 // WIDE: more than 32 warp ranges per row (lanes hold two partials each in
-// the combines); the host launches it for exactly those geometries.
-template <typename T, int NV, bool WIDE>
+// the combines); the host launches it for exactly those geometries.  HOST:
+// the logits are device-mapped host memory, read with 16-byte loads instead
+// of bulk copies (and never prefetched into L2).
+template <typename T, int NV, bool WIDE, bool HOST>
 __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
 {
     using EL = Elem<T>;
@@ -860,7 +862,7 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
         const T* tr = tgt + ((size_t)r.tb + r.i) * (size_t)V + e0;
         const T* dr = ld ? drf + ((size_t)r.db + r.i) * (size_t)V + e0 : nullptr;
         const int nb = a.aligned ? ((n_el * (int)sizeof(T)) & ~15) / (int)sizeof(T) : 0;
-        if (a.host_rows) {
+        if constexpr (HOST) {
             // logits in device-mapped host memory: 16-byte loads (the bulk-copy
             // engine is not used on host memory), eight in flight per lane,
             // stored to the slot (lane l stores the vectors it reads in the
@@ -938,7 +940,7 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
     bool pf_draft = false;   // the spare's draft row is still to prefetch
     const int nb_pf = a.aligned ? ((n_el * (int)sizeof(T)) & ~15) / (int)sizeof(T) : 0;
     auto prefetch_target = [&](int trow) {
-        if (lane == 0 && nb_pf > 0 && !a.host_rows)
+        if (lane == 0 && nb_pf > 0 && !HOST)
             bulk_prefetch_l2(tgt + (size_t)trow * (size_t)V + e0, (uint32_t)nb_pf * (uint32_t)sizeof(T));
     };
     auto prefetch_draft = [&]() {   // (and the target's, packed: its row had to load)
@@ -946,7 +948,7 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
             return;
         if (a.packed)
             prefetch_target(spare_pos.tb);
-        if (lane == 0 && nb_pf > 0 && !a.host_rows && a.has_draft && spare_pos.Kb > 0 && spare_pos.T != 0.0f)
+        if (lane == 0 && nb_pf > 0 && !HOST && a.has_draft && spare_pos.Kb > 0 && spare_pos.T != 0.0f)
             bulk_prefetch_l2(drf + (size_t)spare_pos.db * (size_t)V + e0, (uint32_t)nb_pf * (uint32_t)sizeof(T));
     };
 
