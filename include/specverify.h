@@ -173,6 +173,18 @@ sv_status sv_geometry(int32_t B, int32_t Kmax, int32_t V, sv_dtype dtype, int32_
                       int32_t chunks_per_warp, int32_t* out8);
 
 /*
+ * CUDA graphs.  spec_verify, spec_verify_ws, spec_verify_ex and spec_sample
+ * may be called on a stream that is being captured, once an ordinary
+ * (uncaptured) call of the same shape has run on the device: that call
+ * reserves the pinned header a graph keeps (allocation is not allowed during
+ * a capture) and records the launch geometry.  The graph holds the K and the
+ * claim order of the captured call; at every replay it reads the logits,
+ * tokens, uniforms and temperatures then in the captured buffers.  A capture
+ * with no reserved header of its size returns SV_ERR_UNSUPPORTED, as do
+ * spec_verify_host and spec_verify_noalloc on a capturing stream.
+ */
+
+/*
  * Bytes of device workspace spec_verify_ws / spec_verify_ex need for this
  * shape (0 on invalid arguments).  The workspace holds the error word and
  * the claim counter, reset by every call on its stream; the rest of the

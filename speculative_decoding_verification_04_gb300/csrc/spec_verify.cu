@@ -473,8 +473,57 @@ static HeaderSlot* header_slot(int dev, size_t need, sv_status* st)
     return &sl;
 }
 
+// Headers of calls captured into CUDA graphs: a graph's kernel reads its
+// header at every replay, so each capture takes a pinned slot of its own that
+// is never written again (kept until the process ends).  Slots are allocated
+// by ordinary calls (allocation is not allowed during a capture), so that a
+// few of the size in use are always free.
+struct CapturePool {
+    std::vector<HeaderSlot*> free_slots;   // allocated, not yet taken by a capture
+};
+static CapturePool g_capture[64];
+constexpr int kCaptureSpare = 4;
+
+static void reserve_capture_slots(int dev, size_t need)
+{
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto& fs = g_capture[dev].free_slots;
+    int fit = 0;
+    for (HeaderSlot* h : fs)
+        fit += h->cap >= need ? 1 : 0;
+    for (; fit < kCaptureSpare; ++fit) {
+        HeaderSlot* h = new HeaderSlot;
+        const size_t cap = std::max(need, (size_t)4096);
+        if (cudaHostAlloc(reinterpret_cast<void**>(&h->buf), cap, cudaHostAllocMapped) != cudaSuccess ||
+            cudaHostGetDevicePointer(reinterpret_cast<void**>(&h->dbuf), h->buf, 0) != cudaSuccess) {
+            (void)cudaGetLastError();
+            if (h->buf)
+                (void)cudaFreeHost(h->buf);
+            delete h;
+            return;
+        }
+        h->cap = cap;
+        fs.push_back(h);
+    }
+}
+
+// A slot for a call being captured (nullptr: none of this size was reserved).
+static HeaderSlot* capture_slot(int dev, size_t need)
+{
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto& fs = g_capture[dev].free_slots;
+    for (size_t k = 0; k < fs.size(); ++k) {
+        if (fs[k]->cap >= need) {
+            HeaderSlot* h = fs[k];
+            fs.erase(fs.begin() + (long)k);
+            return h;
+        }
+    }
+    return nullptr;
+}
+
 // host_header: where the per-call header is assembled before its upload
-// (nullptr: a pinned per-thread slot, else a pageable per-thread buffer).
+// (nullptr: a pinned slot, else a pageable per-thread buffer).
 // host_rows: the logits are device-mapped host memory (read in place).
 static sv_status run(const Call& c, int kmax, const sv_options* opt, void* ws, size_t ws_bytes,
                      cudaStream_t stream, unsigned char* host_header = nullptr, bool host_rows = false)
@@ -490,7 +539,11 @@ static sv_status run(const Call& c, int kmax, const sv_options* opt, void* ws, s
     sv_status st = device_sms(&dev, &nsm);
     if (st != SV_OK)
         return st;
-    if (!host_rows) {
+    cudaStreamCaptureStatus cst = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cst) != cudaSuccess)
+        return SV_ERR_CUDA;
+    const bool capturing = cst != cudaStreamCaptureStatusNone;
+    if (!host_rows && !capturing) {   // (not re-checked while a graph is captured)
         cudaPointerAttributes pa;
         if (cudaPointerGetAttributes(&pa, c.tgt) != cudaSuccess)
             return SV_ERR_CUDA;
@@ -521,7 +574,17 @@ static sv_status run(const Call& c, int kmax, const sv_options* opt, void* ws, s
     thread_local std::vector<unsigned char> hdr_tls;
     unsigned char* hdr = host_header;
     HeaderSlot* slot = nullptr;
-    if (!hdr) {
+    if (capturing) {
+        // a slot of the graph's own (reserved by an earlier ordinary call of
+        // this size); pageable staging cannot be captured
+        if (hdr)
+            return SV_ERR_UNSUPPORTED;
+        slot = capture_slot(dev, L.header_end);
+        if (!slot)
+            return SV_ERR_UNSUPPORTED;
+        hdr = slot->buf;
+    } else if (!hdr) {
+        reserve_capture_slots(dev, L.header_end);
         sv_status hs = SV_OK;
         slot = header_slot(dev, L.header_end, &hs);
         if (hs != SV_OK)
@@ -619,7 +682,7 @@ static sv_status run(const Call& c, int kmax, const sv_options* opt, void* ws, s
 
     const cudaError_t e = c.dtype == SV_DTYPE_BF16 ? launch_nv<__nv_bfloat16>(a, g, host_rows, stream, dev)
                                                    : launch_nv<float>(a, g, host_rows, stream, dev);
-    if (slot) {   // the kernel reads the slot: it is free again once the kernel is done
+    if (slot && !capturing) {   // the kernel reads the slot: it is free again once the kernel is done
         if (cudaEventRecord(slot->done, stream) != cudaSuccess)
             return SV_ERR_CUDA;
         slot->used = true;
@@ -874,6 +937,11 @@ sv_status spec_verify_host(const void* h_target_logits, const void* h_draft_logi
     const size_t need = sv_host_staging_size(B, kmax, V, dtype);
     if (!device_staging || staging_bytes < need || ((uintptr_t)device_staging & 255))
         return SV_ERR_NO_MEMORY;
+    cudaStreamCaptureStatus cst = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cst) != cudaSuccess)
+        return SV_ERR_CUDA;
+    if (cst != cudaStreamCaptureStatusNone)   // the call synchronises: not capturable
+        return SV_ERR_UNSUPPORTED;
     const size_t s = (size_t)sv::elem_size(dtype);
     const size_t Bz = (size_t)B, K1 = (size_t)kmax + 1, Vz = (size_t)V;
     unsigned char* p = static_cast<unsigned char*>(device_staging);

@@ -130,3 +130,64 @@ def test_packed_logits_give_the_padded_results(dev, dtype):
     torch.cuda.synchronize()
     assert torch.equal(t1, t0) and torch.equal(n1, n0)
     compare(oracle_ref(inp), t1.cpu().numpy(), n1.cpu().numpy())
+
+
+def test_cuda_graph_replays_the_verification(dev):
+    """A verification captured into a CUDA graph (after one ordinary call of
+    its shape) replays on whatever the captured buffers hold: the oracle's
+    results for the inputs at capture time and for new inputs copied into the
+    same buffers, with ordinary calls of other shapes in between (which reuse
+    the library's rotating header slots, not the graph's)."""
+    import torch
+    B, V = 48, 12345
+    K = W.configs.ragged_k(5, B)
+    temps = np.where(np.arange(B) % 3 == 0, 0.0, 1.0).astype(np.float32)
+    inp1 = W.make_host(B, K, V, "bf16", 2.0, 1.0, temps, seed=71)
+    inp2 = W.make_host(B, K, V, "bf16", 2.0, 1.0, temps, seed=72)
+    d = to_device(inp1, dev)
+    Kmax = int(np.max(K))
+    ws = sv.Workspace(B, Kmax, V, sv.SV_DTYPE_BF16)
+    ot = torch.empty((B, Kmax + 1), dtype=torch.int32, device=dev)
+    on = torch.empty((B,), dtype=torch.int32, device=dev)
+    args = (d["target"], d["draft"], d["tokens"], d["uniforms"], d["temperature"], K)
+    sv.spec_verify_ws(*args, ws, out_tokens=ot, out_num_accepted=on)   # reserves the graph's header
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        sv.spec_verify_ws(*args, ws, out_tokens=ot, out_num_accepted=on)
+    ot.fill_(-7)
+    on.fill_(-7)
+    g.replay()
+    torch.cuda.synchronize()
+    compare(oracle_ref(inp1), ot.cpu().numpy(), on.cpu().numpy())
+    # new inputs in the captured buffers; other calls churn the header slots
+    d2 = to_device(inp2, dev)
+    for key in ("target", "draft", "tokens", "uniforms", "temperature"):
+        d[key].copy_(d2[key])
+    other = W.make_host(16, 3, 9000, "bf16", 2.0, 1.0, 1.0, seed=73)
+    for _ in range(20):
+        run_gpu(to_device(other, dev), "ws")
+    g.replay()
+    torch.cuda.synchronize()
+    compare(oracle_ref(inp2), ot.cpu().numpy(), on.cpu().numpy())
+
+
+def test_host_entry_point_is_refused_under_capture(dev):
+    """The host entry point synchronises: refused on a capturing stream, with
+    the capture left intact."""
+    import torch
+    inp = W.make_host(4, 2, 3000, "bf16", 2.0, 1.0, 1.0, seed=74)
+    staging = torch.empty(sv.sv_host_staging_size(4, 2, 3000, sv.SV_DTYPE_BF16), dtype=torch.uint8,
+                          device=dev)
+    ht = torch.from_numpy(inp["target"].view(np.int16)).view(torch.bfloat16)
+    hd = torch.from_numpy(inp["draft"].view(np.int16)).view(torch.bfloat16)
+    g = torch.cuda.CUDAGraph()
+    x = torch.zeros(4, device=dev)
+    with torch.cuda.graph(g):
+        x += 1
+        with pytest.raises(RuntimeError):
+            sv.spec_verify_host(ht, hd, torch.from_numpy(inp["tokens"]), torch.from_numpy(inp["uniforms"]),
+                                torch.from_numpy(inp["temperature"]), inp["K"], staging)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(x, torch.ones(4, device=dev))
