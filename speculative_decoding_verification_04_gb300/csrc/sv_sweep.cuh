@@ -12,9 +12,12 @@
 //
 // Schedule: a cluster walks one sequence's positions in order.  Row i+1 is
 // read only once x_i has been accepted (the method's own early exit: rows after
-// the first rejection are never read).  Fresh sequences come from one atomic
-// claim per sequence (longest K first), made a row ahead by rank 0 and handed
-// to the cluster with that row's exchange.
+// the first rejection are never read).  Cluster c starts with ticket c (its
+// sequence and K in the launch arguments); later sequences come from one
+// atomic claim each (longest K first), made by rank 0 a row ahead and handed
+// to the cluster with that row's exchange while two waves of tickets remain,
+// else when the current sequence ends (so the last go to the clusters free
+// first).
 //
 // Per row, each warp makes one pass over its slice, from shared memory
 // straight into registers:
