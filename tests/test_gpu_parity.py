@@ -75,6 +75,17 @@ def test_small_workloads_match_oracle(dev, case):
     _check(inp, dev)
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_largest_vocabulary(dev, dtype):
+    """The largest V the library accepts (a row of target and draft resident
+    in one cluster of 16 CTAs): greedy and sampling rows against the oracle."""
+    V = sv.sv_max_vocab(dtype_code(dtype))
+    B = 6
+    temps = np.array([1.0, 0.0, 0.7, 1.0, 0.0, 1.3], np.float32)
+    inp = W.make_host(B, [3, 2, 3, 1, 3, 2], V, dtype, 2.0, 1.0, temps, seed=V % 997)
+    _check(inp, dev)
+
+
 def test_high_acceptance_reaches_bonus_rows(dev):
     inp = W.make_host(24, 6, 9000, "bf16", 2.0, 0.02, 1.0, seed=5)
     ref, got_t, got_n, _ = _check(inp, dev)
