@@ -24,7 +24,7 @@
  *  [P3] issoh.co.jp "Speculative Decoding（投機的デコーディング）とは？仕組みと速くなる条件…",
  *       section 受理・棄却の規則と出力分布が変わらない理由, steps 1-5.
  *
- * Readings where the pages leave a step open (each restated in the design doc):
+ * Readings where the pages leave a step open:
  *  R1 probs(l, T) is softmax(l / T); the pages use it without printing it.
  *  R2 the test is strict, r < min(1, p/q), with r in [0, 1).  When q(x) = 0
  *     the ratio is undefined; the token is then kept iff p(x) > 0.
