@@ -47,6 +47,8 @@ def _load():
         lib.oracle_position_probs.restype = ctypes.c_int
         lib.oracle_final_distribution.argtypes = [P, P, ctypes.c_int, i32, ctypes.c_float, P]
         lib.oracle_final_distribution.restype = ctypes.c_int
+        lib.oracle_tree_verify.argtypes = [P, P, ctypes.c_int, P, P, P, P, i32, P, i32, i32, P, P, P, P]
+        lib.oracle_tree_verify.restype = ctypes.c_int
         lib.oracle_abi_version.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -134,6 +136,35 @@ def verify_inputs(inp: dict, seqs=None):
     seqs = np.asarray(seqs)
     return verify(inp["target"][seqs], inp["draft"][seqs], inp["dtype"], inp["tokens"][seqs],
                   inp["uniforms"][seqs], inp["temperature"][seqs], inp["K"][seqs])
+
+
+def tree_verify(target, draft, dtype, tokens, parent, uniforms, temperature, n_nodes):
+    """Token-tree verification (``oracle_tree_verify`` in oracle.c).
+
+    target / draft logits [B, Nmax, V] (row n: the distribution after node n),
+    tokens / parent / uniforms [B, Nmax] (uniforms[:, 0] is the final draw),
+    temperature [B], n_nodes [B].  Returns out_tokens, out_path [B, Nmax],
+    out_len [B] and tie [B] (bool).
+    """
+    lib = _load()
+    tgt = _logits(target, dtype)
+    drf = _logits(draft, dtype)
+    B, Nmax, V = (int(x) for x in tgt.shape)
+    tok = np.ascontiguousarray(tokens, dtype=np.int32)
+    par = np.ascontiguousarray(parent, dtype=np.int32)
+    uni = np.ascontiguousarray(uniforms, dtype=np.float32)
+    tmp = np.ascontiguousarray(temperature, dtype=np.float32)
+    nn = np.ascontiguousarray(n_nodes, dtype=np.int32)
+    out_tok = np.empty((B, Nmax), np.int32)
+    out_path = np.empty((B, Nmax), np.int32)
+    out_len = np.empty(B, np.int32)
+    tie = np.empty(B, np.uint8)
+    rc = lib.oracle_tree_verify(_ptr(tgt), _ptr(drf), DTYPES[dtype], _ptr(tok), _ptr(par), _ptr(uni),
+                                _ptr(tmp), B, _ptr(nn), Nmax, V, _ptr(out_tok), _ptr(out_path),
+                                _ptr(out_len), _ptr(tie))
+    if rc < 0:
+        raise ValueError("oracle_tree_verify rejected its arguments")
+    return dict(out_tokens=out_tok, out_path=out_path, out_len=out_len, tie=tie.astype(bool))
 
 
 def library_path() -> str:

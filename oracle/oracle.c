@@ -353,6 +353,153 @@ int oracle_final_distribution(const void* target_row, const void* draft_row, int
     return rc;
 }
 
+/*
+ * Token-tree verification: the pages' accept rule applied at every node of a
+ * tree of proposals.  A chain (one child per node) is exactly oracle_verify.
+ *
+ * Per sequence b, nodes 0 .. n_nodes[b] - 1, node 0 the root; parent[b][n] < n
+ * for n >= 1.  The candidates at node v are its children (the nodes whose
+ * parent is v) in increasing index.  Target row n: the target's logits after
+ * node n; draft row n: the draft's logits after node n, the distribution the
+ * children of n were drawn from.  uniforms[b][n] (n >= 1) is the test of node
+ * n; uniforms[b][0] is the final draw.  Layouts: logits [B][Nmax][V], tokens,
+ * parent, uniforms [B][Nmax].
+ *
+ * Walk from the root.  At node v, with P = softmax(target_v / T),
+ * Q = softmax(draft_v / T) and R = P, the children are tested in order: child
+ * c (token x) is kept iff u_c < min(1, R(x) / Q(x)) ([P1][P2][P3], with R in
+ * the place of p); a kept child becomes the node walked next.  After a
+ * rejection R becomes normalize(max(0, R - Q)), the distribution [P1] draws
+ * from after a rejection, against which the next child is tested (R is left
+ * unchanged if that has no mass, as R5 does for a chain).  With no child
+ * kept, the token is drawn from R by inverse CDF with uniforms[b][0]; at a
+ * leaf R = P, the bonus token.  At T = 0 the first child equal to
+ * argmax target_v is kept, and the token is argmax target_v.
+ *
+ * Outputs ([B][Nmax]): out_path[b][0 .. len-1] the kept nodes,
+ * out_tokens[b][0 .. len-1] their tokens and out_tokens[b][len] the drawn
+ * token, -1 after; out_len[b] = len.  Unusable input on the walk (bad tree,
+ * temperature, token, uniform or row) gives len -1 and -1 everywhere.  tie
+ * (nullable) flags a decision within ORC_TIE_BAND of its threshold.
+ * Returns 0, or -1 on a bad argument.
+ */
+int oracle_tree_verify(const void* target, const void* draft, int dtype, const int32_t* tokens,
+                       const int32_t* parent, const float* uniforms, const float* temperature,
+                       int32_t B, const int32_t* n_nodes, int32_t Nmax, int32_t V,
+                       int32_t* out_tokens, int32_t* out_path, int32_t* out_len, uint8_t* tie)
+{
+    if (B < 0 || V < 1 || Nmax < 1 || (dtype != ORC_F32 && dtype != ORC_BF16))
+        return -1;
+    if (B == 0)
+        return 0;
+    if (!target || !tokens || !parent || !uniforms || !temperature || !n_nodes || !out_tokens ||
+        !out_path || !out_len)
+        return -1;
+    double* p = (double*)malloc((size_t)V * sizeof(double));
+    double* q = (double*)malloc((size_t)V * sizeof(double));
+    double* r = (double*)malloc((size_t)V * sizeof(double));
+    int32_t* path = (int32_t*)malloc((size_t)Nmax * sizeof(int32_t));
+    if (!p || !q || !r || !path) {
+        free(p); free(q); free(r); free(path);
+        return -1;
+    }
+    for (int b = 0; b < B; ++b) {
+        const size_t row0 = (size_t)b * Nmax;
+        for (int j = 0; j < Nmax; ++j) {
+            out_tokens[row0 + j] = -1;
+            out_path[row0 + j] = -1;
+        }
+        out_len[b] = -1;
+        if (tie)
+            tie[b] = 0;
+        const int N = n_nodes[b];
+        const float T = temperature[b];
+        if (N < 1 || N > Nmax || !temperature_usable(T))
+            continue;
+        int ok = 1;
+        for (int n = 1; n < N; ++n)
+            if (parent[row0 + n] < 0 || parent[row0 + n] >= n)
+                ok = 0;
+        if (!ok)
+            continue;
+        const int greedy = (T == 0.0f);
+        int v = 0, len = 0, t = 0, token = -1;
+        for (;;) {
+            const size_t off = (row0 + v) * (size_t)V;
+            int moved = 0;
+            if (greedy) {
+                int g = -1;
+                if (!argmax_row(target, dtype, off, V, &g)) { ok = 0; break; }
+                for (int c = v + 1; c < N && ok && !moved; ++c) {
+                    if (parent[row0 + c] != v)
+                        continue;
+                    const int x = tokens[row0 + c];
+                    if (x < 0 || x >= V) { ok = 0; break; }
+                    if (x == g) {
+                        path[len++] = c;
+                        v = c;
+                        moved = 1;
+                    }
+                }
+                if (!ok)
+                    break;
+                if (moved)
+                    continue;
+                token = g;
+                break;
+            }
+            if (!probs(target, dtype, off, V, (double)T, p)) { ok = 0; break; }
+            memcpy(r, p, (size_t)V * sizeof *r);
+            int have_q = 0;
+            for (int c = v + 1; c < N && ok && !moved; ++c) {
+                if (parent[row0 + c] != v)
+                    continue;
+                const int x = tokens[row0 + c];
+                const float u = uniforms[row0 + c];
+                if (x < 0 || x >= V || !uniform_usable(u)) { ok = 0; break; }
+                if (!have_q) {
+                    if (!draft || !probs(draft, dtype, off, V, (double)T, q)) { ok = 0; break; }
+                    have_q = 1;
+                }
+                if (q[x] > 0.0 && fabs((double)u - r[x] / q[x]) < ORC_TIE_BAND)
+                    t = 1;
+                if (keep((double)u, r[x], q[x])) {
+                    path[len++] = c;
+                    v = c;
+                    moved = 1;
+                    break;
+                }
+                double S = 0.0;   // the next residual: normalize(max(0, r - q))
+                for (int j = 0; j < V; ++j)
+                    S += fmax(r[j] - q[j], 0.0);
+                if (S > 0.0)
+                    for (int j = 0; j < V; ++j)
+                        r[j] = fmax(r[j] - q[j], 0.0) / S;
+            }
+            if (!ok)
+                break;
+            if (moved)
+                continue;
+            const float u0 = uniforms[row0];
+            if (!uniform_usable(u0)) { ok = 0; break; }
+            token = draw(r, V, (double)u0, &t);
+            break;
+        }
+        if (!ok)
+            continue;
+        for (int j = 0; j < len; ++j) {
+            out_path[row0 + j] = path[j];
+            out_tokens[row0 + j] = tokens[row0 + path[j]];
+        }
+        out_tokens[row0 + len] = token;
+        out_len[b] = len;
+        if (tie)
+            tie[b] = (uint8_t)t;
+    }
+    free(p); free(q); free(r); free(path);
+    return 0;
+}
+
 int oracle_abi_version(void)
 {
     return 1;

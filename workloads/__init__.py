@@ -5,3 +5,4 @@ from .configs import (SPECS, TOY_P, TOY_Q, as_f32, bf16_bits_to_f32,  # noqa: F4
                       bytes_all_rows, bytes_needed, categorical_draws,
                       f32_to_bf16_bits, make_device, make_geometric, make_host,
                       make_pair_batch, make_spec_host, make_toy)
+from .trees import full_tree, make_tree_host, make_tree_pair  # noqa: F401,E402
