@@ -330,6 +330,47 @@ sv_status spec_verify_host(const void* h_target_logits, const void* h_draft_logi
                            int32_t* h_out_num_accepted, void* device_staging,
                            size_t staging_bytes, cudaStream_t stream);
 
+/*
+ * spec_verify_tree -- token-tree verification: the accept rule of
+ * spec_verify applied at every node of a tree of proposals (a tree of one
+ * child per node is spec_verify).  Pages: tech-tldr.com "投機的デコーディング
+ * とドラフトモデル", section 受理判定の数理 (the accept rule and the
+ * distribution drawn from after a rejection); issoh.co.jp, section 受理・棄却
+ * の規則と出力分布が変わらない理由 (losslessness).
+ *
+ * Per sequence b: nodes 0 .. n_nodes[b] - 1 (1 <= n_nodes[b] <= Nmax <= 32),
+ * node 0 the root; parent[b][n] < n for n >= 1.  The candidates at node v are
+ * its children (the nodes whose parent is v) in increasing index.  Row n of
+ * the target / draft logits ([B][Nmax][V], device, dtype) is the target's /
+ * draft's distribution after node n (the draft row is the one n's children
+ * were drawn from; it is read only at sampling nodes with children, and
+ * draft_logits may be NULL if every sequence is greedy).  tokens[b][n] is
+ * node n's token; uniforms[b][n] (n >= 1) tests node n and uniforms[b][0] is
+ * the final draw; temperature[b] as in spec_verify; all device, [B][Nmax] /
+ * [B]; n_nodes is device memory too.
+ *
+ * Walk from the root: at node v, with R = p = softmax(target_v / T), child c
+ * (token x) is kept iff u_c < min(1, R(x) / q(x)), q = softmax(draft_v / T);
+ * a kept child is the next node; after a rejection R becomes
+ * normalize(max(0, R - q)) (unchanged if that has no mass) and the next
+ * child is tested.  With no child kept the token is drawn from R by inverse
+ * CDF with uniforms[b][0] (at a leaf R = p, the bonus token).  At T = 0 the
+ * child equal to the target argmax is kept, else the token is the argmax.
+ *
+ * Outputs (device, [B][Nmax]): out_path[b][0 .. len-1] the kept nodes,
+ * out_tokens[b][0 .. len-1] their tokens and out_tokens[b][len] the drawn
+ * token, -1 after; out_len[b] = len, or -1 (and -1 everywhere) when the
+ * walk meets unusable input (a malformed tree, temperature, token, uniform
+ * or row).  workspace: >= sv_tree_workspace_size() bytes, 256-byte aligned,
+ * holds the error word (sv_workspace_errors).  Asynchronous on `stream`.
+ */
+size_t sv_tree_workspace_size(void);
+sv_status spec_verify_tree(const void* target_logits, const void* draft_logits, sv_dtype dtype,
+                           const int32_t* tokens, const int32_t* parent, const float* uniforms,
+                           const float* temperature, int32_t B, int32_t Nmax, const int32_t* n_nodes,
+                           int32_t V, int32_t* out_tokens, int32_t* out_path, int32_t* out_len,
+                           void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

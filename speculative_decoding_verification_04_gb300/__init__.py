@@ -76,6 +76,10 @@ def _load():
     lib.spec_verify_host.argtypes = common + [P, sz, P]
     lib.spec_sample.argtypes = [P, ctypes.c_int, P, P, i32, i32, P, P, sz, P]
     lib.spec_sample.restype = ctypes.c_int
+    lib.spec_verify_tree.argtypes = [P, P, ctypes.c_int, P, P, P, P, i32, i32, P, i32, P, P, P, P, sz, P]
+    lib.spec_verify_tree.restype = ctypes.c_int
+    lib.sv_tree_workspace_size.argtypes = []
+    lib.sv_tree_workspace_size.restype = sz
     lib.sv_sample_workspace_size.argtypes = [i32, i32, ctypes.c_int]
     lib.sv_sample_workspace_size.restype = sz
     for f in (lib.spec_verify, lib.spec_verify_ws, lib.spec_verify_ex, lib.spec_verify_host):
@@ -363,6 +367,44 @@ def spec_sample(logits, uniforms, temperature, workspace=None, out_tokens=None, 
                              workspace.numel(), sp)
     _check(st, "spec_sample")
     return out_tokens
+
+
+def spec_verify_tree(target, draft, tokens, parent, uniforms, temperature, n_nodes, workspace=None,
+                     out_tokens=None, out_path=None, out_len=None, stream=None):
+    """spec_verify_tree on torch CUDA tensors: target / draft logits [B, Nmax, V]
+    (row n: the distribution after node n), tokens / parent (int32) and
+    uniforms (float32) [B, Nmax], temperature [B], n_nodes (int32) [B].
+    Returns (out_tokens, out_path, out_len).  ``workspace``: a uint8 CUDA
+    tensor of at least sv_tree_workspace_size() bytes (allocated when omitted)."""
+    import torch
+    if target.dim() != 3:
+        raise ValueError("target logits must be [B, Nmax, V]")
+    B, Nmax, V = (int(x) for x in target.shape)
+    _require(target, "target_logits")
+    if draft is not None:
+        _require(draft, "draft_logits", target.dtype)
+    _require(tokens, "tokens", torch.int32)
+    _require(parent, "parent", torch.int32)
+    _require(uniforms, "uniforms", torch.float32)
+    _require(temperature, "temperature", torch.float32)
+    _require(n_nodes, "n_nodes", torch.int32)
+    dev = target.device
+    if out_tokens is None:
+        out_tokens = torch.empty((B, Nmax), dtype=torch.int32, device=dev)
+    if out_path is None:
+        out_path = torch.empty((B, Nmax), dtype=torch.int32, device=dev)
+    if out_len is None:
+        out_len = torch.empty((B,), dtype=torch.int32, device=dev)
+    if workspace is None:
+        workspace = torch.empty(int(_load().sv_tree_workspace_size()), dtype=torch.uint8, device=dev)
+    sp, _ = _stream(stream)
+    st = _load().spec_verify_tree(_dptr(target), _dptr(draft) if draft is not None else None,
+                                  _dtype_code(target), _dptr(tokens), _dptr(parent), _dptr(uniforms),
+                                  _dptr(temperature), B, Nmax, _dptr(n_nodes), V, _dptr(out_tokens),
+                                  _dptr(out_path), _dptr(out_len), ctypes.c_void_p(workspace.data_ptr()),
+                                  workspace.numel(), sp)
+    _check(st, "spec_verify_tree")
+    return out_tokens, out_path, out_len
 
 
 def spec_verify_host(target, draft, draft_tokens, uniforms, temperature, K, staging,

@@ -27,6 +27,7 @@
 
 #include "../../include/specverify.h"
 #include "sv_sweep.cuh"
+#include "sv_tree.cuh"
 
 namespace sv {
 
@@ -115,7 +116,7 @@ static DeviceInfo g_dev[64];
 // cudaOccupancyMaxActiveClusters per (device, kernel, cluster size, warps, smem)
 static std::map<std::tuple<int, int, int, int, size_t>, int> g_fit;
 // chosen geometry per (device, V, dtype, B, Kmax, tuning overrides)
-static std::map<std::tuple<int, int, int, int, int, int, int, int>, Geom> g_pick;
+static std::map<std::tuple<int, int, int, int, int, int, int, int, int>, Geom> g_pick;
 
 template <typename T, int NV, bool WIDE, bool HOST>
 static cudaError_t prepare_kernels(int dev)
@@ -242,9 +243,9 @@ static sv_status capacity_of(const Geom& g, sv_dtype dt, bool host, int dev, int
 // per row (shorter passes), then larger clusters.  Tuning overrides: chunks
 // per CTA (sets C), chunks per warp (sets the warps per CTA).
 static sv_status pick_geometry(int V, sv_dtype dt, int B, int Kmax, int override_ncpc,
-                               int want_cpw, int dev, bool host, Geom* g)
+                               int want_cpw, int dev, bool host, Geom* g, int max_parts = kMaxParts)
 {
-    const auto key = std::make_tuple(dev, V, (int)dt, B, Kmax, override_ncpc, want_cpw, host ? 1 : 0);
+    const auto key = std::make_tuple(dev, V, (int)dt, B, Kmax, override_ncpc, want_cpw, host ? 1 : 0, max_parts);
     {
         std::lock_guard<std::mutex> lk(g_mu);
         auto it = g_pick.find(key);
@@ -260,7 +261,7 @@ static sv_status pick_geometry(int V, sv_dtype dt, int B, int Kmax, int override
     for (int C = 1; C <= kMaxCluster; ++C) {
         if (override_ncpc > 0 && C != (nch + override_ncpc - 1) / override_ncpc)
             continue;
-        for (int nw = 1; nw <= kMaxWarps && C * nw <= kMaxParts; ++nw) {
+        for (int nw = 1; nw <= kMaxWarps && C * nw <= max_parts; ++nw) {
             if (want_cpw > 0) {
                 const int ncpc = (nch + C - 1) / C;
                 if (nw != std::min({(ncpc + want_cpw - 1) / want_cpw, kMaxParts / C, kMaxWarps}))
@@ -725,6 +726,55 @@ static sv_status geometry_of(int B, int Kmax, int V, sv_dtype dt, int ncpc, int 
     return SV_OK;
 }
 
+// ---------------------------------------------------------------------------
+// token trees: one cluster per sequence (sv_tree_kernel)
+// ---------------------------------------------------------------------------
+template <typename T, int NV>
+static cudaError_t launch_tree(const TreeArgs& ta, const Geom& g, size_t smem, cudaStream_t st)
+{
+    auto kern = sv_tree_kernel<T, NV>;
+    static bool attrs_done[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return cudaErrorInvalidDevice;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (!attrs_done[dev]) {
+            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 kSmemPerCtaMax);
+            if (e != cudaSuccess)
+                return e;
+            e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+            if (e != cudaSuccess)
+                return e;
+            attrs_done[dev] = true;
+        }
+    }
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.gridDim = dim3((unsigned)(ta.B * g.C), 1, 1);
+    cfg.blockDim = dim3((unsigned)(32 * g.nw), 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)g.C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, ta);
+}
+
+template <typename T>
+static cudaError_t launch_tree_nv(const TreeArgs& ta, const Geom& g, size_t smem, cudaStream_t st)
+{
+    switch (g.nv) {
+    case 1: return launch_tree<T, 1>(ta, g, smem, st);
+    case 2: return launch_tree<T, 2>(ta, g, smem, st);
+    default: return launch_tree<T, 4>(ta, g, smem, st);
+    }
+}
+
 }  // namespace sv
 
 // ---------------------------------------------------------------------------
@@ -986,6 +1036,67 @@ sv_status spec_verify_host(const void* h_target_logits, const void* h_draft_logi
         cudaStreamSynchronize(stream) != cudaSuccess)
         return SV_ERR_CUDA;
     return SV_OK;
+}
+
+size_t sv_tree_workspace_size(void) { return 256; }
+
+sv_status spec_verify_tree(const void* target_logits, const void* draft_logits, sv_dtype dtype,
+                           const int32_t* tokens, const int32_t* parent, const float* uniforms,
+                           const float* temperature, int32_t B, int32_t Nmax, const int32_t* n_nodes,
+                           int32_t V, int32_t* out_tokens, int32_t* out_path, int32_t* out_len,
+                           void* workspace, size_t workspace_bytes, cudaStream_t stream)
+{
+    if (B < 0 || V < 1 || Nmax < 1 || Nmax > sv::kTreeMaxNodes ||
+        (dtype != SV_DTYPE_F32 && dtype != SV_DTYPE_BF16))
+        return SV_ERR_INVALID_ARG;
+    if (B == 0)
+        return SV_OK;
+    if (!target_logits || !tokens || !parent || !uniforms || !temperature || !n_nodes || !out_tokens ||
+        !out_path || !out_len)
+        return SV_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < sv_tree_workspace_size() || ((uintptr_t)workspace & 255))
+        return SV_ERR_NO_MEMORY;
+    if (V > sv_max_vocab(dtype) || (long long)B * Nmax > (1LL << 30) || (long long)B * 16 > 0x7fffffffLL)
+        return SV_ERR_UNSUPPORTED;
+    int dev = 0, nsm = 0;
+    sv_status st = sv::device_sms(&dev, &nsm);
+    if (st != SV_OK)
+        return st;
+    sv::Geom g;
+    // at most 32 warp ranges a row: one partial per lane in the combines
+    st = sv::pick_geometry(V, dtype, 1 << 20, 0, 0, 0, dev, false, &g, 32);
+    if (st != SV_OK)
+        return st;
+    const sv::SweepLayout L = sv::sweep_layout(g.nw, g.kc, g.kw, g.ch * g.s, g.C * g.nw);
+    const size_t smem = sv::tree_smem_bytes(L, g.nw);
+    if (smem > (size_t)sv::kSmemPerCtaMax)
+        return SV_ERR_UNSUPPORTED;
+    if (cudaMemsetAsync(workspace, 0, 16, stream) != cudaSuccess)
+        return SV_ERR_CUDA;
+    sv::TreeArgs ta;
+    ta.tgt = target_logits;
+    ta.drf = draft_logits;
+    ta.tok = tokens;
+    ta.parent = parent;
+    ta.uni = uniforms;
+    ta.temp = temperature;
+    ta.n_nodes = n_nodes;
+    ta.out_tok = out_tokens;
+    ta.out_path = out_path;
+    ta.out_len = out_len;
+    ta.err = static_cast<uint32_t*>(workspace);
+    ta.B = B;
+    ta.Nmax = Nmax;
+    ta.V = V;
+    ta.nchunks = g.nchunks;
+    ta.C = g.C;
+    ta.kw = g.kw;
+    const uintptr_t al = (uintptr_t)target_logits | (draft_logits ? (uintptr_t)draft_logits : 0);
+    ta.aligned = ((al & 15) == 0) && (((size_t)V * g.s) % 16 == 0);
+    ta.has_draft = draft_logits != nullptr ? 1 : 0;
+    const cudaError_t e = dtype == SV_DTYPE_BF16 ? sv::launch_tree_nv<__nv_bfloat16>(ta, g, smem, stream)
+                                                 : sv::launch_tree_nv<float>(ta, g, smem, stream);
+    return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
 }  // extern "C"

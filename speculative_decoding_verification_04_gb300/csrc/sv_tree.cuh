@@ -1,0 +1,574 @@
+// sv_tree.cuh -- token-tree verification: the pages' accept rule applied at
+// every node of a tree of proposals (a chain of one child per node is the
+// ordinary verification).
+//
+// One cluster per sequence walks its tree from the root.  At node v the
+// cluster holds the target and draft rows after v resident in shared memory
+// (the same warp ranges and bulk copies as the sweep) and tests v's children
+// in index order: child c (token x) is kept iff u_c q(x) < R(x), with R = p
+// at first; after a rejection R becomes normalize(max(0, R - q)) (left as it
+// was if that has no mass) and the next child is tested.  A kept child is
+// the next node; with none kept the token is drawn from R by inverse CDF (at
+// a leaf R = p, the bonus token).  At T = 0 the child equal to the target
+// argmax is kept, else the token is the argmax.
+//
+// Residual levels are recomputed from the resident slice: level L's term at
+// element j is A_L(j) = max(0, R_{L-1}(j) - q(j)) with R_0 = p and
+// R_l = A_l / S_l (S_l = sum_j A_l(j); a level with S_l = 0 leaves R as it
+// was), so a pass at level L costs two exponentials and L - 1 nested steps per
+// element.  Each pass keeps per-strip partial sums of its terms for the draw,
+// as the sweep's residual pass does.
+#pragma once
+
+#include "sv_sweep.cuh"
+
+namespace sv {
+
+constexpr int kTreeMaxNodes = 32;   // one lane per node
+
+struct TreeArgs {
+    const void* tgt;         // [B][Nmax][V]: row n, the target's logits after node n
+    const void* drf;         // [B][Nmax][V]: row n, the draft's logits after node n
+    const int32_t* tok;      // [B][Nmax]: node n's token (n >= 1)
+    const int32_t* parent;   // [B][Nmax]: parent[n] < n, parent[0] = -1
+    const float* uni;        // [B][Nmax]: uni[n] tests node n; uni[0] is the final draw
+    const float* temp;       // [B]
+    const int32_t* n_nodes;  // [B]
+    int32_t* out_tok;        // [B][Nmax]
+    int32_t* out_path;       // [B][Nmax]
+    int32_t* out_len;        // [B]
+    uint32_t* err;
+    int B, Nmax, V;
+    int nchunks, C, kw;
+    int aligned, has_draft;
+};
+
+// The sweep's shared-memory layout, then [nw][32] floats of per-level
+// inverse sums (each warp keeps its own copy).
+__host__ __device__ inline size_t tree_lvl_offset(const SweepLayout& L) { return (L.total + 15) & ~(size_t)15; }
+
+__host__ __device__ inline size_t tree_smem_bytes(const SweepLayout& L, int nw)
+{
+    return tree_lvl_offset(L) + (size_t)nw * 32 * 4;
+}
+
+// The term of one element at level L: L = 0, p = w_t * ist; L >= 1,
+// A_L = max(0, R_{L-1} - q) with q = w_d * isd and R_0 = p, R_l =
+// A_l * inv[l - 1] (inv[l - 1] = 1 / S_l; 0 marks a level without mass, which
+// leaves R as it was).  The weights are the sweep's: exp2(fma(l, c, -r)).
+__device__ __forceinline__ float level_term(float lt, float ld, float c, float rt, float rd, float ist,
+                                            float isd, int L, const float* inv)
+{
+    const float p = __fmul_rn(ex2_approx(__fmaf_rn(lt, c, -rt)), ist);
+    if (L == 0)
+        return p;
+    const float q = __fmul_rn(ex2_approx(__fmaf_rn(ld, c, -rd)), isd);
+    float r = p;
+    for (int l = 0; l < L - 1; ++l) {
+        const float s = inv[l];
+        if (s > 0.0f)
+            r = __fmul_rn(fmaxf(__fsub_rn(r, q), 0.0f), s);
+    }
+    return fmaxf(__fsub_rn(r, q), 0.0f);
+}
+
+// R_k(x) for the proposal's p(x), q(x) after k rejections (the same nested
+// steps as level_term).
+__device__ __forceinline__ float level_value(float px, float qx, int k, const float* inv)
+{
+    float r = px;
+    for (int l = 0; l < k; ++l) {
+        const float s = inv[l];
+        if (s > 0.0f)
+            r = __fmul_rn(fmaxf(__fsub_rn(r, qx), 0.0f), s);
+    }
+    return r;
+}
+
+// One pass over this warp's slice at level L (whole warp): per-strip partial
+// sums of the level's terms into `stats` ([kw][NV][4], as the sweep's
+// residual pass), and the warp's total (compensated).
+template <typename T, int NV>
+__device__ float level_pass(const T* slot_t, const T* slot_d, int kwm, int lane, float c, float rt, float rd,
+                            float ist, float isd, int L, const float* inv, float* stats)
+{
+    using LN = Lane<T, NV>;
+    constexpr int E = Elem<T>::E;
+    constexpr int CH = 32 * NV * E;
+    float acc = 0.0f, cmp = 0.0f;
+    for (int j = 0; j < kwm; ++j) {
+        uint4 tv[NV], dv[NV];
+        load_chunk<T, NV>(slot_t + (size_t)j * CH, lane, tv);
+        load_chunk<T, NV>(slot_d + (size_t)j * CH, lane, dv);
+        float sv[NV];
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            float sk = 0.0f;
+#pragma unroll
+            for (int e = 0; e < E; ++e)
+                sk += level_term(LN::vec_elem(tv[k], e), LN::vec_elem(dv[k], e), c, rt, rd, ist, isd, L, inv);
+            sv[k] = sk;
+        }
+        strip_partials<NV>(sv, lane, stats + (size_t)j * NV * 4);
+        float v = 0.0f;
+#pragma unroll
+        for (int k = 0; k < NV; ++k)
+            v += sv[k];
+        float t, e;
+        two_sum(acc, v, t, e);
+        acc = t;
+        cmp += e;
+    }
+    __syncwarp();
+    return sum_or_special(acc + cmp);
+}
+
+// The element of one strip that holds the point tc of the level-L
+// distribution (one warp; tv / dv: each lane's vector of the strip): lane
+// sums, a compensated scan, the lane, then the element, the terms computed
+// exactly as in level_pass.  Returns lane * E + e, or -1 if the strip has no
+// mass; beyond the strip's mass (rounding) the last element with mass.
+template <typename T, int NV>
+__device__ int pick_level(const uint4& tv, const uint4& dv, float c, float rt, float rd, float ist, float isd,
+                          int L, const float* inv, float tc, bool beyond, int lane)
+{
+    using LN = Lane<T, NV>;
+    constexpr int E = Elem<T>::E;
+    float tm[E];
+    float ls = 0.0f;
+    int lastpos = -1;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+        tm[e] = level_term(LN::vec_elem(tv, e), LN::vec_elem(dv, e), c, rt, rd, ist, isd, L, inv);
+        ls += tm[e];
+        if (tm[e] > 0.0f)
+            lastpos = lane * E + e;
+    }
+    int cand = -1;
+    if (!beyond) {
+        float ss, sc;
+        warp_incl_scan_comp(ls, lane, ss, sc);
+        const unsigned hit = __ballot_sync(kFull, ls > 0.0f && tc < ss + sc);
+        if (hit) {
+            const int src = __ffs(hit) - 1;
+            const float tl = tc - ((ss - ls) + sc);
+            int ce = -1, lp = -1;
+            float cum = 0.0f;
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+                cum += tm[e];
+                if (tm[e] > 0.0f) {
+                    lp = e;
+                    if (ce < 0 && tl < cum)
+                        ce = e;
+                }
+            }
+            ce = ce >= 0 ? ce : lp;
+            cand = __shfl_sync(kFull, lane * E + ce, src);
+        }
+    }
+    if (cand < 0)
+        cand = __reduce_max_sync(kFull, lastpos);
+    return cand;
+}
+
+template <typename T, int NV>
+__global__ void __maxnreg__(kMaxRegs) sv_tree_kernel(const TreeArgs a)
+{
+    using EL = Elem<T>;
+    using LN = Lane<T, NV>;
+    constexpr int E = EL::E;
+    constexpr int CH = 32 * NV * E;
+    extern __shared__ __align__(128) unsigned char dsm[];
+
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int nw = (int)(blockDim.x >> 5);
+    const int C = a.C, V = a.V, Nmax = a.Nmax, KW = a.kw;
+    const int P = C * nw;
+    const uint32_t rank = cluster_ctarank();
+    const int g = (int)rank * nw + w;
+    const int c_lo = range_lo(g, a.nchunks, P);
+    const int kwm = range_lo(g + 1, a.nchunks, P) - c_lo;
+    const int e0 = c_lo * CH;
+    const int n_el = max(0, min(e0 + kwm * CH, V) - e0);
+    const SweepLayout L = sweep_layout(nw, cta_chunks(a.nchunks, C), KW, CH * (int)sizeof(T), P);
+    const size_t off = (size_t)(c_lo - range_lo((int)rank * nw, a.nchunks, P)) * CH;
+    T* slot_t = reinterpret_cast<T*>(dsm) + off;
+    T* slot_d = reinterpret_cast<T*>(dsm + L.region_bytes) + off;
+    const uint32_t bar = smem_addr(dsm + L.bars + 8 * (size_t)w);
+    uint64_t* xbar = reinterpret_cast<uint64_t*>(dsm + L.xbar);
+    uint64_t* xbar2 = reinterpret_cast<uint64_t*>(dsm + L.xbar2);
+    float4* xbuf = reinterpret_cast<float4*>(dsm + L.xbuf);
+    float2* xbuf2 = reinterpret_cast<float2*>(dsm + L.xbuf2);
+    float* stats = reinterpret_cast<float*>(dsm + L.stats) + (size_t)w * KW * 16;
+    float* inv = reinterpret_cast<float*>(dsm + tree_lvl_offset(L)) + (size_t)w * 32;
+
+    if (lane == 0) {
+        mbar_init(bar, 1);
+        if (w == 0) {
+            mbar_init(smem_addr(&xbar[0]), 1);
+            mbar_init(smem_addr(&xbar[1]), 1);
+            mbar_init(smem_addr(&xbar2[0]), 1);
+            mbar_init(smem_addr(&xbar2[1]), 1);
+        }
+        fence_mbar_init();
+    }
+    for (int j = n_el + lane; j < kwm * CH; j += 32) {
+        EL::set_neg_inf(slot_t + j);
+        EL::set_neg_inf(slot_d + j);
+    }
+    __syncthreads();
+    cluster_arrive();
+    cluster_wait();
+
+    // ---- the sequence (lane n: node n) ----
+    const int b = (int)(blockIdx.x / (unsigned)C);
+    const int N = __ldg(a.n_nodes + b);
+    const float Tb = __ldg(a.temp + b);
+    int par = -2, tokn = 0;
+    float un = 0.0f;
+    if (lane < Nmax) {
+        par = __ldg(a.parent + (size_t)b * Nmax + lane);
+        tokn = __ldg(a.tok + (size_t)b * Nmax + lane);
+        un = __ldg(a.uni + (size_t)b * Nmax + lane);
+    }
+    const bool tree_ok = N >= 1 && N <= Nmax &&
+                         !__any_sync(kFull, lane >= 1 && lane < N && (par < 0 || par >= lane));
+    bool bad = !tree_ok || !temperature_usable(Tb);
+    const bool greedy = Tb == 0.0f;
+    const float c = (!bad && !greedy) ? log2e_over(Tb) : 0.0f;
+    const T* tgt = static_cast<const T*>(a.tgt);
+    const T* drf = static_cast<const T*>(a.drf);
+    const bool writer = rank == 0 && w == 0;
+
+    uint32_t uses = 0, kx = 0, k2 = 0;
+    bool pending = false, xbroken = false, done = false;
+    int path_l = -1;   // lane j: the j-th kept node
+
+    // outputs of the sequence (whole warp; one warp calls it): the kept
+    // nodes and their tokens, then `token`; token < 0 marks unusable input
+    auto write_out = [&](int len, int token) {
+        const bool ok = token >= 0;
+        const int ptok = __shfl_sync(kFull, tokn, path_l & 31);
+        if (lane < Nmax) {
+            a.out_path[(size_t)b * Nmax + lane] = (ok && lane < len) ? path_l : -1;
+            a.out_tok[(size_t)b * Nmax + lane] = !ok ? -1 : (lane < len ? ptok : (lane == len ? token : -1));
+        }
+        if (lane == 0)
+            a.out_len[b] = ok ? len : -1;
+    };
+    // the copies of this warp's range of row `row` (and of the draft row)
+    auto issue = [&](size_t row, bool with_d) {
+        if (n_el <= 0)
+            return;
+        const T* tr = tgt + row * (size_t)V + e0;
+        const T* dr = with_d ? drf + row * (size_t)V + e0 : nullptr;
+        const int nb = a.aligned ? ((n_el * (int)sizeof(T)) & ~15) / (int)sizeof(T) : 0;
+        if (lane == 0) {
+            const uint32_t bytes = (uint32_t)nb * (uint32_t)sizeof(T);
+            const uint32_t tx = bytes * (with_d ? 2u : 1u);
+            if (tx) {
+                fence_proxy_async();
+                mbar_arrive_expect_tx(bar, tx);
+                bulk_copy_g2s(smem_addr(slot_t), tr, bytes, bar);
+                if (with_d)
+                    bulk_copy_g2s(smem_addr(slot_d), dr, bytes, bar);
+            } else {
+                mbar_arrive(bar);
+            }
+        }
+        for (int j = nb + lane; j < n_el; j += 32) {
+            EL::copy(slot_t + j, tr + j);
+            if (with_d)
+                EL::copy(slot_d + j, dr + j);
+        }
+        pending = true;
+    };
+    // a float4 per warp to every CTA; every warp returns the P partials
+    // (lane j: warp j's)
+    auto exchange4 = [&](float4 part) -> float4 {
+        const int p = (int)(kx & 1);
+        const uint32_t par4 = (kx >> 1) & 1u;
+        ++kx;
+        if (w == 0 && lane == 0)
+            mbar_arrive_expect_tx(smem_addr(&xbar[p]), (uint32_t)P * 16u);
+        if (lane < C)
+            st_async_v4(map_to_rank(smem_addr(&xbuf[p * P + g]), (uint32_t)lane), part,
+                        map_to_rank(smem_addr(&xbar[p]), (uint32_t)lane));
+        if (!mbar_wait_bounded(smem_addr(&xbar[p]), par4, kWaitSpins))
+            xbroken = true;
+        return lane < P ? xbuf[p * P + lane] : make_float4(-INFINITY, __int_as_float(INT_MAX), -INFINITY, 0.0f);
+    };
+    auto exchange2 = [&](float v) -> float {
+        const int p = (int)(k2 & 1);
+        const uint32_t par2 = (k2 >> 1) & 1u;
+        ++k2;
+        if (w == 0 && lane == 0)
+            mbar_arrive_expect_tx(smem_addr(&xbar2[p]), (uint32_t)P * 8u);
+        if (lane < C)
+            st_async_v2(map_to_rank(smem_addr(&xbuf2[p * P + g]), (uint32_t)lane), make_float2(v, 0.0f),
+                        map_to_rank(smem_addr(&xbar2[p]), (uint32_t)lane));
+        if (!mbar_wait_bounded(smem_addr(&xbar2[p]), par2, kWaitSpins))
+            xbroken = true;
+        return lane < P ? xbuf2[p * P + lane].x : 0.0f;
+    };
+
+    // ---- the walk: one node per step ----
+    int v = 0, len = 0;
+    for (int step = 0; !bad && step < N; ++step) {
+        const unsigned kids = __ballot_sync(kFull, lane > v && lane < N && par == v);
+        const bool with_d = !greedy && kids != 0;
+        if (with_d && !a.has_draft) {
+            bad = true;
+            break;
+        }
+        const size_t row = (size_t)b * Nmax + v;
+        issue(row, with_d);
+        bool have = false;
+        if (pending) {
+            const bool okw = mbar_wait_bounded(bar, uses & 1u, kWaitSpins);
+            have = !__any_sync(kFull, !okw);
+            if (have) {
+                pending = false;
+                ++uses;
+            } else {
+                xbroken = true;
+            }
+            __syncwarp();
+        }
+        if (__any_sync(kFull, xbroken))
+            break;
+
+        // ---- pass: the argmax, or the (max, sum) of the target and draft rows ----
+        float4 part = make_float4(-INFINITY, __int_as_float(INT_MAX), -INFINITY, 0.0f);
+        if (greedy) {
+            float gm = -INFINITY;
+            int gi = INT_MAX;
+            for (int j = 0; have && j < kwm; ++j) {
+                uint4 tv[NV];
+                load_chunk<T, NV>(slot_t + (size_t)j * CH, lane, tv);
+                const float cm = LN::max(tv);
+                if (cm > gm) {
+                    const int gbase = e0 + j * CH;
+                    int found = INT_MAX;
+#pragma unroll
+                    for (int e = NV * E - 1; e >= 0; --e)
+                        if (LN::elem(tv, e) == cm)
+                            found = gbase + ((e / E) * 32 + lane) * E + (e % E);
+                    gm = cm;
+                    gi = found;
+                } else if (cm != cm) {
+                    gm = cm;
+                }
+            }
+            const float m = warp_max_nan(gm);
+            part = make_float4(m, __int_as_float(__reduce_min_sync(kFull, gm == m ? gi : INT_MAX)), -INFINITY,
+                               0.0f);
+        } else {
+            float mt = -INFINITY, st = 0.0f, md = -INFINITY, sd = 0.0f;
+            for (int j = 0; have && j < kwm; ++j) {
+                uint4 tv[NV];
+                load_chunk<T, NV>(slot_t + (size_t)j * CH, lane, tv);
+                const float nt = max_nan(mt, LN::max(tv));
+                if (nt != mt) {
+                    st = mt == -INFINITY ? 0.0f : st * weight(mt, nt, c);
+                    mt = nt;
+                }
+                st += LN::exp_sum(tv, mt == -INFINITY ? 0.0f : mt, c);
+                if (with_d) {
+                    uint4 dv[NV];
+                    load_chunk<T, NV>(slot_d + (size_t)j * CH, lane, dv);
+                    const float nd = max_nan(md, LN::max(dv));
+                    if (nd != md) {
+                        sd = md == -INFINITY ? 0.0f : sd * weight(md, nd, c);
+                        md = nd;
+                    }
+                    sd += LN::exp_sum(dv, md == -INFINITY ? 0.0f : md, c);
+                }
+            }
+            float m1, S1, m2, S2;
+            combine_ms2(mt, st, md, sd, c, m1, S1, m2, S2);
+            part = make_float4(m1, S1, m2, S2);
+        }
+        const float4 xv = exchange4(part);
+        if (__any_sync(kFull, xbroken))
+            break;
+
+        if (greedy) {
+            const float m_t = warp_max_nan(xv.x);
+            const int gtok = __reduce_min_sync(kFull, (lane < P && xv.x == m_t) ? __float_as_int(xv.y) : INT_MAX);
+            if (!isfinite(m_t) || gtok < 0 || gtok >= V) {
+                bad = true;
+                break;
+            }
+            // children are tested in order up to the first that holds the argmax
+            const unsigned hit = __ballot_sync(kFull, ((kids >> lane) & 1u) && tokn == gtok);
+            const int first = hit ? __ffs(hit) - 1 : 32;
+            if (__any_sync(kFull, ((kids >> lane) & 1u) && lane < first && (tokn < 0 || tokn >= V))) {
+                bad = true;
+                break;
+            }
+            if (hit) {
+                const int cn = __ffs(hit) - 1;
+                if (lane == len)
+                    path_l = cn;
+                ++len;
+                v = cn;
+                continue;
+            }
+            if (writer)
+                write_out(len, gtok);
+            done = true;
+            break;
+        }
+
+        // ---- sampling: p and q of the row, then the children in order ----
+        if (__any_sync(kFull, lane < P && (isnan(xv.x) || isnan(xv.y) || isnan(xv.z) || isnan(xv.w)))) {
+            bad = true;
+            break;
+        }
+        float m_t, S_t, m_d, S_d;
+        combine_ms2(xv.x, xv.y, xv.z, xv.w, c, m_t, S_t, m_d, S_d);
+        if (!(isfinite(m_t) && S_t > 0.0f && isfinite(S_t)) ||
+            (with_d && !(isfinite(m_d) && S_d > 0.0f && isfinite(S_d)))) {
+            bad = true;
+            break;
+        }
+        const float ist = __frcp_rn(S_t), isd = with_d ? __frcp_rn(S_d) : 0.0f;
+        const float rt = ref_of(m_t, c), rd = with_d ? ref_of(m_d, c) : 0.0f;
+        int k = 0;              // rejections so far: residual levels computed
+        int stats_level = -1;   // the level whose terms the strip partials hold
+        int draw_level = 0;     // the last level with mass (0: p itself)
+        float wmass = 0.0f;     // lane j: warp j's total of the stats level
+        bool moved = false;
+        unsigned rest = kids;
+        while (rest) {
+            const int cn = __ffs(rest) - 1;
+            rest &= rest - 1;
+            const int x = __shfl_sync(kFull, tokn, cn);
+            const float u = __shfl_sync(kFull, un, cn);
+            if (x < 0 || x >= V || !(u >= 0.0f && u < 1.0f)) {
+                bad = true;
+                break;
+            }
+            uint32_t rlt = 0u, rld = 0u;
+            if (lane == 0) {
+                rlt = EL::load_raw(tgt + row * (size_t)V + x);
+                rld = EL::load_raw(drf + row * (size_t)V + x);
+            }
+            const float lt = EL::widen(__shfl_sync(kFull, rlt, 0));
+            const float ld = EL::widen(__shfl_sync(kFull, rld, 0));
+            const float px = __fmul_rn(weight_r(lt, rt, c), ist);
+            const float qx = __fmul_rn(weight_r(ld, rd, c), isd);
+            const float r = level_value(px, qx, k, inv);
+            const bool keep = qx > 0.0f ? __fmul_rn(u, qx) < r : r > 0.0f;
+            if (keep) {
+                if (lane == len)
+                    path_l = cn;
+                ++len;
+                v = cn;
+                moved = true;
+                break;
+            }
+            // the next residual level, from the resident slice
+            const float tot =
+                have ? level_pass<T, NV>(slot_t, slot_d, kwm, lane, c, rt, rd, ist, isd, k + 1, inv, stats) : 0.0f;
+            wmass = exchange2(tot);
+            if (__any_sync(kFull, xbroken))
+                break;
+            const float S = warp_sum_comp(wmass);
+            if (!(S >= 0.0f && isfinite(S))) {
+                bad = true;
+                break;
+            }
+            if (lane == 0)
+                inv[k] = S > 0.0f ? __frcp_rn(S) : 0.0f;
+            __syncwarp();
+            ++k;
+            stats_level = k;
+            if (S > 0.0f)
+                draw_level = k;
+        }
+        if (bad || __any_sync(kFull, xbroken))
+            break;
+        if (moved)
+            continue;
+
+        // ---- no child kept: the token from R (at a leaf R = p) ----
+        const float u0 = __shfl_sync(kFull, un, 0);
+        if (!(u0 >= 0.0f && u0 < 1.0f)) {
+            bad = true;
+            break;
+        }
+        if (stats_level != draw_level) {   // strips of the level drawn from
+            const float tot =
+                have ? level_pass<T, NV>(slot_t, slot_d, kwm, lane, c, rt, rd, ist, isd, draw_level, inv, stats)
+                     : 0.0f;
+            wmass = exchange2(tot);
+            if (__any_sync(kFull, xbroken))
+                break;
+        }
+        float t = 0.0f;
+        bool beyond = false;
+        int owner = -1;
+        {
+            float sw, cw;
+            warp_incl_scan_comp(wmass, lane, sw, cw);
+            const float S = __shfl_sync(kFull, sw, 31) + __shfl_sync(kFull, cw, 31);
+            if (S > 0.0f && isfinite(S)) {
+                t = u0 * S;
+                const unsigned hit = __ballot_sync(kFull, lane < P && wmass > 0.0f && t < sw + cw);
+                if (hit) {
+                    owner = __ffs(hit) - 1;
+                    const float os = __shfl_sync(kFull, sw, owner);
+                    const float oc = __shfl_sync(kFull, cw, owner);
+                    const float ow = __shfl_sync(kFull, wmass, owner);
+                    t = t - ((os - ow) + oc);
+                } else {
+                    const unsigned posm = __ballot_sync(kFull, lane < P && wmass > 0.0f);
+                    owner = posm ? 31 - __clz(posm) : -1;
+                    beyond = true;
+                }
+            }
+        }
+        if (owner < 0) {
+            if (writer)
+                write_out(len, -1);
+        } else if (owner == g) {
+            auto strip_mass = [&](int q) -> float {
+                const float4 m4 = *reinterpret_cast<const float4*>(stats + (size_t)q * 4);
+                return (m4.x + m4.y) + (m4.z + m4.w);
+            };
+            float tc = t;
+            int token = -1;
+            const int js = select_cdf(kwm * NV, strip_mass, tc, beyond, lane);
+            if (js >= 0) {
+                const int jc = js / NV, ks = js % NV;
+                const uint4 t4 = reinterpret_cast<const uint4*>(slot_t + (size_t)jc * CH)[ks * 32 + lane];
+                const uint4 d4 = reinterpret_cast<const uint4*>(slot_d + (size_t)jc * CH)[ks * 32 + lane];
+                const int ce = pick_level<T, NV>(t4, d4, c, rt, rd, ist, isd, draw_level, inv, tc, beyond, lane);
+                if (ce >= 0)
+                    token = e0 + jc * CH + ks * 32 * E + ce;
+            }
+            write_out(len, (token >= 0 && token < V) ? token : -1);
+        }
+        done = true;
+        break;
+    }
+    if (!done && writer)
+        write_out(len, -1);
+
+    // ---- wind-down: a copy still in flight (only after a timeout), then
+    // leave together (no CTA exits while a peer may still address it) ----
+    if (xbroken) {
+        if (lane == 0)
+            atomicOr(a.err, kErrWaitTimeout);
+        if (pending)
+            (void)mbar_wait_bounded(bar, uses & 1u, kWaitSpins);
+    }
+    __syncwarp();
+    cluster_arrive();
+    cluster_wait();
+}
+
+}  // namespace sv

@@ -146,3 +146,28 @@ def test_option_pointer_alignment_is_checked():
         st = lib.spec_verify_ex(P(), P(), 0, P(), P(), P(), 2, k.ctypes.data_as(ctypes.c_void_p), 10,
                                 P(), P(), ctypes.byref(opt), ctypes.c_void_p(0x100000), 1 << 20, None)
         assert st == sv.SV_ERR_INVALID_ARG, field
+
+
+def test_tree_entry_validation():
+    """spec_verify_tree rejects bad arguments on the host (fake, never
+    dereferenced pointers) before any device work."""
+    lib = sv.library()
+    P = lambda f: ctypes.c_void_p(0x1000) if f else None  # noqa: E731
+    assert sv.library().sv_tree_workspace_size() >= 16
+
+    def call(B=4, Nmax=7, V=10, dtype=0, tgt=1, tok=1, par=1, uni=1, tmp=1, nn=1, out=1, ws=1, nbytes=256):
+        w = ctypes.c_void_p(0x100000) if ws else None
+        return lib.spec_verify_tree(P(tgt), P(1), dtype, P(tok), P(par), P(uni), P(tmp), B, Nmax, P(nn), V,
+                                    P(out), P(out), P(out), w, nbytes, None)
+
+    assert call(B=0) == sv.SV_OK
+    assert call(B=-1) == sv.SV_ERR_INVALID_ARG
+    assert call(V=0) == sv.SV_ERR_INVALID_ARG
+    assert call(Nmax=0) == sv.SV_ERR_INVALID_ARG
+    assert call(Nmax=33) == sv.SV_ERR_INVALID_ARG
+    assert call(dtype=5) == sv.SV_ERR_INVALID_ARG
+    for k in ("tgt", "tok", "par", "uni", "tmp", "nn", "out"):
+        assert call(**{k: 0}) == sv.SV_ERR_INVALID_ARG, k
+    assert call(ws=0) == sv.SV_ERR_NO_MEMORY
+    assert call(nbytes=8) == sv.SV_ERR_NO_MEMORY
+    assert call(V=sv.sv_max_vocab(0) + 1) == sv.SV_ERR_UNSUPPORTED

@@ -1,0 +1,112 @@
+"""Token-tree verification on the GPU against the oracle, element by element
+(bit-exact outside the oracle's tie band)."""
+import numpy as np
+import pytest
+
+import oracle
+import speculative_decoding_verification_04_gb300 as sv
+import workloads as W
+from helpers import run_gpu, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    d = torch.device("cuda:0")
+    torch.cuda.set_device(d)
+    return d
+
+
+def _to_dev(d, dev):
+    import torch
+    out = {}
+    for k in ("target", "draft"):
+        a = d[k]
+        t = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16) if d["dtype"] == "bf16" else torch.from_numpy(a)
+        out[k] = t.to(dev)
+    for k in ("tokens", "parent", "n_nodes"):
+        out[k] = torch.from_numpy(np.ascontiguousarray(d[k], np.int32)).to(dev)
+    for k in ("uniforms", "temperature"):
+        out[k] = torch.from_numpy(np.ascontiguousarray(d[k], np.float32)).to(dev)
+    return out
+
+
+def _run(d, dev):
+    import torch
+    t = _to_dev(d, dev)
+    ot, op, ol = sv.spec_verify_tree(t["target"], t["draft"], t["tokens"], t["parent"], t["uniforms"],
+                                     t["temperature"], t["n_nodes"])
+    torch.cuda.synchronize()
+    return ot.cpu().numpy(), op.cpu().numpy(), ol.cpu().numpy()
+
+
+def _compare(d, got):
+    ref = oracle.tree_verify(d["target"], d["draft"], d["dtype"], d["tokens"], d["parent"], d["uniforms"],
+                             d["temperature"], d["n_nodes"])
+    ot, op, ol = got
+    bad = (ol != ref["out_len"]) | np.any(ot != ref["out_tokens"], axis=1) | np.any(op != ref["out_path"], axis=1)
+    hard = bad & ~ref["tie"]
+    assert not np.any(hard), (f"{int(hard.sum())} trees differ outside ties; first b={int(np.flatnonzero(hard)[0])}: "
+                              f"gpu {ol[hard][0]} {ot[hard][0].tolist()} oracle "
+                              f"{ref['out_len'][hard][0]} {ref['out_tokens'][hard][0].tolist()}")
+    return ref
+
+
+TREES = [  # name, parents, B, V, dtype, sigma_t, sigma_d
+    ("binary3_f32", W.full_tree(2, 3), 24, 5003, "f32", 2.0, 1.0),
+    ("ternary2_bf16", W.full_tree(3, 2), 24, 12345, "bf16", 2.0, 1.0),
+    ("wide_root_bf16", W.full_tree(8, 1), 16, 4097, "bf16", 2.0, 2.0),
+    ("close_draft_f32", W.full_tree(2, 4), 12, 3000, "f32", 2.0, 0.05),
+    ("tiny_vocab_bf16", W.full_tree(3, 2), 40, 3, "bf16", 1.0, 1.0),
+    ("chain_f32", np.arange(-1, 7, dtype=np.int32), 16, 700, "f32", 2.0, 1.0),
+    ("large_vocab_bf16", W.full_tree(2, 3), 6, 128256, "bf16", 2.0, 1.0),
+    ("large_vocab_f32", W.full_tree(2, 2), 4, 151936, "f32", 2.0, 1.5),
+]
+
+
+@pytest.mark.parametrize("case", TREES, ids=[c[0] for c in TREES])
+def test_trees_match_oracle(dev, case):
+    name, parents, B, V, dtype, st, sd = case
+    temps = np.where(np.arange(B) % 4 == 0, 0.0, np.where(np.arange(B) % 4 == 1, 0.7, 1.0)).astype(np.float32)
+    d = W.make_tree_host(B, parents, V, dtype, st, sd, temps, seed=sum(map(ord, name)))
+    ref = _compare(d, _run(d, dev))
+    assert np.all(ref["out_len"] >= 0)
+
+
+def test_ragged_trees_and_unusable_input(dev):
+    B, V = 12, 2000
+    d = W.make_tree_host(B, W.full_tree(2, 3), V, "f32", 2.0, 1.0, 1.0, seed=5)
+    d["n_nodes"] = np.array([15, 1, 2, 7, 3, 15, 15, 15, 15, 0, 15, 15], np.int32)
+    d["parent"][5, 4] = 9         # a parent after its child
+    d["tokens"][6, 1] = V         # a token outside [0, V)
+    d["uniforms"][7, 0] = 1.0     # a final uniform outside [0, 1)
+    d["temperature"][8] = -1.0    # an unusable temperature
+    d["target"][10, 0, 17] = np.nan
+    ref = _compare(d, _run(d, dev))
+    assert ref["out_len"][[5, 6, 8, 9, 10]].tolist() == [-1] * 5
+
+
+def test_chain_tree_is_spec_verify(dev):
+    """A tree of one child per node is the ordinary verification."""
+    B, K, V = 16, 6, 9000
+    temps = np.where(np.arange(B) % 3 == 0, 0.0, 1.0).astype(np.float32)
+    inp = W.make_host(B, K, V, "bf16", 2.0, 1.0, temps, seed=41)
+    t_chain, n_chain = run_gpu(to_device(inp, dev), "ws")
+    N = K + 1
+    tok = np.zeros((B, N), np.int32)
+    tok[:, 1:] = inp["tokens"]
+    uni = np.zeros((B, N), np.float32)
+    uni[:, 1:] = inp["uniforms"][:, :K]
+    uni[:, 0] = inp["uniforms"][:, K]
+    drf = np.zeros((B, N, V), inp["draft"].dtype)
+    drf[:, :K] = inp["draft"]
+    d = dict(target=inp["target"], draft=drf, dtype="bf16", tokens=tok, uniforms=uni,
+             parent=np.tile(np.arange(-1, N - 1, dtype=np.int32), (B, 1)), temperature=temps,
+             n_nodes=np.full(B, N, np.int32))
+    ot, op, ol = _run(d, dev)
+    assert np.array_equal(ol, n_chain)
+    assert np.array_equal(ot, t_chain)
