@@ -488,6 +488,87 @@ def run_sample(args):
     return 0
 
 
+def run_tree(args):
+    """Token-tree verification (spec_verify_tree): B = 256 full binary trees
+    of 15 nodes (3 levels of proposals), V = 128256 bf16 target logits
+    N(0, 2^2), draft = target + N(0, 1), T = 1, the proposals drawn from the
+    draft by Gumbel-max on the device; L2 flushed before every step."""
+    import torch
+
+    import speculative_decoding_verification_04_gb300 as sv
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    B = args.sequences or 256
+    V, N = 128256, 15
+    parent = torch.from_numpy(W.full_tree(2, 3)).to(dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(1005)
+    tgt = (torch.randn((B, N, V), generator=g, device=dev) * 2.0).to(torch.bfloat16)
+    drf = (tgt.float() + torch.randn((B, N, V), generator=g, device=dev)).to(torch.bfloat16)
+    tok = torch.zeros((B, N), dtype=torch.int32, device=dev)
+    for n in range(1, N):
+        gum = -torch.log(-torch.log(torch.rand((B, V), generator=g, device=dev).clamp_(1e-30, 1.0)))
+        tok[:, n] = torch.argmax(drf[:, int(parent[n])].float() + gum, dim=-1).to(torch.int32)
+        del gum
+    uni = torch.rand((B, N), generator=g, device=dev)
+    temp = torch.ones(B, device=dev)
+    par = parent.to(torch.int32).repeat(B, 1).contiguous()
+    nn = torch.full((B,), N, dtype=torch.int32, device=dev)
+    ws = torch.empty(int(sv.library().sv_tree_workspace_size()), dtype=torch.uint8, device=dev)
+    ot = torch.empty((B, N), dtype=torch.int32, device=dev)
+    op = torch.empty((B, N), dtype=torch.int32, device=dev)
+    ol = torch.empty((B,), dtype=torch.int32, device=dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 1 << 30), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        sv.spec_verify_tree(tgt, drf, tok, par, uni, temp, nn, workspace=ws, out_tokens=ot,
+                            out_path=op, out_len=ol)
+
+    for _ in range(max(args.warmup, 3)):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize()
+    evs = []
+    for _ in range(args.steps):
+        flush.fill_(1)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        step()
+        e1.record(stream)
+        evs.append((e0, e1))
+    torch.cuda.synchronize()
+    med = statistics.median([a.elapsed_time(b) for a, b in evs])
+    # algorithmic bytes: every node the walk visits reads its target row, and
+    # its draft row when it has children (all nodes are sampling nodes)
+    path = op.cpu().numpy()
+    lens = ol.cpu().numpy()
+    par_h = W.full_tree(2, 3)
+    has_kids = np.array([np.any(par_h == v) for v in range(N)])
+    rows = 0
+    for b in range(B):
+        visited = [0] + [int(x) for x in path[b, :max(int(lens[b]), 0)]]
+        rows += sum(2 if has_kids[v] else 1 for v in visited)
+    nbytes = rows * V * 2
+    peaks = _peaks()
+    achieved = nbytes / (med / 1e3) / 1e9
+    line = dict(metric="tree proposals/sec (spec_verify_tree)", value=B * (N - 1) / (med / 1e3),
+                unit="proposals/s", n_gpus=1, steps=args.steps, warmup=args.warmup, ms_per_step=med,
+                higher_is_better=True, dtype="bf16", data="synthetic",
+                config=dict(workload=f"B={B} full binary trees of {N} nodes, V={V} bf16 N(0,2^2) "
+                                     f"draft+N(0,1^2) T=1", l2="flushed before every step",
+                            mean_kept=float(np.mean(lens))),
+                roofline=dict(bound="hbm", achieved=round(achieved, 1), peak=peaks["hbm_gbs"],
+                              unit="GB/s", frac=round(achieved / peaks["hbm_gbs"], 4),
+                              bytes_algorithmic=int(nbytes), kernel="sv_tree_kernel"),
+                gpu_launches=args.steps)
+    print(json.dumps(line))
+    return 0
+
+
 def _rows_to_host(d, seqs):
     import torch
     idx = torch.as_tensor(np.asarray(seqs), device=d["target"].device, dtype=torch.long)
@@ -513,8 +594,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sequences", type=int, default=None,
                     help="the workload's first N sequences only (profiling captures)")
-    ap.add_argument("--op", choices=["verify", "sample"], default="verify",
-                    help="sample: time the draft-side sampler (spec_sample) instead")
+    ap.add_argument("--op", choices=["verify", "sample", "tree"], default="verify",
+                    help="sample: time the draft-side sampler (spec_sample); tree: token-tree "
+                         "verification (spec_verify_tree)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -522,6 +604,8 @@ def main():
         return run_reference(args)
     if args.op == "sample":
         return run_sample(args)
+    if args.op == "tree":
+        return run_tree(args)
     return run_ours(args)
 
 
