@@ -52,28 +52,40 @@ __host__ __device__ inline size_t tree_smem_bytes(const SweepLayout& L, int nw)
     return tree_lvl_offset(L) + (size_t)nw * 32 * 4;
 }
 
-// The term of one element at level L: L = 0, p = w_t * ist; L >= 1,
-// A_L = max(0, R_{L-1} - q) with q = w_d * isd and R_0 = p, R_l =
-// A_l * inv[l - 1] (inv[l - 1] = 1 / S_l; 0 marks a level without mass, which
-// leaves R as it was).  The weights are the sweep's: exp2(fma(l, c, -r)).
-__device__ __forceinline__ float level_term(float lt, float ld, float c, float rt, float rd, float ist,
-                                            float isd, int L, const float* inv)
+// The level-L terms of one 16-byte vector pair (E elements, lane order):
+// p and q of each element first, then the levels applied to all of them
+// (one read of each level's inverse sum per vector); the same rounding
+// sequence as level_term.
+template <typename T, int NV>
+__device__ __forceinline__ void level_terms_vec(const uint4& tv, const uint4& dv, float c, float rt, float rd,
+                                                float ist, float isd, int L, const float* inv,
+                                                float (&out)[Elem<T>::E])
 {
-    const float p = __fmul_rn(ex2_approx(__fmaf_rn(lt, c, -rt)), ist);
-    if (L == 0)
-        return p;
-    const float q = __fmul_rn(ex2_approx(__fmaf_rn(ld, c, -rd)), isd);
-    float r = p;
-    for (int l = 0; l < L - 1; ++l) {
-        const float s = inv[l];
-        if (s > 0.0f)
-            r = __fmul_rn(fmaxf(__fsub_rn(r, q), 0.0f), s);
+    using LN = Lane<T, NV>;
+    constexpr int E = Elem<T>::E;
+    float q[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+        out[e] = __fmul_rn(ex2_approx(__fmaf_rn(LN::vec_elem(tv, e), c, -rt)), ist);
+        q[e] = L > 0 ? __fmul_rn(ex2_approx(__fmaf_rn(LN::vec_elem(dv, e), c, -rd)), isd) : 0.0f;
     }
-    return fmaxf(__fsub_rn(r, q), 0.0f);
+    if (L == 0)
+        return;
+    for (int l = 0; l < L - 1; ++l) {
+        const float sl = inv[l];
+        if (sl > 0.0f) {
+#pragma unroll
+            for (int e = 0; e < E; ++e)
+                out[e] = __fmul_rn(fmaxf(__fsub_rn(out[e], q[e]), 0.0f), sl);
+        }
+    }
+#pragma unroll
+    for (int e = 0; e < E; ++e)
+        out[e] = fmaxf(__fsub_rn(out[e], q[e]), 0.0f);
 }
 
 // R_k(x) for the proposal's p(x), q(x) after k rejections (the same nested
-// steps as level_term).
+// steps as level_terms_vec).
 __device__ __forceinline__ float level_value(float px, float qx, int k, const float* inv)
 {
     float r = px;
@@ -87,7 +99,10 @@ __device__ __forceinline__ float level_value(float px, float qx, int k, const fl
 
 // One pass over this warp's slice at level L (whole warp): per-strip partial
 // sums of the level's terms into `stats` ([kw][NV][4], as the sweep's
-// residual pass), and the warp's total (compensated).
+// residual pass), and the warp's total (compensated).  Level terms: L = 0,
+// p = w_t * ist; L >= 1, A_L = max(0, R_{L-1} - q) with q = w_d * isd,
+// R_0 = p and R_l = A_l * inv[l - 1] (inv[l - 1] = 1 / S_l; 0 marks a level
+// without mass, which leaves R as it was); weights exp2(fma(l, c, -r)).
 template <typename T, int NV>
 __device__ float level_pass(const T* slot_t, const T* slot_d, int kwm, int lane, float c, float rt, float rd,
                             float ist, float isd, int L, const float* inv, float* stats)
@@ -103,10 +118,12 @@ __device__ float level_pass(const T* slot_t, const T* slot_d, int kwm, int lane,
         float sv[NV];
 #pragma unroll
         for (int k = 0; k < NV; ++k) {
+            float tm[E];
+            level_terms_vec<T, NV>(tv[k], dv[k], c, rt, rd, ist, isd, L, inv, tm);
             float sk = 0.0f;
 #pragma unroll
             for (int e = 0; e < E; ++e)
-                sk += level_term(LN::vec_elem(tv[k], e), LN::vec_elem(dv[k], e), c, rt, rd, ist, isd, L, inv);
+                sk += tm[e];
             sv[k] = sk;
         }
         strip_partials<NV>(sv, lane, stats + (size_t)j * NV * 4);
@@ -126,7 +143,7 @@ __device__ float level_pass(const T* slot_t, const T* slot_d, int kwm, int lane,
 // The element of one strip that holds the point tc of the level-L
 // distribution (one warp; tv / dv: each lane's vector of the strip): lane
 // sums, a compensated scan, the lane, then the element, the terms computed
-// exactly as in level_pass.  Returns lane * E + e, or -1 if the strip has no
+// exactly as in level_pass (level_terms_vec).  Returns lane * E + e, or -1 if the strip has no
 // mass; beyond the strip's mass (rounding) the last element with mass.
 template <typename T, int NV>
 __device__ int pick_level(const uint4& tv, const uint4& dv, float c, float rt, float rd, float ist, float isd,
@@ -137,9 +154,9 @@ __device__ int pick_level(const uint4& tv, const uint4& dv, float c, float rt, f
     float tm[E];
     float ls = 0.0f;
     int lastpos = -1;
+    level_terms_vec<T, NV>(tv, dv, c, rt, rd, ist, isd, L, inv, tm);
 #pragma unroll
     for (int e = 0; e < E; ++e) {
-        tm[e] = level_term(LN::vec_elem(tv, e), LN::vec_elem(dv, e), c, rt, rd, ist, isd, L, inv);
         ls += tm[e];
         if (tm[e] > 0.0f)
             lastpos = lane * E + e;
