@@ -341,6 +341,13 @@ __global__ void __maxnreg__(kMaxRegs) sv_tree_kernel(const TreeArgs a)
         }
         const size_t row = (size_t)b * Nmax + v;
         issue(row, with_d);
+        // each child's lane loads the two logits at its token now; the tests
+        // read them after the pass
+        uint32_t klt = 0u, kld = 0u;
+        if (with_d && ((kids >> lane) & 1u) && tokn >= 0 && tokn < V) {
+            klt = EL::load_raw(tgt + row * (size_t)V + tokn);
+            kld = EL::load_raw(drf + row * (size_t)V + tokn);
+        }
         bool have = false;
         if (pending) {
             const bool okw = mbar_wait_bounded(bar, uses & 1u, kWaitSpins);
@@ -468,13 +475,8 @@ __global__ void __maxnreg__(kMaxRegs) sv_tree_kernel(const TreeArgs a)
                 bad = true;
                 break;
             }
-            uint32_t rlt = 0u, rld = 0u;
-            if (lane == 0) {
-                rlt = EL::load_raw(tgt + row * (size_t)V + x);
-                rld = EL::load_raw(drf + row * (size_t)V + x);
-            }
-            const float lt = EL::widen(__shfl_sync(kFull, rlt, 0));
-            const float ld = EL::widen(__shfl_sync(kFull, rld, 0));
+            const float lt = EL::widen(__shfl_sync(kFull, klt, cn));
+            const float ld = EL::widen(__shfl_sync(kFull, kld, cn));
             const float px = __fmul_rn(weight_r(lt, rt, c), ist);
             const float qx = __fmul_rn(weight_r(ld, rd, c), isd);
             const float r = level_value(px, qx, k, inv);
