@@ -752,7 +752,39 @@ static cudaError_t launch_tree(const TreeArgs& ta, const Geom& g, size_t smem, c
     }
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
-    cfg.gridDim = dim3((unsigned)(ta.B * g.C), 1, 1);
+    // persistent: as many clusters as the device holds at once (at most B),
+    // cluster c verifying sequences c, c + clusters, ...
+    static std::map<std::tuple<int, int, int, size_t>, int> cap_cache;
+    int cap = 0;
+    {
+        const auto key = std::make_tuple(dev, g.C, g.nw, smem);
+        std::lock_guard<std::mutex> lk(g_mu);
+        auto it = cap_cache.find(key);
+        if (it != cap_cache.end()) {
+            cap = it->second;
+        } else {
+            cudaLaunchConfig_t q = {};
+            cudaLaunchAttribute qa[1];
+            q.gridDim = dim3((unsigned)g.C, 1, 1);
+            q.blockDim = dim3((unsigned)(32 * g.nw), 1, 1);
+            q.dynamicSmemBytes = smem;
+            qa[0].id = cudaLaunchAttributeClusterDimension;
+            qa[0].val.clusterDim.x = (unsigned)g.C;
+            qa[0].val.clusterDim.y = 1;
+            qa[0].val.clusterDim.z = 1;
+            q.attrs = qa;
+            q.numAttrs = 1;
+            if (cudaOccupancyMaxActiveClusters(&cap, kern, &q) != cudaSuccess) {
+                (void)cudaGetLastError();
+                cap = 0;
+            }
+            cap_cache[key] = cap;
+        }
+    }
+    if (cap <= 0)
+        return cudaErrorInvalidConfiguration;
+    const int clusters = std::min(cap, ta.B);
+    cfg.gridDim = dim3((unsigned)(clusters * g.C), 1, 1);
     cfg.blockDim = dim3((unsigned)(32 * g.nw), 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;

@@ -238,29 +238,19 @@ __global__ void __maxnreg__(kMaxRegs) sv_tree_kernel(const TreeArgs a)
     cluster_arrive();
     cluster_wait();
 
-    // ---- the sequence (lane n: node n) ----
-    const int b = (int)(blockIdx.x / (unsigned)C);
-    const int N = __ldg(a.n_nodes + b);
-    const float Tb = __ldg(a.temp + b);
-    int par = -2, tokn = 0;
-    float un = 0.0f;
-    if (lane < Nmax) {
-        par = __ldg(a.parent + (size_t)b * Nmax + lane);
-        tokn = __ldg(a.tok + (size_t)b * Nmax + lane);
-        un = __ldg(a.uni + (size_t)b * Nmax + lane);
-    }
-    const bool tree_ok = N >= 1 && N <= Nmax &&
-                         !__any_sync(kFull, lane >= 1 && lane < N && (par < 0 || par >= lane));
-    bool bad = !tree_ok || !temperature_usable(Tb);
-    const bool greedy = Tb == 0.0f;
-    const float c = (!bad && !greedy) ? log2e_over(Tb) : 0.0f;
     const T* tgt = static_cast<const T*>(a.tgt);
     const T* drf = static_cast<const T*>(a.drf);
     const bool writer = rank == 0 && w == 0;
+    const int n_clusters = (int)(gridDim.x / (unsigned)C);
+    const int cid = (int)(blockIdx.x / (unsigned)C);
 
     uint32_t uses = 0, kx = 0, k2 = 0;
-    bool pending = false, xbroken = false, done = false;
+    bool pending = false, xbroken = false;
+    // the current sequence (lane n: node n), set when it starts
+    int b = 0, N = 0, par = -2, tokn = 0;
     int path_l = -1;   // lane j: the j-th kept node
+    float Tb = 0.0f, un = 0.0f, c = 0.0f;
+    bool bad = false, greedy = false, done = false;
 
     // outputs of the sequence (whole warp; one warp calls it): the kept
     // nodes and their tokens, then `token`; token < 0 marks unusable input
@@ -329,6 +319,27 @@ __global__ void __maxnreg__(kMaxRegs) sv_tree_kernel(const TreeArgs a)
             xbroken = true;
         return lane < P ? xbuf2[p * P + lane].x : 0.0f;
     };
+
+    // ---- sequences cid, cid + clusters, ... ----
+    for (int bb = cid; bb < a.B && !xbroken; bb += n_clusters) {
+    b = bb;
+    N = __ldg(a.n_nodes + b);
+    Tb = __ldg(a.temp + b);
+    par = -2;
+    tokn = 0;
+    un = 0.0f;
+    if (lane < Nmax) {
+        par = __ldg(a.parent + (size_t)b * Nmax + lane);
+        tokn = __ldg(a.tok + (size_t)b * Nmax + lane);
+        un = __ldg(a.uni + (size_t)b * Nmax + lane);
+    }
+    const bool tree_ok = N >= 1 && N <= Nmax &&
+                         !__any_sync(kFull, lane >= 1 && lane < N && (par < 0 || par >= lane));
+    bad = !tree_ok || !temperature_usable(Tb);
+    greedy = Tb == 0.0f;
+    c = (!bad && !greedy) ? log2e_over(Tb) : 0.0f;
+    path_l = -1;
+    done = false;
 
     // ---- the walk: one node per step ----
     int v = 0, len = 0;
@@ -576,6 +587,7 @@ __global__ void __maxnreg__(kMaxRegs) sv_tree_kernel(const TreeArgs a)
     }
     if (!done && writer)
         write_out(len, -1);
+    }
 
     // ---- wind-down: a copy still in flight (only after a timeout), then
     // leave together (no CTA exits while a peer may still address it) ----
