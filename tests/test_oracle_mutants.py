@@ -35,6 +35,38 @@ MUTANTS = [
 ]
 
 
+# token-tree verification (oracle_tree_verify), against tests/test_oracle_tree.py
+TREE_MUTANTS = [
+    ("                if (S > 0.0)", "                if (S < 0.0)"),          # no residual after a rejection
+    ("if (keep((double)u, r[x], q[x])) {", "if (keep((double)u, p[x], q[x])) {"),   # siblings tested against p
+    ("const float u0 = uniforms[row0];", "const float u0 = uniforms[row0 + 1];"),  # wrong final uniform
+    ("                    if (x == g) {", "                    if (x != g) {"),     # greedy test flipped
+    ("out_tokens[row0 + j] = tokens[row0 + path[j]];", "out_tokens[row0 + j] = tokens[row0 + j + 1];"),
+]
+
+
+def _run_pins(tmp_path, before, after, pins):
+    src = open(os.path.join(ROOT, "oracle", "oracle.c")).read()
+    assert before in src, "mutation site no longer present in oracle.c"
+    for sub in ("oracle", "workloads"):
+        shutil.copytree(os.path.join(ROOT, sub), tmp_path / sub,
+                        ignore=shutil.ignore_patterns("*.so", "__pycache__"))
+    os.makedirs(tmp_path / "tests")
+    for f in ("conftest.py", pins):
+        shutil.copy(os.path.join(ROOT, "tests", f), tmp_path / "tests" / f)
+    shutil.copytree(os.path.join(ROOT, "tests", "golden"), tmp_path / "tests" / "golden")
+    (tmp_path / "oracle" / "oracle.c").write_text(src.replace(before, after, 1))
+    return subprocess.run([sys.executable, "-m", "pytest", f"tests/{pins}", "-q",
+                           "-x", "-p", "no:cacheprovider"], cwd=tmp_path, capture_output=True,
+                          text=True, timeout=600)
+
+
+@pytest.mark.parametrize("before,after", TREE_MUTANTS, ids=[f"t{i}" for i in range(len(TREE_MUTANTS))])
+def test_tree_pins_detect_planted_mistake(tmp_path, before, after):
+    r = _run_pins(tmp_path, before, after, "test_oracle_tree.py")
+    assert r.returncode != 0, "no tree pin failed for mutant:\n" + after + "\n" + r.stdout[-2000:]
+
+
 @pytest.mark.parametrize("before,after", MUTANTS, ids=[f"m{i}" for i in range(len(MUTANTS))])
 def test_pins_detect_planted_mistake(tmp_path, before, after):
     src = open(os.path.join(ROOT, "oracle", "oracle.c")).read()
