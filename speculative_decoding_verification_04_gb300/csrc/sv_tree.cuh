@@ -2,7 +2,8 @@
 // every node of a tree of proposals (a chain of one child per node is the
 // ordinary verification).
 //
-// One cluster per sequence walks its tree from the root.  At node v the
+// A persistent cluster walks its sequences' trees (sequences c, c + clusters,
+// ...), each from the root.  At node v the
 // cluster holds the target and draft rows after v resident in shared memory
 // (the same warp ranges and bulk copies as the sweep) and tests v's children
 // in index order: child c (token x) is kept iff u_c q(x) < R(x), with R = p
@@ -54,8 +55,11 @@ __host__ __device__ inline size_t tree_smem_bytes(const SweepLayout& L, int nw)
 
 // The level-L terms of one 16-byte vector pair (E elements, lane order):
 // p and q of each element first, then the levels applied to all of them
-// (one read of each level's inverse sum per vector); the same rounding
-// sequence as level_term.
+// (one read of each level's inverse sum per vector).  L = 0: p = w_t * ist;
+// L >= 1: A_L = max(0, R_{L-1} - q) with q = w_d * isd, R_0 = p and
+// R_l = A_l * inv[l - 1] (inv[l - 1] = 1 / S_l; 0 marks a level without
+// mass, which leaves R as it was); weights exp2(fma(l, c, -r)) as in the
+// sweep.
 template <typename T, int NV>
 __device__ __forceinline__ void level_terms_vec(const uint4& tv, const uint4& dv, float c, float rt, float rd,
                                                 float ist, float isd, int L, const float* inv,
@@ -99,10 +103,8 @@ __device__ __forceinline__ float level_value(float px, float qx, int k, const fl
 
 // One pass over this warp's slice at level L (whole warp): per-strip partial
 // sums of the level's terms into `stats` ([kw][NV][4], as the sweep's
-// residual pass), and the warp's total (compensated).  Level terms: L = 0,
-// p = w_t * ist; L >= 1, A_L = max(0, R_{L-1} - q) with q = w_d * isd,
-// R_0 = p and R_l = A_l * inv[l - 1] (inv[l - 1] = 1 / S_l; 0 marks a level
-// without mass, which leaves R as it was); weights exp2(fma(l, c, -r)).
+// residual pass), and the warp's total (compensated); terms as in
+// level_terms_vec.
 template <typename T, int NV>
 __device__ float level_pass(const T* slot_t, const T* slot_d, int kwm, int lane, float c, float rt, float rd,
                             float ist, float isd, int L, const float* inv, float* stats)
