@@ -753,7 +753,7 @@ static cudaError_t launch_tree(const TreeArgs& ta, const Geom& g, size_t smem, c
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     // persistent: as many clusters as the device holds at once (at most B),
-    // cluster c verifying sequences c, c + clusters, ...
+    // cluster c verifying sequence c, then claiming the next
     static std::map<std::tuple<int, int, int, size_t>, int> cap_cache;
     int cap = 0;
     {
@@ -1117,6 +1117,7 @@ sv_status spec_verify_tree(const void* target_logits, const void* draft_logits, 
     ta.out_path = out_path;
     ta.out_len = out_len;
     ta.err = static_cast<uint32_t*>(workspace);
+    ta.next = reinterpret_cast<int*>(static_cast<unsigned char*>(workspace) + 4);
     ta.B = B;
     ta.Nmax = Nmax;
     ta.V = V;

@@ -2,8 +2,8 @@
 // every node of a tree of proposals (a chain of one child per node is the
 // ordinary verification).
 //
-// A persistent cluster walks its sequences' trees (sequences c, c + clusters,
-// ...), each from the root.  At node v the
+// A persistent cluster walks its sequences' trees (sequence c first, later
+// ones claimed with an atomic ticket), each from the root.  At node v the
 // cluster holds the target and draft rows after v resident in shared memory
 // (the same warp ranges and bulk copies as the sweep) and tests v's children
 // in index order: child c (token x) is kept iff u_c q(x) < R(x), with R = p
@@ -39,6 +39,7 @@ struct TreeArgs {
     int32_t* out_path;       // [B][Nmax]
     int32_t* out_len;        // [B]
     uint32_t* err;
+    int* next;               // claim counter of the sequences after the first wave
     int B, Nmax, V;
     int nchunks, C, kw;
     int aligned, has_draft;
@@ -217,6 +218,8 @@ __global__ void __maxnreg__(kMaxRegs) sv_tree_kernel(const TreeArgs a)
     const uint32_t bar = smem_addr(dsm + L.bars + 8 * (size_t)w);
     uint64_t* xbar = reinterpret_cast<uint64_t*>(dsm + L.xbar);
     uint64_t* xbar2 = reinterpret_cast<uint64_t*>(dsm + L.xbar2);
+    const uint32_t xbarc = smem_addr(dsm + L.xbarc);
+    const int* first_seq = reinterpret_cast<const int*>(dsm + L.first);
     float4* xbuf = reinterpret_cast<float4*>(dsm + L.xbuf);
     float2* xbuf2 = reinterpret_cast<float2*>(dsm + L.xbuf2);
     float* stats = reinterpret_cast<float*>(dsm + L.stats) + (size_t)w * KW * 16;
@@ -229,6 +232,7 @@ __global__ void __maxnreg__(kMaxRegs) sv_tree_kernel(const TreeArgs a)
             mbar_init(smem_addr(&xbar[1]), 1);
             mbar_init(smem_addr(&xbar2[0]), 1);
             mbar_init(smem_addr(&xbar2[1]), 1);
+            mbar_init(xbarc, 1);
         }
         fence_mbar_init();
     }
@@ -246,7 +250,8 @@ __global__ void __maxnreg__(kMaxRegs) sv_tree_kernel(const TreeArgs a)
     const int n_clusters = (int)(gridDim.x / (unsigned)C);
     const int cid = (int)(blockIdx.x / (unsigned)C);
 
-    uint32_t uses = 0, kx = 0, k2 = 0;
+    uint32_t uses = 0, kx = 0, k2 = 0, kc = 0;
+    uint32_t kx_claim = 0;   // row exchanges run when the last claim was read
     bool pending = false, xbroken = false;
     // the current sequence (lane n: node n), set when it starts
     int b = 0, N = 0, par = -2, tokn = 0;
@@ -322,8 +327,8 @@ __global__ void __maxnreg__(kMaxRegs) sv_tree_kernel(const TreeArgs a)
         return lane < P ? xbuf2[p * P + lane].x : 0.0f;
     };
 
-    // ---- sequences cid, cid + clusters, ... ----
-    for (int bb = cid; bb < a.B && !xbroken; bb += n_clusters) {
+    // ---- sequence cid, then claimed ones ----
+    for (int bb = cid; bb >= 0 && bb < a.B && !xbroken;) {
     b = bb;
     N = __ldg(a.n_nodes + b);
     Tb = __ldg(a.temp + b);
@@ -589,6 +594,35 @@ __global__ void __maxnreg__(kMaxRegs) sv_tree_kernel(const TreeArgs a)
     }
     if (!done && writer)
         write_out(len, -1);
+    if (__any_sync(kFull, xbroken))
+        break;
+    // the next sequence: rank 0's writer takes a ticket and sends it to every
+    // CTA (st.async onto each CTA's claim mbarrier, bounded wait).  Every
+    // warp must have read the previous claim first: a row exchange since then
+    // shows it; a sequence rejected before its walk (no exchange) waits at a
+    // cluster barrier instead (uniform: it follows from the sequence's data).
+    {
+        if (kc > 0 && kx == kx_claim) {
+            cluster_arrive();
+            cluster_wait();
+        }
+        if (w == 0 && lane == 0)
+            mbar_arrive_expect_tx(xbarc, 8u);
+        int nb = -1;
+        if (writer && lane == 0)
+            nb = atomicAdd(a.next, 1) + n_clusters;
+        nb = __shfl_sync(kFull, nb, 0);
+        if (writer && lane < C)
+            st_async_v2(map_to_rank(smem_addr(first_seq), (uint32_t)lane),
+                        make_float2(__int_as_float(nb), 0.0f), map_to_rank(xbarc, (uint32_t)lane));
+        if (!mbar_wait_bounded(xbarc, kc & 1u, kWaitSpins))
+            xbroken = true;
+        ++kc;
+        if (__any_sync(kFull, xbroken))
+            break;
+        bb = *first_seq;
+        kx_claim = kx;
+    }
     }
 
     // ---- wind-down: a copy still in flight (only after a timeout), then
