@@ -110,3 +110,29 @@ def test_chain_tree_is_spec_verify(dev):
     ot, op, ol = _run(d, dev)
     assert np.array_equal(ol, n_chain)
     assert np.array_equal(ot, t_chain)
+
+
+def test_tree_verification_replays_in_a_cuda_graph(dev):
+    """spec_verify_tree captured into a CUDA graph (after one ordinary call)
+    replays on the captured buffers' current contents."""
+    import torch
+    B, V = 12, 6000
+    d1 = W.make_tree_host(B, W.full_tree(2, 3), V, "bf16", 2.0, 1.0, 1.0, seed=61)
+    d2 = W.make_tree_host(B, W.full_tree(2, 3), V, "bf16", 2.0, 1.0, 1.0, seed=62)
+    t = _to_dev(d1, dev)
+    ot, op, ol = sv.spec_verify_tree(t["target"], t["draft"], t["tokens"], t["parent"], t["uniforms"],
+                                     t["temperature"], t["n_nodes"])
+    ws = torch.empty(int(sv.library().sv_tree_workspace_size()), dtype=torch.uint8, device=dev)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        sv.spec_verify_tree(t["target"], t["draft"], t["tokens"], t["parent"], t["uniforms"], t["temperature"],
+                            t["n_nodes"], workspace=ws, out_tokens=ot, out_path=op, out_len=ol)
+    for d in (d1, d2):
+        src = _to_dev(d, dev)
+        for k in t:
+            t[k].copy_(src[k])
+        ol.fill_(-7)
+        g.replay()
+        torch.cuda.synchronize()
+        _compare(d, (ot.cpu().numpy(), op.cpu().numpy(), ol.cpu().numpy()))
