@@ -45,25 +45,21 @@ struct TreeArgs {
     int aligned, has_draft;
 };
 
-// The sweep's shared-memory layout, then [nw][32] floats of per-level
-// inverse sums (each warp keeps its own copy).
-__host__ __device__ inline size_t tree_lvl_offset(const SweepLayout& L) { return (L.total + 15) & ~(size_t)15; }
-
-__host__ __device__ inline size_t tree_smem_bytes(const SweepLayout& L, int nw)
-{
-    return tree_lvl_offset(L) + (size_t)nw * 32 * 4;
-}
+// The sweep's shared-memory layout (the per-level inverse sums live in lane
+// registers: lane l holds 1 / S_{l+1}), so a row's CTAs fit three to an SM
+// as the sweep's do.
+__host__ __device__ inline size_t tree_smem_bytes(const SweepLayout& L, int /*nw*/) { return L.total; }
 
 // The level-L terms of one 16-byte vector pair (E elements, lane order):
 // p and q of each element first, then the levels applied to all of them
-// (one read of each level's inverse sum per vector).  L = 0: p = w_t * ist;
+// (each level's inverse sum shuffled from its lane once per vector).  L = 0: p = w_t * ist;
 // L >= 1: A_L = max(0, R_{L-1} - q) with q = w_d * isd, R_0 = p and
-// R_l = A_l * inv[l - 1] (inv[l - 1] = 1 / S_l; 0 marks a level without
+// R_l = A_l / S_l (lane l - 1 of `inv` holds 1 / S_l; 0 marks a level without
 // mass, which leaves R as it was); weights exp2(fma(l, c, -r)) as in the
 // sweep.
 template <typename T, int NV>
 __device__ __forceinline__ void level_terms_vec(const uint4& tv, const uint4& dv, float c, float rt, float rd,
-                                                float ist, float isd, int L, const float* inv,
+                                                float ist, float isd, int L, float inv,
                                                 float (&out)[Elem<T>::E])
 {
     using LN = Lane<T, NV>;
@@ -77,7 +73,7 @@ __device__ __forceinline__ void level_terms_vec(const uint4& tv, const uint4& dv
     if (L == 0)
         return;
     for (int l = 0; l < L - 1; ++l) {
-        const float sl = inv[l];
+        const float sl = __shfl_sync(kFull, inv, l);
         if (sl > 0.0f) {
 #pragma unroll
             for (int e = 0; e < E; ++e)
@@ -91,11 +87,11 @@ __device__ __forceinline__ void level_terms_vec(const uint4& tv, const uint4& dv
 
 // R_k(x) for the proposal's p(x), q(x) after k rejections (the same nested
 // steps as level_terms_vec).
-__device__ __forceinline__ float level_value(float px, float qx, int k, const float* inv)
+__device__ __forceinline__ float level_value(float px, float qx, int k, float inv)
 {
     float r = px;
     for (int l = 0; l < k; ++l) {
-        const float s = inv[l];
+        const float s = __shfl_sync(kFull, inv, l);
         if (s > 0.0f)
             r = __fmul_rn(fmaxf(__fsub_rn(r, qx), 0.0f), s);
     }
@@ -108,7 +104,7 @@ __device__ __forceinline__ float level_value(float px, float qx, int k, const fl
 // level_terms_vec.
 template <typename T, int NV>
 __device__ float level_pass(const T* slot_t, const T* slot_d, int kwm, int lane, float c, float rt, float rd,
-                            float ist, float isd, int L, const float* inv, float* stats)
+                            float ist, float isd, int L, float inv, float* stats)
 {
     using LN = Lane<T, NV>;
     constexpr int E = Elem<T>::E;
@@ -150,7 +146,7 @@ __device__ float level_pass(const T* slot_t, const T* slot_d, int kwm, int lane,
 // mass; beyond the strip's mass (rounding) the last element with mass.
 template <typename T, int NV>
 __device__ int pick_level(const uint4& tv, const uint4& dv, float c, float rt, float rd, float ist, float isd,
-                          int L, const float* inv, float tc, bool beyond, int lane)
+                          int L, float inv, float tc, bool beyond, int lane)
 {
     using LN = Lane<T, NV>;
     constexpr int E = Elem<T>::E;
@@ -223,7 +219,6 @@ __global__ void __maxnreg__(kMaxRegs) sv_tree_kernel(const TreeArgs a)
     float4* xbuf = reinterpret_cast<float4*>(dsm + L.xbuf);
     float2* xbuf2 = reinterpret_cast<float2*>(dsm + L.xbuf2);
     float* stats = reinterpret_cast<float*>(dsm + L.stats) + (size_t)w * KW * 16;
-    float* inv = reinterpret_cast<float*>(dsm + tree_lvl_offset(L)) + (size_t)w * 32;
 
     if (lane == 0) {
         mbar_init(bar, 1);
@@ -252,6 +247,7 @@ __global__ void __maxnreg__(kMaxRegs) sv_tree_kernel(const TreeArgs a)
 
     uint32_t uses = 0, kx = 0, k2 = 0, kc = 0;
     uint32_t kx_claim = 0;   // row exchanges run when the last claim was read
+    float inv = 0.0f;        // lane l: 1 / S_{l+1} of the node's residual levels
     bool pending = false, xbroken = false;
     // the current sequence (lane n: node n), set when it starts
     int b = 0, N = 0, par = -2, tokn = 0;
@@ -518,9 +514,8 @@ __global__ void __maxnreg__(kMaxRegs) sv_tree_kernel(const TreeArgs a)
                 bad = true;
                 break;
             }
-            if (lane == 0)
-                inv[k] = S > 0.0f ? __frcp_rn(S) : 0.0f;
-            __syncwarp();
+            if (lane == k)
+                inv = S > 0.0f ? __frcp_rn(S) : 0.0f;
             ++k;
             stats_level = k;
             if (S > 0.0f)
