@@ -32,6 +32,14 @@ MUTANTS = [
     ("if (x != g) { rejected = 1; break; }", "if (x == g) { rejected = 1; break; }"),
     ("if (logit_at(base, dtype, off + (size_t)j) == m) {",
      "if (logit_at(base, dtype, off + (size_t)j) == m && j > 0) {"),
+    # the tie flag (parity exempts the sequences it marks)
+    ("if (fabs(u - Cprev) < ORC_TIE_BAND || fabs(u - C) < ORC_TIE_BAND)", "if (1)"),   # every draw flagged
+    ("#define ORC_TIE_BAND 1e-6", "#define ORC_TIE_BAND 1e-3"),                        # a band 1000x wider
+    ("if (q[x] > 0.0 && fabs((double)u - p[x] / q[x]) < ORC_TIE_BAND)", "if (0)"),     # accept ties dropped
+    ("if (q[x] > 0.0 && fabs((double)u - p[x] / q[x]) < ORC_TIE_BAND)", "if (q[x] > 0.0)"),  # every test flagged
+    ("fabs(u - Cprev) < ORC_TIE_BAND || fabs(u - C)", "fabs(u - Cprev) < ORC_TIE_BAND && fabs(u - C)"),
+    ("if (fabs(u - Cprev) < ORC_TIE_BAND || ", "if ("),                                 # lower boundary dropped
+    ("|| fabs(u - C) < ORC_TIE_BAND)", ")"),                                            # upper boundary dropped
 ]
 
 
@@ -42,6 +50,9 @@ TREE_MUTANTS = [
     ("const float u0 = uniforms[row0];", "const float u0 = uniforms[row0 + 1];"),  # wrong final uniform
     ("                    if (x == g) {", "                    if (x != g) {"),     # greedy test flipped
     ("out_tokens[row0 + j] = tokens[row0 + path[j]];", "out_tokens[row0 + j] = tokens[row0 + j + 1];"),
+    ("if (q[x] > 0.0 && fabs((double)u - r[x] / q[x]) < ORC_TIE_BAND)", "if (0)"),    # child ties dropped
+    ("if (q[x] > 0.0 && fabs((double)u - r[x] / q[x]) < ORC_TIE_BAND)",
+     "if (q[x] > 0.0 && fabs((double)u - p[x] / q[x]) < ORC_TIE_BAND)"),              # band around p/q, not R/q
 ]
 
 

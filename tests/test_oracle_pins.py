@@ -334,3 +334,93 @@ def test_output_layout_and_padding():
         assert list(row[:n]) == list(inp["tokens"][b, :n])
         assert 0 <= row[n] < 37
         assert np.all(row[n + 1:] == -1)
+
+
+# ---------------------------------------------------------------------------
+# P-tie: the tie flag marks exactly the decisions whose uniform lies within
+# 1e-6 of its threshold.  The pages state the rule as a comparison with
+# min(1, p/q) (tech-tldr.com, section 受理判定の数理：修正版棄却サンプリング)
+# and note that floating-point precision can change the outcome of such
+# comparisons (issoh.co.jp, section 受理・棄却の規則と出力分布が変わらない理由,
+# the vLLM caveat); parity exempts flagged sequences, so the flag must be set
+# inside the band and clear outside it.  Thresholds here come from scipy's
+# softmax of the float32 logits, not from the oracle.
+# ---------------------------------------------------------------------------
+TIE_T = np.array([[0.3, -1.2, 1.1, 0.2, -0.4],     # tested row 0
+                  [0.9, 0.1, -0.6, 0.4, -1.3]], np.float32)   # bonus row 1
+TIE_D = np.array([[1.4, 0.2, -0.5, 0.6, -0.9]], np.float32)
+INSIDE = (-5e-7, 5e-7)      # within the 1e-6 band
+OUTSIDE = (-2e-6, 2e-6)     # clear of it
+
+
+def _tie_dists():
+    p, q = _f32_softmax(TIE_T[0]), _f32_softmax(TIE_D[0])
+    resid = np.maximum(p - q, 0.0)
+    return p, q, np.cumsum(resid / resid.sum()), np.cumsum(_f32_softmax(TIE_T[1]))
+
+
+def _near(u, delta):
+    """The float32 uniform closest to u + delta (its distance from u stays
+    within 0.3 of |delta|: float32 spacing below 1 is at most 6e-8)."""
+    v = np.float32(u + delta)
+    assert abs(float(v) - u - delta) < 0.3 * abs(delta)
+    return v
+
+
+@pytest.mark.parametrize("x", [3, 0])
+def test_tie_flag_at_the_accept_threshold(x):
+    p, q, cdf_r, cdf_b = _tie_dists()
+    ratio = p[x] / q[x]
+    assert 0.05 < ratio < 0.95
+    u_final = 0.3     # far from every boundary of both final distributions
+    assert min(np.min(np.abs(cdf_r - u_final)), np.min(np.abs(cdf_b - u_final))) > 0.05
+    for delta in INSIDE + OUTSIDE:
+        r = _one(TIE_T, TIE_D, [x], [_near(ratio, delta), u_final])
+        assert r["num_accepted"][0] == (1 if delta < 0 else 0), delta
+        assert bool(r["tie"][0]) == (delta in INSIDE), (x, delta)
+
+
+def test_tie_flag_at_the_residual_cdf_boundaries():
+    """Proposal 0 rejected (u = 0.999, far above p/q = 0.41); the residual
+    has mass at tokens 2 and 4 only, so its one interior boundary C lies
+    between them: just below C the token is 2 (C is its upper end), just
+    above it the token is 4 (C is its lower end, token 3 holding no mass)."""
+    p, q, cdf_r, _ = _tie_dists()
+    C = cdf_r[2]
+    assert 0.5 < C < 0.99 and cdf_r[3] == C
+    for delta in INSIDE + OUTSIDE:
+        r = _one(TIE_T, TIE_D, [0], [0.999, _near(C, delta)])
+        assert r["num_accepted"][0] == 0
+        assert r["out_tokens"][0, 0] == (2 if delta < 0 else 4), delta
+        assert bool(r["tie"][0]) == (delta in INSIDE), delta
+
+
+@pytest.mark.parametrize("j", [0, 1, 2, 3])
+def test_tie_flag_at_the_bonus_cdf_boundaries(j):
+    """Proposal 3 accepted (u = 0, far below p/q = 0.83): the bonus token is
+    drawn from p of row 1; at each interior boundary C_j the token is j just
+    below it and j + 1 just above it."""
+    _, _, _, cdf_b = _tie_dists()
+    C = cdf_b[j]
+    for delta in INSIDE + OUTSIDE:
+        r = _one(TIE_T, TIE_D, [3], [0.0, _near(C, delta)])
+        assert r["num_accepted"][0] == 1
+        assert r["out_tokens"][0, 1] == (j if delta < 0 else j + 1), (j, delta)
+        assert bool(r["tie"][0]) == (delta in INSIDE), (j, delta)
+
+
+def test_greedy_decisions_are_never_flagged():
+    p, q, _, cdf_b = _tie_dists()
+    for u in (p[3] / q[3], cdf_b[1], 0.0):
+        r = _one(TIE_T, TIE_D, [2], [np.float32(u), np.float32(u)], T=0.0)
+        assert not r["tie"][0]
+
+
+def test_ties_are_rare_on_random_batches():
+    """A uniform lands in a 2e-6-wide band around a threshold with
+    probability 2e-6 per decision: a random batch of 20,000 sequences (about
+    three decisions each) should flag well under 1e-4 of them."""
+    B = 20000
+    inp = W.make_host(B, 4, 48, "f32", 2.0, 1.0, 1.0, seed=2718)
+    res = oracle.verify_inputs(inp)
+    assert int(res["tie"].sum()) <= max(2, int(1e-4 * B))

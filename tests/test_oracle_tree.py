@@ -114,3 +114,53 @@ def test_leaf_root_is_a_draw_from_p():
     assert np.all(got["out_len"] == 0)
     counts = np.bincount(got["out_tokens"][:, 0], minlength=V)
     assert stats.chisquare(counts, W.TOY_P * B).pvalue > 1e-3
+
+
+def _f32_softmax(logits32):
+    from scipy import special
+    return special.softmax(np.asarray(logits32, np.float64))
+
+
+def _two_children(tl, dl, x1, x2, u1, u2, u0):
+    """Root with children 1 and 2 (tokens x1, x2) tested in that order;
+    uniforms u1, u2 test them, u0 is the final draw."""
+    V = len(tl)
+    tgt = np.zeros((1, 3, V), np.float32)
+    drf = np.zeros((1, 3, V), np.float32)
+    tgt[0, :] = tl
+    drf[0, 0] = dl
+    d = dict(target=tgt, draft=drf, dtype="f32", tokens=np.array([[0, x1, x2]], np.int32),
+             parent=np.array([[-1, 0, 0]], np.int32),
+             uniforms=np.array([[u0, u1, u2]], np.float32), temperature=np.ones(1, np.float32),
+             n_nodes=np.array([3], np.int32))
+    return _tree(d)
+
+
+def test_tree_tie_flag_at_each_sibling_threshold():
+    """The tie flag marks a child test whose uniform lies within 1e-6 of its
+    threshold R(x)/q(x): R = p for the first child, and R =
+    normalize(max(0, p - q)) (the distribution tech-tldr.com, section
+    受理判定の数理, draws from after a rejection) for the second; inside the
+    band (5e-7 away) the flag is set, outside it (2e-6 away) clear, and the
+    decision follows the side of the threshold.  Thresholds come from scipy's
+    softmax of the float32 logits."""
+    tl = np.log(np.array([0.30, 0.25, 0.25, 0.20])).astype(np.float32)
+    dl = np.log(np.array([0.50, 0.22, 0.18, 0.10])).astype(np.float32)
+    p, q = _f32_softmax(tl), _f32_softmax(dl)
+    R1 = np.maximum(p - q, 0.0)
+    R1 /= R1.sum()
+    th1, th2 = p[0] / q[0], R1[1] / q[1]
+    assert 0.5 < th1 < 0.7 and 0.6 < th2 < 0.75
+    u_final = 0.05    # far from the boundaries of every distribution drawn from here
+    for delta in (-5e-7, 5e-7, -2e-6, 2e-6):
+        inside = abs(delta) < 1e-6
+        # first child at its threshold; the second (token 3, R(3)/q(3) = 2) is
+        # then kept whatever happens, with u = 0.5 far from it
+        g = _two_children(tl, dl, 0, 3, np.float32(th1 + delta), 0.5, u_final)
+        assert g["out_path"][0, 0] == (1 if delta < 0 else 2)
+        assert bool(g["tie"][0]) == inside, delta
+        # first child rejected far from its threshold (u = 0.95), the second
+        # at its threshold against R1
+        g = _two_children(tl, dl, 0, 1, 0.95, np.float32(th2 + delta), u_final)
+        assert g["out_len"][0] == (1 if delta < 0 else 0)
+        assert bool(g["tie"][0]) == inside, delta
