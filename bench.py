@@ -187,6 +187,32 @@ def oracle_rate(inp):
     return float(np.sum(inp["K"])) / dt, dt
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), for the baseline lines."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.split(":")[0].strip() == "Model name":
+                vendor = next((ln.split(":", 1)[1].strip() for ln in out.splitlines()
+                               if ln.split(":")[0].strip() == "Vendor ID"), "")
+                return f"{vendor} {line.split(':', 1)[1].strip()}".strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        fields = {}
+        for line in open("/proc/cpuinfo"):
+            if ":" in line:
+                k, v = line.split(":", 1)
+                fields.setdefault(k.strip(), v.strip())
+        if "model name" in fields:
+            return fields["model name"]
+        if "CPU part" in fields:
+            return f"CPU implementer {fields.get('CPU implementer', '?')} part {fields['CPU part']}"
+    except OSError:
+        pass
+    return platform.processor() or platform.machine()
+
+
 def host_cores() -> int:
     try:
         return len(os.sched_getaffinity(0))
@@ -194,10 +220,11 @@ def host_cores() -> int:
         return os.cpu_count() or 1
 
 
-def oracle_rate_cores(inp, threads: int):
+def oracle_rate_cores(inp, threads: int, results: list | None = None):
     """Oracle throughput with the batch cut into `threads` contiguous shards of
     sequences run at once (the oracle's C loop runs outside the GIL; the
-    oracle itself is unchanged): (positions/s, seconds)."""
+    oracle itself is unchanged): (positions/s, seconds).  The shards' results
+    are appended to `results` when given."""
     import oracle
     from concurrent.futures import ThreadPoolExecutor
     B = int(len(inp["K"]))
@@ -208,8 +235,10 @@ def oracle_rate_cores(inp, threads: int):
     with ThreadPoolExecutor(max_workers=len(shards)) as ex:
         list(ex.map(lambda _: None, range(len(shards))))
         t0 = time.perf_counter()
-        list(ex.map(oracle.verify_inputs, shards))
+        parts = list(ex.map(oracle.verify_inputs, shards))
         dt = time.perf_counter() - t0
+    if results is not None:
+        results.extend(parts)
     return float(np.sum(inp["K"])) / dt, dt
 
 
@@ -235,7 +264,7 @@ def run_reference(args):
         steps=args.steps, warmup=args.warmup, ms_per_step=round(1e3 * statistics.median(secs), 3),
         higher_is_better=True, scaling="weak", vs_baseline=None, dtype="f64", data="synthetic",
         config=dict(workload=WORKLOAD_TEXT[widx], bench_workload=widx, sample_sequences=n),
-        cpu_baseline=dict(value=value, unit=UNIT, cores=cores, kind="oracle",
+        cpu_baseline=dict(value=value, unit=UNIT, cores=cores, kind="oracle", cpu_model=cpu_model(),
                           sample=f"first {n} of {W.SPECS[widx].B} sequences of the workload "
                                  f"({int(np.sum(inp['K']))} positions) per step, host-generated "
                                  f"with the same recipe, cut into {cores} shards of sequences "
@@ -265,7 +294,8 @@ def run_ours(args):
     d = W.make_device(widx, dev, B=args.sequences)
     B, Kmax, V = d["B"], d["Kmax"], d["V"]
     K = np.asarray(d["K"], np.int32)
-    dcode = sv.SV_DTYPE_BF16 if d["dtype"] == "bf16" else sv.SV_DTYPE_F32
+    ldtype = d["dtype"]
+    dcode = sv.SV_DTYPE_BF16 if ldtype == "bf16" else sv.SV_DTYPE_F32
     ws = sv.Workspace(B, Kmax, V, dcode, dev)
     out_t = torch.empty((B, Kmax + 1), dtype=torch.int32, device=dev)
     out_n = torch.empty((B,), dtype=torch.int32, device=dev)
@@ -327,6 +357,7 @@ def run_ours(args):
     # verify-every-row variant of the same step (same outputs, all bytes read)
     times_all = timed(max(3, args.steps // 2), verify_all=True)
     ms_all = statistics.median(times_all)
+    geometry = sv.sv_geometry(B, Kmax, V, dcode)
 
     peaks = _peaks()
     med_ms = statistics.median(times)
@@ -392,19 +423,41 @@ def run_ours(args):
 
     # ---- CPU oracle baseline on a bounded sample (rank 0, N=1 only) ----
     cpu = None
+    parity = None
     if world == 1 and not args.no_cpu_baseline:
         def host_rows(n):
             return _rows_to_host(d, np.arange(n))
         inp, n = oracle_sample(widx, step_s=12.0, host=host_rows)
         rate1, dt1 = oracle_rate(inp)
         cores = host_cores()
-        rate, dt = oracle_rate_cores(inp, cores)
-        cpu = dict(value=rate, unit=UNIT, cores=cores, kind="oracle",
+        parts = []
+        rate, dt = oracle_rate_cores(inp, cores, parts)
+        cpu = dict(value=rate, unit=UNIT, cores=cores, kind="oracle", cpu_model=cpu_model(),
                    sample=f"first {n} of {B} sequences of this workload "
                           f"({int(np.sum(inp['K']))} positions) cut into {cores} shards of "
                           f"sequences run at once on {cores} threads ({platform.machine()}), "
                           f"{dt:.2f} s",
                    single_thread=dict(value=rate1, seconds=round(dt1, 2)))
+        parity = _parity(parts, out_t.cpu().numpy()[:n], nacc[:n])
+
+    # ---- the other workloads of the set, timed the same way (rank 0, N=1) ----
+    others = None
+    if world == 1 and widx == 4 and args.sequences is None and not args.no_other_workloads:
+        del d, call_args, ws, out_t, out_n
+        torch.cuda.empty_cache()
+        others = {}
+        for key in ("0", "0-toy", "1", "2", "3"):
+            if key == "0-toy":
+                dw = _host_to_device(W.make_toy(200_000, seed=1000), dev)
+            elif key == "0":
+                dw = _host_to_device(W.make_spec_host(0), dev)
+            else:
+                dw = W.make_device(int(key), dev)
+            name = ("the p/q toy pair x200000 K=1 V=5 fp32 T=1" if key == "0-toy"
+                    else WORKLOAD_TEXT[int(key)])
+            others[key] = _time_workload(sv, dw, name, max(5, args.steps // 2), flush, stream, peaks)
+            del dw
+            torch.cuda.empty_cache()
 
     if rank == 0:
         line = dict(
@@ -413,7 +466,7 @@ def run_ours(args):
             scaling="weak", vs_baseline=None, dtype="f32", data="synthetic",
             config=dict(workload=WORKLOAD_TEXT[widx] if args.sequences is None
                         else f"first {B} sequences of: {WORKLOAD_TEXT[widx]}",
-                        bench_workload=widx, logits=d["dtype"],
+                        bench_workload=widx, logits=ldtype,
                         B=B, Kmax=Kmax, V=V, positions_per_step=pos_per_step,
                         l2="flushed before every step (1 GiB write, > 2x L2)", parallelism=f"dp{world}"),
             roofline=roofline, cpu_baseline=cpu, e2e=e2e, gpu_launches=args.steps,
@@ -426,7 +479,7 @@ def run_ours(args):
                                 gbs=round(bytes_all / (ms_all / 1e3) / 1e9, 1),
                                 frac=round(bytes_all / (ms_all / 1e3) / 1e9 / peaks["hbm_gbs"], 4)),
                 device_errors=errs, kernel_source_sha256_16=_source_hash(),
-                geometry=sv.sv_geometry(B, Kmax, V, dcode)))
+                geometry=geometry, parity=parity, workloads=others))
         print(json.dumps(line), flush=True)
     if dist:
         dist.barrier()
@@ -569,6 +622,72 @@ def run_tree(args):
     return 0
 
 
+def _parity(parts, got_t, got_n) -> dict:
+    """The GPU's outputs on the oracle's sample against the oracle's: hard
+    mismatches (outside the oracle's tie flag, must be 0), the oracle's ties
+    (a uniform within 1e-6 of a threshold or CDF boundary) and the ties on
+    which the two differ."""
+    ref_t = np.concatenate([p["out_tokens"] for p in parts])
+    ref_n = np.concatenate([p["num_accepted"] for p in parts])
+    tie = np.concatenate([p["tie"] for p in parts])
+    bad = (ref_n != got_n) | np.any(ref_t != got_t, axis=1)
+    return dict(sequences_checked=int(len(tie)), hard_mismatch=int((bad & ~tie).sum()),
+                ties=int(tie.sum()), tie_mismatch=int((bad & tie).sum()))
+
+
+def _host_to_device(inp, dev) -> dict:
+    """A host-generated workload (numpy) on the device, in the layout
+    make_device returns."""
+    import torch
+    out = dict(inp)
+    for k in ("target", "draft"):
+        a = np.ascontiguousarray(inp[k])
+        t = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16) if inp["dtype"] == "bf16" \
+            else torch.from_numpy(a.astype(np.float32))
+        out[k] = t.to(dev)
+    out["tokens"] = torch.from_numpy(np.ascontiguousarray(inp["tokens"], np.int32)).to(dev)
+    out["uniforms"] = torch.from_numpy(np.ascontiguousarray(inp["uniforms"], np.float32)).to(dev)
+    out["temperature"] = torch.from_numpy(np.ascontiguousarray(inp["temperature"], np.float32)).to(dev)
+    out["temperature_host"] = np.asarray(inp["temperature"], np.float32)
+    return out
+
+
+def _time_workload(sv, d, name, steps, flush, stream, peaks) -> dict:
+    """One workload of the set through spec_verify_ws, timed as the headline
+    (L2 flushed before every step, CUDA events on the launching stream)."""
+    import torch
+    B, Kmax, V = d["B"], d["Kmax"], d["V"]
+    K = np.asarray(d["K"], np.int32)
+    dcode = sv.SV_DTYPE_BF16 if d["dtype"] == "bf16" else sv.SV_DTYPE_F32
+    ws = sv.Workspace(B, Kmax, V, dcode, d["target"].device)
+    out_t = torch.empty((B, Kmax + 1), dtype=torch.int32, device=d["target"].device)
+    out_n = torch.empty((B,), dtype=torch.int32, device=d["target"].device)
+    args = (d["target"], d["draft"], d["tokens"], d["uniforms"], d["temperature"], K)
+    for _ in range(3):
+        flush.fill_(1)
+        sv.spec_verify_ws(*args, ws, out_tokens=out_t, out_num_accepted=out_n)
+    torch.cuda.synchronize()
+    evs = []
+    for _ in range(steps):
+        flush.fill_(1)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        sv.spec_verify_ws(*args, ws, out_tokens=out_t, out_num_accepted=out_n)
+        e1.record(stream)
+        evs.append((e0, e1))
+    torch.cuda.synchronize()
+    times = [a.elapsed_time(b) for a, b in evs]
+    med = statistics.median(times)
+    nacc = out_n.cpu().numpy()
+    need = W.bytes_needed(K, d["temperature_host"], nacc, V, d["dtype"], Kmax)
+    gbs = need / (med / 1e3) / 1e9
+    return dict(workload=name, B=B, Kmax=Kmax, V=V, logits=d["dtype"], steps=steps, ms_median=round(med, 5),
+                ms_min=round(min(times), 5), positions_per_s=float(K.sum()) / (med / 1e3),
+                bytes_needed=int(need), gbs=round(gbs, 1), frac=round(gbs / peaks["hbm_gbs"], 4),
+                mean_accepted=float(np.mean(nacc)), device_errors=sv.sv_workspace_errors(ws),
+                geometry=sv.sv_geometry(B, Kmax, V, dcode))
+
+
 def _rows_to_host(d, seqs):
     import torch
     idx = torch.as_tensor(np.asarray(seqs), device=d["target"].device, dtype=torch.long)
@@ -592,6 +711,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", type=int, default=4, choices=[0, 1, 2, 3, 4])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-other-workloads", action="store_true",
+                    help="time only the selected workload (the default run also times "
+                         "workloads 0-3 and the 200k toy pair into detail.workloads)")
     ap.add_argument("--sequences", type=int, default=None,
                     help="the workload's first N sequences only (profiling captures)")
     ap.add_argument("--op", choices=["verify", "sample", "tree"], default="verify",

@@ -58,7 +58,7 @@
 extern "C" {
 #endif
 
-#define SV_ABI_VERSION 2
+#define SV_ABI_VERSION 3
 /* Largest per-sequence draft count: one warp ballot covers the accept bits. */
 #define SV_K_MAX 32
 
@@ -138,6 +138,15 @@ typedef struct {
  *                   draft_logits [sum_b K[b]][V] with sequence b's rows from
  *                   row sum_{c<b} K[c].  Tokens, uniforms and outputs keep
  *                   their padded layouts.
+ *   expire_copy_waits  testing only; 0 in normal use.  1: every bounded wait
+ *                   for a row's copy into shared memory gives up before its
+ *                   first poll, as a wait that ran out would.  This exercises
+ *                   the timeout path: the rows of the affected sequences are
+ *                   poisoned (their outputs -1), the workspace error word is
+ *                   set (sv_workspace_errors returns SV_ERR_TIMEOUT), and the
+ *                   copies already issued still land and are waited for, with
+ *                   the normal bound, before the kernel exits.  Nothing faults
+ *                   or hangs; the next call on the workspace is unaffected.
  * Tuning options change only the fp32 summation grouping: results agree
  * with the automatic geometry except within the rounding of those sums.
  */
@@ -149,6 +158,7 @@ typedef struct {
     sv_stats* stats;
     int32_t* kv_len;
     int32_t packed_logits;
+    int32_t expire_copy_waits;
 } sv_options;
 
 /* Human-readable name of a status code (static storage). */
@@ -235,8 +245,7 @@ sv_status spec_verify(const void* target_logits, const void* draft_logits, sv_dt
  * whose sv_workspace_size(B, Kmax, V, dtype) exceeds SV_STATIC_SCRATCH_BYTES
  * return SV_ERR_NO_MEMORY before any work is queued.  Nothing in the array
  * needs to start at zero: each call uploads the header it uses (error word,
- * claim counter, per-row decisions, K and the claim order) before its kernels
- * run.  The per-call header is assembled in a static host array.
+ * claim counter, K and the claim order) before its kernel runs.  The per-call header is assembled in a static host array.
  *
  * Set-up: the first call on a device resolves the array's address on that
  * device (cudaGetSymbolAddress, with the device current) and sets kernel

@@ -52,7 +52,7 @@ class SVOptions(ctypes.Structure):
     _fields_ = [("diag", SVDiag), ("verify_all", ctypes.c_int32),
                 ("chunks_per_cta", ctypes.c_int32), ("chunks_per_warp", ctypes.c_int32),
                 ("stats", ctypes.c_void_p), ("kv_len", ctypes.c_void_p),
-                ("packed_logits", ctypes.c_int32)]
+                ("packed_logits", ctypes.c_int32), ("expire_copy_waits", ctypes.c_int32)]
 
 
 STATS_FIELDS = ("sequences", "invalid", "tested", "accepted", "committed", "near_ties")
@@ -312,11 +312,13 @@ def spec_verify_ex(target, draft, draft_tokens, uniforms, temperature, K, worksp
                    diag: dict | None = None, verify_all: bool = False, chunks_per_cta: int = 0,
                    chunks_per_warp: int = 0, out_tokens=None,
                    out_num_accepted=None, stream=None, stats: "Stats | None" = None,
-                   kv_len=None, packed: bool = False):
+                   kv_len=None, packed: bool = False, expire_copy_waits: bool = False):
     """spec_verify_ex; ``diag`` maps p_x / q_x / resid_mass / final_row to tensors,
     ``stats`` accumulates the call's counters, ``kv_len`` (int32 [B] CUDA
     tensor) is advanced in place by 1 + n_b for every valid sequence; ``packed``
-    takes target [sum(K+1), V] and draft [sum(K), V] packed by K."""
+    takes target [sum(K+1), V] and draft [sum(K), V] packed by K;
+    ``expire_copy_waits`` (testing only) makes every bounded copy wait give up
+    at once, to exercise the timeout path."""
     k, kp, B, Kmax, V = _common(target, draft, draft_tokens, uniforms, temperature, K)
     out_tokens, out_num_accepted = _outputs(B, Kmax, target.device, out_tokens, out_num_accepted)
     opt = SVOptions()
@@ -335,6 +337,7 @@ def spec_verify_ex(target, draft, draft_tokens, uniforms, temperature, K, worksp
         _require(kv_len, "kv_len")
         opt.kv_len = kv_len.data_ptr()
     opt.packed_logits = 1 if packed else 0
+    opt.expire_copy_waits = 1 if expire_copy_waits else 0
     sp, _ = _stream(stream)
     st = _load().spec_verify_ex(_dptr(target), _dptr(draft), _dtype_code(target),
                                 _dptr(draft_tokens), _dptr(uniforms), _dptr(temperature), B, kp, V,

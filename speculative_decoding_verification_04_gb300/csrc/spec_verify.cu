@@ -13,9 +13,10 @@
 //  * issoh.co.jp "Speculative Decoding（投機的デコーディング）とは？…", section
 //    受理・棄却の規則と出力分布が変わらない理由, steps 1-5.
 //
-// One call = one small host-to-device copy (zeroed counters, the per-sequence
-// K and the claim order) + one launch of the persistent cluster kernel
-// (sv_sweep.cuh), which also draws the tokens and writes the outputs.
+// One call = a 16-byte memset of the error word and the claim counter on the
+// stream + one launch of the persistent cluster kernel (sv_sweep.cuh), which
+// reads the rest of the per-call header (K, the claim order) from a pinned,
+// device-mapped host buffer, draws the tokens and writes the outputs.
 #include <cuda_runtime.h>
 #include <string.h>
 
@@ -415,7 +416,8 @@ static sv_status check_args(const Call& c, int* kmax_out)
 // word and claim counter are reset on the device, by a memset on the
 // stream.  An event recorded after each launch guards a buffer's reuse, so a
 // call blocks only if the GPU is kHeaderSlots calls behind.  The buffers live
-// as long as the thread (they are small: the header is B * 16 bytes and up).
+// as long as the thread (they are small: the header is B * 16 bytes and up)
+// and are released when it exits, once the kernels reading them are done.
 constexpr int kHeaderSlots = 16;
 struct HeaderSlot {
     unsigned char* buf = nullptr;
@@ -427,6 +429,18 @@ struct HeaderSlot {
 struct HeaderRing {
     HeaderSlot slot[kHeaderSlots];
     int next = 0;
+    ~HeaderRing()
+    {
+        for (HeaderSlot& s : slot) {
+            if (s.used && s.done)
+                (void)cudaEventSynchronize(s.done);   // a kernel may still read the buffer
+            if (s.buf)
+                (void)cudaFreeHost(s.buf);
+            if (s.done)
+                (void)cudaEventDestroy(s.done);
+            s = HeaderSlot{};
+        }
+    }
 };
 static thread_local HeaderRing tl_header[64];
 
@@ -478,12 +492,15 @@ static HeaderSlot* header_slot(int dev, size_t need, sv_status* st)
 // header at every replay, so each capture takes a pinned slot of its own that
 // is never written again (kept until the process ends).  Slots are allocated
 // by ordinary calls (allocation is not allowed during a capture), so that a
-// few of the size in use are always free.
+// few of the size in use are always free.  The spare pool is bounded: when
+// larger slots are added, the smallest spares beyond kCaptureSpareMax go
+// (no kernel reads a spare slot).
 struct CapturePool {
     std::vector<HeaderSlot*> free_slots;   // allocated, not yet taken by a capture
 };
 static CapturePool g_capture[64];
 constexpr int kCaptureSpare = 4;
+constexpr int kCaptureSpareMax = 8;
 
 static void reserve_capture_slots(int dev, size_t need)
 {
@@ -492,6 +509,22 @@ static void reserve_capture_slots(int dev, size_t need)
     int fit = 0;
     for (HeaderSlot* h : fs)
         fit += h->cap >= need ? 1 : 0;
+    if (fit >= kCaptureSpare)
+        return;
+    while ((int)fs.size() + (kCaptureSpare - fit) > kCaptureSpareMax) {
+        size_t k_min = 0;   // the smallest spare that is too small for this shape
+        bool found = false;
+        for (size_t k = 0; k < fs.size(); ++k)
+            if (fs[k]->cap < need && (!found || fs[k]->cap < fs[k_min]->cap)) {
+                k_min = k;
+                found = true;
+            }
+        if (!found)
+            break;
+        (void)cudaFreeHost(fs[k_min]->buf);
+        delete fs[k_min];
+        fs.erase(fs.begin() + (long)k_min);
+    }
     for (; fit < kCaptureSpare; ++fit) {
         HeaderSlot* h = new HeaderSlot;
         const size_t cap = std::max(need, (size_t)4096);
@@ -570,8 +603,9 @@ static sv_status run(const Call& c, int kmax, const sv_options* opt, void* ws, s
     if (want_diag && ((dg->p_x == nullptr) != (dg->q_x == nullptr)))
         return SV_ERR_INVALID_ARG;   // p_x and q_x are written together
 
-    // Header: zeroed error word, claim counter and decisions; K; the claim
-    // order (sequences by K, longest first, so the tail holds short ones).
+    // Header: zeroed error word and claim counter; K; the claim order
+    // (sequences by K, longest first, so the tail holds short ones); the
+    // packed row starts.
     thread_local std::vector<unsigned char> hdr_tls;
     unsigned char* hdr = host_header;
     HeaderSlot* slot = nullptr;
@@ -679,6 +713,7 @@ static sv_status run(const Call& c, int kmax, const sv_options* opt, void* ws, s
     a.want_stats = (opt && opt->stats) ? 1 : 0;
     a.stats = a.want_stats ? reinterpret_cast<unsigned long long*>(opt->stats) : nullptr;
     a.want_kv = (opt && opt->kv_len) ? 1 : 0;
+    a.expire_waits = (opt && opt->expire_copy_waits) ? 1 : 0;
     a.kv_len = a.want_kv ? opt->kv_len : nullptr;
 
     const cudaError_t e = c.dtype == SV_DTYPE_BF16 ? launch_nv<__nv_bfloat16>(a, g, host_rows, stream, dev)
@@ -876,6 +911,8 @@ sv_status spec_verify_ex(const void* target_logits, const void* draft_logits, sv
     if (options && ((((uintptr_t)options->stats) & 7) || (((uintptr_t)options->kv_len) & 3)))
         return SV_ERR_INVALID_ARG;   // 64-bit counters, 32-bit lengths
     if (options && (options->packed_logits < 0 || options->packed_logits > 1))
+        return SV_ERR_INVALID_ARG;
+    if (options && (options->expire_copy_waits < 0 || options->expire_copy_waits > 1))
         return SV_ERR_INVALID_ARG;
     if (options && options->packed_logits) {
         long long rows = 0;   // row indices of the packed arrays must fit 32 bits

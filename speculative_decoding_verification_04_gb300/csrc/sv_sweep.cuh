@@ -20,7 +20,8 @@
 // first).
 //
 // Per row, each warp makes one pass over its slice, from shared memory
-// straight into registers:
+// straight into registers (the chunk loops are not unrolled: the smaller loop
+// body ran workload 4 3% and workload 2 7% faster):
 //   greedy row       lane max (packed bf16x2 / three-input fp32 max) and the
 //                    lowest index holding it;
 //   tested sampling  lane-online max and sum of exp2((l - m) log2(e)/T) of the
@@ -201,12 +202,13 @@ __device__ __forceinline__ Tok tok_of(const Args& a, const Row& r, const SeqVals
     return t;
 }
 
-// The logits at the proposed token: the decision needs them, and a tested
-// row's pass weighs its logits against them.
+// The logits at the proposed token: a tested sampling row's pass weighs its
+// logits against them, and its decision needs them.  Greedy rows need
+// neither (loading them anyway made their pass wait for the load).
 template <typename T>
 __device__ __forceinline__ void tok_logits(const Args& a, const Row& r, Tok& t)
 {
-    if (!t.ok || !(r.flags & kFTest))
+    if (!t.ok || !(r.flags & kFTest) || (r.flags & kFGreedy))
         return;
     const size_t trow = (size_t)r.tb + r.i;
     t.lt = Elem<T>::load_raw(static_cast<const T*>(a.tgt) + trow * (size_t)a.V + t.x);
@@ -925,9 +927,11 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
         }
         pending = true;
     };
-    // wait for the slot fill (whole warp); false if any lane gave up
+    // wait for the slot fill (whole warp); false if any lane gave up (at
+    // once when the caller asked for expired waits, to test this path)
+    const uint32_t slot_spins = a.expire_waits ? 0u : kWaitSpins;
     auto wait_slot = [&]() -> bool {
-        const bool ok = mbar_wait_bounded(bar, uses & 1u, kWaitSpins);
+        const bool ok = mbar_wait_bounded(bar, uses & 1u, slot_spins);
         const bool all = !__any_sync(kFull, !ok);
         if (all) {
             pending = false;
@@ -1025,22 +1029,28 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
             float gm = -INFINITY;
             int gi = INT_MAX;
             if (have) {
+                // the lane's maximum and the first chunk holding it (selects,
+                // no branch: a search inside the loop ran whenever any lane's
+                // maximum grew, which is nearly every chunk), then one search
+                // of that chunk for the lowest element holding it
+                int gj = -1;
+#pragma unroll 1
                 for (int j = 0; j < kwm; ++j) {
                     uint4 tv[NV];
                     load_chunk<T, NV>(slot_t + (size_t)j * CH, lane, tv);
                     const float cm = LN::max(tv);
-                    if (cm > gm) {   // strictly greater: an earlier index keeps a tie
-                        const int gbase = e0 + j * CH;
-                        int found = INT_MAX;
+                    const bool up = cm > gm;   // strictly greater: an earlier chunk keeps a tie
+                    gj = up ? j : gj;
+                    gm = up ? cm : (cm != cm ? cm : gm);
+                }
+                if (gj >= 0 && gm == gm) {
+                    uint4 tv[NV];
+                    load_chunk<T, NV>(slot_t + (size_t)gj * CH, lane, tv);
+                    const int gbase = e0 + gj * CH;
 #pragma unroll
-                        for (int e = NV * E - 1; e >= 0; --e)   // the lowest match wins
-                            if (LN::elem(tv, e) == cm)
-                                found = gbase + ((e / E) * 32 + lane) * E + (e % E);
-                        gm = cm;
-                        gi = found;
-                    } else if (cm != cm) {
-                        gm = cm;
-                    }
+                    for (int e = NV * E - 1; e >= 0; --e)   // the lowest match wins
+                        if (LN::elem(tv, e) == gm)
+                            gi = gbase + ((e / E) * 32 + lane) * E + (e % E);
                 }
             }
             const float m = warp_max_nan(gm);
@@ -1051,7 +1061,7 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
             // warp's sums share the reference, so the partials simply add
             float st = 0.0f, sd = 0.0f;
             if (have) {
-#pragma unroll 2
+#pragma unroll 1
                 for (int j = 0; j < kwm; ++j) {
                     uint4 v[NV];
                     load_chunk<T, NV>(slot_t + (size_t)j * CH, lane, v);
@@ -1068,6 +1078,7 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
             // weights against the running lane maxima
             float mt = -INFINITY, st = 0.0f, md = -INFINITY, sd = 0.0f;
             if (have) {
+#pragma unroll 1
                 for (int j = 0; j < kwm; ++j) {
                     uint4 tv[NV], dv[NV];
                     load_chunk<T, NV>(slot_t + (size_t)j * CH, lane, tv);
@@ -1095,6 +1106,7 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
             float mm = -INFINITY, acc = 0.0f, cmp = 0.0f;
             if (have) {
                 float lm = -INFINITY;
+#pragma unroll 1
                 for (int j = 0; j < kwm; ++j) {
                     uint4 tv[NV];
                     load_chunk<T, NV>(slot_t + (size_t)j * CH, lane, tv);
@@ -1102,6 +1114,7 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
                 }
                 mm = warp_max_nan(lm);
                 const float mu = mm == -INFINITY ? 0.0f : mm;
+#pragma unroll 1
                 for (int j = 0; j < kwm; ++j) {
                     uint4 tv[NV];
                     load_chunk<T, NV>(slot_t + (size_t)j * CH, lane, tv);
@@ -1260,6 +1273,7 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
         float2 wtot2 = make_float2(0.0f, 0.0f);   // and warp j + 32's
         if (resid_pass) {
             float rs_s = 0.0f, rs_c = 0.0f, ps_s = 0.0f, ps_c = 0.0f;
+#pragma unroll 1
             for (int j = 0; j < kwm; ++j) {
                 uint4 tv[NV], dv[NV];
                 load_chunk<T, NV>(slot_t + (size_t)j * CH, lane, tv);
@@ -1371,6 +1385,7 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
                     // element.  Zero residual mass: p's strip sums are made
                     // first (the residual pass kept only p's warp totals).
                     if (!bonus && !use_r) {
+#pragma unroll 1
                         for (int j = 0; j < kwm; ++j) {
                             uint4 tv[NV];
                             load_chunk<T, NV>(slot_t + (size_t)j * CH, lane, tv);

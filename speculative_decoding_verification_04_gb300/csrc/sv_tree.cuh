@@ -380,24 +380,26 @@ __global__ void __maxnreg__(kMaxRegs) sv_tree_kernel(const TreeArgs a)
         // ---- pass: the argmax, or the (max, sum) of the target and draft rows ----
         float4 part = make_float4(-INFINITY, __int_as_float(INT_MAX), -INFINITY, 0.0f);
         if (greedy) {
+            // the lane's maximum and the first chunk holding it (selects, no
+            // branch), then one search of that chunk for the lowest element
             float gm = -INFINITY;
-            int gi = INT_MAX;
+            int gi = INT_MAX, gj = -1;
             for (int j = 0; have && j < kwm; ++j) {
                 uint4 tv[NV];
                 load_chunk<T, NV>(slot_t + (size_t)j * CH, lane, tv);
                 const float cm = LN::max(tv);
-                if (cm > gm) {
-                    const int gbase = e0 + j * CH;
-                    int found = INT_MAX;
+                const bool up = cm > gm;   // strictly greater: an earlier chunk keeps a tie
+                gj = up ? j : gj;
+                gm = up ? cm : (cm != cm ? cm : gm);
+            }
+            if (gj >= 0 && gm == gm) {
+                uint4 tv[NV];
+                load_chunk<T, NV>(slot_t + (size_t)gj * CH, lane, tv);
+                const int gbase = e0 + gj * CH;
 #pragma unroll
-                    for (int e = NV * E - 1; e >= 0; --e)
-                        if (LN::elem(tv, e) == cm)
-                            found = gbase + ((e / E) * 32 + lane) * E + (e % E);
-                    gm = cm;
-                    gi = found;
-                } else if (cm != cm) {
-                    gm = cm;
-                }
+                for (int e = NV * E - 1; e >= 0; --e)   // the lowest match wins
+                    if (LN::elem(tv, e) == gm)
+                        gi = gbase + ((e / E) * 32 + lane) * E + (e % E);
             }
             const float m = warp_max_nan(gm);
             part = make_float4(m, __int_as_float(__reduce_min_sync(kFull, gm == m ? gi : INT_MAX)), -INFINITY,

@@ -40,7 +40,7 @@ def test_status_strings_and_version():
                        (3, "SV_ERR_UNSUPPORTED"), (4, "SV_ERR_NO_MEMORY"), (5, "SV_ERR_TIMEOUT")]:
         assert sv.sv_status_string(code) == name
     assert sv.sv_status_string(99) == "SV_UNKNOWN_STATUS"
-    assert sv.sv_abi_version() == 2
+    assert sv.sv_abi_version() == 3
 
 
 def test_limits_and_workspace_sizes():
@@ -136,7 +136,8 @@ def test_sample_entry_validation():
 
 def test_option_pointer_alignment_is_checked():
     """sv_stats holds 64-bit counters and kv_len 32-bit lengths: misaligned
-    option pointers are refused before any work."""
+    option pointers are refused before any work, as are flag options outside
+    {0, 1}."""
     lib = sv.library()
     P = lambda: ctypes.c_void_p(0x1000)  # noqa: E731
     k = np.asarray([1, 2], np.int32)
@@ -146,6 +147,12 @@ def test_option_pointer_alignment_is_checked():
         st = lib.spec_verify_ex(P(), P(), 0, P(), P(), P(), 2, k.ctypes.data_as(ctypes.c_void_p), 10,
                                 P(), P(), ctypes.byref(opt), ctypes.c_void_p(0x100000), 1 << 20, None)
         assert st == sv.SV_ERR_INVALID_ARG, field
+    for field, value in (("packed_logits", 2), ("expire_copy_waits", -1), ("expire_copy_waits", 2)):
+        opt = sv.SVOptions()
+        setattr(opt, field, value)
+        st = lib.spec_verify_ex(P(), P(), 0, P(), P(), P(), 2, k.ctypes.data_as(ctypes.c_void_p), 10,
+                                P(), P(), ctypes.byref(opt), ctypes.c_void_p(0x100000), 1 << 20, None)
+        assert st == sv.SV_ERR_INVALID_ARG, (field, value)
 
 
 def test_tree_entry_validation():

@@ -7,6 +7,7 @@ import pytest
 
 torch = pytest.importorskip("torch")
 
+import oracle  # noqa: E402
 import speculative_decoding_verification_04_gb300 as sv  # noqa: E402
 import workloads as W  # noqa: E402
 from helpers import compare, dtype_code, oracle_ref, run_gpu, to_device  # noqa: E402
@@ -37,7 +38,7 @@ def test_spec_sample_is_the_oracles_draw_from_p(dev, dtype, V, B):
     logits = d["target"].view(B, V)
     out = sv.spec_sample(logits, d["uniforms"].view(B), d["temperature"])
     got = out.cpu().numpy().astype(np.int32)
-    compare(ref, got.reshape(B, 1), np.zeros(B, np.int32))
+    compare(ref, got.reshape(B, 1), np.zeros(B, np.int32), inp=inp)
 
 
 def test_spec_sample_marks_unusable_rows(dev):
@@ -58,29 +59,64 @@ def test_spec_sample_marks_unusable_rows(dev):
     assert np.array_equal(got[keep][ok], ref["out_tokens"][keep, 0][ok])
 
 
-def _implied_counts(K, n):
+def _oracle_counts(inp: dict, ref: dict) -> dict:
+    """The sv_stats counters the oracle's walk implies.  tested: the positions
+    up to and including the first rejection (n_b, plus one when n_b < K_b);
+    accepted: sum n_b; committed: sum (n_b + 1); over valid sequences.
+    near_ties: the walked sampling tests whose uniform lies within 1e-6 of
+    p(x)/q(x), from the oracle's per-position probabilities (fp64)."""
+    K = np.asarray(inp["K"])
+    n = ref["num_accepted"]
     valid = n >= 0
     tested = np.where(valid, n + (n < K), 0)
+    px, qx, _ = oracle.position_probs(inp["target"], inp["draft"], inp["dtype"], inp["tokens"],
+                                      inp["temperature"], inp["K"])
+    near = 0
+    for b in np.flatnonzero(valid & (np.asarray(inp["temperature"]) > 0)):
+        for i in range(int(tested[b])):
+            if qx[b, i] > 0 and abs(float(inp["uniforms"][b, i]) - px[b, i] / qx[b, i]) < 1e-6:
+                near += 1
     return dict(sequences=int(valid.sum()), invalid=int((~valid).sum()), tested=int(tested.sum()),
-                accepted=int(np.where(valid, n, 0).sum()), committed=int(np.where(valid, n + 1, 0).sum()))
+                accepted=int(np.where(valid, n, 0).sum()), committed=int(np.where(valid, n + 1, 0).sum()),
+                near_ties=near)
 
 
-def test_stats_count_the_walked_positions(dev):
-    """The counters agree with what the outputs imply (tested = n_b, plus the
-    rejected position when n_b < K_b; committed = n_b + 1), are the same
-    under verify_all (rows after the stop are not counted), and accumulate."""
-    B = 40
-    inp = W.make_host(B, W.configs.ragged_k(5, B), 6000, "bf16", 2.0, 0.6,
-                      np.where(np.arange(B) % 3 == 0, 0.0, 1.0).astype(np.float32), seed=17)
+def test_stats_match_the_oracles_walk(dev):
+    """The per-call counters equal what the oracle's walk implies (counts of
+    tested and accepted positions as the acceptance rate is counted on the
+    pages: r-jc.jp, section 投機的デコーディングを実装して受理率と速度を実測,
+    decisions after the first rejection are not taken).  Uniforms are planted
+    5e-7 below or above p/q at position 0 of the sampling sequences whose p/q
+    lies below 1, so near_ties is nonzero, and must be exact; the planted
+    sequences are the oracle's ties.  The counts are the same under
+    verify_all (rows after the stop do not count), and a second call
+    accumulates."""
+    B, V = 48, 6000
+    temps = np.where(np.arange(B) % 3 == 0, 0.0, 1.0).astype(np.float32)
+    inp = W.make_host(B, W.configs.ragged_k(5, B), V, "bf16", 2.0, 0.6, temps, seed=17)
+    px, qx, _ = oracle.position_probs(inp["target"], inp["draft"], "bf16", inp["tokens"],
+                                      inp["temperature"], inp["K"])
+    planted = []
+    for b in np.flatnonzero(temps > 0):
+        ratio = px[b, 0] / qx[b, 0]
+        if 1e-3 < ratio < 1 - 1e-3:
+            inp["uniforms"][b, 0] = np.float32(ratio + (5e-7 if len(planted) % 2 else -5e-7))
+            planted.append(b)
+    assert len(planted) >= 8
+    ref = oracle_ref(inp)
+    assert ref["tie"][planted].all()
+    want = _oracle_counts(inp, ref)
+    assert want["near_ties"] >= len(planted)
     d = to_device(inp, dev)
-    ws = sv.Workspace(B, int(inp["Kmax"]), 6000, dtype_code("bf16"), dev)
+    ws = sv.Workspace(B, int(inp["Kmax"]), V, dtype_code("bf16"), dev)
     st = sv.Stats(dev)
     t, n = run_gpu(d, "ex", workspace=ws, stats=st)
+    # the walks agree everywhere, the planted decisions included (5e-7 is far
+    # beyond the fp32 rounding of p/q at this size)
+    assert np.array_equal(n, ref["num_accepted"]) and np.array_equal(t, ref["out_tokens"])
     got = st.read()
-    want = _implied_counts(np.asarray(inp["K"]), n)
     for k, v in want.items():
         assert got[k] == v, (k, got[k], v)
-    assert 0 <= got["near_ties"] <= got["tested"]
     st_all = sv.Stats(dev)
     t2, n2 = run_gpu(d, "ex", workspace=ws, stats=st_all, verify_all=True)
     assert np.array_equal(n, n2) and st_all.read() == got
@@ -106,7 +142,7 @@ def test_kv_len_advances_by_committed_tokens(dev):
     valid = n >= 0
     assert np.array_equal(kvh[valid], bh[valid] + 1 + n[valid])
     assert st.read()["invalid"] == 1
-    compare(oracle_ref(inp), t, n)
+    compare(oracle_ref(inp), t, n, inp=inp)
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
@@ -129,7 +165,7 @@ def test_packed_logits_give_the_padded_results(dev, dtype):
     t0, n0 = sv.spec_verify_ex(d["target"], d["draft"], *args, ws)
     torch.cuda.synchronize()
     assert torch.equal(t1, t0) and torch.equal(n1, n0)
-    compare(oracle_ref(inp), t1.cpu().numpy(), n1.cpu().numpy())
+    compare(oracle_ref(inp), t1.cpu().numpy(), n1.cpu().numpy(), inp=inp)
 
 
 def test_cuda_graph_replays_the_verification(dev):
@@ -159,7 +195,7 @@ def test_cuda_graph_replays_the_verification(dev):
     on.fill_(-7)
     g.replay()
     torch.cuda.synchronize()
-    compare(oracle_ref(inp1), ot.cpu().numpy(), on.cpu().numpy())
+    compare(oracle_ref(inp1), ot.cpu().numpy(), on.cpu().numpy(), inp=inp1)
     # new inputs in the captured buffers; other calls churn the header slots
     d2 = to_device(inp2, dev)
     for key in ("target", "draft", "tokens", "uniforms", "temperature"):
@@ -169,7 +205,7 @@ def test_cuda_graph_replays_the_verification(dev):
         run_gpu(to_device(other, dev), "ws")
     g.replay()
     torch.cuda.synchronize()
-    compare(oracle_ref(inp2), ot.cpu().numpy(), on.cpu().numpy())
+    compare(oracle_ref(inp2), ot.cpu().numpy(), on.cpu().numpy(), inp=inp2)
 
 
 def test_host_entry_point_is_refused_under_capture(dev):

@@ -51,7 +51,7 @@ def test_noalloc_matches_workspace_entry_point(case):
     ws = sv.Workspace(B, inp["Kmax"], inp["V"], code, dev)
     ref_t, ref_n = sv.spec_verify_ws(*args, ws)
     ref_t, ref_n = ref_t.cpu().numpy(), ref_n.cpu().numpy()
-    compare(oracle_ref(inp), ref_t, ref_n)
+    compare(oracle_ref(inp), ref_t, ref_n, inp=inp)
     out_t = torch.full((B, inp["Kmax"] + 1), -9, dtype=torch.int32, device=dev)
     out_n = torch.full((B,), -9, dtype=torch.int32, device=dev)
     for _ in range(2):   # two calls in a row: the second reuses the scratch the first left
