@@ -74,7 +74,7 @@ static int n_chunks(int V, int s)
 
 // ---- workspace layout: the per-call header, uploaded by every call ----
 struct WsLayout {
-    size_t err, next_unit, K, order, seq_end, cu_t, cu_d, header_end, total;
+    size_t err, next_unit, ready, K, order, seq_end, cu_t, cu_d, header_end, total;
 };
 
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -88,6 +88,7 @@ static bool ws_layout(int B, int Kmax, int V, sv_dtype dt, WsLayout* L)
     size_t o = 0;
     L->err = o;
     L->next_unit = o + 4;
+    L->ready = o + 8;   // CTAs done copying the mapped header into K and order
     o = align256(o + 16);
     L->K = o;        o = align256(o + (size_t)B * 4);
     L->order = o;    o = align256(o + (size_t)B * 4);
@@ -692,6 +693,15 @@ static sv_status run(const Call& c, int kmax, const sv_options* opt, void* ws, s
     a.next_unit = reinterpret_cast<int*>(base + L.next_unit);
     a.K = reinterpret_cast<const int32_t*>(hbase + L.K);
     a.order = reinterpret_cast<const int32_t*>(hbase + L.order);
+    // the kernel copies K and the order from the mapped header into the
+    // workspace (where the uploaded header already is for pageable staging),
+    // when there are tickets to claim after the first wave: the claims then
+    // read device memory instead of crossing the host link (with no claims
+    // the copy only delayed the first rows: 2 us on a batch of one)
+    a.copy_hdr = (hbase != base && c.B > g.clusters) ? 1 : 0;
+    a.ready = reinterpret_cast<int*>(base + L.ready);
+    a.K_dev = reinterpret_cast<int32_t*>(base + L.K);
+    a.order_dev = reinterpret_cast<int32_t*>(base + L.order);
     {
         const int32_t* ord = reinterpret_cast<const int32_t*>(hdr + L.order);
         const int nf = std::min(g.clusters, kFirstUnits);   // clusters <= B

@@ -59,6 +59,13 @@ struct Args {
     int* next_unit;        // claim counter of the persistent sweep
     const int32_t* K;
     const int32_t* order;  // sequences in claim order (longest K first)
+    // device copies of K and order in the workspace, filled by the kernel's
+    // CTAs at start when the header is in mapped host memory (copy_hdr); a
+    // lookup reads them once `ready` counts every CTA, else the header
+    int copy_hdr;
+    int* ready;
+    int32_t* K_dev;
+    int32_t* order_dev;
     // ticket c's sequence and its K, c < min(clusters, kFirstUnits): the first
     // wave starts without a claim or a header read
     int32_t first_b[kFirstUnits];

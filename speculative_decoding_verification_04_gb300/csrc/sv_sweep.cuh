@@ -236,6 +236,30 @@ __device__ __forceinline__ TokF shfl_tok(const Tok& t)
     return o;
 }
 
+// The per-call header's K and claim order: the device copies once every CTA
+// has written its slice (`ok`, sticky per thread, set by one acquire load),
+// else the pinned, device-mapped header itself (a round trip over the host
+// link).  Both hold the same values, so either read is correct.
+__device__ __forceinline__ bool header_on_device(const Args& a, bool& ok)
+{
+    if (!ok && a.copy_hdr) {
+        int v;
+        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(a.ready) : "memory");
+        ok = v >= (int)gridDim.x;
+    }
+    return ok;
+}
+
+__device__ __forceinline__ int header_order(const Args& a, int t, bool& ok)
+{
+    return header_on_device(a, ok) ? __ldcg(a.order_dev + t) : __ldg(a.order + t);
+}
+
+__device__ __forceinline__ int header_K(const Args& a, int b, bool& ok)
+{
+    return header_on_device(a, ok) ? __ldcg(a.K_dev + b) : __ldg(a.K + b);
+}
+
 // Claims (one thread): a ticket now, its sequence later (the ticket's value
 // is not waited for until the sequence is needed).  The first wave's tickets
 // 0 .. n_clusters - 1 are the clusters' own; the counter hands out the rest.
@@ -245,20 +269,20 @@ __device__ __forceinline__ int claim_ticket(const Args& a, int n_clusters)
     return atomicAdd(a.next_unit, 1) + n_clusters;
 }
 
-__device__ __forceinline__ int ticket_unit(const Args& a, int t)
+__device__ __forceinline__ int ticket_unit(const Args& a, int t, bool& ok)
 {
     if (t < 0 || t >= a.B)
         return -1;
-    const int b = __ldg(a.order + t);
+    const int b = header_order(a, t, ok);
     return (b >= 0 && b < a.B) ? b : -1;
 }
 
 // The same in two steps, so that the order lookup's latency hides behind
 // other work: the load (at a clamped index, always in bounds; B >= 1), then
 // the range checks once its value is needed.
-__device__ __forceinline__ int ticket_load(const Args& a, int t)
+__device__ __forceinline__ int ticket_load(const Args& a, int t, bool& ok)
 {
-    return __ldg(a.order + min(max(t, 0), a.B - 1));
+    return header_order(a, min(max(t, 0), a.B - 1), ok);
 }
 
 __device__ __forceinline__ int ticket_check(const Args& a, int t, int b)
@@ -285,18 +309,18 @@ __device__ __forceinline__ int seq_drow(const Args& a, int b)
     return a.packed ? __ldg(a.cu_d + b) : b * a.Kmax;
 }
 
-__device__ __forceinline__ UnitPos unit_pos(const Args& a, int b)
+__device__ __forceinline__ UnitPos unit_pos(const Args& a, int b, bool& ok)
 {
-    return UnitPos{b, __ldg(a.K + b), __ldg(a.temp + b), seq_trow(a, b), seq_drow(a, b)};
+    return UnitPos{b, header_K(a, b, ok), __ldg(a.temp + b), seq_trow(a, b), seq_drow(a, b)};
 }
 
 // The first sequence of cluster `cid` (ticket cid): from the launch
 // arguments for the first kFirstUnits clusters, else from the header.
-__device__ __forceinline__ UnitPos first_unit_pos(const Args& a, int cid, int b)
+__device__ __forceinline__ UnitPos first_unit_pos(const Args& a, int cid, int b, bool& ok)
 {
     if (cid < kFirstUnits)
         return UnitPos{b, a.first_K[cid], __ldg(a.temp + b), seq_trow(a, b), seq_drow(a, b)};
-    return unit_pos(a, b);
+    return unit_pos(a, b, ok);
 }
 
 // The sequence's final-draw uniform (slot K_b), sampling sequences only.
@@ -819,14 +843,28 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
         EL::set_neg_inf(slot_t + j);
         EL::set_neg_inf(slot_d + j);
     }
+    // this CTA's slice of the header's K and order, into the workspace
+    if (a.copy_hdr) {
+        const int per = (a.B + (int)gridDim.x - 1) / (int)gridDim.x;
+        const int lo = (int)blockIdx.x * per, hi = min(a.B, lo + per);
+        for (int j = lo + (int)threadIdx.x; j < hi; j += (int)blockDim.x) {
+            a.K_dev[j] = __ldg(a.K + j);
+            a.order_dev[j] = __ldg(a.order + j);
+        }
+    }
     __syncthreads();
+    if (a.copy_hdr && threadIdx.x == 0) {
+        __threadfence();   // the slice before the count that publishes it
+        atomicAdd(a.ready, 1);
+    }
     cluster_arrive();   // every CTA's barriers exist before any peer signals them
     cluster_wait();
 
     // ---- per-warp schedule state (the same in every warp of the cluster) ----
     const int n_clusters = (int)(gridDim.x / (unsigned)C);
     const int cid = (int)(blockIdx.x / (unsigned)C);   // this cluster: ticket cid first
-    const int u0 = cid < kFirstUnits ? a.first_b[cid] : ticket_unit(a, cid);
+    bool hdr_dev = false;   // the header's device copy is complete (sticky)
+    const int u0 = cid < kFirstUnits ? a.first_b[cid] : ticket_unit(a, cid, hdr_dev);
     bool active = u0 >= 0 && u0 < a.B;
     int spare = -1;
     UnitPos spare_pos{0, 0, 0.0f};
@@ -834,7 +872,8 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
     // A cluster claims its next sequence a row ahead (hiding the claim's
     // latency) only while at least two waves of tickets remain; nearer the
     // end it claims when it finishes a sequence, so that the last sequences
-    // go to the clusters that are free first.
+    // go to the clusters that are free first.  (The ticket of a row-ahead
+    // claim is taken when the previous row is issued; see claim_next.)
     int last_t = cid;        // the ticket of the cluster's latest claim
     uint32_t kc = 0;         // claims made between sequences (xbarc phase)
     bool broken = false;     // a slot wait gave up: no more copies, rows poisoned
@@ -843,7 +882,7 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
     Row row = make_row(a, 0, 0, 0, 0.0f, 0, 0);
     SeqVals cur_sv{0, 0.0f}, spare_sv{0, 0.0f};   // the current and the spare sequence's
     if (active) {
-        const UnitPos p0 = first_unit_pos(a, cid, u0);
+        const UnitPos p0 = first_unit_pos(a, cid, u0, hdr_dev);
         row = make_row(a, 0, p0.b, p0.Kb, p0.T, p0.tb, p0.db);
         cur_sv = seq_vals(a, u0, lane);
     }
@@ -986,8 +1025,17 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
         }
     };
 
+    // A cluster claims its next sequence a row ahead.  The ticket (an atomic
+    // on the claim counter) is taken when the row that needs it is issued,
+    // one row before its order lookup: taken at the top of that row, the
+    // lookup's address waited on the atomic's round trip and the claiming
+    // warp started its pass about a microsecond after the others, holding
+    // up every row that carried a claim.
+    bool claim_next = spare < 0 && !exhausted && (long long)last_t + 2LL * n_clusters < (long long)a.B;
     if (active) {
         issue(row);
+        if (writer && lane == 0 && claim_next)
+            ticket = claim_ticket(a, n_clusters);
         tk = tok_of(a, row, cur_sv);
         if (lane == 0) {
             tok_logits<T>(a, row, tk);
@@ -1003,11 +1051,9 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
         const bool draft = (row.flags & kFDraft) != 0;
         const bool usable = (row.flags & kFUsable) != 0;
         const float c = (usable && !greedy) ? log2e_over(row.T) : 0.0f;
-        const bool want_claim = spare < 0 && !exhausted && (long long)last_t + 2LL * n_clusters < (long long)a.B;
+        const bool want_claim = claim_next;   // this row carries a claim (ticket taken)
         if (w == 0 && lane == 0)
             mbar_arrive_expect_tx(smem_addr(&xbar[p]), (uint32_t)P * 16u + (want_claim ? 8u : 0u));
-        if (writer && lane == 0 && want_claim)
-            ticket = claim_ticket(a, n_clusters);
 
         // ---- the slice, then the proposal's logits and the claim's sequence ----
         bool have = false;
@@ -1018,7 +1064,7 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
         }
         int claimed = -1;   // the order lookup now, its checks after the pass
         if (writer && lane == 0 && want_claim)
-            claimed = ticket_load(a, ticket);
+            claimed = ticket_load(a, ticket, hdr_dev);
 
         // ---- one pass over this warp's slice ----
         const float ref_t = EL::widen(__shfl_sync(kFull, tk.lt, 0));
@@ -1257,7 +1303,7 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
             if (spare >= 0)
                 last_t = clv.y;
             if (spare >= 0) {
-                spare_pos = unit_pos(a, spare);   // loads now, used when the unit starts
+                spare_pos = unit_pos(a, spare, hdr_dev);   // loads now, used when the unit starts
                 spare_sv = seq_vals(a, spare, lane);
                 if (!a.packed)
                     prefetch_target(spare * (Kmax + 1));
@@ -1454,7 +1500,7 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
                 int cb = -1, ct = -1;
                 if (writer && lane == 0) {
                     ct = claim_ticket(a, n_clusters);
-                    cb = ticket_unit(a, ct);
+                    cb = ticket_unit(a, ct, hdr_dev);
                 }
                 cb = __shfl_sync(kFull, cb, 0);
                 ct = __shfl_sync(kFull, ct, 0);
@@ -1471,7 +1517,7 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
                 if (nb >= 0 && nb < a.B) {
                     spare = nb;
                     last_t = first[1];
-                    spare_pos = unit_pos(a, nb);
+                    spare_pos = unit_pos(a, nb, hdr_dev);
                     spare_sv = seq_vals(a, nb, lane);
                 } else {
                     exhausted = true;
@@ -1485,6 +1531,9 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
             drawn = false;
         }
         issue(row);   // copies first: the logit loads overlap with them
+        claim_next = spare < 0 && !exhausted && (long long)last_t + 2LL * n_clusters < (long long)a.B;
+        if (writer && lane == 0 && claim_next)
+            ticket = claim_ticket(a, n_clusters);
         tk = tok_of(a, row, cur_sv);
         if (lane == 0) {
             tok_logits<T>(a, row, tk);
