@@ -110,6 +110,7 @@ __device__ float level_pass(const T* slot_t, const T* slot_d, int kwm, int lane,
     constexpr int E = Elem<T>::E;
     constexpr int CH = 32 * NV * E;
     float acc = 0.0f, cmp = 0.0f;
+#pragma unroll 1
     for (int j = 0; j < kwm; ++j) {
         uint4 tv[NV], dv[NV];
         load_chunk<T, NV>(slot_t + (size_t)j * CH, lane, tv);
@@ -218,6 +219,7 @@ __global__ void __maxnreg__(kMaxRegs) sv_tree_kernel(const TreeArgs a)
     const int* first_seq = reinterpret_cast<const int*>(dsm + L.first);
     float4* xbuf = reinterpret_cast<float4*>(dsm + L.xbuf);
     float2* xbuf2 = reinterpret_cast<float2*>(dsm + L.xbuf2);
+    int2* xclaim = reinterpret_cast<int2*>(dsm + L.xclaim);   // [2]: the next tree, sent with a row exchange
     float* stats = reinterpret_cast<float*>(dsm + L.stats) + (size_t)w * KW * 16;
 
     if (lane == 0) {
@@ -247,6 +249,14 @@ __global__ void __maxnreg__(kMaxRegs) sv_tree_kernel(const TreeArgs a)
 
     uint32_t uses = 0, kx = 0, k2 = 0, kc = 0;
     uint32_t kx_claim = 0;   // row exchanges run when the last claim was read
+    // The next tree is claimed a tree ahead: rank 0's writer takes a ticket
+    // when a tree starts and sends it with the tree's first row exchange, so
+    // the claim's round trip and the next root rows' reads overlap the walk
+    // (-2: not known yet; -1: none left).
+    int next_tree = -2;
+    float next_T = 0.0f;   // its temperature (its draft row is prefetched only if > 0)
+    int ticket = -1;       // the writer's ticket for the next tree
+    const int nb_pf = a.aligned ? ((n_el * (int)sizeof(T)) & ~15) / (int)sizeof(T) : 0;
     float inv = 0.0f;        // lane l: 1 / S_{l+1} of the node's residual levels
     bool pending = false, xbroken = false;
     // the current sequence (lane n: node n), set when it starts
@@ -295,18 +305,29 @@ __global__ void __maxnreg__(kMaxRegs) sv_tree_kernel(const TreeArgs a)
         pending = true;
     };
     // a float4 per warp to every CTA; every warp returns the P partials
-    // (lane j: warp j's)
-    auto exchange4 = [&](float4 part) -> float4 {
+    // (lane j: warp j's).  With `claim`, rank 0's writer also sends the next
+    // tree (`claimed`, its lane 0) and every warp reads it into next_tree.
+    auto exchange4 = [&](float4 part, bool claim, int claimed, float claimedT) -> float4 {
         const int p = (int)(kx & 1);
         const uint32_t par4 = (kx >> 1) & 1u;
         ++kx;
         if (w == 0 && lane == 0)
-            mbar_arrive_expect_tx(smem_addr(&xbar[p]), (uint32_t)P * 16u);
-        if (lane < C)
-            st_async_v4(map_to_rank(smem_addr(&xbuf[p * P + g]), (uint32_t)lane), part,
-                        map_to_rank(smem_addr(&xbar[p]), (uint32_t)lane));
+            mbar_arrive_expect_tx(smem_addr(&xbar[p]), (uint32_t)P * 16u + (claim ? 8u : 0u));
+        const int cb = __shfl_sync(kFull, claimed, 0);
+        const float cT = __shfl_sync(kFull, claimedT, 0);
+        if (lane < C) {
+            const uint32_t rb = map_to_rank(smem_addr(&xbar[p]), (uint32_t)lane);
+            st_async_v4(map_to_rank(smem_addr(&xbuf[p * P + g]), (uint32_t)lane), part, rb);
+            if (writer && claim)
+                st_async_v2(map_to_rank(smem_addr(&xclaim[p]), (uint32_t)lane),
+                            make_float2(__int_as_float(cb), cT), rb);
+        }
         if (!mbar_wait_bounded(smem_addr(&xbar[p]), par4, kWaitSpins))
             xbroken = true;
+        if (claim && !xbroken) {
+            next_tree = xclaim[p].x;
+            next_T = __int_as_float(xclaim[p].y);
+        }
         return lane < P ? xbuf[p * P + lane] : make_float4(-INFINITY, __int_as_float(INT_MAX), -INFINITY, 0.0f);
     };
     auto exchange2 = [&](float v) -> float {
@@ -343,6 +364,9 @@ __global__ void __maxnreg__(kMaxRegs) sv_tree_kernel(const TreeArgs a)
     c = (!bad && !greedy) ? log2e_over(Tb) : 0.0f;
     path_l = -1;
     done = false;
+    next_tree = -2;
+    if (writer && lane == 0)
+        ticket = atomicAdd(a.next, 1) + n_clusters;
 
     // ---- the walk: one node per step ----
     int v = 0, len = 0;
@@ -377,13 +401,37 @@ __global__ void __maxnreg__(kMaxRegs) sv_tree_kernel(const TreeArgs a)
         if (__any_sync(kFull, xbroken))
             break;
 
-        // ---- pass: the argmax, or the (max, sum) of the target and draft rows ----
+        // the next tree: rank 0's writer sends it (and its temperature) with
+        // this tree's first row exchange; its ticket was taken at the start
+        const bool claim_now = next_tree == -2;
+        int cl = -1;
+        float clT = 0.0f;
+        if (claim_now && writer && lane == 0) {
+            cl = (ticket >= 0 && ticket < a.B) ? ticket : -1;
+            clT = cl >= 0 ? __ldg(a.temp + cl) : 0.0f;
+        }
+
+        // ---- pass: the argmax; at a sampling node with children the sums of
+        // the target and draft weights against the first child's logits (no
+        // max pass, and every warp's partials share the reference and add;
+        // weighed again against the maxima if a weight overflows); at a leaf
+        // the maximum, then per-strip sums of p's weights against it, which
+        // the draw uses as they are ----
+        const int c1 = kids ? __ffs(kids) - 1 : 0;
+        const float ref_t = EL::widen(__shfl_sync(kFull, klt, c1));
+        const float ref_d = EL::widen(__shfl_sync(kFull, kld, c1));
+        const int x1 = __shfl_sync(kFull, tokn, c1);
+        bool refmode = !greedy && with_d && x1 >= 0 && x1 < V && isfinite(ref_t) && isfinite(ref_d);
+        const bool leaf = !greedy && !with_d;
+        float4 xv;
+        for (int attempt = 0; attempt < 2; ++attempt) {
         float4 part = make_float4(-INFINITY, __int_as_float(INT_MAX), -INFINITY, 0.0f);
         if (greedy) {
             // the lane's maximum and the first chunk holding it (selects, no
             // branch), then one search of that chunk for the lowest element
             float gm = -INFINITY;
             int gi = INT_MAX, gj = -1;
+#pragma unroll 1
             for (int j = 0; have && j < kwm; ++j) {
                 uint4 tv[NV];
                 load_chunk<T, NV>(slot_t + (size_t)j * CH, lane, tv);
@@ -404,8 +452,49 @@ __global__ void __maxnreg__(kMaxRegs) sv_tree_kernel(const TreeArgs a)
             const float m = warp_max_nan(gm);
             part = make_float4(m, __int_as_float(__reduce_min_sync(kFull, gm == m ? gi : INT_MAX)), -INFINITY,
                                0.0f);
+        } else if (refmode) {
+            float st = 0.0f, sd = 0.0f;
+#pragma unroll 1
+            for (int j = 0; have && j < kwm; ++j) {
+                uint4 vv[NV];
+                load_chunk<T, NV>(slot_t + (size_t)j * CH, lane, vv);
+                st += LN::exp_sum(vv, ref_t, c);
+                load_chunk<T, NV>(slot_d + (size_t)j * CH, lane, vv);
+                sd += LN::exp_sum(vv, ref_d, c);
+            }
+            sum_or_special2(st, sd);   // an overflowed weight gives +inf
+            part = make_float4(ref_t, st, ref_d, sd);
+        } else if (leaf) {
+            float lm = -INFINITY, acc = 0.0f, cmp = 0.0f;
+#pragma unroll 1
+            for (int j = 0; have && j < kwm; ++j) {
+                uint4 tv[NV];
+                load_chunk<T, NV>(slot_t + (size_t)j * CH, lane, tv);
+                lm = max_nan(lm, LN::max(tv));
+            }
+            const float mm = warp_max_nan(lm);
+            const float mu = mm == -INFINITY ? 0.0f : mm;
+#pragma unroll 1
+            for (int j = 0; have && j < kwm; ++j) {
+                uint4 tv[NV];
+                load_chunk<T, NV>(slot_t + (size_t)j * CH, lane, tv);
+                float sv[NV];
+                LN::exp_strips(tv, mu, c, sv);
+                strip_partials<NV>(sv, lane, stats + (size_t)j * NV * 4);
+                float v = 0.0f;
+#pragma unroll
+                for (int k = 0; k < NV; ++k)
+                    v += sv[k];
+                float t, e;
+                two_sum(acc, v, t, e);
+                acc = t;
+                cmp += e;
+            }
+            __syncwarp();
+            part = make_float4(mm, sum_or_special(acc + cmp), -INFINITY, 0.0f);
         } else {
             float mt = -INFINITY, st = 0.0f, md = -INFINITY, sd = 0.0f;
+#pragma unroll 1
             for (int j = 0; have && j < kwm; ++j) {
                 uint4 tv[NV];
                 load_chunk<T, NV>(slot_t + (size_t)j * CH, lane, tv);
@@ -430,7 +519,29 @@ __global__ void __maxnreg__(kMaxRegs) sv_tree_kernel(const TreeArgs a)
             combine_ms2(mt, st, md, sd, c, m1, S1, m2, S2);
             part = make_float4(m1, S1, m2, S2);
         }
-        const float4 xv = exchange4(part);
+        xv = exchange4(part, claim_now && attempt == 0, cl, clT);
+        if (claim_now && attempt == 0 && !xbroken) {
+            // this warp's range of the next tree's root rows, into L2
+            if (next_tree >= 0 && lane == 0 && nb_pf > 0) {
+                const size_t nrow = (size_t)next_tree * Nmax;
+                bulk_prefetch_l2(tgt + nrow * (size_t)V + e0, (uint32_t)nb_pf * (uint32_t)sizeof(T));
+                if (a.has_draft && next_T != 0.0f)
+                    bulk_prefetch_l2(drf + nrow * (size_t)V + e0, (uint32_t)nb_pf * (uint32_t)sizeof(T));
+            }
+        }
+        if (__any_sync(kFull, xbroken))
+            break;
+        if (refmode) {
+            const bool any_inf = __any_sync(kFull, lane < P && (isinf(xv.y) || isinf(xv.w)));
+            const bool any_nan = __any_sync(kFull, lane < P && (isnan(xv.x) || isnan(xv.y) || isnan(xv.z) ||
+                                                               isnan(xv.w)));
+            if (any_inf && !any_nan) {   // the same slice again, weighed against the maxima
+                refmode = false;
+                continue;
+            }
+        }
+        break;
+        }
         if (__any_sync(kFull, xbroken))
             break;
 
@@ -468,7 +579,15 @@ __global__ void __maxnreg__(kMaxRegs) sv_tree_kernel(const TreeArgs a)
             break;
         }
         float m_t, S_t, m_d, S_d;
-        combine_ms2(xv.x, xv.y, xv.z, xv.w, c, m_t, S_t, m_d, S_d);
+        if (refmode) {   // every warp weighed against the first child's logits
+            m_t = ref_t;
+            m_d = ref_d;
+            S_t = lane < P ? xv.y : 0.0f;
+            S_d = lane < P ? xv.w : 0.0f;
+            warp_sum_comp2(S_t, S_d);
+        } else {
+            combine_ms2(xv.x, xv.y, xv.z, xv.w, c, m_t, S_t, m_d, S_d);
+        }
         if (!(isfinite(m_t) && S_t > 0.0f && isfinite(S_t)) ||
             (with_d && !(isfinite(m_d) && S_d > 0.0f && isfinite(S_d)))) {
             bad = true;
@@ -480,6 +599,10 @@ __global__ void __maxnreg__(kMaxRegs) sv_tree_kernel(const TreeArgs a)
         int stats_level = -1;   // the level whose terms the strip partials hold
         int draw_level = 0;     // the last level with mass (0: p itself)
         float wmass = 0.0f;     // lane j: warp j's total of the stats level
+        if (leaf) {   // the pass kept p's strips (against each warp's maximum)
+            stats_level = 0;
+            wmass = (lane < P && xv.x != -INFINITY) ? __fmul_rn(xv.y * weight(xv.x, m_t, c), ist) : 0.0f;
+        }
         bool moved = false;
         unsigned rest = kids;
         while (rest) {
@@ -569,9 +692,14 @@ __global__ void __maxnreg__(kMaxRegs) sv_tree_kernel(const TreeArgs a)
             if (writer)
                 write_out(len, -1);
         } else if (owner == g) {
+            // a leaf's strips were summed against this warp's own maximum
+            const float own_m = __shfl_sync(kFull, xv.x, g & 31);
+            const float sscale = (leaf && draw_level == 0)
+                                     ? (own_m == -INFINITY ? 0.0f : __fmul_rn(weight(own_m, m_t, c), ist))
+                                     : 1.0f;
             auto strip_mass = [&](int q) -> float {
                 const float4 m4 = *reinterpret_cast<const float4*>(stats + (size_t)q * 4);
-                return (m4.x + m4.y) + (m4.z + m4.w);
+                return ((m4.x + m4.y) + (m4.z + m4.w)) * sscale;
             };
             float tc = t;
             int token = -1;
@@ -598,7 +726,9 @@ __global__ void __maxnreg__(kMaxRegs) sv_tree_kernel(const TreeArgs a)
     // warp must have read the previous claim first: a row exchange since then
     // shows it; a sequence rejected before its walk (no exchange) waits at a
     // cluster barrier instead (uniform: it follows from the sequence's data).
-    {
+    if (next_tree != -2) {   // claimed with the tree's first row exchange
+        bb = next_tree;
+    } else {
         if (kc > 0 && kx == kx_claim) {
             cluster_arrive();
             cluster_wait();
@@ -607,7 +737,7 @@ __global__ void __maxnreg__(kMaxRegs) sv_tree_kernel(const TreeArgs a)
             mbar_arrive_expect_tx(xbarc, 8u);
         int nb = -1;
         if (writer && lane == 0)
-            nb = atomicAdd(a.next, 1) + n_clusters;
+            nb = ticket;   // taken when the tree started
         nb = __shfl_sync(kFull, nb, 0);
         if (writer && lane < C)
             st_async_v2(map_to_rank(smem_addr(first_seq), (uint32_t)lane),
