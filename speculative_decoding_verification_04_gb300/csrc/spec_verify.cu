@@ -27,6 +27,7 @@
 #include <vector>
 
 #include "../../include/specverify.h"
+#include "sv_small.cuh"
 #include "sv_sweep.cuh"
 #include "sv_tree.cuh"
 
@@ -326,6 +327,54 @@ static cudaError_t launch_nv(const Args& a, const Geom& g, bool host, cudaStream
     }
 }
 
+// Small vocabularies: one warp per sequence (sv_small.cuh), NE elements a
+// lane (32 NE >= V).  The grid holds as many blocks of four warps as the
+// device keeps resident (at most what the batch needs); a warp takes `tile`
+// consecutive sequences at a time.
+template <typename T, int NE>
+static cudaError_t launch_small_ne(Args& a, int nsm, cudaStream_t st)
+{
+    static int occ[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return cudaErrorInvalidDevice;
+    int per_sm;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        per_sm = occ[dev];
+    }
+    if (per_sm == 0) {
+        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sv_small_kernel<T, NE>, 128, 0);
+        if (e != cudaSuccess)
+            return e;
+        per_sm = std::max(per_sm, 1);
+        std::lock_guard<std::mutex> lk(g_mu);
+        occ[dev] = per_sm;
+    }
+    const long long max_warps = (long long)nsm * per_sm * 4;
+    a.small_tile = (int)std::min<long long>(32, std::max<long long>(1, (a.B + max_warps - 1) / max_warps));
+    const long long tiles = (a.B + a.small_tile - 1) / a.small_tile;
+    const int blocks = (int)std::max<long long>(1, std::min<long long>((tiles + 3) / 4, (long long)nsm * per_sm));
+    sv_small_kernel<T, NE><<<blocks, 128, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+template <typename T>
+static cudaError_t launch_small(Args& a, int nsm, cudaStream_t st)
+{
+    if (a.V <= 32)
+        return launch_small_ne<T, 1>(a, nsm, st);
+    if (a.V <= 64)
+        return launch_small_ne<T, 2>(a, nsm, st);
+    if (a.V <= 128)
+        return launch_small_ne<T, 4>(a, nsm, st);
+    if (a.V <= 256)
+        return launch_small_ne<T, 8>(a, nsm, st);
+    if (a.V <= 512)
+        return launch_small_ne<T, 16>(a, nsm, st);
+    return launch_small_ne<T, 32>(a, nsm, st);
+}
+
 static sv_status device_sms(int* dev_out, int* nsm_out)
 {
     int dev = 0;
@@ -450,9 +499,22 @@ static thread_local HeaderRing tl_header[64];
 static HeaderSlot* header_slot(int dev, size_t need, sv_status* st)
 {
     HeaderRing& hr = tl_header[dev];
+    *st = SV_OK;
+    // a slot that is large enough and whose last kernel is done, nearest the
+    // ring's position first: no allocation and no wait (each fresh slot of a
+    // new size costs a page-locked allocation, milliseconds for a large batch)
+    for (int k = 0; k < kHeaderSlots; ++k) {
+        const int idx = (hr.next + k) % kHeaderSlots;
+        HeaderSlot& s = hr.slot[idx];
+        if (s.buf && s.cap >= need && s.done && (!s.used || cudaEventQuery(s.done) == cudaSuccess)) {
+            s.used = false;
+            hr.next = (idx + 1) % kHeaderSlots;
+            return &s;
+        }
+    }
+    (void)cudaGetLastError();   // a query that reported cudaErrorNotReady
     HeaderSlot& sl = hr.slot[hr.next];
     hr.next = (hr.next + 1) % kHeaderSlots;
-    *st = SV_OK;
     if (sl.used) {
         if (cudaEventSynchronize(sl.done) != cudaSuccess) {
             *st = SV_ERR_CUDA;
@@ -587,17 +649,22 @@ static sv_status run(const Call& c, int kmax, const sv_options* opt, void* ws, s
         if (pa.type == cudaMemoryTypeDevice && pa.device != dev)
             return SV_ERR_INVALID_ARG;
     }
+    // small vocabularies: the warp-per-sequence kernel (no geometry, claims
+    // or header copy); the tuning options, which shape the cluster sweep, and
+    // the expired-wait test (it has no waits) do not apply to it
+    const bool small = c.V <= kSmallVocab && !(opt && (opt->chunks_per_cta || opt->chunks_per_warp ||
+                                                      opt->expire_copy_waits));
     Geom g;
-    st = pick_geometry(c.V, c.dtype, c.B, kmax, opt ? opt->chunks_per_cta : 0,
-                       opt ? opt->chunks_per_warp : 0, dev, host_rows, &g);
-    if (st != SV_OK)
-        return st;
-    if (host_rows && g.nv != 4)   // the in-place path reads 16-byte vectors
-        return SV_ERR_UNSUPPORTED;
-    if (st != SV_OK)
-        return st;
-    if ((long long)g.clusters * g.C > 0x7fffffffLL)
-        return SV_ERR_UNSUPPORTED;
+    if (!small) {
+        st = pick_geometry(c.V, c.dtype, c.B, kmax, opt ? opt->chunks_per_cta : 0,
+                           opt ? opt->chunks_per_warp : 0, dev, host_rows, &g);
+        if (st != SV_OK)
+            return st;
+        if (host_rows && g.nv != 4)   // the in-place path reads 16-byte vectors
+            return SV_ERR_UNSUPPORTED;
+        if ((long long)g.clusters * g.C > 0x7fffffffLL)
+            return SV_ERR_UNSUPPORTED;
+    }
 
     const sv_diag* dg = opt ? &opt->diag : nullptr;
     const bool want_diag = dg && (dg->p_x || dg->q_x || dg->resid_mass || dg->final_row);
@@ -634,9 +701,9 @@ static sv_status run(const Call& c, int kmax, const sv_options* opt, void* ws, s
     }
     const bool packed = opt && opt->packed_logits;
     const size_t up_bytes = packed ? L.header_end : L.seq_end;   // row starts only when packed
-    memset(hdr, 0, up_bytes);
+    memset(hdr, 0, L.K);   // error word, claim counter, ready count; every other field is written
     memcpy(hdr + L.K, c.K, (size_t)c.B * 4);
-    {
+    if (!small) {   // the claim order (the small-vocabulary kernel takes sequences in index order)
         int32_t* ord = reinterpret_cast<int32_t*>(hdr + L.order);
         int cnt[SV_K_MAX + 2] = {0};
         for (int b = 0; b < c.B; ++b)
@@ -698,7 +765,7 @@ static sv_status run(const Call& c, int kmax, const sv_options* opt, void* ws, s
     // when there are tickets to claim after the first wave: the claims then
     // read device memory instead of crossing the host link (with no claims
     // the copy only delayed the first rows: 2 us on a batch of one)
-    a.copy_hdr = (hbase != base && c.B > g.clusters) ? 1 : 0;
+    a.copy_hdr = (!small && hbase != base && c.B > g.clusters) ? 1 : 0;
     a.ready = reinterpret_cast<int*>(base + L.ready);
     a.K_dev = reinterpret_cast<int32_t*>(base + L.K);
     a.order_dev = reinterpret_cast<int32_t*>(base + L.order);
@@ -726,8 +793,11 @@ static sv_status run(const Call& c, int kmax, const sv_options* opt, void* ws, s
     a.expire_waits = (opt && opt->expire_copy_waits) ? 1 : 0;
     a.kv_len = a.want_kv ? opt->kv_len : nullptr;
 
-    const cudaError_t e = c.dtype == SV_DTYPE_BF16 ? launch_nv<__nv_bfloat16>(a, g, host_rows, stream, dev)
-                                                   : launch_nv<float>(a, g, host_rows, stream, dev);
+    a.small_tile = 1;
+    const cudaError_t e = small ? (c.dtype == SV_DTYPE_BF16 ? launch_small<__nv_bfloat16>(a, nsm, stream)
+                                                            : launch_small<float>(a, nsm, stream))
+                                : (c.dtype == SV_DTYPE_BF16 ? launch_nv<__nv_bfloat16>(a, g, host_rows, stream, dev)
+                                                            : launch_nv<float>(a, g, host_rows, stream, dev));
     if (slot && !capturing) {   // the kernel reads the slot: it is free again once the kernel is done
         if (cudaEventRecord(slot->done, stream) != cudaSuccess)
             return SV_ERR_CUDA;

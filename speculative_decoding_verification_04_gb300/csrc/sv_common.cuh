@@ -78,6 +78,8 @@ struct Args {
     const int32_t* cu_d;
     // testing: every wait for a slot fill gives up before its first poll
     int expire_waits;
+    // small vocabularies (sv_small_kernel): consecutive sequences a warp takes
+    int small_tile;
     // per-call counters and the caller's KV lengths (used only if flagged)
     int want_stats, want_kv;
     unsigned long long* stats;   // sv_stats: sequences, invalid, tested, accepted, committed, near_ties
