@@ -250,7 +250,21 @@ def run_reference(args):
     if rank != 0:
         return 0
     widx = args.workload
-    inp, n = oracle_sample(widx, step_s=0.5)
+    inp, n, how = None, 0, "host-generated with the same recipe"
+    try:   # the whole batch of our arm, generated as it generates it (seeded, on the device), to host
+        import torch
+        if torch.cuda.is_available():
+            dev = torch.device("cuda", 0)
+            d = W.make_device(widx, dev)
+            n = d["B"]
+            inp = _rows_to_host(d, np.arange(n))
+            del d
+            torch.cuda.empty_cache()
+            how = "generated on the device by the benchmark's own seeded recipe, copied to the host"
+    except (ImportError, RuntimeError):
+        inp = None
+    if inp is None:
+        inp, n = oracle_sample(widx, step_s=0.5)
     cores = host_cores()
     rates, secs = [], []
     for step in range(args.warmup + args.steps):
@@ -263,12 +277,13 @@ def run_reference(args):
         impl="reference", metric=METRIC, value=value, unit=UNIT, n_gpus=args.gpus,
         steps=args.steps, warmup=args.warmup, ms_per_step=round(1e3 * statistics.median(secs), 3),
         higher_is_better=True, scaling="weak", vs_baseline=None, dtype="f64", data="synthetic",
-        config=dict(workload=WORKLOAD_TEXT[widx], bench_workload=widx, sample_sequences=n),
+        config=dict(workload=WORKLOAD_TEXT[widx], bench_workload=widx, sample_sequences=n,
+                    same_batch=bool(n == W.SPECS[widx].B)),
         cpu_baseline=dict(value=value, unit=UNIT, cores=cores, kind="oracle", cpu_model=cpu_model(),
                           sample=f"first {n} of {W.SPECS[widx].B} sequences of the workload "
-                                 f"({int(np.sum(inp['K']))} positions) per step, host-generated "
-                                 f"with the same recipe, cut into {cores} shards of sequences "
-                                 f"run at once on {cores} threads ({platform.machine()})"),
+                                 f"({int(np.sum(inp['K']))} positions) per step, {how}, cut into "
+                                 f"{cores} shards of sequences run at once on {cores} threads "
+                                 f"({platform.machine()})"),
         e2e=dict(value=value, unit=UNIT, h2d_bytes_per_step=0, d2h_bytes_per_step=0))
     print(json.dumps(line), flush=True)
     return 0
@@ -350,8 +365,9 @@ def run_ours(args):
     # nvidia-smi samples every 200 ms while the timed steps take a few ms: the
     # same step runs back to back for ~1.5 s before and ~0.5 s after them, so
     # the clock samples see the load the timed steps run under
-    clocks = ClockSampler(local) if rank == 0 else None
-    load_for(1.5)
+    clocks = ClockSampler(local) if rank == 0 and not args.no_clock_window else None
+    if clocks:
+        load_for(1.5)
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
@@ -361,7 +377,8 @@ def run_ours(args):
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
-    load_for(0.5)
+    if clocks:
+        load_for(0.5)
     clk = clocks.stop() if clocks else None
     if clk:
         clk["window"] = ("sampled every 200 ms while the timed step ran back to back for ~2 s "
@@ -728,6 +745,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", type=int, default=4, choices=[0, 1, 2, 3, 4])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-clock-window", action="store_true",
+                    help="skip the ~2 s of back-to-back steps that let the clock samples see the "
+                         "load (profiling captures)")
     ap.add_argument("--no-other-workloads", action="store_true",
                     help="time only the selected workload (the default run also times "
                          "workloads 0-3 and the 200k toy pair into detail.workloads)")

@@ -93,6 +93,35 @@ def test_small_vocab_options(dev, dtype):
     assert np.array_equal(t1.cpu().numpy(), t0) and np.array_equal(n1.cpu().numpy(), n0)
 
 
+@pytest.mark.parametrize("V,dtype", [(5, "f32"), (257, "bf16"), (1024, "f32"), (1024, "bf16")])
+def test_small_vocab_diagnostics_and_verify_all(dev, V, dtype):
+    """Diagnostics (which force verify_all) on the warp kernel: p(x_i), q(x_i)
+    within 1e-5 relative and the residual mass within 1e-5 at every sampling
+    position below K_b, rows after the stop included; NaN where the oracle has
+    none (greedy sequences, positions past K_b); outputs unchanged."""
+    import oracle
+    B = 40
+    inp = _mixed(B, V, dtype, seed=V + 11)
+    d = to_device(inp, dev)
+    Kmax = int(inp["Kmax"])
+    bufs = [torch.full((B, Kmax), -7.0, device=dev) for _ in range(3)]
+    fr = torch.full((B,), -7, dtype=torch.int32, device=dev)
+    t0, n0 = run_gpu(d, "ws")
+    t1, n1 = run_gpu(d, "ex", diag=dict(p_x=bufs[0], q_x=bufs[1], resid_mass=bufs[2], final_row=fr))
+    assert np.array_equal(t0, t1) and np.array_equal(n0, n1)
+    compare(oracle_ref(inp), t1, n1, inp=inp)
+    opx, oqx, orm = oracle.position_probs(inp["target"], inp["draft"], dtype, inp["tokens"],
+                                          inp["temperature"], inp["K"])
+    gpx, gqx, grm = (b.cpu().numpy().astype(np.float64) for b in bufs)
+    want = np.isfinite(opx)
+    assert want.sum() > B            # rows after the stop are among them
+    assert np.array_equal(np.isnan(gpx), ~want) and np.array_equal(np.isnan(gqx), ~want)
+    for g, o in ((gpx, opx), (gqx, oqx)):
+        assert np.max(np.abs(g[want] - o[want]) / o[want]) < 1e-5
+    assert np.max(np.abs(grm[want] - orm[want])) < 1e-5
+    assert np.array_equal(fr.cpu().numpy(), n1)
+
+
 def test_toy_pair_through_the_small_kernel_is_fast(dev):
     """The pages' V = 5 pair replicated 200,000 times: the oracle's results,
     and the whole batch in well under a millisecond (the cluster sweep took
