@@ -13,12 +13,17 @@
 // a leaf R = p, the bonus token).  At T = 0 the child equal to the target
 // argmax is kept, else the token is the argmax.
 //
-// Residual levels are recomputed from the resident slice: level L's term at
-// element j is A_L(j) = max(0, R_{L-1}(j) - q(j)) with R_0 = p and
-// R_l = A_l / S_l (S_l = sum_j A_l(j); a level with S_l = 0 leaves R as it
-// was), so a pass at level L costs two exponentials and L - 1 nested steps per
-// element.  Each pass keeps per-strip partial sums of its terms for the draw,
-// as the sweep's residual pass does.
+// Residual levels are recomputed from the resident slice, unnormalised: with
+// the weights W_t = exp2(fma(l_t, c, -r_t)) and W_d (the sweep's), p = W_t / S_t
+// and q = W_d / S_d, level l holds B_l = max(0, B_{l-1} - s_{l-1} W_d) with
+// B_0 = W_t and s_l = sum(B_l) / S_d.  Then R_l = B_l / sum(B_l): for
+// R_{l-1} = B_{l-1} / sum(B_{l-1}), max(0, R_{l-1} - q) is
+// max(0, B_{l-1} - s_{l-1} W_d) / sum(B_{l-1}), and normalising it gives
+// R_l.  A level without mass leaves R as it was, and then every later level
+// has none either (its terms are the same), so no further level is computed.
+// A pass at level L costs two exponentials and L multiply-adds per element.
+// Each pass keeps per-strip partial sums of its terms for the draw, as the
+// sweep's residual pass does.
 #pragma once
 
 #include "sv_sweep.cuh"
@@ -45,70 +50,81 @@ struct TreeArgs {
     int aligned, has_draft;
 };
 
-// The sweep's shared-memory layout (the per-level inverse sums live in lane
-// registers: lane l holds 1 / S_{l+1}), so a row's CTAs fit three to an SM
-// as the sweep's do.
+// The sweep's shared-memory layout (the per-level factors live in lane
+// registers: lane l holds s_l), so a row's CTAs fit three to an SM as the
+// sweep's do.
 __host__ __device__ inline size_t tree_smem_bytes(const SweepLayout& L, int /*nw*/) { return L.total; }
 
-// The level-L terms of one 16-byte vector pair (E elements, lane order):
-// p and q of each element first, then the levels applied to all of them
-// (each level's inverse sum shuffled from its lane once per vector).  L = 0: p = w_t * ist;
-// L >= 1: A_L = max(0, R_{L-1} - q) with q = w_d * isd, R_0 = p and
-// R_l = A_l / S_l (lane l - 1 of `inv` holds 1 / S_l; 0 marks a level without
-// mass, which leaves R as it was); weights exp2(fma(l, c, -r)) as in the
-// sweep.
-template <typename T, int NV>
-__device__ __forceinline__ void level_terms_vec(const uint4& tv, const uint4& dv, float c, float rt, float rd,
-                                                float ist, float isd, int L, float inv,
+// The level-L terms B_L of one 16-byte vector pair (E elements, lane order),
+// elements in packed pairs: W_t and W_d by a packed fma and two ex2 each,
+// then per level one packed multiply-add and a clamp at 0.  LC = min(L, 3)
+// (a compile-time level class); n0, n1 hold -s_0 and -s_1 packed, levels
+// from 2 on shuffle s_l from lane l of `sig`.  Every element's value is the
+// same rounding sequence whichever way the factors arrive.
+template <typename T, int NV, int LC>
+__device__ __forceinline__ void level_terms_vec(const uint4& tv, const uint4& dv, uint64_t Cc, uint64_t NT,
+                                                uint64_t ND, int L, uint64_t n0, uint64_t n1, float sig,
                                                 float (&out)[Elem<T>::E])
 {
     using LN = Lane<T, NV>;
     constexpr int E = Elem<T>::E;
-    float q[E];
 #pragma unroll
-    for (int e = 0; e < E; ++e) {
-        out[e] = __fmul_rn(ex2_approx(__fmaf_rn(LN::vec_elem(tv, e), c, -rt)), ist);
-        q[e] = L > 0 ? __fmul_rn(ex2_approx(__fmaf_rn(LN::vec_elem(dv, e), c, -rd)), isd) : 0.0f;
-    }
-    if (L == 0)
-        return;
-    for (int l = 0; l < L - 1; ++l) {
-        const float sl = __shfl_sync(kFull, inv, l);
-        if (sl > 0.0f) {
-#pragma unroll
-            for (int e = 0; e < E; ++e)
-                out[e] = __fmul_rn(fmaxf(__fsub_rn(out[e], q[e]), 0.0f), sl);
+    for (int h = 0; h < E / 2; ++h) {
+        float a0, a1;
+        f2_unpack(f2_fma(LN::vpair(tv, h), Cc, NT), a0, a1);
+        uint64_t b = f2_pack(ex2_approx(a0), ex2_approx(a1));
+        if (LC > 0) {
+            f2_unpack(f2_fma(LN::vpair(dv, h), Cc, ND), a0, a1);
+            const uint64_t wd = f2_pack(ex2_approx(a0), ex2_approx(a1));
+            f2_unpack(f2_fma(n0, wd, b), a0, a1);
+            b = f2_pack(fmaxf(a0, 0.0f), fmaxf(a1, 0.0f));
+            if (LC > 1) {
+                f2_unpack(f2_fma(n1, wd, b), a0, a1);
+                b = f2_pack(fmaxf(a0, 0.0f), fmaxf(a1, 0.0f));
+            }
+            if (LC > 2) {
+                for (int l = 2; l < L; ++l) {
+                    const float s = __shfl_sync(kFull, sig, l);
+                    f2_unpack(f2_fma(f2_pack(-s, -s), wd, b), a0, a1);
+                    b = f2_pack(fmaxf(a0, 0.0f), fmaxf(a1, 0.0f));
+                }
+            }
         }
+        f2_unpack(b, out[2 * h], out[2 * h + 1]);
     }
-#pragma unroll
-    for (int e = 0; e < E; ++e)
-        out[e] = fmaxf(__fsub_rn(out[e], q[e]), 0.0f);
 }
 
-// R_k(x) for the proposal's p(x), q(x) after k rejections (the same nested
-// steps as level_terms_vec).
-__device__ __forceinline__ float level_value(float px, float qx, int k, float inv)
+// -s_0 and -s_1, packed, for level_terms_vec (every lane).
+__device__ __forceinline__ void level_factors(float sig, uint64_t& n0, uint64_t& n1)
 {
-    float r = px;
-    for (int l = 0; l < k; ++l) {
-        const float s = __shfl_sync(kFull, inv, l);
-        if (s > 0.0f)
-            r = __fmul_rn(fmaxf(__fsub_rn(r, qx), 0.0f), s);
-    }
-    return r;
+    const float s0 = __shfl_sync(kFull, sig, 0), s1 = __shfl_sync(kFull, sig, 1);
+    n0 = f2_pack(-s0, -s0);
+    n1 = f2_pack(-s1, -s1);
+}
+
+// B_k(x) for the proposal's weights W_t(x), W_d(x) (the same steps as
+// level_terms_vec, one lane of them).
+__device__ __forceinline__ float level_value(float wt, float wd, int k, float sig)
+{
+    float b = wt;
+    for (int l = 0; l < k; ++l)
+        b = fmaxf(__fmaf_rn(-__shfl_sync(kFull, sig, l), wd, b), 0.0f);
+    return b;
 }
 
 // One pass over this warp's slice at level L (whole warp): per-strip partial
 // sums of the level's terms into `stats` ([kw][NV][4], as the sweep's
 // residual pass), and the warp's total (compensated); terms as in
 // level_terms_vec.
-template <typename T, int NV>
-__device__ float level_pass(const T* slot_t, const T* slot_d, int kwm, int lane, float c, float rt, float rd,
-                            float ist, float isd, int L, float inv, float* stats)
+template <typename T, int NV, int LC>
+__device__ float level_pass_lc(const T* slot_t, const T* slot_d, int kwm, int lane, float c, float rt, float rd,
+                               int L, float sig, float* stats)
 {
-    using LN = Lane<T, NV>;
     constexpr int E = Elem<T>::E;
     constexpr int CH = 32 * NV * E;
+    const uint64_t Cc = f2_pack(c, c), NT = f2_pack(-rt, -rt), ND = f2_pack(-rd, -rd);
+    uint64_t n0, n1;
+    level_factors(sig, n0, n1);
     float acc = 0.0f, cmp = 0.0f;
 #pragma unroll 1
     for (int j = 0; j < kwm; ++j) {
@@ -119,7 +135,7 @@ __device__ float level_pass(const T* slot_t, const T* slot_d, int kwm, int lane,
 #pragma unroll
         for (int k = 0; k < NV; ++k) {
             float tm[E];
-            level_terms_vec<T, NV>(tv[k], dv[k], c, rt, rd, ist, isd, L, inv, tm);
+            level_terms_vec<T, NV, LC>(tv[k], dv[k], Cc, NT, ND, L, n0, n1, sig, tm);
             float sk = 0.0f;
 #pragma unroll
             for (int e = 0; e < E; ++e)
@@ -140,21 +156,40 @@ __device__ float level_pass(const T* slot_t, const T* slot_d, int kwm, int lane,
     return sum_or_special(acc + cmp);
 }
 
+template <typename T, int NV>
+__device__ float level_pass(const T* slot_t, const T* slot_d, int kwm, int lane, float c, float rt, float rd,
+                            int L, float sig, float* stats)
+{
+    switch (L) {
+    case 0: return level_pass_lc<T, NV, 0>(slot_t, slot_d, kwm, lane, c, rt, rd, L, sig, stats);
+    case 1: return level_pass_lc<T, NV, 1>(slot_t, slot_d, kwm, lane, c, rt, rd, L, sig, stats);
+    case 2: return level_pass_lc<T, NV, 2>(slot_t, slot_d, kwm, lane, c, rt, rd, L, sig, stats);
+    default: return level_pass_lc<T, NV, 3>(slot_t, slot_d, kwm, lane, c, rt, rd, L, sig, stats);
+    }
+}
+
 // The element of one strip that holds the point tc of the level-L
 // distribution (one warp; tv / dv: each lane's vector of the strip): lane
 // sums, a compensated scan, the lane, then the element, the terms computed
 // exactly as in level_pass (level_terms_vec).  Returns lane * E + e, or -1 if the strip has no
 // mass; beyond the strip's mass (rounding) the last element with mass.
 template <typename T, int NV>
-__device__ int pick_level(const uint4& tv, const uint4& dv, float c, float rt, float rd, float ist, float isd,
-                          int L, float inv, float tc, bool beyond, int lane)
+__device__ int pick_level(const uint4& tv, const uint4& dv, float c, float rt, float rd, int L, float sig,
+                          float tc, bool beyond, int lane)
 {
-    using LN = Lane<T, NV>;
     constexpr int E = Elem<T>::E;
     float tm[E];
     float ls = 0.0f;
     int lastpos = -1;
-    level_terms_vec<T, NV>(tv, dv, c, rt, rd, ist, isd, L, inv, tm);
+    uint64_t n0, n1;
+    level_factors(sig, n0, n1);
+    const uint64_t Cc = f2_pack(c, c), NT = f2_pack(-rt, -rt), ND = f2_pack(-rd, -rd);
+    switch (L) {
+    case 0: level_terms_vec<T, NV, 0>(tv, dv, Cc, NT, ND, L, n0, n1, sig, tm); break;
+    case 1: level_terms_vec<T, NV, 1>(tv, dv, Cc, NT, ND, L, n0, n1, sig, tm); break;
+    case 2: level_terms_vec<T, NV, 2>(tv, dv, Cc, NT, ND, L, n0, n1, sig, tm); break;
+    default: level_terms_vec<T, NV, 3>(tv, dv, Cc, NT, ND, L, n0, n1, sig, tm); break;
+    }
 #pragma unroll
     for (int e = 0; e < E; ++e) {
         ls += tm[e];
@@ -257,7 +292,7 @@ __global__ void __maxnreg__(kMaxRegs) sv_tree_kernel(const TreeArgs a)
     float next_T = 0.0f;   // its temperature (its draft row is prefetched only if > 0)
     int ticket = -1;       // the writer's ticket for the next tree
     const int nb_pf = a.aligned ? ((n_el * (int)sizeof(T)) & ~15) / (int)sizeof(T) : 0;
-    float inv = 0.0f;        // lane l: 1 / S_{l+1} of the node's residual levels
+    float sig = 0.0f;        // lane l: s_l = sum(B_l) / S_d of the node's residual levels
     bool pending = false, xbroken = false;
     // the current sequence (lane n: node n), set when it starts
     int b = 0, N = 0, par = -2, tokn = 0;
@@ -595,13 +630,16 @@ __global__ void __maxnreg__(kMaxRegs) sv_tree_kernel(const TreeArgs a)
         }
         const float ist = __frcp_rn(S_t), isd = with_d ? __frcp_rn(S_d) : 0.0f;
         const float rt = ref_of(m_t, c), rd = with_d ? ref_of(m_d, c) : 0.0f;
-        int k = 0;              // rejections so far: residual levels computed
+        int k = 0;              // residual levels applied (each with mass): R = B_k / sum(B_k)
+        bool dead = false;      // a level came out without mass: R stays as it is
+        float ib = ist;         // 1 / sum(B_k)
+        if (lane == 0)
+            sig = __fmul_rn(S_t, isd);   // s_0 = sum(B_0) / S_d
         int stats_level = -1;   // the level whose terms the strip partials hold
-        int draw_level = 0;     // the last level with mass (0: p itself)
         float wmass = 0.0f;     // lane j: warp j's total of the stats level
         if (leaf) {   // the pass kept p's strips (against each warp's maximum)
             stats_level = 0;
-            wmass = (lane < P && xv.x != -INFINITY) ? __fmul_rn(xv.y * weight(xv.x, m_t, c), ist) : 0.0f;
+            wmass = (lane < P && xv.x != -INFINITY) ? __fmul_rn(xv.y, weight(xv.x, m_t, c)) : 0.0f;   // B_0 units
         }
         bool moved = false;
         unsigned rest = kids;
@@ -616,9 +654,9 @@ __global__ void __maxnreg__(kMaxRegs) sv_tree_kernel(const TreeArgs a)
             }
             const float lt = EL::widen(__shfl_sync(kFull, klt, cn));
             const float ld = EL::widen(__shfl_sync(kFull, kld, cn));
-            const float px = __fmul_rn(weight_r(lt, rt, c), ist);
-            const float qx = __fmul_rn(weight_r(ld, rd, c), isd);
-            const float r = level_value(px, qx, k, inv);
+            const float wd = weight_r(ld, rd, c);
+            const float qx = __fmul_rn(wd, isd);
+            const float r = __fmul_rn(level_value(weight_r(lt, rt, c), wd, k, sig), ib);   // R_k(x)
             const bool keep = qx > 0.0f ? __fmul_rn(u, qx) < r : r > 0.0f;
             if (keep) {
                 if (lane == len)
@@ -628,9 +666,11 @@ __global__ void __maxnreg__(kMaxRegs) sv_tree_kernel(const TreeArgs a)
                 moved = true;
                 break;
             }
+            if (dead)
+                continue;   // R unchanged: the next child is tested against it
             // the next residual level, from the resident slice
             const float tot =
-                have ? level_pass<T, NV>(slot_t, slot_d, kwm, lane, c, rt, rd, ist, isd, k + 1, inv, stats) : 0.0f;
+                have ? level_pass<T, NV>(slot_t, slot_d, kwm, lane, c, rt, rd, k + 1, sig, stats) : 0.0f;
             wmass = exchange2(tot);
             if (__any_sync(kFull, xbroken))
                 break;
@@ -639,13 +679,17 @@ __global__ void __maxnreg__(kMaxRegs) sv_tree_kernel(const TreeArgs a)
                 bad = true;
                 break;
             }
-            if (lane == k)
-                inv = S > 0.0f ? __frcp_rn(S) : 0.0f;
-            ++k;
-            stats_level = k;
-            if (S > 0.0f)
-                draw_level = k;
+            stats_level = k + 1;
+            if (S > 0.0f) {
+                ++k;
+                if (lane == k)
+                    sig = __fmul_rn(S, isd);
+                ib = __frcp_rn(S);
+            } else {
+                dead = true;
+            }
         }
+        const int draw_level = k;   // the last level with mass (0: p itself)
         if (bad || __any_sync(kFull, xbroken))
             break;
         if (moved)
@@ -659,7 +703,7 @@ __global__ void __maxnreg__(kMaxRegs) sv_tree_kernel(const TreeArgs a)
         }
         if (stats_level != draw_level) {   // strips of the level drawn from
             const float tot =
-                have ? level_pass<T, NV>(slot_t, slot_d, kwm, lane, c, rt, rd, ist, isd, draw_level, inv, stats)
+                have ? level_pass<T, NV>(slot_t, slot_d, kwm, lane, c, rt, rd, draw_level, sig, stats)
                      : 0.0f;
             wmass = exchange2(tot);
             if (__any_sync(kFull, xbroken))
@@ -692,10 +736,11 @@ __global__ void __maxnreg__(kMaxRegs) sv_tree_kernel(const TreeArgs a)
             if (writer)
                 write_out(len, -1);
         } else if (owner == g) {
-            // a leaf's strips were summed against this warp's own maximum
+            // a leaf's strips were summed against this warp's own maximum:
+            // rescaled to B_0 = W_t (against the row's maximum)
             const float own_m = __shfl_sync(kFull, xv.x, g & 31);
             const float sscale = (leaf && draw_level == 0)
-                                     ? (own_m == -INFINITY ? 0.0f : __fmul_rn(weight(own_m, m_t, c), ist))
+                                     ? (own_m == -INFINITY ? 0.0f : weight(own_m, m_t, c))
                                      : 1.0f;
             auto strip_mass = [&](int q) -> float {
                 const float4 m4 = *reinterpret_cast<const float4*>(stats + (size_t)q * 4);
@@ -708,7 +753,7 @@ __global__ void __maxnreg__(kMaxRegs) sv_tree_kernel(const TreeArgs a)
                 const int jc = js / NV, ks = js % NV;
                 const uint4 t4 = reinterpret_cast<const uint4*>(slot_t + (size_t)jc * CH)[ks * 32 + lane];
                 const uint4 d4 = reinterpret_cast<const uint4*>(slot_d + (size_t)jc * CH)[ks * 32 + lane];
-                const int ce = pick_level<T, NV>(t4, d4, c, rt, rd, ist, isd, draw_level, inv, tc, beyond, lane);
+                const int ce = pick_level<T, NV>(t4, d4, c, rt, rd, draw_level, sig, tc, beyond, lane);
                 if (ce >= 0)
                     token = e0 + jc * CH + ks * 32 * E + ce;
             }
