@@ -480,11 +480,6 @@ template <int NV> struct Lane<__nv_bfloat16, NV> {
         const uint32_t wd = h == 0 ? q.x : h == 1 ? q.y : h == 2 ? q.z : q.w;
         return (e & 1) ? __uint_as_float(wd & 0xffff0000u) : __uint_as_float(wd << 16);
     }
-    // elements 2h and 2h + 1 of a lane vector (h = 0..3), packed
-    __device__ static __forceinline__ uint64_t vpair(const uint4& q, int h)
-    {
-        return pair(h == 0 ? q.x : h == 1 ? q.y : h == 2 ? q.z : q.w);
-    }
 };
 
 template <int NV> struct Lane<float, NV> {
@@ -588,12 +583,6 @@ template <int NV> struct Lane<float, NV> {
     __device__ static __forceinline__ float vec_elem(const uint4& q, int e)
     {
         return __uint_as_float(e == 0 ? q.x : e == 1 ? q.y : e == 2 ? q.z : q.w);
-    }
-    // elements 2h and 2h + 1 of a lane vector (h = 0, 1), packed
-    __device__ static __forceinline__ uint64_t vpair(const uint4& q, int h)
-    {
-        return h == 0 ? f2_pack(__uint_as_float(q.x), __uint_as_float(q.y))
-                      : f2_pack(__uint_as_float(q.z), __uint_as_float(q.w));
     }
 };
 

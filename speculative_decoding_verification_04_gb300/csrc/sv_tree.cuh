@@ -55,6 +55,23 @@ struct TreeArgs {
 // sweep's do.
 __host__ __device__ inline size_t tree_smem_bytes(const SweepLayout& L, int /*nw*/) { return L.total; }
 
+// Elements 2h and 2h + 1 of a lane vector as a packed fp32 pair (lower index
+// in the low lane): h = 0..3 for bf16, 0..1 for fp32.
+template <typename T> struct VecPair;
+template <> struct VecPair<__nv_bfloat16> {
+    __device__ static __forceinline__ uint64_t get(const uint4& q, int h)
+    {
+        return Lane<__nv_bfloat16, 1>::pair(h == 0 ? q.x : h == 1 ? q.y : h == 2 ? q.z : q.w);
+    }
+};
+template <> struct VecPair<float> {
+    __device__ static __forceinline__ uint64_t get(const uint4& q, int h)
+    {
+        return h == 0 ? f2_pack(__uint_as_float(q.x), __uint_as_float(q.y))
+                      : f2_pack(__uint_as_float(q.z), __uint_as_float(q.w));
+    }
+};
+
 // The level-L terms B_L of one 16-byte vector pair (E elements, lane order),
 // elements in packed pairs: W_t and W_d by a packed fma and two ex2 each,
 // then per level one packed multiply-add and a clamp at 0.  LC = min(L, 3)
@@ -66,15 +83,14 @@ __device__ __forceinline__ void level_terms_vec(const uint4& tv, const uint4& dv
                                                 uint64_t ND, int L, uint64_t n0, uint64_t n1, float sig,
                                                 float (&out)[Elem<T>::E])
 {
-    using LN = Lane<T, NV>;
     constexpr int E = Elem<T>::E;
 #pragma unroll
     for (int h = 0; h < E / 2; ++h) {
         float a0, a1;
-        f2_unpack(f2_fma(LN::vpair(tv, h), Cc, NT), a0, a1);
+        f2_unpack(f2_fma(VecPair<T>::get(tv, h), Cc, NT), a0, a1);
         uint64_t b = f2_pack(ex2_approx(a0), ex2_approx(a1));
         if (LC > 0) {
-            f2_unpack(f2_fma(LN::vpair(dv, h), Cc, ND), a0, a1);
+            f2_unpack(f2_fma(VecPair<T>::get(dv, h), Cc, ND), a0, a1);
             const uint64_t wd = f2_pack(ex2_approx(a0), ex2_approx(a1));
             f2_unpack(f2_fma(n0, wd, b), a0, a1);
             b = f2_pack(fmaxf(a0, 0.0f), fmaxf(a1, 0.0f));
