@@ -300,10 +300,11 @@ __global__ void __maxnreg__(kMaxRegs) sv_tree_kernel(const TreeArgs a)
 
     uint32_t uses = 0, kx = 0, k2 = 0, kc = 0;
     uint32_t kx_claim = 0;   // row exchanges run when the last claim was read
-    // The next tree is claimed a tree ahead: rank 0's writer takes a ticket
-    // when a tree starts and sends it with the tree's first row exchange, so
-    // the claim's round trip and the next root rows' reads overlap the walk
-    // (-2: not known yet; -1: none left).
+    // While two waves of trees remain, the next tree is claimed a tree
+    // ahead: rank 0's writer takes a ticket when a tree starts and sends it
+    // with the tree's first row exchange, so the claim's round trip and the
+    // next root rows' reads overlap the walk (-2: not known yet; -1: none
+    // left).  Nearer the end it is claimed when the tree ends.
     int next_tree = -2;
     float next_T = 0.0f;   // its temperature (its draft row is prefetched only if > 0)
     int ticket = -1;       // the writer's ticket for the next tree
@@ -416,7 +417,11 @@ __global__ void __maxnreg__(kMaxRegs) sv_tree_kernel(const TreeArgs a)
     path_l = -1;
     done = false;
     next_tree = -2;
-    if (writer && lane == 0)
+    // claimed ahead (tree ids are tickets); else when this tree ends, so
+    // that the last trees go to the clusters that are free first
+    const bool ahead = (long long)b + 2LL * n_clusters < (long long)a.B;
+    ticket = -1;
+    if (ahead && writer && lane == 0)
         ticket = atomicAdd(a.next, 1) + n_clusters;
 
     // ---- the walk: one node per step ----
@@ -452,9 +457,10 @@ __global__ void __maxnreg__(kMaxRegs) sv_tree_kernel(const TreeArgs a)
         if (__any_sync(kFull, xbroken))
             break;
 
-        // the next tree: rank 0's writer sends it (and its temperature) with
-        // this tree's first row exchange; its ticket was taken at the start
-        const bool claim_now = next_tree == -2;
+        // the next tree (claimed ahead): rank 0's writer sends it (and its
+        // temperature) with this tree's first row exchange; its ticket was
+        // taken at the start
+        const bool claim_now = ahead && next_tree == -2;
         int cl = -1;
         float clT = 0.0f;
         if (claim_now && writer && lane == 0) {
@@ -798,7 +804,7 @@ __global__ void __maxnreg__(kMaxRegs) sv_tree_kernel(const TreeArgs a)
             mbar_arrive_expect_tx(xbarc, 8u);
         int nb = -1;
         if (writer && lane == 0)
-            nb = ticket;   // taken when the tree started
+            nb = ahead ? ticket : atomicAdd(a.next, 1) + n_clusters;
         nb = __shfl_sync(kFull, nb, 0);
         if (writer && lane < C)
             st_async_v2(map_to_rank(smem_addr(first_seq), (uint32_t)lane),
