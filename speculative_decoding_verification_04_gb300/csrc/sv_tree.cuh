@@ -664,22 +664,26 @@ __global__ void __maxnreg__(kMaxRegs) sv_tree_kernel(const TreeArgs a)
             wmass = (lane < P && xv.x != -INFINITY) ? __fmul_rn(xv.y, weight(xv.x, m_t, c)) : 0.0f;   // B_0 units
         }
         bool moved = false;
+        // each child's weights W_t(x), W_d(x) and q(x) in its own lane, and
+        // which children are usable (token in range, uniform in [0, 1))
+        const bool is_kid = (kids >> lane) & 1u;
+        const float wt_l = is_kid ? weight_r(EL::widen(klt), rt, c) : 0.0f;
+        const float wd_l = is_kid ? weight_r(EL::widen(kld), rd, c) : 0.0f;
+        const float qx_l = __fmul_rn(wd_l, isd);
+        const unsigned kid_ok =
+            __ballot_sync(kFull, is_kid && tokn >= 0 && tokn < V && un >= 0.0f && un < 1.0f);
         unsigned rest = kids;
         while (rest) {
             const int cn = __ffs(rest) - 1;
             rest &= rest - 1;
-            const int x = __shfl_sync(kFull, tokn, cn);
-            const float u = __shfl_sync(kFull, un, cn);
-            if (x < 0 || x >= V || !(u >= 0.0f && u < 1.0f)) {
+            if (!((kid_ok >> cn) & 1u)) {
                 bad = true;
                 break;
             }
-            const float lt = EL::widen(__shfl_sync(kFull, klt, cn));
-            const float ld = EL::widen(__shfl_sync(kFull, kld, cn));
-            const float wd = weight_r(ld, rd, c);
-            const float qx = __fmul_rn(wd, isd);
-            const float r = __fmul_rn(level_value(weight_r(lt, rt, c), wd, k, sig), ib);   // R_k(x)
-            const bool keep = qx > 0.0f ? __fmul_rn(u, qx) < r : r > 0.0f;
+            // every child lane tests itself against R_k; child cn's result counts
+            const float r_l = __fmul_rn(level_value(wt_l, wd_l, k, sig), ib);   // R_k(x)
+            const bool keep_l = qx_l > 0.0f ? __fmul_rn(un, qx_l) < r_l : r_l > 0.0f;
+            const bool keep = (__ballot_sync(kFull, keep_l) >> cn) & 1u;
             if (keep) {
                 if (lane == len)
                     path_l = cn;
