@@ -196,13 +196,15 @@ sv_status sv_geometry(int32_t B, int32_t Kmax, int32_t V, sv_dtype dtype, int32_
 
 /*
  * Bytes of device workspace spec_verify_ws / spec_verify_ex need for this
- * shape (0 on invalid arguments).  The workspace holds the error word and
- * the claim counter, reset by every call on its stream; the rest of the
- * per-call header (K, the order in which sequences are claimed, the packed
- * row starts) is read by the kernel from a pinned, device-mapped host buffer
- * of the library's, or, where pinned memory is unavailable or the caller's
- * own host staging is used (spec_verify_noalloc), uploaded into the
- * workspace.  The buffer needs no clearing.
+ * shape (0 on invalid arguments).  The workspace holds the error word, the
+ * claim counter and a header-ready count, reset by every call on its stream.
+ * The rest of the per-call header (K, the order in which sequences are
+ * claimed, the packed row starts) is read by the kernel from a pinned,
+ * device-mapped host buffer of the library's, which the kernel first copies
+ * into the workspace when the batch has more sequences than the grid has
+ * clusters; where pinned memory is unavailable or the caller's own host
+ * staging is used (spec_verify_noalloc) it is uploaded into the workspace.
+ * The buffer needs no clearing.
  */
 size_t sv_workspace_size(int32_t B, int32_t Kmax, int32_t V, sv_dtype dtype);
 
@@ -245,7 +247,8 @@ sv_status spec_verify(const void* target_logits, const void* draft_logits, sv_dt
  * whose sv_workspace_size(B, Kmax, V, dtype) exceeds SV_STATIC_SCRATCH_BYTES
  * return SV_ERR_NO_MEMORY before any work is queued.  Nothing in the array
  * needs to start at zero: each call uploads the header it uses (error word,
- * claim counter, K and the claim order) before its kernel runs.  The per-call header is assembled in a static host array.
+ * claim counter, K and the claim order) before its kernel runs.  The per-call
+ * header is assembled in a static host array.
  *
  * Set-up: the first call on a device resolves the array's address on that
  * device (cudaGetSymbolAddress, with the device current) and sets kernel

@@ -13,10 +13,13 @@
 //  * issoh.co.jp "Speculative Decoding（投機的デコーディング）とは？…", section
 //    受理・棄却の規則と出力分布が変わらない理由, steps 1-5.
 //
-// One call = a 16-byte memset of the error word and the claim counter on the
-// stream + one launch of the persistent cluster kernel (sv_sweep.cuh), which
-// reads the rest of the per-call header (K, the claim order) from a pinned,
-// device-mapped host buffer, draws the tokens and writes the outputs.
+// One call = a 16-byte memset of the error word, the claim counter and the
+// header-ready count on the stream + one kernel launch: the persistent cluster
+// kernel (sv_sweep.cuh), or for V <= 1024 the warp-per-sequence kernel
+// (sv_small.cuh).  The cluster kernel reads the rest of the per-call header
+// (K, the claim order) from a pinned, device-mapped host buffer, copying it
+// into the workspace first when the batch is larger than the grid; it draws
+// the tokens and writes the outputs.
 #include <cuda_runtime.h>
 #include <string.h>
 
@@ -73,7 +76,9 @@ static int n_chunks(int V, int s)
     return (V + ch - 1) / ch;
 }
 
-// ---- workspace layout: the per-call header, uploaded by every call ----
+// ---- workspace layout: the per-call header (the first 16 bytes reset by
+// every call; K, the order and the packed row starts written by the kernel
+// from the mapped header, or uploaded from pageable staging) ----
 struct WsLayout {
     size_t err, next_unit, ready, K, order, seq_end, cu_t, cu_d, header_end, total;
 };
@@ -89,11 +94,11 @@ static bool ws_layout(int B, int Kmax, int V, sv_dtype dt, WsLayout* L)
     size_t o = 0;
     L->err = o;
     L->next_unit = o + 4;
-    L->ready = o + 8;   // CTAs done copying the mapped header into K and order
+    L->ready = o + 8;   // CTAs done copying the mapped header's K and order here
     o = align256(o + 16);
     L->K = o;        o = align256(o + (size_t)B * 4);
     L->order = o;    o = align256(o + (size_t)B * 4);
-    L->seq_end = o;   // the header every call uploads ends here
+    L->seq_end = o;   // K and the order end here (the packed row starts follow)
     L->cu_t = o;     o = align256(o + (size_t)B * 4);
     L->cu_d = o;     o = align256(o + (size_t)B * 4);
     L->header_end = o;

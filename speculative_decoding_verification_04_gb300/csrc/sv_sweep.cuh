@@ -22,25 +22,29 @@
 // Per row, each warp makes one pass over its slice, from shared memory
 // straight into registers (the chunk loops are not unrolled: the smaller loop
 // body ran workload 4 3% and workload 2 7% faster):
-//   greedy row       lane max (packed bf16x2 / three-input fp32 max) and the
-//                    lowest index holding it;
-//   tested sampling  lane-online max and sum of exp2((l - m) log2(e)/T) of the
-//   row              target and the draft row (rescaled when the lane max
-//                    grows), in packed two-lane fp32 arithmetic;
-//   bonus row        per-chunk (max, sum) of the target, kept for the draw.
+//   greedy row       lane max (packed bf16x2 / three-input fp32 max), the
+//                    first chunk holding it, then the lowest index holding it;
+//   tested sampling  sums of the target and draft weights exp2(fma(l, c, -r))
+//   row              (c = log2(e)/T) weighed against the proposal's own logits
+//                    (r = l_x c), so no maximum is needed and every warp's
+//                    partials add; a row whose weights overflow is weighed
+//                    again against its maxima; packed two-lane fp32;
+//   bonus row        the warp's maximum, then per-strip sums of the target's
+//                    weights against it, kept for the draw.
 // exchange  every warp pushes a 16-byte partial to every CTA of the cluster
 //           with st.async, completing on the receiver's exchange mbarrier
 //           (double-buffered by row parity);
 // decide    every warp combines all P partials (identical arithmetic, so
 //           identical results) and decides u q(x) < p(x), or x == argmax at
 //           temperature 0;
-// residual  rejected rows (every tested row in verify-all mode): per-chunk sums
-//           of max(0, p - q) and of p from the resident slice, and a second
-//           exchange of the per-warp totals;
+// residual  rejected rows (every tested row in verify-all mode): per-strip
+//           sums of max(0, p - q) and the warp's sum of p, from the resident
+//           slice, and a second exchange of the per-warp totals;
 // draw      at the sequence's final row the warp whose range holds u * S (a
-//           compensated prefix over the warps, then over its chunks, then
-//           over lane spans of one chunk) picks the token by inverse CDF from
-//           its resident slice and writes the sequence's outputs.
+//           compensated prefix over the warps, then over its strips in index
+//           order, then over the lanes of one strip, then inside the lane)
+//           picks the token by inverse CDF from its resident slice and writes
+//           the sequence's outputs.
 #pragma once
 
 #include "sv_common.cuh"
