@@ -58,7 +58,7 @@
 extern "C" {
 #endif
 
-#define SV_ABI_VERSION 3
+#define SV_ABI_VERSION 4
 /* Largest per-sequence draft count: one warp ballot covers the accept bits. */
 #define SV_K_MAX 32
 
@@ -101,8 +101,12 @@ typedef struct {
  *   near_ties   sampling accept tests whose uniform lies within 1e-6 of its
  *               threshold p/q (the decisions a change of summation order
  *               could flip)
+ *   draw_near_ties  final draws (sampling sequences with valid outputs)
+ *               whose point u lies within 1e-6 of a bound of the drawn
+ *               token's interval [C_{j-1}, C_j) of the normalised CDF
  * The acceptance rate is accepted / tested; tokens per round is
- * committed / sequences.
+ * committed / sequences.  (Before ABI version 4 the struct ended at
+ * near_ties.)
  */
 typedef struct {
     unsigned long long sequences;
@@ -111,6 +115,7 @@ typedef struct {
     unsigned long long accepted;
     unsigned long long committed;
     unsigned long long near_ties;
+    unsigned long long draw_near_ties;
 } sv_stats;
 
 /*

@@ -55,7 +55,7 @@ class SVOptions(ctypes.Structure):
                 ("packed_logits", ctypes.c_int32), ("expire_copy_waits", ctypes.c_int32)]
 
 
-STATS_FIELDS = ("sequences", "invalid", "tested", "accepted", "committed", "near_ties")
+STATS_FIELDS = ("sequences", "invalid", "tested", "accepted", "committed", "near_ties", "draw_near_ties")
 
 
 def _load():
@@ -222,7 +222,7 @@ class Workspace:
 
 
 class Stats:
-    """A device sv_stats (six 64-bit counters), zeroed; calls accumulate into it."""
+    """A device sv_stats (seven 64-bit counters), zeroed; calls accumulate into it."""
 
     def __init__(self, device="cuda"):
         import torch

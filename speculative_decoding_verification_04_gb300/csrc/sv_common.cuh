@@ -82,7 +82,8 @@ struct Args {
     int small_tile;
     // per-call counters and the caller's KV lengths (used only if flagged)
     int want_stats, want_kv;
-    unsigned long long* stats;   // sv_stats: sequences, invalid, tested, accepted, committed, near_ties
+    unsigned long long* stats;   // sv_stats: sequences, invalid, tested, accepted, committed,
+                                 // near_ties, draw_near_ties
     int32_t* kv_len;
     // diagnostics (nullable)
     float* p_x;

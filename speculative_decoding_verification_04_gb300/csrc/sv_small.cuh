@@ -96,9 +96,10 @@ __device__ __forceinline__ int small_argmax(const float (&x)[NE], int lane)
 // Inverse CDF over non-negative masses a (lane-interleaved, index order e
 // then lane): the smallest j with u S < a_0 + ... + a_j, prefix sums
 // compensated; beyond the total (rounding) the last element with mass; -1 if
-// none has mass.  Every lane gets the result.
+// none has mass.  Every lane gets the result, and `near`: the point u S lies
+// within 1e-6 S of a bound of the element taken (always so beyond the total).
 template <int NE>
-__device__ __forceinline__ int small_draw(const float (&a)[NE], float S, float u, int lane)
+__device__ __forceinline__ int small_draw(const float (&a)[NE], float S, float u, int lane, bool& near)
 {
     const float t = u * S;
     float base_s = 0.0f, base_c = 0.0f;
@@ -112,14 +113,19 @@ __device__ __forceinline__ int small_draw(const float (&a)[NE], float S, float u
         warp_incl_scan_comp(d, lane, s, cc);
         const float rel = (t - base_s) - base_c;
         const unsigned hit = __ballot_sync(kFull, d > 0.0f && rel < s + cc);
-        if (hit)
-            return e * 32 + (__ffs(hit) - 1);
+        if (hit) {
+            const int src = __ffs(hit) - 1;
+            const float dist = fminf(rel - ((s + cc) - d), (s + cc) - rel);   // in lane src
+            near = __shfl_sync(kFull, dist < 1e-6f * S ? 1 : 0, src) != 0;
+            return e * 32 + src;
+        }
         const float gs = __shfl_sync(kFull, s, 31), gc = __shfl_sync(kFull, cc, 31);
         float ts, te;
         two_sum(base_s, gs, ts, te);
         base_s = ts;
         base_c += gc + te;
     }
+    near = true;
     return __reduce_max_sync(kFull, last_pos);
 }
 
@@ -136,7 +142,7 @@ __global__ void __launch_bounds__(128, 4) sv_small_kernel(const Args a)
     const int V = a.V, Kmax = a.Kmax, tile = a.small_tile;
     const T* tgt = static_cast<const T*>(a.tgt);
     const T* drf = static_cast<const T*>(a.drf);
-    uint32_t c_seq = 0, c_inv = 0, c_test = 0, c_acc = 0, c_commit = 0, c_tie = 0;   // lane 0
+    uint32_t c_seq = 0, c_inv = 0, c_test = 0, c_acc = 0, c_commit = 0, c_tie = 0, c_dtie = 0;   // lane 0
     const bool want_diag = a.want_pq || a.want_resid;
 
     for (long long b0 = (long long)warp * tile; b0 < a.B; b0 += (long long)nwarps * tile) {
@@ -162,6 +168,7 @@ __global__ void __launch_bounds__(128, 4) sv_small_kernel(const Args a)
             bool bad = !temperature_usable(Tb);
             const float c = (!bad && !greedy) ? log2e_over(Tb) : 0.0f;
             int n = -1, token = -1;   // the outputs, once the walk stops
+            bool dnear = false;       // the final draw's point near a bound of its token
             int next_pos = 0;         // diagnostics written for positions below it
             // the walk; after its stop, rows are read only for diagnostics
             // (verify-all), as long as they are usable
@@ -211,7 +218,7 @@ __global__ void __launch_bounds__(128, 4) sv_small_kernel(const Args a)
                         break;
                     }
                     n = i;
-                    token = small_draw<NE>(at, St, uf, lane);
+                    token = small_draw<NE>(at, St, uf, lane, dnear);
                     break;
                 }
                 float ad[NE];   // the draft row; its weights; then the residual
@@ -259,7 +266,8 @@ __global__ void __launch_bounds__(128, 4) sv_small_kernel(const Args a)
                     }
                     n = i;
                     // no residual mass (p and q equal to rounding): p of the row
-                    token = SR > 0.0f ? small_draw<NE>(ad, SR, uf, lane) : small_draw<NE>(at, St, uf, lane);
+                    token = SR > 0.0f ? small_draw<NE>(ad, SR, uf, lane, dnear)
+                                      : small_draw<NE>(at, St, uf, lane, dnear);
                 }
             }
             if (bad)
@@ -289,6 +297,7 @@ __global__ void __launch_bounds__(128, 4) sv_small_kernel(const Args a)
                 if (ok) {
                     ++c_seq;
                     c_commit += (uint32_t)n + 1u;
+                    c_dtie += dnear ? 1u : 0u;
                 } else {
                     ++c_inv;
                 }
@@ -296,9 +305,9 @@ __global__ void __launch_bounds__(128, 4) sv_small_kernel(const Args a)
         }
     }
     if (a.want_stats && lane == 0) {
-        const uint32_t cs[6] = {c_seq, c_inv, c_test, c_acc, c_commit, c_tie};
+        const uint32_t cs[7] = {c_seq, c_inv, c_test, c_acc, c_commit, c_tie, c_dtie};
 #pragma unroll
-        for (int k = 0; k < 6; ++k)
+        for (int k = 0; k < 7; ++k)
             if (cs[k])
                 atomicAdd(a.stats + k, (unsigned long long)cs[k]);
     }

@@ -736,11 +736,13 @@ __device__ __forceinline__ int select_cdf(int n, F D, float& t, bool& beyond, in
 // The terms are computed exactly as in the residual pass (or the bonus pass).
 // Returns lane * E + e, or -1 if the strip has no mass; when the point lies
 // beyond the strip's mass (rounding, or `beyond` already set) the last
-// element with mass is taken.
-template <typename T, int NV>
+// element with mass is taken.  NEAR: also set `near` (every lane): the point
+// lies within `band` of a bound of the element taken (always so beyond the
+// mass); without NEAR the distances are not tracked.
+template <typename T, int NV, bool NEAR>
 __device__ __forceinline__ int pick_in_strip(const uint4& tv, const uint4& dv, bool use_r, float m_t,
                                              float inv_st, float m_d, float inv_sd, float c, float tc,
-                                             bool beyond, int lane)
+                                             bool beyond, int lane, float band, bool& near)
 {
     using LN = Lane<T, NV>;
     constexpr int E = Elem<T>::E;
@@ -772,23 +774,49 @@ __device__ __forceinline__ int pick_in_strip(const uint4& tv, const uint4& dv, b
             const int src = __ffs(hit) - 1;
             const float tl = tc - ((ss - ls) + sc);   // the point's place in the lane (src)
             int ce = -1, lp = -1;
-            float cum = 0.0f;
+            float cum = 0.0f, dlo = 0.0f, dhi = 0.0f;   // the point's distances to ce's bounds
 #pragma unroll
             for (int e = 0; e < E; ++e) {   // the same sums as ls
+                const float prev = cum;
                 cum += tm[e];
                 if (tm[e] > 0.0f) {
                     lp = e;
-                    if (ce < 0 && tl < cum)
+                    if (ce < 0 && tl < cum) {
                         ce = e;
+                        if (NEAR) {
+                            dlo = tl - prev;
+                            dhi = cum - tl;
+                        }
+                    }
                 }
             }
-            ce = ce >= 0 ? ce : lp;   // rounding: the lane's last element with mass
+            if (ce < 0) {   // rounding: the lane's last element with mass, at its bound
+                ce = lp;
+                dlo = 0.0f;
+            }
             cand = __shfl_sync(kFull, lane * E + ce, src);
+            if (NEAR)
+                near = __shfl_sync(kFull, fminf(dlo, dhi) < band ? 1 : 0, src) != 0;
         }
     }
-    if (cand < 0)   // beyond the mass (rounding): the strip's last element with mass
+    if (cand < 0) {   // beyond the mass (rounding): the strip's last element with mass
         cand = __reduce_max_sync(kFull, lastpos);
+        near = true;
+    }
     return cand;
+}
+
+// Whether the draw's point lies within `band` of a bound of the token the
+// pick takes (the same pick, with the distances tracked): a separate call,
+// made only when counters are requested, so the draw path itself is the
+// plain pick.
+template <typename T, int NV>
+__device__ __noinline__ bool draw_is_near(uint4 tv, uint4 dv, bool use_r, float m_t, float inv_st, float m_d,
+                                          float inv_sd, float c, float tc, bool beyond, int lane, float band)
+{
+    bool near = false;
+    (void)pick_in_strip<T, NV, true>(tv, dv, use_r, m_t, inv_st, m_d, inv_sd, c, tc, beyond, lane, band, near);
+    return near;
 }
 
 // WIDE: more than 32 warp ranges per row (lanes hold two partials each in
@@ -1398,12 +1426,13 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
                     Wj2 = bonus ? (xw.x == -INFINITY ? 0.0f : xw.y * weight(xw.x, m_t, c))
                                 : (use_r ? wtot2.x : wtot2.y);
                 // the warp whose range holds u * S, and the mass left inside it
-                float t = 0.0f;
+                float t = 0.0f, S_draw = 0.0f;   // the point and the total mass
                 bool beyond = false;
                 int owner = -1;
                 if constexpr (WIDE) {
                     const float S = warp_sum_comp(Wj + Wj2);
                     if (S > 0.0f && isfinite(S)) {
+                        S_draw = S;
                         t = ufb * S;
                         owner = select_cdf(P, [&](int j) { return j < 32 ? Wj : Wj2; }, t, beyond, lane);
                     }
@@ -1412,6 +1441,7 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
                     warp_incl_scan_comp(Wj, lane, s, cc);
                     const float S = __shfl_sync(kFull, s, 31) + __shfl_sync(kFull, cc, 31);
                     if (S > 0.0f && isfinite(S)) {
+                        S_draw = S;
                         t = ufb * S;
                         const unsigned hit = __ballot_sync(kFull, lane < P && Wj > 0.0f && t < s + cc);
                         if (hit) {
@@ -1464,10 +1494,15 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
                             const uint4* vd = reinterpret_cast<const uint4*>(slot_d + (size_t)jc * CH);
                             const uint4 tk = vt[ks * 32 + lane];
                             const uint4 dk = use_r ? vd[ks * 32 + lane] : tk;
-                            const int ce = pick_in_strip<T, NV>(tk, dk, use_r, m_t, inv_st, m_d, inv_sd, c, tc,
-                                                                beyond, lane);
+                            bool near = false;
+                            const int ce = pick_in_strip<T, NV, false>(tk, dk, use_r, m_t, inv_st, m_d, inv_sd, c,
+                                                                       tc, beyond, lane, 0.0f, near);
                             if (ce >= 0)
                                 token = e0 + jc * CH + ks * 32 * E + ce;
+                            if (a.want_stats && token >= 0 && token < V &&
+                                draw_is_near<T, NV>(tk, dk, use_r, m_t, inv_st, m_d, inv_sd, c, tc, beyond, lane,
+                                                    1e-6f * S_draw) && lane == 0)
+                                atomicAdd(a.stats + 6, 1ull);
                         }
                     }
                     write_outputs(row.b, n, (token >= 0 && token < V) ? token : -1, cur_sv.tok);

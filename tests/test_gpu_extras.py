@@ -126,6 +126,82 @@ def test_stats_match_the_oracles_walk(dev):
         assert again[k] == 2 * got[k]
 
 
+def _draw_rows(inp: dict, ref: dict, b: int):
+    """The oracle's final-draw distribution of sequence b (fp64, normalised)
+    and its CDF, or None when the draw is not a sampling draw with mass."""
+    K = int(inp["K"][b])
+    n = int(ref["num_accepted"][b])
+    T = float(inp["temperature"][b])
+    if n < 0 or T == 0.0:
+        return None
+    drow = inp["draft"][b, n] if n < K else None
+    r, code = oracle.final_distribution(inp["target"][b, n], drow, inp["dtype"], T)
+    if code == 0:   # (2: no residual mass, r is p: the distribution drawn from all the same)
+        return None
+    return np.cumsum(r)
+
+
+def _draw_tie_counts(inp: dict, ref: dict):
+    """(draws within 1e-6 of a bound of the drawn token's CDF interval, draws
+    whose distance lies in [0.8e-6, 1.2e-6], where fp32 rounding may decide
+    either way), from the oracle's fp64 CDF."""
+    near = amb = 0
+    for b in range(inp["B"]):
+        C = _draw_rows(inp, ref, b)
+        if C is None:
+            continue
+        K, n = int(inp["K"][b]), int(ref["num_accepted"][b])
+        j = int(ref["out_tokens"][b, n])
+        u = float(inp["uniforms"][b, K])
+        lo = C[j - 1] if j > 0 else 0.0
+        dist = min(abs(u - lo), abs(C[j] - u))
+        near += dist < 1e-6
+        amb += 0.8e-6 <= dist <= 1.2e-6
+    return near, amb
+
+
+@pytest.mark.parametrize("dtype,V", [("bf16", 6000), ("f32", 5003), ("f32", 700), ("bf16", 257)])
+def test_draw_near_ties_match_the_oracle(dev, dtype, V):
+    """sv_stats.draw_near_ties counts the final draws whose point lies within
+    1e-6 of a bound of the drawn token's interval, as the oracle flags them
+    (V = 700 and 257 take the small-vocabulary kernel).  The final uniforms
+    of most sampling sequences are planted 5e-7 below or above a CDF bound
+    in the middle of the distribution (the tokens on both sides with mass
+    above 1e-5), so the count is large; draws that fall near the band's own edge
+    by chance are the only slack allowed."""
+    B = 40
+    temps = np.where(np.arange(B) % 4 == 0, 0.0, 1.0).astype(np.float32)
+    inp = W.make_host(B, W.configs.ragged_k(7, B), V, dtype, 2.0, 0.6, temps, seed=V + 5)
+    ref = oracle_ref(inp)
+    planted = 0
+    for b in range(B):
+        C = _draw_rows(inp, ref, b)
+        if C is None or b % 5 == 4:   # leave some draws as they are
+            continue
+        j = int(np.searchsorted(C, 0.5))
+        r = np.diff(np.concatenate([[0.0], C]))
+        after = np.flatnonzero(r[j + 1:] > 0)   # the next token with mass starts at C_j
+        if r[j] < 1e-5 or len(after) == 0 or r[j + 1 + after[0]] < 1e-5:
+            continue
+        u = np.float32(C[j] + (5e-7 if planted % 2 else -5e-7))
+        if abs(float(u) - C[j]) >= 9e-7:   # the float32 grid near C_j is coarser than the band
+            continue
+        inp["uniforms"][b, int(inp["K"][b])] = u
+        planted += 1
+    assert planted >= 10
+    ref = oracle_ref(inp)   # the walks are unchanged; the draws moved
+    want, amb = _draw_tie_counts(inp, ref)
+    assert want >= planted
+    d = to_device(inp, dev)
+    ws = sv.Workspace(B, int(inp["Kmax"]), V, dtype_code(dtype), dev)
+    st = sv.Stats(dev)
+    t, n = run_gpu(d, "ex", workspace=ws, stats=st)
+    # every planted draw is a tie: only the counted ties may differ
+    compare(ref, t, n, inp=inp, max_ties=B)
+    got = st.read()["draw_near_ties"]
+    assert abs(got - want) <= amb, (got, want, amb)
+
+
 def test_kv_len_advances_by_committed_tokens(dev):
     """kv_len[b] += 1 + n_b for valid sequences, unchanged for invalid ones."""
     import torch
