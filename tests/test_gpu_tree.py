@@ -142,3 +142,30 @@ def test_tree_verification_replays_in_a_cuda_graph(dev):
         g.replay()
         torch.cuda.synchronize()
         _compare(d, (ot.cpu().numpy(), op.cpu().numpy(), ol.cpu().numpy()))
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_random_tree_shapes_match_oracle(dev, seed):
+    """Seeded random trees: node count 1..32, each node's parent drawn among
+    the earlier nodes (wide, deep and uneven trees), vocabulary, dtype,
+    noise and temperature mix drawn per case; every output against the
+    oracle, bit-exact outside ties."""
+    rng = np.random.default_rng(7000 + seed)
+    N = int(rng.integers(1, 33))
+    parents = np.array([-1] + [int(rng.integers(0, n)) for n in range(1, N)], np.int32)
+    V = int(rng.choice([1031, 3001, 7000, 20011]))
+    dtype = "bf16" if rng.random() < 0.5 else "f32"
+    B = int(rng.integers(4, 24))
+    temps = rng.choice(np.array([0.0, 0.6, 1.0, 1.5], np.float32), size=B)
+    d = W.make_tree_host(B, parents, V, dtype, float(rng.choice([1.0, 2.0, 3.0])),
+                         float(rng.choice([0.3, 1.0, 2.0])), temps, seed=7000 + seed)
+    _compare(d, _run(d, dev))
+
+
+def test_many_trees_exercise_both_claim_paths(dev):
+    """More trees than two waves of clusters: trees are claimed a tree ahead
+    (with the next root's rows prefetched) early in the batch and when a tree
+    ends near its end; every tree against the oracle."""
+    d = W.make_tree_host(300, W.full_tree(2, 3), 1031, "bf16", 2.0, 1.0,
+                         np.where(np.arange(300) % 5 == 0, 0.0, 1.0).astype(np.float32), seed=7100)
+    _compare(d, _run(d, dev))
