@@ -10,7 +10,7 @@
 //  * st.async: a store into another cluster CTA's shared memory that
 //    completes on that CTA's mbarrier transaction count;
 //  * ex2.approx, the NaN-propagating max (scalar, three-input and bf16x2) and
-//    the packed two-lane fp32 arithmetic of sm_100+ (add/mul/fma .f32x2,
+//    the packed two-lane fp32 arithmetic of sm_100+ (add/sub/mul/fma .f32x2,
 //    each lane rounded to nearest like its scalar form).
 #pragma once
 
@@ -196,6 +196,13 @@ __device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c)
 {
     uint64_t y;
     asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(y) : "l"(a), "l"(b), "l"(c));
+    return y;
+}
+
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b)
+{
+    uint64_t y;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(y) : "l"(a), "l"(b));
     return y;
 }
 

@@ -434,40 +434,42 @@ template <int NV> struct Lane<__nv_bfloat16, NV> {
         r = fmaxf(__fsub_rn(p, q), 0.0f);
     }
     // per strip, the lane's sum of residual terms; over all strips, the
-    // lane's sum of the weights of p
+    // lane's sum of the weights of p.  Element pairs of each word: the same
+    // per-element steps as resid_term2 (fma, ex2, multiply by the inverse
+    // sum, subtract, clamp), fewer instructions.
     __device__ static __forceinline__ void resid_strips(const uint4 (&t)[NV], const uint4 (&d)[NV],
                                                         float mt, float ist, float md, float isd,
                                                         float c, float (&rs)[NV], float& ps)
     {
-        const uint64_t Cc = f2_pack(c, c), NR = f2_pack(-ref_of(mt, c), -ref_of(md, c));
-        const uint64_t IS = f2_pack(ist, isd);
-        // (residual, p) pairs accumulated with one packed add per element,
-        // two accumulators per strip; p's sums carried over the strips
-        float p_all = 0.0f;
+        const uint64_t Cc = f2_pack(c, c);
+        const float rt = ref_of(mt, c), rd = ref_of(md, c);
+        const uint64_t NT = f2_pack(-rt, -rt), ND = f2_pack(-rd, -rd);
+        const uint64_t IT = f2_pack(ist, ist), ID = f2_pack(isd, isd);
+        uint64_t pacc = f2_pack(0.0f, 0.0f);
 #pragma unroll
         for (int k = 0; k < NV; ++k) {
             const uint32_t wt[4] = {t[k].x, t[k].y, t[k].z, t[k].w};
             const uint32_t wd[4] = {d[k].x, d[k].y, d[k].z, d[k].w};
-            uint64_t acc0 = f2_pack(0.0f, 0.0f), acc1 = acc0;
+            uint64_t racc = f2_pack(0.0f, 0.0f);
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    float r, et;
-                    resid_term2(wt[h], wd[h], half, Cc, NR, IS, r, et);
-                    if (half)
-                        acc1 = f2_add(acc1, f2_pack(r, et));
-                    else
-                        acc0 = f2_add(acc0, f2_pack(r, et));
-                }
+                float a0, a1, b0, b1;
+                f2_unpack(f2_fma(pair(wt[h]), Cc, NT), a0, a1);
+                f2_unpack(f2_fma(pair(wd[h]), Cc, ND), b0, b1);
+                const uint64_t et = f2_pack(ex2_approx(a0), ex2_approx(a1));
+                const uint64_t ed = f2_pack(ex2_approx(b0), ex2_approx(b1));
+                float r0, r1;
+                f2_unpack(f2_sub(f2_mul(et, IT), f2_mul(ed, ID)), r0, r1);
+                racc = f2_add(racc, f2_pack(fmaxf(r0, 0.0f), fmaxf(r1, 0.0f)));
+                pacc = f2_add(pacc, et);
             }
-            float r0, e0, r1, e1;
-            f2_unpack(acc0, r0, e0);
-            f2_unpack(acc1, r1, e1);
+            float r0, r1;
+            f2_unpack(racc, r0, r1);
             rs[k] = r0 + r1;
-            p_all += e0 + e1;
         }
-        ps = p_all;
+        float p0, p1;
+        f2_unpack(pacc, p0, p1);
+        ps = p0 + p1;
     }
     __device__ static __forceinline__ void resid_elem(const uint4& t, const uint4& d, int e, uint64_t Cc,
                                                       uint64_t NR, uint64_t IS, float& r, float& et)
@@ -552,30 +554,37 @@ template <int NV> struct Lane<float, NV> {
                                                         float mt, float ist, float md, float isd,
                                                         float c, float (&rs)[NV], float& ps)
     {
-        const uint64_t Cc = f2_pack(c, c), NR = f2_pack(-ref_of(mt, c), -ref_of(md, c));
-        const uint64_t IS = f2_pack(ist, isd);
-        float p_all = 0.0f;
+        const uint64_t Cc = f2_pack(c, c);
+        const float rt = ref_of(mt, c), rd = ref_of(md, c);
+        const uint64_t NT = f2_pack(-rt, -rt), ND = f2_pack(-rd, -rd);
+        const uint64_t IT = f2_pack(ist, ist), ID = f2_pack(isd, isd);
+        uint64_t pacc = f2_pack(0.0f, 0.0f);
 #pragma unroll
         for (int k = 0; k < NV; ++k) {
-            const uint32_t wt[4] = {t[k].x, t[k].y, t[k].z, t[k].w};
-            const uint32_t wd[4] = {d[k].x, d[k].y, d[k].z, d[k].w};
-            uint64_t acc0 = f2_pack(0.0f, 0.0f), acc1 = acc0;
+            const uint64_t tp[2] = {f2_pack(__uint_as_float(t[k].x), __uint_as_float(t[k].y)),
+                                    f2_pack(__uint_as_float(t[k].z), __uint_as_float(t[k].w))};
+            const uint64_t dp[2] = {f2_pack(__uint_as_float(d[k].x), __uint_as_float(d[k].y)),
+                                    f2_pack(__uint_as_float(d[k].z), __uint_as_float(d[k].w))};
+            uint64_t racc = f2_pack(0.0f, 0.0f);
 #pragma unroll
-            for (int h = 0; h < 4; ++h) {
-                float r, et;
-                resid_term2(wt[h], wd[h], 0, Cc, NR, IS, r, et);
-                if (h & 1)
-                    acc1 = f2_add(acc1, f2_pack(r, et));
-                else
-                    acc0 = f2_add(acc0, f2_pack(r, et));
+            for (int h = 0; h < 2; ++h) {
+                float a0, a1, b0, b1;
+                f2_unpack(f2_fma(tp[h], Cc, NT), a0, a1);
+                f2_unpack(f2_fma(dp[h], Cc, ND), b0, b1);
+                const uint64_t et = f2_pack(ex2_approx(a0), ex2_approx(a1));
+                const uint64_t ed = f2_pack(ex2_approx(b0), ex2_approx(b1));
+                float r0, r1;
+                f2_unpack(f2_sub(f2_mul(et, IT), f2_mul(ed, ID)), r0, r1);
+                racc = f2_add(racc, f2_pack(fmaxf(r0, 0.0f), fmaxf(r1, 0.0f)));
+                pacc = f2_add(pacc, et);
             }
-            float r0, e0, r1, e1;
-            f2_unpack(acc0, r0, e0);
-            f2_unpack(acc1, r1, e1);
+            float r0, r1;
+            f2_unpack(racc, r0, r1);
             rs[k] = r0 + r1;
-            p_all += e0 + e1;
         }
-        ps = p_all;
+        float p0, p1;
+        f2_unpack(pacc, p0, p1);
+        ps = p0 + p1;
     }
     __device__ static __forceinline__ void resid_elem(const uint4& t, const uint4& d, int e, uint64_t Cc,
                                                       uint64_t NR, uint64_t IS, float& r, float& et)
