@@ -244,14 +244,16 @@ def test_packed_logits_give_the_padded_results(dev, dtype):
     compare(oracle_ref(inp), t1.cpu().numpy(), n1.cpu().numpy(), inp=inp)
 
 
-def test_cuda_graph_replays_the_verification(dev):
+@pytest.mark.parametrize("V", [12345, 700])
+def test_cuda_graph_replays_the_verification(dev, V):
     """A verification captured into a CUDA graph (after one ordinary call of
     its shape) replays on whatever the captured buffers hold: the oracle's
     results for the inputs at capture time and for new inputs copied into the
     same buffers, with ordinary calls of other shapes in between (which reuse
-    the library's rotating header slots, not the graph's)."""
+    the library's rotating header slots, not the graph's).  V = 700 takes
+    the small-vocabulary kernel."""
     import torch
-    B, V = 48, 12345
+    B = 48
     K = W.configs.ragged_k(5, B)
     temps = np.where(np.arange(B) % 3 == 0, 0.0, 1.0).astype(np.float32)
     inp1 = W.make_host(B, K, V, "bf16", 2.0, 1.0, temps, seed=71)
