@@ -93,6 +93,18 @@ def test_high_acceptance_reaches_bonus_rows(dev):
     assert np.mean(got_n == 6) > 0.5
 
 
+@pytest.mark.parametrize("dtype,V", [("bf16", 3001), ("f32", 2500), ("bf16", 700), ("f32", 600)])
+def test_longest_walks_reach_position_32(dev, dtype, V):
+    """K = 32 (the most a call takes) with drafts close to the target, so
+    that walks run through all 32 tests to the bonus row at position 32:
+    the last lane's token and uniform, the final uniform in slot 32 and a
+    33-token output row (V = 700 and 600 take the small-vocabulary kernel)."""
+    T = np.where(np.arange(8) % 4 == 0, 0.0, 1.0).astype(np.float32)
+    inp = W.make_host(8, 32, V, dtype, 2.0, 0.01, T, seed=V + 32)
+    ref, got_t, got_n, _ = _check(inp, dev)
+    assert np.any(got_n == 32)
+
+
 def test_greedy_ties_lowest_index(dev):
     inp = W.make_host(16, 4, 6000, "bf16", 2.0, 1.0, 0.0, seed=6)
     # coarse logits: many exact ties at the row maximum
