@@ -400,6 +400,8 @@ def run_ours(args):
     roofline = dict(bound="hbm", achieved=round(achieved, 1), peak=peaks["hbm_gbs"], unit="GB/s",
                     frac=round(achieved / peaks["hbm_gbs"], 4), traffic=traffic,
                     bytes_algorithmic=bytes_need, peak_source=peaks["source"],
+                    traffic_ratio=round(traffic / bytes_need, 4) if traffic else None,
+                    frac_of_nominal_8000_gbs=round(achieved / 8000.0, 4),
                     kernel="sv_sweep_kernel",
                     duration="CUDA events around each spec_verify_ws call: the 1-kernel step "
                              "plus its 16-byte counter reset")
@@ -507,6 +509,7 @@ def run_ours(args):
             clocks=clk,
             detail=dict(
                 mean_accepted=float(np.mean(nacc)), bytes_needed=bytes_need,
+                rows_per_s=round(bytes_need / (V * (2 if ldtype == "bf16" else 4)) / (med_ms / 1e3), 1),
                 bytes_all_rows=bytes_all, ms_median=round(med_ms, 5),
                 ms_min=round(min(times), 5),
                 verify_all=dict(ms_median=round(ms_all, 5),
