@@ -323,21 +323,28 @@ def run_ours(args):
     # between the step's events.
     flush = torch.empty(max(2 * l2, 1 << 30), dtype=torch.uint8, device=dev)
 
-    def step(verify_all=False):
+    # the host copy of the temperatures a serving loop holds anyway: with it the
+    # launch gives the greedy sequences to split clusters (same outputs)
+    hint = None if args.no_temperature_hint else np.asarray(d["temperature_host"], np.float32)
+
+    def step(verify_all=False, use_hint=True):
         if verify_all:
             sv.spec_verify_ex(*call_args, ws, verify_all=True, out_tokens=out_t,
                               out_num_accepted=out_n)
+        elif hint is not None and use_hint:
+            sv.spec_verify_ex(*call_args, ws, out_tokens=out_t, out_num_accepted=out_n,
+                              temperature_host=hint)
         else:
             sv.spec_verify_ws(*call_args, ws, out_tokens=out_t, out_num_accepted=out_n)
 
-    def timed(nsteps, verify_all=False):
+    def timed(nsteps, verify_all=False, use_hint=True):
         evs = []
         for _ in range(nsteps):
             flush.fill_(1)
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-            step(verify_all)
+            step(verify_all, use_hint)
             e1.record(stream)
             evs.append((e0, e1))
         torch.cuda.synchronize()
@@ -391,6 +398,12 @@ def run_ours(args):
     # verify-every-row variant of the same step (same outputs, all bytes read)
     times_all = timed(max(3, args.steps // 2), verify_all=True)
     ms_all = statistics.median(times_all)
+    # the same step without the temperature hint (spec_verify_ws: no split)
+    nacc_hinted = out_n.cpu().numpy()
+    times_plain = timed(max(3, args.steps // 2), use_hint=False) if hint is not None else times
+    ms_plain = statistics.median(times_plain)
+    torch.cuda.synchronize()
+    plain_same = bool(np.array_equal(out_n.cpu().numpy(), nacc_hinted))
     geometry = sv.sv_geometry(B, Kmax, V, dcode)
 
     peaks = _peaks()
@@ -403,8 +416,10 @@ def run_ours(args):
                     traffic_ratio=round(traffic / bytes_need, 4) if traffic else None,
                     frac_of_nominal_8000_gbs=round(achieved / 8000.0, 4),
                     kernel="sv_sweep_kernel",
-                    duration="CUDA events around each spec_verify_ws call: the 1-kernel step "
-                             "plus its 16-byte counter reset")
+                    duration=("CUDA events around each spec_verify_ex call with the host "
+                              "temperature copy: " if hint is not None else
+                              "CUDA events around each spec_verify_ws call: ") +
+                             "the 1-kernel step plus its 16-byte counter reset")
 
     # ---- end to end through the host entry point (pinned buffers) ----
     e2e = None
@@ -504,6 +519,7 @@ def run_ours(args):
                         else f"first {B} sequences of: {WORKLOAD_TEXT[widx]}",
                         bench_workload=widx, logits=ldtype,
                         B=B, Kmax=Kmax, V=V, positions_per_step=pos_per_step,
+                        temperature_hint=hint is not None,
                         l2="flushed before every step (1 GiB write, > 2x L2)", parallelism=f"dp{world}"),
             roofline=roofline, cpu_baseline=cpu, e2e=e2e, gpu_launches=args.steps,
             clocks=clk,
@@ -512,6 +528,10 @@ def run_ours(args):
                 rows_per_s=round(bytes_need / (V * (2 if ldtype == "bf16" else 4)) / (med_ms / 1e3), 1),
                 bytes_all_rows=bytes_all, ms_median=round(med_ms, 5),
                 ms_min=round(min(times), 5),
+                without_temperature_hint=dict(ms_median=round(ms_plain, 5),
+                                              frac=round(bytes_need / (ms_plain / 1e3) / 1e9 /
+                                                         peaks["hbm_gbs"], 4),
+                                              same_outputs=plain_same),
                 verify_all=dict(ms_median=round(ms_all, 5),
                                 gbs=round(bytes_all / (ms_all / 1e3) / 1e9, 1),
                                 frac=round(bytes_all / (ms_all / 1e3) / 1e9 / peaks["hbm_gbs"], 4)),
@@ -754,6 +774,9 @@ def main():
     ap.add_argument("--no-other-workloads", action="store_true",
                     help="time only the selected workload (the default run also times "
                          "workloads 0-3 and the 200k toy pair into detail.workloads)")
+    ap.add_argument("--no-temperature-hint", action="store_true",
+                    help="time spec_verify_ws (no host copy of the temperatures, so no split "
+                         "clusters) instead of spec_verify_ex with temperature_host")
     ap.add_argument("--sequences", type=int, default=None,
                     help="the workload's first N sequences only (profiling captures)")
     ap.add_argument("--op", choices=["verify", "sample", "tree"], default="verify",

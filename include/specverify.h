@@ -58,7 +58,7 @@
 extern "C" {
 #endif
 
-#define SV_ABI_VERSION 4
+#define SV_ABI_VERSION 5
 /* Largest per-sequence draft count: one warp ballot covers the accept bits. */
 #define SV_K_MAX 32
 
@@ -152,6 +152,20 @@ typedef struct {
  *                   copies already issued still land and are waited for, with
  *                   the normal bound, before the kernel exits.  Nothing faults
  *                   or hangs; the next call on the workspace is unaffected.
+ *   temperature_host  host [B] float32, or NULL: a host copy of the device
+ *                   `temperature` array, read during the call only.  It lets
+ *                   the launch give the greedy sequences (T = 0, which read no
+ *                   draft rows) to clusters split in two independent halves,
+ *                   two greedy rows in the shared memory a sampling row
+ *                   takes, while the other clusters take the sampling
+ *                   sequences first.  The outputs are the same as without it.
+ *                   Used by plain calls (no diagnostics, verify_all or tuning)
+ *                   of the cluster kernel (V > 1024, 16-byte aligned rows)
+ *                   with enough sequences of both kinds; ignored otherwise.
+ *                   It must match the device array: a sequence it calls
+ *                   greedy whose device temperature is not 0 may get outputs
+ *                   -1 and set bit 1 of the workspace error word
+ *                   (sv_workspace_errors returns SV_ERR_INVALID_ARG).
  * Tuning options change only the fp32 summation grouping: results agree
  * with the automatic geometry except within the rounding of those sums.
  */
@@ -164,6 +178,7 @@ typedef struct {
     int32_t* kv_len;
     int32_t packed_logits;
     int32_t expire_copy_waits;
+    const float* temperature_host;   /* since ABI version 5 */
 } sv_options;
 
 /* Human-readable name of a status code (static storage). */
@@ -296,9 +311,11 @@ sv_status spec_verify_ex(const void* target_logits, const void* draft_logits, sv
 
 /*
  * Device-side error flags recorded in a workspace by the last call that used
- * it (bit 0: a bounded shared-memory copy wait gave up).  Copies the word to
- * *flags, clears it, and synchronises `stream`.  Returns SV_ERR_TIMEOUT when
- * bit 0 was set, SV_OK otherwise.
+ * it (bit 0: a bounded shared-memory copy wait gave up; bit 1: a sequence
+ * sv_options.temperature_host called greedy had a nonzero device
+ * temperature).  Copies the word to *flags, clears it, and synchronises
+ * `stream`.  Returns SV_ERR_TIMEOUT when bit 0 was set, else
+ * SV_ERR_INVALID_ARG when bit 1 was, SV_OK otherwise.
  */
 sv_status sv_workspace_errors(void* workspace, uint32_t* flags, cudaStream_t stream);
 

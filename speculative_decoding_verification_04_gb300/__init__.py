@@ -52,7 +52,8 @@ class SVOptions(ctypes.Structure):
     _fields_ = [("diag", SVDiag), ("verify_all", ctypes.c_int32),
                 ("chunks_per_cta", ctypes.c_int32), ("chunks_per_warp", ctypes.c_int32),
                 ("stats", ctypes.c_void_p), ("kv_len", ctypes.c_void_p),
-                ("packed_logits", ctypes.c_int32), ("expire_copy_waits", ctypes.c_int32)]
+                ("packed_logits", ctypes.c_int32), ("expire_copy_waits", ctypes.c_int32),
+                ("temperature_host", ctypes.c_void_p)]
 
 
 STATS_FIELDS = ("sequences", "invalid", "tested", "accepted", "committed", "near_ties", "draw_near_ties")
@@ -312,13 +313,16 @@ def spec_verify_ex(target, draft, draft_tokens, uniforms, temperature, K, worksp
                    diag: dict | None = None, verify_all: bool = False, chunks_per_cta: int = 0,
                    chunks_per_warp: int = 0, out_tokens=None,
                    out_num_accepted=None, stream=None, stats: "Stats | None" = None,
-                   kv_len=None, packed: bool = False, expire_copy_waits: bool = False):
+                   kv_len=None, packed: bool = False, expire_copy_waits: bool = False,
+                   temperature_host=None):
     """spec_verify_ex; ``diag`` maps p_x / q_x / resid_mass / final_row to tensors,
     ``stats`` accumulates the call's counters, ``kv_len`` (int32 [B] CUDA
     tensor) is advanced in place by 1 + n_b for every valid sequence; ``packed``
     takes target [sum(K+1), V] and draft [sum(K), V] packed by K;
     ``expire_copy_waits`` (testing only) makes every bounded copy wait give up
-    at once, to exercise the timeout path."""
+    at once, to exercise the timeout path; ``temperature_host`` (a host copy
+    of ``temperature``, anything numpy turns into float32 [B]) lets the
+    launch give the greedy sequences to split clusters."""
     k, kp, B, Kmax, V = _common(target, draft, draft_tokens, uniforms, temperature, K)
     out_tokens, out_num_accepted = _outputs(B, Kmax, target.device, out_tokens, out_num_accepted)
     opt = SVOptions()
@@ -338,6 +342,13 @@ def spec_verify_ex(target, draft, draft_tokens, uniforms, temperature, K, worksp
         opt.kv_len = kv_len.data_ptr()
     opt.packed_logits = 1 if packed else 0
     opt.expire_copy_waits = 1 if expire_copy_waits else 0
+    th = None
+    if temperature_host is not None:
+        import numpy as np
+        th = np.ascontiguousarray(np.asarray(temperature_host, dtype=np.float32))
+        if th.shape != (B,):
+            raise ValueError("temperature_host must have shape [B]")
+        opt.temperature_host = th.ctypes.data
     sp, _ = _stream(stream)
     st = _load().spec_verify_ex(_dptr(target), _dptr(draft), _dtype_code(target),
                                 _dptr(draft_tokens), _dptr(uniforms), _dptr(temperature), B, kp, V,
@@ -441,10 +452,12 @@ def spec_verify_host(target, draft, draft_tokens, uniforms, temperature, K, stag
 
 
 def sv_workspace_errors(workspace: Workspace, stream=None) -> int:
-    """Device-side error flags of the last call on ``workspace`` (synchronises)."""
+    """Device-side error flags of the last call on ``workspace`` (synchronises):
+    bit 0 a bounded wait gave up, bit 1 a wrong temperature hint."""
     flags = ctypes.c_uint32(0)
     sp, _ = _stream(stream)
     st = _load().sv_workspace_errors(workspace.ptr, ctypes.byref(flags), sp)
-    if st not in (SV_OK, SV_ERR_TIMEOUT):
+    # the status only restates the flags (timeout: bit 0; invalid argument: bit 1)
+    if st not in (SV_OK, SV_ERR_TIMEOUT) and not (st == SV_ERR_INVALID_ARG and flags.value & 2):
         _check(st, "sv_workspace_errors")
     return int(flags.value)

@@ -80,7 +80,7 @@ static int n_chunks(int V, int s)
 // every call; K, the order and the packed row starts written by the kernel
 // from the mapped header, or uploaded from pageable staging) ----
 struct WsLayout {
-    size_t err, next_unit, ready, K, order, seq_end, cu_t, cu_d, header_end, total;
+    size_t err, next_unit, ready, next_unit_g, K, order, seq_end, cu_t, cu_d, header_end, total;
 };
 
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -95,6 +95,7 @@ static bool ws_layout(int B, int Kmax, int V, sv_dtype dt, WsLayout* L)
     L->err = o;
     L->next_unit = o + 4;
     L->ready = o + 8;   // CTAs done copying the mapped header's K and order here
+    L->next_unit_g = o + 12;   // the greedy queue's claim counter (split launches)
     o = align256(o + 16);
     L->K = o;        o = align256(o + (size_t)B * 4);
     L->order = o;    o = align256(o + (size_t)B * 4);
@@ -108,7 +109,7 @@ static bool ws_layout(int B, int Kmax, int V, sv_dtype dt, WsLayout* L)
 
 struct DeviceInfo {
     int nsm = 0;
-    bool attrs_set[2][6] = {};
+    bool attrs_set[2][7] = {};
     void* static_scratch = nullptr;   // device address of g_static_scratch on this device
 };
 
@@ -126,14 +127,14 @@ static std::map<std::tuple<int, int, int, int, size_t>, int> g_fit;
 // chosen geometry per (device, V, dtype, B, Kmax, tuning overrides)
 static std::map<std::tuple<int, int, int, int, int, int, int, int, int>, Geom> g_pick;
 
-template <typename T, int NV, bool WIDE, bool HOST>
+template <typename T, int NV, bool WIDE, bool HOST, bool SPLIT = false>
 static cudaError_t prepare_kernels(int dev)
 {
     const int ti = sizeof(T) == 2 ? 1 : 0;
-    const int ni = NV == 1 ? 0 : NV == 2 ? 1 : (WIDE ? 3 : 2) + (HOST ? 2 : 0);
+    const int ni = SPLIT ? 6 : NV == 1 ? 0 : NV == 2 ? 1 : (WIDE ? 3 : 2) + (HOST ? 2 : 0);
     std::lock_guard<std::mutex> lk(g_mu);
     if (!g_dev[dev].attrs_set[ti][ni]) {
-        auto kern = sv_sweep_kernel<T, NV, WIDE, HOST>;
+        auto kern = sv_sweep_kernel<T, NV, WIDE, HOST, SPLIT>;
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              kSmemPerCtaMax);
         if (e != cudaSuccess)
@@ -304,21 +305,23 @@ static sv_status pick_geometry(int V, sv_dtype dt, int B, int Kmax, int override
     return SV_OK;
 }
 
-template <typename T, int NV, bool WIDE, bool HOST>
+template <typename T, int NV, bool WIDE, bool HOST, bool SPLIT = false>
 static cudaError_t launch_sweep(const Args& a, const Geom& g, cudaStream_t st, int dev)
 {
-    cudaError_t e = prepare_kernels<T, NV, WIDE, HOST>(dev);
+    cudaError_t e = prepare_kernels<T, NV, WIDE, HOST, SPLIT>(dev);
     if (e != cudaSuccess)
         return e;
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[1];
     sweep_config(&cfg, attr, g, g.clusters, st);
-    return cudaLaunchKernelEx(&cfg, sv_sweep_kernel<T, NV, WIDE, HOST>, a);
+    return cudaLaunchKernelEx(&cfg, sv_sweep_kernel<T, NV, WIDE, HOST, SPLIT>, a);
 }
 
 template <typename T>
 static cudaError_t launch_nv(const Args& a, const Geom& g, bool host, cudaStream_t st, int dev)
 {
+    if (a.split_clusters > 0)   // (the host checked: NV = 4, at most 32 ranges, device rows)
+        return launch_sweep<T, 4, false, false, true>(a, g, st, dev);
     const bool wide = g.C * g.nw > 32;
     switch (g.nv) {
     case 1: return launch_sweep<T, 1, false, false>(a, g, st, dev);
@@ -708,15 +711,51 @@ static sv_status run(const Call& c, int kmax, const sv_options* opt, void* ws, s
     const size_t up_bytes = packed ? L.header_end : L.seq_end;   // row starts only when packed
     memset(hdr, 0, L.K);   // error word, claim counter, ready count; every other field is written
     memcpy(hdr + L.K, c.K, (size_t)c.B * 4);
+    // Split launch: given the caller's host copy of the temperatures, the
+    // greedy sequences (T = 0) can go to split clusters, whose two halves
+    // each walk greedy rows in the shared memory one sampling row takes.
+    // Cg = clusters * nG / (nG + 6 nS) clusters are split: a sampling
+    // sequence keeps a whole cluster about six times as long as a greedy one
+    // keeps a half on the 1:1 mix of V = 128256 bf16 sequences, K ~ U{1..8};
+    // the whole clusters take what is left of the greedy queue once the
+    // sampling one is empty, so a low Cg costs less than a high one.  Only
+    // plain calls split (no diagnostics, verify-all or tuning), and only when
+    // the sampling sequences fill the whole clusters' first wave and the
+    // greedy ones the halves'.
+    int split_cg = 0, split_ns = c.B;
+    const float* th = opt ? opt->temperature_host : nullptr;
+    if (!small && th && !host_rows && !want_diag && !opt->verify_all &&
+        !(opt->chunks_per_cta || opt->chunks_per_warp || opt->expire_copy_waits) && g.nv == 4 &&
+        g.nw % 2 == 0 && g.C * g.nw <= 32 && g.clusters >= 2) {
+        int ng = 0;
+        for (int b = 0; b < c.B; ++b)
+            ng += th[b] == 0.0f ? 1 : 0;
+        const int ns = c.B - ng;
+        const long long cg = (long long)g.clusters * ng / ((long long)ng + 6LL * ns);
+        const int cgi = (int)std::min<long long>({cg, (long long)g.clusters - 1, (long long)ng / 2});
+        if (cgi >= 1 && ns >= g.clusters - cgi && g.clusters + cgi <= kFirstUnits) {
+            split_cg = cgi;
+            split_ns = ns;
+        }
+    }
     if (!small) {   // the claim order (the small-vocabulary kernel takes sequences in index order)
+        // by K, longest first; split: the sampling sequences, then the greedy ones
         int32_t* ord = reinterpret_cast<int32_t*>(hdr + L.order);
-        int cnt[SV_K_MAX + 2] = {0};
-        for (int b = 0; b < c.B; ++b)
-            ++cnt[SV_K_MAX - c.K[b] + 1];
-        for (int k = 1; k <= SV_K_MAX + 1; ++k)
-            cnt[k] += cnt[k - 1];
-        for (int b = 0; b < c.B; ++b)
-            ord[cnt[SV_K_MAX - c.K[b]]++] = b;
+        int pos = 0;
+        for (int cls = 0; cls < (split_cg > 0 ? 2 : 1); ++cls) {
+            auto in = [&](int b) { return split_cg == 0 || ((th[b] == 0.0f) == (cls == 1)); };
+            int cnt[SV_K_MAX + 2] = {0};
+            for (int b = 0; b < c.B; ++b)
+                if (in(b))
+                    ++cnt[SV_K_MAX - c.K[b] + 1];
+            cnt[0] = pos;
+            for (int k = 1; k <= SV_K_MAX + 1; ++k)
+                cnt[k] += cnt[k - 1];
+            for (int b = 0; b < c.B; ++b)
+                if (in(b))
+                    ord[cnt[SV_K_MAX - c.K[b]]++] = b;
+            pos = cnt[SV_K_MAX + 1];   // this class's end: the next one's start
+        }
     }
     if (packed) {
         int32_t* ct = reinterpret_cast<int32_t*>(hdr + L.cu_t);
@@ -774,12 +813,23 @@ static sv_status run(const Call& c, int kmax, const sv_options* opt, void* ws, s
     a.ready = reinterpret_cast<int*>(base + L.ready);
     a.K_dev = reinterpret_cast<int32_t*>(base + L.K);
     a.order_dev = reinterpret_cast<int32_t*>(base + L.order);
-    {
+    a.split_clusters = split_cg;
+    a.split_ns = split_ns;
+    a.next_unit_g = reinterpret_cast<int*>(base + L.next_unit_g);
+    if (!small) {
+        // first-wave slots: the first tickets of the queue (split: the
+        // sampling queue's for the whole clusters, then the greedy queue's,
+        // two for each split cluster)
         const int32_t* ord = reinterpret_cast<const int32_t*>(hdr + L.order);
-        const int nf = std::min(g.clusters, kFirstUnits);   // clusters <= B
+        const int nfull = g.clusters - split_cg;
+        const int nf = std::min(nfull, kFirstUnits);   // clusters <= B
         for (int k = 0; k < nf; ++k) {
             a.first_b[k] = ord[k];
             a.first_K[k] = c.K[ord[k]];
+        }
+        for (int k = 0; k < 2 * split_cg; ++k) {   // nfull + 2 split_cg <= kFirstUnits
+            a.first_b[nfull + k] = ord[split_ns + k];
+            a.first_K[nfull + k] = c.K[ord[split_ns + k]];
         }
     }
     a.p_x = want_diag ? dg->p_x : nullptr;
@@ -1111,7 +1161,7 @@ sv_status sv_workspace_errors(void* workspace, uint32_t* flags, cudaStream_t str
     if (cudaMemsetAsync(workspace, 0, 4, stream) != cudaSuccess)
         return SV_ERR_CUDA;
     *flags = v;
-    return (v & sv::kErrWaitTimeout) ? SV_ERR_TIMEOUT : SV_OK;
+    return (v & sv::kErrWaitTimeout) ? SV_ERR_TIMEOUT : (v & sv::kErrHint) ? SV_ERR_INVALID_ARG : SV_OK;
 }
 
 size_t sv_host_staging_size(int32_t B, int32_t Kmax, int32_t V, sv_dtype dtype)

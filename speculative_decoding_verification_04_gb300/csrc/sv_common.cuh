@@ -33,7 +33,9 @@ enum : int {
     kDecRedo = 5       // weigh the row again against its maxima
 };
 
-enum : uint32_t { kErrWaitTimeout = 1u };
+// bit 0: a bounded wait gave up; bit 1: a sequence the caller's temperature
+// hint called greedy has a nonzero device temperature (its outputs are -1)
+enum : uint32_t { kErrWaitTimeout = 1u, kErrHint = 2u };
 
 struct Args {
     const void* tgt;
@@ -57,6 +59,12 @@ struct Args {
     // workspace
     uint32_t* err;
     int* next_unit;        // claim counter of the persistent sweep
+    // split launches (sv_options.temperature_host): the last split_clusters
+    // clusters walk greedy sequences in two halves each; the claim order holds
+    // the split_ns sampling sequences first, then the greedy ones, and
+    // next_unit_g hands out the greedy queue's tickets after its first wave
+    int split_clusters, split_ns;
+    int* next_unit_g;
     const int32_t* K;
     const int32_t* order;  // sequences in claim order (longest K first)
     // device copies of K and order in the workspace, filled by the kernel's

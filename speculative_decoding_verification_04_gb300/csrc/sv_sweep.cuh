@@ -327,6 +327,20 @@ __device__ __forceinline__ UnitPos first_unit_pos(const Args& a, int cid, int b,
     return unit_pos(a, b, ok);
 }
 
+// A half of a split cluster takes greedy sequences only (its slices have no
+// draft region): a sequence the caller's temperature hint placed in the greedy
+// queue but whose device temperature is not 0 is made unusable (outputs -1)
+// and flagged in the error word.
+__device__ __forceinline__ Row greedy_only(const Args& a, Row r, int lane)
+{
+    if (!(r.flags & kFGreedy)) {
+        r.flags &= ~kFUsable;
+        if (lane == 0)
+            atomicOr(a.err, kErrHint);
+    }
+    return r;
+}
+
 // The sequence's final-draw uniform (slot K_b), sampling sequences only.
 __device__ __forceinline__ float final_uniform(const Args& a, const Row& r)
 {
@@ -831,8 +845,16 @@ __device__ __noinline__ bool draw_is_near(uint4 tv, uint4 dv, bool use_r, float 
 // WIDE: more than 32 warp ranges per row (lanes hold two partials each in
 // the combines); the host launches it for exactly those geometries.  HOST:
 // the logits are device-mapped host memory, read with 16-byte loads instead
-// of bulk copies (and never prefetched into L2).
-template <typename T, int NV, bool WIDE, bool HOST>
+// of bulk copies (and never prefetched into L2).  SPLIT: the last
+// a.split_clusters clusters of the grid are split in two halves (warps
+// 0 .. nw/2 - 1 and nw/2 .. nw - 1 of every CTA), each half an independent
+// row walker over half the warp ranges, its slices in one region (target or
+// draft) of the CTA: they take the greedy sequences, which read no draft
+// rows, from a queue of their own (order entries from a.split_ns on; the
+// sampling sequences come first), two greedy rows in the shared memory one
+// row of a sampling sequence takes.  The other clusters take the sampling
+// queue, then what is left of the greedy one.
+template <typename T, int NV, bool WIDE, bool HOST, bool SPLIT = false>
 __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
 {
     using EL = Elem<T>;
@@ -844,27 +866,39 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const int nw = (int)(blockDim.x >> 5);
     const int C = a.C, V = a.V, Kmax = a.Kmax, KW = a.kw;
-    const int P = C * nw;   // warps per row
     const uint32_t rank = cluster_ctarank();
-    const int g = (int)rank * nw + w;   // this warp's range of the row
+    const int n_clusters = (int)(gridDim.x / (unsigned)C);
+    const int cid = (int)(blockIdx.x / (unsigned)C);   // this cluster: ticket cid first
+    // SPLIT: this warp's half (hv) and its place in it (wv); nwv warps of a
+    // CTA walk together
+    const bool half = SPLIT && cid >= n_clusters - a.split_clusters;
+    const int nwv = half ? (nw >> 1) : nw;
+    const int hv = half ? w / nwv : 0;
+    const int wv = half ? w - hv * nwv : w;
+    const int P = C * nwv;   // warps per row
+    const int g = (int)rank * nwv + wv;   // this warp's range of the row
     const int c_lo = range_lo(g, a.nchunks, P);
-    const int kwm = range_lo(g + 1, a.nchunks, P) - c_lo;   // chunks in range (0..KW)
+    const int kwm = range_lo(g + 1, a.nchunks, P) - c_lo;   // chunks in range
     const int e0 = c_lo * CH;                               // first element of the range
     const int n_el = max(0, min(e0 + kwm * CH, V) - e0);
-    const SweepLayout L = sweep_layout(nw, cta_chunks(a.nchunks, C), KW, CH * (int)sizeof(T), P);
+    const SweepLayout L = sweep_layout(nw, cta_chunks(a.nchunks, C), KW, CH * (int)sizeof(T), C * nw);
 
-    // the slice's place in the CTA's target and draft regions
-    const size_t off = (size_t)(c_lo - range_lo((int)rank * nw, a.nchunks, P)) * CH;
-    T* slot_t = reinterpret_cast<T*>(dsm) + off;
-    T* slot_d = reinterpret_cast<T*>(dsm + L.region_bytes) + off;
+    // the slice's place in the CTA's target and draft regions (a half's
+    // slices: in the target region for half 0, the draft region for half 1)
+    const size_t off = (size_t)(c_lo - range_lo((int)rank * nwv, a.nchunks, P)) * CH;
+    T* slot_t = reinterpret_cast<T*>(dsm + (hv ? L.region_bytes : 0)) + off;
+    T* slot_d = half ? slot_t : reinterpret_cast<T*>(dsm + L.region_bytes) + off;
     const uint32_t bar = smem_addr(dsm + L.bars + 8 * (size_t)w);
-    uint64_t* xbar = reinterpret_cast<uint64_t*>(dsm + L.xbar);
+    // a split cluster never takes a sampling row: half 1 exchanges its rows on
+    // the residual exchange's barriers and buffers, and keeps its claims in
+    // the (unused) strip-partial area
+    uint64_t* xbar = reinterpret_cast<uint64_t*>(dsm + (hv ? L.xbar2 : L.xbar));
     uint64_t* xbar2 = reinterpret_cast<uint64_t*>(dsm + L.xbar2);
-    float4* xbuf = reinterpret_cast<float4*>(dsm + L.xbuf);    // [2][P]
-    float2* xbuf2 = reinterpret_cast<float2*>(dsm + L.xbuf2);  // [2][P]
-    int2* xclaim = reinterpret_cast<int2*>(dsm + L.xclaim);    // [2]
-    const uint32_t xbarc = smem_addr(dsm + L.xbarc);
-    int* first = reinterpret_cast<int*>(dsm + L.first);
+    float4* xbuf = reinterpret_cast<float4*>(dsm + (hv ? L.xbuf2 : L.xbuf));   // [2][P]
+    float2* xbuf2 = reinterpret_cast<float2*>(dsm + L.xbuf2);                  // [2][P]
+    int2* xclaim = reinterpret_cast<int2*>(dsm + (hv ? L.stats + 16 : L.xclaim));   // [2]
+    const uint32_t xbarc = smem_addr(dsm + (hv ? L.stats : L.xbarc));
+    int* first = reinterpret_cast<int*>(dsm + (hv ? L.stats + 8 : L.first));
     float* stats = reinterpret_cast<float*>(dsm + L.stats) + (size_t)w * KW * 16;   // [kw][NV][4]
 
     // ---- set-up: barriers; -inf past V in this warp's range (copies never
@@ -878,6 +912,8 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
             mbar_init(smem_addr(&xbar2[1]), 1);
             mbar_init(xbarc, 1);
         }
+        if (half && wv == 0 && hv == 1)   // half 1's claim barrier
+            mbar_init(xbarc, 1);
         fence_mbar_init();
     }
     for (int j = n_el + lane; j < kwm * CH; j += 32) {
@@ -901,11 +937,15 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
     cluster_arrive();   // every CTA's barriers exist before any peer signals them
     cluster_wait();
 
-    // ---- per-warp schedule state (the same in every warp of the cluster) ----
-    const int n_clusters = (int)(gridDim.x / (unsigned)C);
-    const int cid = (int)(blockIdx.x / (unsigned)C);   // this cluster: ticket cid first
+    // ---- per-warp schedule state (the same in every warp of the walker) ----
+    // first-wave slot and ticket: cluster cid; with SPLIT, the sampling queue's
+    // tickets 0 .. n_full - 1 go to the whole clusters and the greedy queue's
+    // first 2 split_clusters tickets to the halves
+    const int n_full = n_clusters - (SPLIT ? a.split_clusters : 0);
+    const int fslot = half ? n_full + 2 * (cid - n_full) + hv : cid;
+    const int t0 = half ? a.split_ns + 2 * (cid - n_full) + hv : cid;
     bool hdr_dev = false;   // the header's device copy is complete (sticky)
-    const int u0 = cid < kFirstUnits ? a.first_b[cid] : ticket_unit(a, cid, hdr_dev);
+    const int u0 = fslot < kFirstUnits ? a.first_b[fslot] : ticket_unit(a, t0, hdr_dev);
     bool active = u0 >= 0 && u0 < a.B;
     int spare = -1;
     UnitPos spare_pos{0, 0, 0.0f};
@@ -915,7 +955,7 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
     // end it claims when it finishes a sequence, so that the last sequences
     // go to the clusters that are free first.  (The ticket of a row-ahead
     // claim is taken when the previous row is issued; see claim_next.)
-    int last_t = cid;        // the ticket of the cluster's latest claim
+    int last_t = t0;         // the ticket of the walker's latest claim
     uint32_t kc = 0;         // claims made between sequences (xbarc phase)
     bool broken = false;     // a slot wait gave up: no more copies, rows poisoned
     bool xbroken = false;    // an exchange wait gave up: leave the loop
@@ -923,9 +963,11 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
     Row row = make_row(a, 0, 0, 0, 0.0f, 0, 0);
     SeqVals cur_sv{0, 0.0f}, spare_sv{0, 0.0f};   // the current and the spare sequence's
     if (active) {
-        const UnitPos p0 = first_unit_pos(a, cid, u0, hdr_dev);
+        const UnitPos p0 = first_unit_pos(a, fslot, u0, hdr_dev);
         row = make_row(a, 0, p0.b, p0.Kb, p0.T, p0.tb, p0.db);
         cur_sv = seq_vals(a, u0, lane);
+        if (half)
+            row = greedy_only(a, row, lane);
     }
     Tok tk{0, 0.0f, 0u, 0u, 0};       // lane 0
     float uf = 0.0f;                  // lane 0: the sequence's final uniform
@@ -937,7 +979,22 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
 
     const T* tgt = static_cast<const T*>(a.tgt);
     const T* drf = static_cast<const T*>(a.drf);
-    const bool writer = rank == 0 && w == 0;   // writes per-row results and short outputs
+    const bool writer = rank == 0 && wv == 0;   // writes per-row results and short outputs
+    // (wv == 0: the warp of each CTA that arms its walker's exchange barriers)
+    // the walker's claims: whole clusters take the sampling queue, then the
+    // greedy one; halves the greedy one
+    auto claim = [&]() -> int {
+        if constexpr (SPLIT) {
+            if (!half) {
+                const int t = atomicAdd(a.next_unit, 1) + n_full;
+                if (t < a.split_ns)
+                    return t;
+            }
+            return a.split_ns + atomicAdd(a.next_unit_g, 1) + 2 * a.split_clusters;
+        } else {
+            return claim_ticket(a, n_clusters);
+        }
+    };
 
     // copies of this warp's range of row r into the slot (whole warp)
     auto issue = [&](const Row& r) {
@@ -1076,7 +1133,7 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
     if (active) {
         issue(row);
         if (writer && lane == 0 && claim_next)
-            ticket = claim_ticket(a, n_clusters);
+            ticket = claim();
         tk = tok_of(a, row, cur_sv);
         if (lane == 0) {
             tok_logits<T>(a, row, tk);
@@ -1093,7 +1150,7 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
         const bool usable = (row.flags & kFUsable) != 0;
         const float c = (usable && !greedy) ? log2e_over(row.T) : 0.0f;
         const bool want_claim = claim_next;   // this row carries a claim (ticket taken)
-        if (w == 0 && lane == 0)
+        if (wv == 0 && lane == 0)
             mbar_arrive_expect_tx(smem_addr(&xbar[p]), (uint32_t)P * 16u + (want_claim ? 8u : 0u));
 
         // ---- the slice, then the proposal's logits and the claim's sequence ----
@@ -1543,11 +1600,11 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
                 // claim now: rank 0's writer takes a ticket and sends the
                 // sequence to every CTA (st.async onto each CTA's claim
                 // mbarrier, bounded wait, as the row exchange)
-                if (w == 0 && lane == 0)
+                if (wv == 0 && lane == 0)
                     mbar_arrive_expect_tx(xbarc, 8u);
                 int cb = -1, ct = -1;
                 if (writer && lane == 0) {
-                    ct = claim_ticket(a, n_clusters);
+                    ct = claim();
                     cb = ticket_unit(a, ct, hdr_dev);
                 }
                 cb = __shfl_sync(kFull, cb, 0);
@@ -1574,6 +1631,8 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
             if (spare < 0)
                 break;
             row = make_row(a, 0, spare_pos.b, spare_pos.Kb, spare_pos.T, spare_pos.tb, spare_pos.db);
+            if (half)
+                row = greedy_only(a, row, lane);
             cur_sv = spare_sv;
             spare = -1;
             drawn = false;
@@ -1581,7 +1640,7 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
         issue(row);   // copies first: the logit loads overlap with them
         claim_next = spare < 0 && !exhausted && (long long)last_t + 2LL * n_clusters < (long long)a.B;
         if (writer && lane == 0 && claim_next)
-            ticket = claim_ticket(a, n_clusters);
+            ticket = claim();
         tk = tok_of(a, row, cur_sv);
         if (lane == 0) {
             tok_logits<T>(a, row, tk);

@@ -40,7 +40,7 @@ def test_status_strings_and_version():
                        (3, "SV_ERR_UNSUPPORTED"), (4, "SV_ERR_NO_MEMORY"), (5, "SV_ERR_TIMEOUT")]:
         assert sv.sv_status_string(code) == name
     assert sv.sv_status_string(99) == "SV_UNKNOWN_STATUS"
-    assert sv.sv_abi_version() == 4
+    assert sv.sv_abi_version() == 5
 
 
 def test_limits_and_workspace_sizes():
