@@ -165,7 +165,10 @@ typedef struct {
  *                   It must match the device array: a sequence it calls
  *                   greedy whose device temperature is not 0 may get outputs
  *                   -1 and set bit 1 of the workspace error word
- *                   (sv_workspace_errors returns SV_ERR_INVALID_ARG).
+ *                   (sv_workspace_errors returns SV_ERR_INVALID_ARG).  A call
+ *                   captured into a CUDA graph keeps the split it was
+ *                   captured with: its replays need the same sequences
+ *                   greedy.
  * Tuning options change only the fp32 summation grouping: results agree
  * with the automatic geometry except within the rounding of those sums.
  */

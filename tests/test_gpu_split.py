@@ -180,3 +180,46 @@ def test_hint_shape_is_checked():
     ws = sv.Workspace(4, 2, 3000, dtype_code("bf16"), dev)
     with pytest.raises(ValueError):
         run_gpu(d, "ex", workspace=ws, temperature_host=np.zeros(3, np.float32))
+
+
+def test_hint_with_packed_logits_counters_kv_and_graph(dev):
+    """Packed logits, the counters and the KV-length commit under a split
+    launch give the unhinted call's results; a hinted call captured into a
+    CUDA graph replays them."""
+    B = 300
+    d = _sampling_first(W.make_device(4, dev, B=B))
+    _check_splits(d)
+    K = np.asarray(d["K"], np.int32)
+    th = d["temperature"].cpu().numpy()
+    ws = sv.Workspace(B, d["Kmax"], d["V"], dtype_code(d["dtype"]), dev)
+    tp = torch.cat([d["target"][b, : K[b] + 1] for b in range(B)]).contiguous()
+    dp = torch.cat([d["draft"][b, : K[b]] for b in range(B)]).contiguous()
+    res = []
+    for hint in (None, th):
+        st = sv.Stats()
+        kv = torch.arange(B, dtype=torch.int32, device=dev)
+        t, n = sv.spec_verify_ex(tp, dp, d["tokens"], d["uniforms"], d["temperature"], K, ws,
+                                 packed=True, stats=st, kv_len=kv, temperature_host=hint)
+        torch.cuda.synchronize()
+        res.append((t.cpu().numpy(), n.cpu().numpy(), st.read(), kv.cpu().numpy()))
+        assert sv.sv_workspace_errors(ws) == 0
+    (t0, n0, s0, k0), (t1, n1, s1, k1) = res
+    assert np.array_equal(t0, t1) and np.array_equal(n0, n1)
+    assert s0 == s1 and np.array_equal(k0, k1)
+    assert s0["sequences"] == B
+    # captured after one ordinary call of the shape (which reserves the
+    # graph's header slot), replayed into cleared outputs
+    ot = torch.empty((B, d["Kmax"] + 1), dtype=torch.int32, device=dev)
+    on = torch.empty((B,), dtype=torch.int32, device=dev)
+    args = (d["target"], d["draft"], d["tokens"], d["uniforms"], d["temperature"], K)
+    sv.spec_verify_ex(*args, ws, out_tokens=ot, out_num_accepted=on, temperature_host=th)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        sv.spec_verify_ex(*args, ws, out_tokens=ot, out_num_accepted=on, temperature_host=th)
+    ot.fill_(-7)
+    on.fill_(-7)
+    g.replay()
+    torch.cuda.synchronize()
+    assert np.array_equal(ot.cpu().numpy(), t0) and np.array_equal(on.cpu().numpy(), n0)
+    assert sv.sv_workspace_errors(ws) == 0
