@@ -1128,8 +1128,21 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
     // one row before its order lookup: taken at the top of that row, the
     // lookup's address waited on the atomic's round trip and the claiming
     // warp started its pass about a microsecond after the others, holding
-    // up every row that carried a claim.
-    bool claim_next = spare < 0 && !exhausted && (long long)last_t + 2LL * n_clusters < (long long)a.B;
+    // up every row that carried a claim.  It claims ahead only while two
+    // waves of its queue remain (with SPLIT: the sampling queue for a whole
+    // cluster still taking from it, else the greedy queue, which every walker
+    // takes from in the end; a whole cluster that kept claiming ahead up to
+    // the end of the sampling queue made workload 4 1.2% slower).
+    auto ahead_ok = [&](int t) -> bool {
+        if constexpr (SPLIT) {
+            if (!half && t < a.split_ns)
+                return (long long)t + 2LL * n_full < (long long)a.split_ns;
+            return (long long)t + 2LL * (n_full + 2 * a.split_clusters) < (long long)a.B;
+        } else {
+            return (long long)t + 2LL * n_clusters < (long long)a.B;
+        }
+    };
+    bool claim_next = spare < 0 && !exhausted && ahead_ok(last_t);
     if (active) {
         issue(row);
         if (writer && lane == 0 && claim_next)
@@ -1638,7 +1651,7 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
             drawn = false;
         }
         issue(row);   // copies first: the logit loads overlap with them
-        claim_next = spare < 0 && !exhausted && (long long)last_t + 2LL * n_clusters < (long long)a.B;
+        claim_next = spare < 0 && !exhausted && ahead_ok(last_t);
         if (writer && lane == 0 && claim_next)
             ticket = claim();
         tk = tok_of(a, row, cur_sv);
