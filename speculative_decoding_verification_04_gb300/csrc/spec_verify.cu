@@ -19,7 +19,9 @@
 // (sv_small.cuh).  The cluster kernel reads the rest of the per-call header
 // (K, the claim order) from a pinned, device-mapped host buffer, copying it
 // into the workspace first when the batch is larger than the grid; it draws
-// the tokens and writes the outputs.
+// the tokens and writes the outputs.  With sv_options.temperature_host the
+// host may launch its split variant, which walks greedy sequences on half
+// clusters (run() says when).
 #include <cuda_runtime.h>
 #include <string.h>
 

@@ -17,7 +17,10 @@
 // atomic claim each (longest K first), made by rank 0 a row ahead and handed
 // to the cluster with that row's exchange while two waves of tickets remain,
 // else when the current sequence ends (so the last go to the clusters free
-// first).
+// first).  A split launch (the caller's host copy of the temperatures) turns
+// the last clusters into two half-walkers each, which take the greedy
+// sequences from a queue of their own, two greedy rows in the shared memory
+// one sampling row takes (see the SPLIT flag of the kernel).
 //
 // Per row, each warp makes one pass over its slice, from shared memory
 // straight into registers (the chunk loops are not unrolled: the smaller loop
