@@ -147,6 +147,30 @@ def test_mix_f32(dev):
     _wrong_hint(d, ws, th, t0, n0)
 
 
+def test_ragged_k_with_zeros_and_three_temperatures(dev):
+    """K drawn from 0..8 (K = 0: the bonus draw alone, greedy or sampling),
+    temperatures 0 / 0.8 / 1.5, bf16 logits of the first vocabulary in a
+    short list whose geometry splits: every sequence against the oracle."""
+    B = 500
+    rng = np.random.default_rng(123)
+    K = rng.integers(0, 9, size=B).astype(np.int32)
+    K[0] = 8
+    assert np.sum(K == 0) > 20
+    temps = rng.choice(np.array([0.0, 0.0, 0.8, 1.5], np.float32), size=B)
+    temps[0] = 1.5
+    bad = temps.copy()
+    bad[0] = 0.0
+    V = next((v for v in (128256, 100000, 64000, 50000, 32000)
+              if _split_clusters(B, 8, v, "bf16", temps) and _split_clusters(B, 8, v, "bf16", bad)),
+             None)
+    assert V is not None, "no bf16 vocabulary of the list splits"
+    inp = W.make_host(B, K, V, "bf16", 2.0, 1.0, temps, seed=123)
+    d = to_device(inp, dev)
+    ws = sv.Workspace(B, 8, V, dtype_code("bf16"), dev)
+    th, t0, n0 = _hinted_equals_unhinted(d, ws)
+    _wrong_hint(d, ws, th, t0, n0)
+
+
 def test_hint_ignored_where_it_does_not_apply(dev):
     """All-sampling and all-greedy batches, a small vocabulary, verify-all:
     no split, the same outputs, no flag."""
