@@ -178,3 +178,44 @@ def test_tree_entry_validation():
     assert call(ws=0) == sv.SV_ERR_NO_MEMORY
     assert call(nbytes=8) == sv.SV_ERR_NO_MEMORY
     assert call(V=sv.sv_max_vocab(0) + 1) == sv.SV_ERR_UNSUPPORTED
+
+
+def test_binding_structs_match_the_header(tmp_path):
+    """The ctypes structs of the binding have the C header's layout: a small C
+    program built with gcc against include/specverify.h prints each field's
+    offset and each struct's size, and the binding's must agree (a field added
+    on one side only would shift every field after it)."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    cuda_inc = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "include")
+    if gcc is None or not os.path.exists(os.path.join(cuda_inc, "cuda_runtime_api.h")):
+        pytest.skip("needs gcc and the CUDA headers")
+    fields = {
+        "sv_diag": ["p_x", "q_x", "resid_mass", "final_row"],
+        "sv_options": [n for n, _ in sv.SVOptions._fields_],
+        "sv_stats": list(sv.STATS_FIELDS),
+    }
+    lines = ["#include <stdio.h>", "#include <stddef.h>", '#include "specverify.h"', "int main(void) {"]
+    for st, names in fields.items():
+        lines.append(f'  printf("{st} size %zu\\n", sizeof({st}));')
+        for n in names:
+            lines.append(f'  printf("{st} {n} %zu\\n", offsetof({st}, {n}));')
+    lines += ["  return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    subprocess.run([gcc, "-I", os.path.join(ROOT, "include"), "-I", cuda_inc, str(src), "-o", str(exe)],
+                   check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split("\n")
+    c = {tuple(l.split()[:2]): int(l.split()[2]) for l in out if l.strip()}
+    assert c[("sv_diag", "size")] == ctypes.sizeof(sv.SVDiag)
+    for n in fields["sv_diag"]:
+        assert c[("sv_diag", n)] == getattr(sv.SVDiag, n).offset
+    assert c[("sv_options", "size")] == ctypes.sizeof(sv.SVOptions)
+    for n in fields["sv_options"]:
+        assert c[("sv_options", n)] == getattr(sv.SVOptions, n).offset, n
+    # the counters are read back as consecutive unsigned 64-bit words
+    assert c[("sv_stats", "size")] == 8 * len(sv.STATS_FIELDS)
+    for k, n in enumerate(sv.STATS_FIELDS):
+        assert c[("sv_stats", n)] == 8 * k, n
