@@ -163,8 +163,9 @@ typedef struct {
  *                   of the cluster kernel (V > 1024, 16-byte aligned rows)
  *                   with enough sequences of both kinds; ignored otherwise.
  *                   It must match the device array: a sequence it calls
- *                   greedy whose device temperature is not 0 may get outputs
- *                   -1 and set bit 1 of the workspace error word
+ *                   greedy whose device temperature is not 0 (and K > 0, so
+ *                   that it has draft rows to read) may get outputs -1 and
+ *                   set bit 1 of the workspace error word
  *                   (sv_workspace_errors returns SV_ERR_INVALID_ARG).  A call
  *                   captured into a CUDA graph keeps the split it was
  *                   captured with: its replays need the same sequences
@@ -325,7 +326,10 @@ sv_status sv_workspace_errors(void* workspace, uint32_t* flags, cudaStream_t str
 /*
  * spec_sample -- draw one token per row from softmax(logits[b] / T_b) by the
  * inverse CDF at uniforms[b] (the draft model's own sampling step, with the
- * machinery of the final draw: a K = 0 verification of every row).
+ * machinery of the final draw: a K = 0 verification of every row).  A batch
+ * of at least twice as many rows as the launch has clusters runs on split
+ * clusters, two rows in the shared memory one verification row takes (as
+ * does any all-K = 0 call of spec_verify_ws / spec_verify_ex).
  *   logits        device, [B][V], dtype.
  *   uniforms      device, [B] float32 in [0, 1).
  *   temperature   device, [B] float32 (0 = argmax, lowest index on ties).

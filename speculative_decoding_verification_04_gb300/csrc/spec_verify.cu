@@ -19,8 +19,9 @@
 // (sv_small.cuh).  The cluster kernel reads the rest of the per-call header
 // (K, the claim order) from a pinned, device-mapped host buffer, copying it
 // into the workspace first when the batch is larger than the grid; it draws
-// the tokens and writes the outputs.  With sv_options.temperature_host the
-// host may launch its split variant, which walks greedy sequences on half
+// the tokens and writes the outputs.  With sv_options.temperature_host, or
+// for a batch of K = 0 sequences only (spec_sample), the host may launch its
+// split variant, which walks sequences that read no draft rows on half
 // clusters (run() says when).
 #include <cuda_runtime.h>
 #include <string.h>
@@ -726,11 +727,22 @@ static sv_status run(const Call& c, int kmax, const sv_options* opt, void* ws, s
     // (with fewer, the last long sampling sequences set the step's length: a
     // batch of 60 sampling and 196 greedy sequences took 59 us split against
     // 53 whole) and the greedy ones the halves' first wave.
+    //
+    // A batch of K = 0 sequences only (spec_sample: one bonus draw per row,
+    // no draft rows) splits every cluster, with no hint needed, when it has
+    // a sequence for each half's first wave.
     int split_cg = 0, split_ns = c.B;
     const float* th = opt ? opt->temperature_host : nullptr;
-    if (!small && th && !host_rows && !want_diag && !opt->verify_all &&
-        !(opt->chunks_per_cta || opt->chunks_per_warp || opt->expire_copy_waits) && g.nv == 4 &&
-        g.nw % 2 == 0 && g.C * g.nw <= 32 && g.clusters >= 2) {
+    const bool plain = !host_rows && !want_diag && !(opt && (opt->verify_all || opt->chunks_per_cta ||
+                                                             opt->chunks_per_warp || opt->expire_copy_waits));
+    const bool splittable = !small && plain && g.nv == 4 && g.nw % 2 == 0 && g.C * g.nw <= 32;
+    bool all_k0 = kmax == 0;
+    for (int b = 0; all_k0 && b < c.B; ++b)
+        all_k0 = c.K[b] == 0;
+    if (splittable && all_k0 && c.B >= 2 * g.clusters && 2 * g.clusters <= kFirstUnits) {
+        split_cg = g.clusters;
+        split_ns = 0;
+    } else if (splittable && th && g.clusters >= 2) {
         int ng = 0;
         for (int b = 0; b < c.B; ++b)
             ng += th[b] == 0.0f ? 1 : 0;
@@ -743,11 +755,13 @@ static sv_status run(const Call& c, int kmax, const sv_options* opt, void* ws, s
         }
     }
     if (!small) {   // the claim order (the small-vocabulary kernel takes sequences in index order)
-        // by K, longest first; split: the sampling sequences, then the greedy ones
+        // by K, longest first; split with a hint: the sampling sequences, then
+        // the greedy ones
         int32_t* ord = reinterpret_cast<int32_t*>(hdr + L.order);
         int pos = 0;
-        for (int cls = 0; cls < (split_cg > 0 ? 2 : 1); ++cls) {
-            auto in = [&](int b) { return split_cg == 0 || ((th[b] == 0.0f) == (cls == 1)); };
+        const bool by_kind = split_cg > 0 && split_ns > 0;   // (th is set: a hinted split)
+        for (int cls = 0; cls < (by_kind ? 2 : 1); ++cls) {
+            auto in = [&](int b) { return !by_kind || ((th[b] == 0.0f) == (cls == 1)); };
             int cnt[SV_K_MAX + 2] = {0};
             for (int b = 0; b < c.B; ++b)
                 if (in(b))

@@ -20,7 +20,8 @@
 // first).  A split launch (the caller's host copy of the temperatures) turns
 // the last clusters into two half-walkers each, which take the greedy
 // sequences from a queue of their own, two greedy rows in the shared memory
-// one sampling row takes (see the SPLIT flag of the kernel).
+// one sampling row takes; a batch of K = 0 sequences only splits every
+// cluster (see the SPLIT flag of the kernel).
 //
 // Per row, each warp makes one pass over its slice, from shared memory
 // straight into registers (the chunk loops are not unrolled: the smaller loop
@@ -330,13 +331,14 @@ __device__ __forceinline__ UnitPos first_unit_pos(const Args& a, int cid, int b,
     return unit_pos(a, b, ok);
 }
 
-// A half of a split cluster takes greedy sequences only (its slices have no
-// draft region): a sequence the caller's temperature hint placed in the greedy
-// queue but whose device temperature is not 0 is made unusable (outputs -1)
-// and flagged in the error word.
-__device__ __forceinline__ Row greedy_only(const Args& a, Row r, int lane)
+// A half of a split cluster takes only sequences that read no draft rows
+// (greedy ones, and K = 0 ones: a bonus draw alone), since its slices have no
+// draft region: a sequence in its queue that has draft rows to read (the
+// caller's temperature hint called it greedy, but its device temperature is
+// not 0) is made unusable (outputs -1) and flagged in the error word.
+__device__ __forceinline__ Row no_draft_only(const Args& a, Row r, int lane)
 {
-    if (!(r.flags & kFGreedy)) {
+    if (r.flags & kFDraft) {
         r.flags &= ~kFUsable;
         if (lane == 0)
             atomicOr(a.err, kErrHint);
@@ -630,8 +632,9 @@ __device__ __forceinline__ void load_chunk(const T* p, int lane, uint4 (&v)[NV])
 // values each lane carries while there is more than one (a transpose-reduce:
 // four shuffles for four strips), leave each strip's sum as four partials
 // (partial q over the eight lanes whose lane index is q modulo 4), stored as
-// dst[k * 4 + q].
-template <int NV>
+// dst[k * 4 + q].  SINGLE: two more levels add the four partials, and the
+// strip's sum is stored alone as dst[k] (a quarter of the space).
+template <int NV, bool SINGLE = false>
 __device__ __forceinline__ void strip_partials(const float (&v)[NV], int lane, float* dst)
 {
     float x;
@@ -658,8 +661,15 @@ __device__ __forceinline__ void strip_partials(const float (&v)[NV], int lane, f
     }
     x += __shfl_xor_sync(kFull, x, 4);
     const int keep = NV == 4 ? 4 : (NV == 2 ? 12 : 28);   // lanes holding a distinct partial
-    if ((lane & keep) == 0)
-        dst[k * 4 + (lane & 3)] = x;
+    if constexpr (SINGLE) {
+        x += __shfl_xor_sync(kFull, x, 1);
+        x += __shfl_xor_sync(kFull, x, 2);
+        if ((lane & (keep | 3)) == 0)
+            dst[k] = x;
+    } else {
+        if ((lane & keep) == 0)
+            dst[k * 4 + (lane & 3)] = x;
+    }
 }
 
 // Warp sum of non-negative lane sums, compensated; +inf if a lane overflowed
@@ -856,7 +866,9 @@ __device__ __noinline__ bool draw_is_near(uint4 tv, uint4 dv, bool use_r, float 
 // rows, from a queue of their own (order entries from a.split_ns on; the
 // sampling sequences come first), two greedy rows in the shared memory one
 // row of a sampling sequence takes.  The other clusters take the sampling
-// queue, then what is left of the greedy one.
+// queue, then what is left of the greedy one.  A batch of K = 0 sequences
+// only (bonus draws, no draft rows) is split whole: a.split_clusters is the
+// grid, a.split_ns is 0, and the halves keep one sum per strip for the draw.
 template <typename T, int NV, bool WIDE, bool HOST, bool SPLIT = false>
 __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
 {
@@ -903,6 +915,10 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
     const uint32_t xbarc = smem_addr(dsm + (hv ? L.stats : L.xbarc));
     int* first = reinterpret_cast<int*>(dsm + (hv ? L.stats + 8 : L.first));
     float* stats = reinterpret_cast<float*>(dsm + L.stats) + (size_t)w * KW * 16;   // [kw][NV][4]
+    // a half's strip sums, one per strip ([2 kw][NV]: a half's ranges are at
+    // most twice as long), after half 1's claim slots (32 bytes): 32 + nw *
+    // 2 kw * NV * 4 bytes fit in the area's nw * kw * 64 at NV = 4
+    float* hstats = reinterpret_cast<float*>(dsm + L.stats + 32) + (size_t)w * 2 * KW * NV;
 
     // ---- set-up: barriers; -inf past V in this warp's range (copies never
     // write there); the cluster's first unit from rank 0 ----
@@ -970,7 +986,7 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
         row = make_row(a, 0, p0.b, p0.Kb, p0.T, p0.tb, p0.db);
         cur_sv = seq_vals(a, u0, lane);
         if (half)
-            row = greedy_only(a, row, lane);
+            row = no_draft_only(a, row, lane);
     }
     Tok tk{0, 0.0f, 0u, 0u, 0};       // lane 0
     float uf = 0.0f;                  // lane 0: the sequence's final uniform
@@ -1280,7 +1296,10 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
                     load_chunk<T, NV>(slot_t + (size_t)j * CH, lane, tv);
                     float sv[NV];
                     LN::exp_strips(tv, mu, c, sv);
-                    strip_partials<NV>(sv, lane, stats + (size_t)j * NV * 4);
+                    if (half)
+                        strip_partials<NV, true>(sv, lane, hstats + (size_t)j * NV);
+                    else
+                        strip_partials<NV>(sv, lane, stats + (size_t)j * NV * 4);
                     float v = 0.0f;
 #pragma unroll
                     for (int k = 0; k < NV; ++k)
@@ -1562,7 +1581,10 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
                     const float own_m = __shfl_sync(kFull, (WIDE && g >= 32) ? xw.x : xv.x, g & 31);
                     const float wscale = bonus ? (own_m == -INFINITY ? 0.0f : weight(own_m, m_t, c)) : 1.0f;
                     // strips in index order: chunk j's strip k is entry j * NV + k
+                    // (a half keeps each strip's sum alone)
                     auto strip_mass = [&](int q) -> float {
+                        if (half)
+                            return hstats[q] * wscale;
                         const float4 v = *reinterpret_cast<const float4*>(stats + (size_t)q * 4);
                         return ((v.x + v.y) + (v.z + v.w)) * wscale;
                     };
@@ -1648,7 +1670,7 @@ __global__ void __maxnreg__(kMaxRegs) sv_sweep_kernel(const Args a)
                 break;
             row = make_row(a, 0, spare_pos.b, spare_pos.Kb, spare_pos.T, spare_pos.tb, spare_pos.db);
             if (half)
-                row = greedy_only(a, row, lane);
+                row = no_draft_only(a, row, lane);
             cur_sv = spare_sv;
             spare = -1;
             drawn = false;

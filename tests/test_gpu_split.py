@@ -171,6 +171,37 @@ def test_ragged_k_with_zeros_and_three_temperatures(dev):
     _wrong_hint(d, ws, th, t0, n0)
 
 
+def _all_k0_splits(B, V, dtype):
+    """Whether a batch of K = 0 sequences splits every cluster (the library's
+    rule, restated)."""
+    g = sv.sv_geometry(B, 0, V, dtype_code(dtype))
+    nv4 = V >= (2048 if dtype == "bf16" else 1024)
+    return (V > 1024 and nv4 and g["warps"] % 2 == 0 and g["warp_ranges"] <= 32 and
+            B >= 2 * g["clusters"] and 2 * g["clusters"] <= 256)
+
+
+@pytest.mark.parametrize("dtype,vocabs,B", [("bf16", (128256,), 400),
+                                            ("f32", (50000, 40000, 64000, 32000, 24000), 500)])
+def test_k0_batches_split_every_cluster(dev, dtype, vocabs, B):
+    """A batch of K = 0 sequences (the draft model's sampling step) runs on
+    half clusters with no hint: spec_sample and a K = 0 verification give
+    the oracle's draws for every row (temperatures 0, 0.7, 1 and 1.6)."""
+    V = next((v for v in vocabs if _all_k0_splits(B, v, dtype)), None)
+    assert V is not None, "no vocabulary of the list splits"
+    temps = np.array([0.0, 0.7, 1.0, 1.6], np.float32)[np.arange(B) % 4]
+    inp = W.make_host(B, 0, V, dtype, 2.0, 1.0, temps, seed=B + 7)
+    ref = oracle_ref_threaded(inp)
+    d = to_device(inp, dev)
+    out = sv.spec_sample(d["target"].view(B, V), d["uniforms"].view(B), d["temperature"])
+    got = out.cpu().numpy().astype(np.int32).reshape(B, 1)
+    c = compare(ref, got, np.zeros(B, np.int32), inp=inp)
+    assert c["n"] == B
+    ws = sv.Workspace(B, 0, V, dtype_code(dtype), dev)
+    t, n = run_gpu(d, "ws", workspace=ws)
+    assert sv.sv_workspace_errors(ws) == 0
+    assert np.array_equal(t, got) and np.all(n == 0)
+
+
 def test_hint_ignored_where_it_does_not_apply(dev):
     """All-sampling and all-greedy batches, a small vocabulary, verify-all:
     no split, the same outputs, no flag."""
