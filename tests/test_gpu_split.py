@@ -1,4 +1,5 @@
-"""The temperature hint (sv_options.temperature_host).
+"""Split launches: the temperature hint (sv_options.temperature_host), and
+batches of K = 0 sequences, which split every cluster without a hint.
 
 With a host copy of the temperatures the launch may split some clusters in
 two halves that walk the greedy sequences, while the whole clusters take the
